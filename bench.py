@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark: ring-allreduce gradient sync of N logical ranks on one GB300.
+
+    python bench.py [--gpus G] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: N = 8 logical ranks, one 1 GiB fp32 bucket per rank
+(268,435,456 elements, N(0, 1e-2^2) from seed r), ring allreduce divided by
+8.  A step is one ring_allreduce_fused call over the resident bucket (the
+bucket is the rank's whole gradient vector, so the pack and unpack copies
+are identities here; the bucketed DDP step with pack/unpack is timed on the
+355M-parameter decoder and reported under "ddp_step").
+
+Prints ONE JSON line.  value = bus bandwidth 2(N-1)/N * S_bytes / t summed
+over GPUs (GB/s, 1e9 B/s); roofline.achieved = algorithmic HBM bytes
+2*N*S_bytes per launch / average launch time.  With G > 1 (torchrun, one
+process per GPU) each GPU runs an independent replica of the workload
+(the N logical ranks never span GPUs); time is the max over GPUs.
+
+--impl reference times the CPU oracle (the plain ring simulation) on a
+bounded sample of the same workload on the host cores, as the comparison arm.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ring allreduce busbw GB/s and achieved HBM GB/s vs peak, N logical ranks, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+N_RANKS = 8
+NUMEL = 1 << 28
+MiB = 1 << 20
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("ring_kernels.cu", "ddp_device.cuh", "ddp_internal.h"):
+        with open(os.path.join(ROOT, "gradient_sync_plan_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/<name>,
+    or None if absent or taken on a different version of the kernel sources."""
+    p = os.path.join(ROOT, "profiles", name)
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None, None
+    m = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    d = re.search(r"kernel_sources_digest:\s*([0-9a-f]+)", txt)
+    if not m or not d or d.group(1) != kernel_sources_digest():
+        return None, p
+    return float(m.group(1)), p
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-i", str(self.gpu_index), "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def mark_start(self):
+        self.t0 = _dt.datetime.now()
+
+    def mark_end(self):
+        self.t1 = _dt.datetime.now()
+
+    def stop(self):
+        time.sleep(0.15)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
+        use = inside if inside else [p for _, p in rows]
+
+        def num(s):
+            m = re.match(r"([0-9.]+)", s)
+            return float(m.group(1)) if m else None
+
+        sm = sorted(v for v in (num(p[2]) for p in use) if v is not None)
+        mx = [v for v in (num(p[3]) for p in use) if v is not None]
+        reasons = set()
+        for p in use:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((num(p[4]) or 0.0) for p in use) if use else None}
+
+
+def cpu_oracle_run(n_ranks: int, budget_s: float, max_numel: int, reps_cap: int = 1000):
+    """Time the CPU oracle's ring on a bounded sample; returns a dict."""
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    # calibrate on a small sample, then size the sample to the budget
+    cal = 1 << 18
+    x = workloads.rank_vectors(n_ranks, cal, "randn", std=1e-2).numpy()
+    rows = [x[r] for r in range(n_ranks)]
+    t = time.perf_counter()
+    oracle.ring_allreduce(rows, oracle.F32, n_ranks)
+    per_elem = max((time.perf_counter() - t) / cal, 1e-10)
+    numel = int(min(max_numel, max(1 << 16, budget_s / 3.0 / per_elem)))
+    numel = 1 << int(math.log2(numel))
+    x = workloads.rank_vectors(n_ranks, numel, "randn", std=1e-2).numpy()
+    rows = [x[r] for r in range(n_ranks)]
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < reps_cap and (time.perf_counter() - t_start) < budget_s:
+        t = time.perf_counter()
+        oracle.ring_allreduce(rows, oracle.F32, n_ranks)
+        times.append(time.perf_counter() - t)
+    tm = sorted(times)[len(times) // 2]
+    s_bytes = numel * 4
+    return {"numel": numel, "reps": len(times), "median_s": tm, "total_s": sum(times),
+            "busbw_gbs": 2 * (n_ranks - 1) / n_ranks * s_bytes / tm / 1e9,
+            "hbm_equiv_gbs": 2 * n_ranks * s_bytes / tm / 1e9}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# --------------------------------------------------------------------------
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    # per-step sample sized so that warmup + steps fit in about two minutes
+    cal = 1 << 18
+    x = workloads.rank_vectors(N_RANKS, cal, "randn", std=1e-2).numpy()
+    rows = [x[r] for r in range(N_RANKS)]
+    t = time.perf_counter()
+    oracle.ring_allreduce(rows, oracle.F32, N_RANKS)
+    per_elem = max((time.perf_counter() - t) / cal, 1e-10)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    numel = int(min(NUMEL, max(1 << 12, budget / per_elem)))
+    numel = 1 << int(math.log2(numel))
+    x = workloads.rank_vectors(N_RANKS, numel, "randn", std=1e-2).numpy()
+    rows = [x[r] for r in range(N_RANKS)]
+    for _ in range(args.warmup):
+        oracle.ring_allreduce(rows, oracle.F32, N_RANKS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.ring_allreduce(rows, oracle.F32, N_RANKS)
+    dt = time.perf_counter() - t0
+    s_bytes = numel * 4
+    value = 2 * (N_RANKS - 1) / N_RANKS * s_bytes * args.steps / dt / 1e9
+    part = "the whole" if numel == NUMEL else "a bounded sample of the"
+    sample = (f"N={N_RANKS} ranks x {numel} fp32 per rank ({s_bytes // MiB} MiB) per step, {part} "
+              f"1 GiB-per-rank bucket; single-threaded C oracle")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": "N=8 logical ranks, one 1 GiB fp32 bucket per rank, ring allreduce / 8",
+                      "ranks": N_RANKS, "numel": NUMEL, "sample_numel": numel, "parallelism": "host cores"},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ddp.lib()
+    numel = args.numel
+    N = N_RANKS
+    s_bytes = numel * 4
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    x = torch.empty((N, numel), dtype=torch.float32, device=dev)
+    for r in range(N):
+        x[r].copy_(workloads.randn_f32(numel, r, 1e-2, device=str(dev)))
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        ddp.ring_allreduce_fused(x, N)
+    torch.cuda.synchronize()
+
+    sampler = None
+    if rank == 0 and not args.no_clocks:
+        phys = local_rank
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            try:
+                phys = int(vis.split(",")[local_rank])
+            except Exception:
+                phys = local_rank
+        sampler = ClockSampler(phys)
+        sampler.start()
+
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ddp.ring_allreduce_fused(x, N)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if sampler:
+        sampler.stop()
+    ms_step = ms / args.steps
+    busbw_total = world * 2 * (N - 1) / N * s_bytes * args.steps / (ms / 1e3) / 1e9
+    hbm = 2 * N * s_bytes / (ms_step / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic, traffic_src = profiled_traffic("ring_fused_n8_1gib.md")
+    if traffic is not None and numel != NUMEL:
+        traffic = traffic * numel / NUMEL
+
+    out = {"metric": METRIC, "value": busbw_total, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": f"N={N} logical ranks, one fp32 bucket of {numel} elements "
+                                  f"({s_bytes / MiB:.0f} MiB) per rank, fused ring allreduce / {N}",
+                      "ranks": N, "numel": numel, "bucket_bytes": s_bytes, "algorithm": "ring_allreduce_fused",
+                      "l2": f"inputs {N * s_bytes / 2**30:.2f} GiB per step, larger than L2; no flush",
+                      "parallelism": "replicas" if world > 1 else "single GPU"},
+           "algbw_gbs": s_bytes / (ms_step / 1e3) / 1e9,
+           "hbm_gbs": hbm,
+           "hbm_frac_of_nominal_8tbs": hbm / NOMINAL_HBM_GBS,
+           "roofline": {"bound": "hbm", "achieved": hbm, "peak": peak, "unit": "GB/s", "frac": hbm / peak,
+                        "traffic": traffic, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                        if peak_kind == "measured" else "fallback 6.8 TB/s",
+                        "kernel": "k_ring_fused", "algorithmic_bytes_per_launch": 2 * N * s_bytes},
+           "gpu_launches": args.steps}
+    if sampler:
+        out["clocks"] = sampler.summary()
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    if not args.no_e2e:
+        host = torch.empty((N, numel), dtype=torch.float32).pin_memory()
+        host.copy_(x)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        ddp.ring_allreduce_fused_from_host(host, host, x, N)
+        torch.cuda.synchronize()
+        barrier()
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            ddp.ring_allreduce_fused_from_host(host, host, x, N)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        out["e2e"] = {"value": world * 2 * (N - 1) / N * s_bytes * e2e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "h2d_bytes_per_step": N * s_bytes, "d2h_bytes_per_step": N * s_bytes,
+                      "steps": e2e_steps, "ms_per_step": e_ms / e2e_steps,
+                      "api": "ring_allreduce_fused_from_host (pinned host buffers, copies on the same stream)"}
+        out["gpu_launches"] += e2e_steps
+        del host
+
+    # ---- extra measurements ------------------------------------------------
+    if not args.no_extras:
+        extra_steps = max(3, min(20, args.steps // 10))
+        a = x
+        ev0.record(stream)
+        for _ in range(extra_steps):
+            ddp.ring_allreduce_staged(a, N)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        st_ms = ev0.elapsed_time(ev1) / extra_steps
+        out["staged"] = {"ms_per_step": st_ms, "launches_per_step": 2 * (N - 1),
+                         "busbw_gbs": 2 * (N - 1) / N * s_bytes / (st_ms / 1e3) / 1e9,
+                         "hbm_alg_gbs": 5 * (N - 1) * s_bytes / (st_ms / 1e3) / 1e9,
+                         "useful_gbs": 2 * N * s_bytes / (st_ms / 1e3) / 1e9}
+        del a, x
+        torch.cuda.empty_cache()
+        out["ddp_step"] = ddp_step_bench(ddp, workloads, torch, dev, stream, extra_steps)
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_oracle_run(N, args.cpu_budget, NUMEL)
+        out["cpu_baseline"] = {"value": cpu["busbw_gbs"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": f"N={N} ranks x {cpu['numel']} fp32 per rank "
+                                         f"({cpu['numel'] * 4 // MiB} MiB), {cpu['reps']} runs, median; "
+                                         f"single-threaded C ring simulation on the host "
+                                         f"({host_cores()} cores present)",
+                               "median_s": cpu["median_s"]}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def ddp_step_bench(ddp, workloads, torch, dev, stream, steps):
+    """The bucketed DDP step on the 355M-parameter decoder, N = 8, fp32."""
+    numels = workloads.param_numels(workloads.decoder_param_shapes())
+    N, total = N_RANKS, sum(numels)
+    p_bytes = total * 4
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, MiB, 25 * MiB)
+    g = torch.empty((N, total), dtype=torch.float32, device=dev)
+    for r in range(N):
+        g[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)))
+    offs = [0]
+    for n in numels:
+        offs.append(offs[-1] + n)
+    views = [[g[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+    buckets = [[torch.empty(int(n), dtype=torch.float32, device=dev) for n in plan[2]] for _ in range(N)]
+    res = {"workload": "decoder 24x1024, 292 tensors, 354,823,168 fp32 params, N=8, caps 1 MiB / 25 MiB",
+           "buckets": int(len(plan[2])), "bucket_sizes_bytes_first_last": [int(plan[2][0]) * 4, int(plan[2][-1]) * 4]}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, algo, bytes_alg in (("fused", ddp.DDP_ALGO_FUSED, 6 * N * p_bytes),
+                                  ("staged", ddp.DDP_ALGO_STAGED, (2 * N + 5 * (N - 1)) * p_bytes + 2 * N * p_bytes),
+                                  ("view", ddp.DDP_ALGO_VIEW, 2 * N * p_bytes)):
+        call = ddp.SyncCall(views, plan, None if algo == ddp.DDP_ALGO_VIEW else buckets, N, algo)
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        res[name] = {"ms_per_step": ms, "hbm_alg_gbs": bytes_alg / (ms / 1e3) / 1e9,
+                     "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
+    # no_sync: 3 local accumulations of a micro-batch, then one sync (view)
+    scratch = torch.empty_like(g)
+    scratch.copy_(g)
+    call = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW)
+    ev0.record(stream)
+    for _ in range(steps):
+        for _m in range(3):
+            ddp.ddp_grad_accumulate(g, scratch)
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    res["no_sync_4_micro_view"] = {"ms_per_step": ms,
+                                   "hbm_alg_gbs": (3 * 3 * N * p_bytes + 2 * N * p_bytes) / (ms / 1e3) / 1e9,
+                                   "allreduce_calls_per_step": int(len(plan[2]))}
+    del g, scratch, buckets, views
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--numel", type=int, default=NUMEL, help="elements per rank (default: the 1 GiB bucket)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU-oracle work")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and args.steps >= 10:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,323 @@
+"""GB300-native DDP gradient synchronisation: Python binding of libddp_gb300.
+
+Every function here marshals arguments (torch tensors -> device pointers,
+Python lists -> pointer tables, torch streams -> cudaStream_t) and calls the
+C ABI declared in include/ddp.h, whose names it keeps.  All computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback -- if the
+library is missing or cannot be built, every call raises.
+
+The N data-parallel ranks are N logical replicas in one GPU: "rank r" is the
+r-th row of an [N, S] tensor, or the r-th entry of a list of tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional, Sequence, Tuple, Union
+
+import numpy as np
+
+from . import build as _build
+
+F32 = 0
+BF16 = 1
+DDP_ALGO_FUSED = 0
+DDP_ALGO_STAGED = 1
+DDP_ALGO_VIEW = 2
+DDP_MAX_WORLD = 512
+FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
+BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
+
+STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_CUDA",
+          -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY"}
+
+# every symbol include/ddp.h declares
+EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_plan_buckets", "ddp_bucket_pack", "ddp_bucket_unpack",
+           "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
+           "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
+
+
+class DDPError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libddp_gb300.so (building it from source first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                _build.build()
+            L = ctypes.CDLL(path)
+            i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+            P = ctypes.POINTER
+            L.ddp_status_string.argtypes = [i32]
+            L.ddp_status_string.restype = ctypes.c_char_p
+            L.ddp_abi_version.argtypes = []
+            L.ddp_abi_version.restype = i32
+            L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
+            L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
+            L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
+            L.ring_allreduce_fused.argtypes = [i32, P(vp), i64, i32, i32, vp]
+            L.ring_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
+            L.ring_allreduce_fused_from_host.argtypes = [i32, P(vp), P(vp), P(vp), i64, i32, i32, vp]
+            L.ddp_grad_accumulate.argtypes = [i32, P(vp), P(vp), i64, i32, vp]
+            L.ddp_sync_buckets.argtypes = [i32, i32, P(vp), P(i64), P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
+                                           i32, vp]
+            L.ddp_bucket_allreduce_view.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, i32, vp]
+            for name in EXPORTS[2:]:
+                getattr(L, name).restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise DDPError(fn, status)
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _vp_array(ptrs: Sequence[int]):
+    return (ctypes.c_void_p * max(len(ptrs), 1))(*[int(p) for p in ptrs])
+
+
+def _i64_array(vals: Sequence[int]):
+    return (ctypes.c_int64 * max(len(vals), 1))(*[int(v) for v in vals])
+
+
+def _i32_array(vals: Sequence[int]):
+    return (ctypes.c_int32 * max(len(vals), 1))(*[int(v) for v in vals])
+
+
+def _rank_tensors(bufs) -> list:
+    """[N, S] tensor -> list of its rows; list of tensors -> itself."""
+    torch = _torch()
+    if isinstance(bufs, torch.Tensor):
+        if bufs.dim() != 2 or not bufs.is_contiguous():
+            raise ValueError("rank buffers: a contiguous [N, S] tensor or a list of 1-D tensors")
+        return [bufs[r] for r in range(bufs.shape[0])]
+    return list(bufs)
+
+
+def _rank_ptrs(bufs) -> Tuple[list, int, int]:
+    ts = _rank_tensors(bufs)
+    if not ts:
+        raise ValueError("no rank buffers")
+    numel = ts[0].numel()
+    code = dtype_code(ts[0])
+    for t in ts:
+        if t.numel() != numel or dtype_code(t) != code or not t.is_contiguous():
+            raise ValueError("rank buffers must be contiguous with equal numel and dtype")
+    return [t.data_ptr() for t in ts], numel, code
+
+
+# --------------------------------------------------------------------------
+# C ABI, one Python function per entry point
+# --------------------------------------------------------------------------
+
+def ddp_status_string(status: int) -> str:
+    return lib().ddp_status_string(int(status)).decode()
+
+
+def ddp_abi_version() -> int:
+    return int(lib().ddp_abi_version())
+
+
+def ddp_plan_buckets(numels: Sequence[int], dtype: int = F32, first_bucket_bytes: int = FIRST_BUCKET_BYTES,
+                     bucket_cap_bytes: int = BUCKET_CAP_BYTES):
+    """Reverse-registration-order bucket plan -> (bucket_of[P], offset_of[P], bucket_numel[K])."""
+    P = len(numels)
+    b_of = (ctypes.c_int32 * max(P, 1))()
+    off = (ctypes.c_int64 * max(P, 1))()
+    bn = (ctypes.c_int64 * max(P, 1))()
+    nb = ctypes.c_int32(0)
+    _check("ddp_plan_buckets", lib().ddp_plan_buckets(P, _i64_array(numels), dtype, first_bucket_bytes,
+                                                      bucket_cap_bytes, b_of, off, bn, ctypes.byref(nb)))
+    K = nb.value
+    return (np.array(b_of[:P], dtype=np.int32), np.array(off[:P], dtype=np.int64),
+            np.array(bn[:K], dtype=np.int64))
+
+
+def ring_allreduce_fused(bufs, divisor: int = 0, stream=None) -> None:
+    """In-place ring allreduce of the N rank buffers (+ divide), one pass."""
+    ptrs, numel, code = _rank_ptrs(bufs)
+    _check("ring_allreduce_fused", lib().ring_allreduce_fused(len(ptrs), _vp_array(ptrs), numel, code, divisor,
+                                                              _stream(stream)))
+
+
+def ring_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
+    """In-place ring allreduce reproduced hop by hop (2(N-1) launches)."""
+    ptrs, numel, code = _rank_ptrs(bufs)
+    _check("ring_allreduce_staged", lib().ring_allreduce_staged(len(ptrs), _vp_array(ptrs), numel, code, divisor,
+                                                                _stream(stream)))
+
+
+def ring_allreduce_fused_from_host(host_in, host_out, dev_bufs, divisor: int = 0, stream=None) -> None:
+    """Host buffers in and out, device scratch in between (copies + kernel on one stream)."""
+    hi, numel, code = _rank_ptrs(host_in)
+    ho, n2, c2 = _rank_ptrs(host_out)
+    dv, n3, c3 = _rank_ptrs(dev_bufs)
+    if not (numel == n2 == n3 and code == c2 == c3 and len(hi) == len(ho) == len(dv)):
+        raise ValueError("host_in, host_out and dev_bufs must match")
+    _check("ring_allreduce_fused_from_host",
+           lib().ring_allreduce_fused_from_host(len(hi), _vp_array(hi), _vp_array(ho), _vp_array(dv), numel, code,
+                                                divisor, _stream(stream)))
+
+
+def ddp_grad_accumulate(acc, grads, stream=None) -> None:
+    """acc[r] += grads[r] for every rank (one no_sync micro-batch)."""
+    pa, numel, code = _rank_ptrs(acc)
+    pg, n2, c2 = _rank_ptrs(grads)
+    if numel != n2 or code != c2 or len(pa) != len(pg):
+        raise ValueError("acc and grads must match")
+    _check("ddp_grad_accumulate", lib().ddp_grad_accumulate(len(pa), _vp_array(pa), _vp_array(pg), numel, code,
+                                                            _stream(stream)))
+
+
+def _member_tables(grads: Sequence[Sequence], offsets: Sequence[int]):
+    world = len(grads)
+    n = len(offsets)
+    code = None
+    ptrs, numels = [], []
+    for r in range(world):
+        if len(grads[r]) != n:
+            raise ValueError("every rank needs one gradient per member")
+        for i, g in enumerate(grads[r]):
+            c = dtype_code(g)
+            if code is None:
+                code = c
+            if c != code or not g.is_contiguous():
+                raise ValueError("gradients must be contiguous and of one dtype")
+            ptrs.append(g.data_ptr())
+            if r == 0:
+                numels.append(g.numel())
+            elif g.numel() != numels[i]:
+                raise ValueError("member numel differs across ranks")
+    return world, n, ptrs, numels, (F32 if code is None else code)
+
+
+def ddp_bucket_pack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
+    """buckets[r][offset_i : offset_i + numel_i] = grads[r][i] for every rank r and member i."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    bp, bnumel, bcode = _rank_ptrs(buckets)
+    if n and bcode != code:
+        raise ValueError("bucket dtype differs from gradients")
+    _check("ddp_bucket_pack", lib().ddp_bucket_pack(world, n, _vp_array(ptrs), _i64_array(numels),
+                                                    _i64_array(offsets), _vp_array(bp), bnumel, bcode,
+                                                    _stream(stream)))
+
+
+def ddp_bucket_unpack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
+    """grads[r][i] = buckets[r][offset_i : offset_i + numel_i] for every rank r and member i."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    bp, bnumel, bcode = _rank_ptrs(buckets)
+    if n and bcode != code:
+        raise ValueError("bucket dtype differs from gradients")
+    _check("ddp_bucket_unpack", lib().ddp_bucket_unpack(world, n, _vp_array(ptrs), _i64_array(numels),
+                                                        _i64_array(offsets), _vp_array(bp), bnumel, bcode,
+                                                        _stream(stream)))
+
+
+def ddp_bucket_allreduce_view(grads: Sequence[Sequence], offsets: Sequence[int], bucket_numel: int,
+                              divisor: int = 0, stream=None) -> None:
+    """Pack + ring allreduce + divide + unpack of one bucket in one pass over the gradients."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    _check("ddp_bucket_allreduce_view",
+           lib().ddp_bucket_allreduce_view(world, n, _vp_array(ptrs), _i64_array(numels), _i64_array(offsets),
+                                           int(bucket_numel), code, divisor, _stream(stream)))
+
+
+def ddp_sync_buckets(grads: Sequence[Sequence], plan, buckets: Optional[Sequence[Sequence]] = None,
+                     divisor: Optional[int] = None, algo: int = DDP_ALGO_FUSED, stream=None) -> None:
+    """Reducer step over a whole model: every bucket packed, reduced, averaged, unpacked.
+
+    grads[r][p]: rank r's gradient of parameter p (registration order).
+    plan: (bucket_of, offset_of, bucket_numel) from ddp_plan_buckets.
+    buckets[r][k]: rank r's buffer for bucket k (not needed for DDP_ALGO_VIEW).
+    divisor: defaults to the world size.
+    """
+    call = SyncCall(grads, plan, buckets, divisor, algo)
+    call(stream)
+
+
+class SyncCall:
+    """Pre-marshalled ddp_sync_buckets call: builds the pointer tables once so
+    that repeated steps over the same tensors cost one ctypes call each."""
+
+    def __init__(self, grads, plan, buckets=None, divisor=None, algo=DDP_ALGO_FUSED):
+        b_of, off, bn = plan
+        self.world = len(grads)
+        self.n_params = len(b_of)
+        flat, numels, code = [], [], None
+        for r in range(self.world):
+            if len(grads[r]) != self.n_params:
+                raise ValueError("every rank needs one gradient per parameter")
+            for p, g in enumerate(grads[r]):
+                c = dtype_code(g)
+                code = c if code is None else code
+                if c != code or not g.is_contiguous():
+                    raise ValueError("gradients must be contiguous and of one dtype")
+                flat.append(g.data_ptr())
+                if r == 0:
+                    numels.append(g.numel())
+        self.dtype = F32 if code is None else code
+        self.K = len(bn)
+        self._grads = _vp_array(flat)
+        self._numel = _i64_array(numels)
+        self._b_of = _i32_array(b_of)
+        self._off = _i64_array(off)
+        self._bn = _i64_array(bn)
+        if buckets is not None:
+            bflat = [buckets[r][k].data_ptr() for r in range(self.world) for k in range(self.K)]
+            self._buckets = _vp_array(bflat)
+        else:
+            if algo != DDP_ALGO_VIEW:
+                raise ValueError("bucket buffers are required unless algo is DDP_ALGO_VIEW")
+            self._buckets = None
+        self.divisor = self.world if divisor is None else int(divisor)
+        self.algo = int(algo)
+        self._keep = (grads, buckets)     # the tensors must outlive the call object
+
+    def __call__(self, stream=None) -> None:
+        _check("ddp_sync_buckets",
+               lib().ddp_sync_buckets(self.world, self.n_params, self._grads, self._numel, self._b_of, self._off,
+                                      self.K, self._bn, self._buckets, self.dtype, self.divisor, self.algo,
+                                      _stream(stream)))

@@ -1,0 +1,243 @@
+// bucket_kernels.cu -- gradient <-> bucket copies and the fused view path.
+//
+// DDP copies every gradient into its bucket before the bucket's allreduce and
+// copies the averaged bucket back afterwards when gradient_as_bucket_view is
+// off ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03
+// "Overlap" and section 05 steps 2-3; "Day 17 · 梯度的集体行动" Reducer
+// pseudo-code).  k_copy_items does one launch's worth of those copies: a
+// table of (src, dst, bytes) items, cut into fixed-size tiles, distributed
+// over a persistent grid.  The table travels in the kernel's parameter space,
+// so a call needs no device workspace and no host-to-device copy.
+//
+// With gradient_as_bucket_view on, a gradient *is* a slice of its bucket.
+// k_bucket_view takes that to its end: it reads every member's elements from
+// every rank's gradient, folds them in the ring order of the chunk their
+// bucket position falls in, divides and writes back -- the pack, the ring
+// allreduce, the average and the unpack in one pass.
+#include <algorithm>
+#include <cstdio>
+#include <vector>
+
+#include "ddp_device.cuh"
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+// ---------------------------------------------------------------------------
+// Multi-tensor copy
+// ---------------------------------------------------------------------------
+
+constexpr int kCopyItems = 256;          // items per launch (8 KB of parameters)
+constexpr int64_t kCopyTile = 32768;     // bytes per tile
+
+struct CopyBatch {
+    int32_t n;
+    int32_t pad_;
+    int64_t tile_end[kCopyItems];   // inclusive prefix sum of tiles per item
+    const char* src[kCopyItems];
+    char* dst[kCopyItems];
+    int64_t bytes[kCopyItems];
+};
+
+// Copy [b0, b1) bytes from src to dst with the whole block.  Element pointers
+// are at least 2-byte aligned; when src and dst agree modulo 16 the middle is
+// copied in 16-byte vectors, four in flight per thread.
+__device__ __forceinline__ void block_copy(const char* src, char* dst, int64_t b0, int64_t b1) {
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(src + b0), da = reinterpret_cast<uintptr_t>(dst + b0);
+    const int64_t n = b1 - b0;
+    if (((sa ^ da) & 15u) == 0) {
+        const int64_t head = std::min<int64_t>((16 - (da & 15u)) & 15u, n);
+        for (int64_t k = 2 * (int64_t)threadIdx.x; k < head; k += 2 * blockDim.x)
+            *reinterpret_cast<uint16_t*>(dst + b0 + k) = *reinterpret_cast<const uint16_t*>(src + b0 + k);
+        const int64_t a0 = b0 + head;
+        const int64_t nv = (b1 - a0) >> 4;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + a0);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + a0);
+        int64_t k = threadIdx.x;
+        for (; k + 3 * (int64_t)blockDim.x < nv; k += 4 * (int64_t)blockDim.x) {
+            uint4 x0 = s4[k], x1 = s4[k + blockDim.x], x2 = s4[k + 2 * blockDim.x], x3 = s4[k + 3 * blockDim.x];
+            d4[k] = x0;
+            d4[k + blockDim.x] = x1;
+            d4[k + 2 * blockDim.x] = x2;
+            d4[k + 3 * blockDim.x] = x3;
+        }
+        for (; k < nv; k += blockDim.x) d4[k] = s4[k];
+        const int64_t a1 = a0 + (nv << 4);
+        for (int64_t q = a1 + 2 * (int64_t)threadIdx.x; q < b1; q += 2 * blockDim.x)
+            *reinterpret_cast<uint16_t*>(dst + q) = *reinterpret_cast<const uint16_t*>(src + q);
+    } else if (((sa | da | (uintptr_t)n) & 3u) == 0) {
+        for (int64_t k = 4 * (int64_t)threadIdx.x; k < n; k += 4 * blockDim.x)
+            *reinterpret_cast<uint32_t*>(dst + b0 + k) = *reinterpret_cast<const uint32_t*>(src + b0 + k);
+    } else {
+        for (int64_t k = 2 * (int64_t)threadIdx.x; k < n; k += 2 * blockDim.x)
+            *reinterpret_cast<uint16_t*>(dst + b0 + k) = *reinterpret_cast<const uint16_t*>(src + b0 + k);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_copy_items(const __grid_constant__ CopyBatch b) {
+    const int64_t tiles = b.tile_end[b.n - 1];
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        int lo = 0, hi = b.n - 1;            // first item whose tile_end > tile
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (b.tile_end[mid] > tile) hi = mid; else lo = mid + 1;
+        }
+        const int64_t first = lo ? b.tile_end[lo - 1] : 0;
+        const int64_t b0 = (tile - first) * kCopyTile;
+        const int64_t b1 = std::min(b0 + kCopyTile, b.bytes[lo]);
+        block_copy(b.src[lo], b.dst[lo], b0, b1);
+    }
+}
+
+cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t stream) {
+    CopyBatch b;
+    int64_t i = 0;
+    while (i < n) {
+        b.n = 0;
+        b.pad_ = 0;
+        int64_t tiles = 0;
+        for (; i < n && b.n < kCopyItems; ++i) {
+            if (items[i].bytes <= 0) continue;
+            tiles += (items[i].bytes + kCopyTile - 1) / kCopyTile;
+            b.tile_end[b.n] = tiles;
+            b.src[b.n] = static_cast<const char*>(items[i].src);
+            b.dst[b.n] = static_cast<char*>(items[i].dst);
+            b.bytes[b.n] = items[i].bytes;
+            ++b.n;
+        }
+        if (b.n == 0) continue;
+        const int grid = grid_for((const void*)k_copy_items, tiles * kThreads);
+        k_copy_items<<<std::max<int64_t>(1, std::min<int64_t>(grid, tiles)), kThreads, 0, stream>>>(b);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (debug_enabled())
+            fprintf(stderr, "[ddp] copy_items n=%d tiles=%lld\n", b.n, (long long)tiles);
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Fused view: pack + ring allreduce + average + unpack of one bucket
+// ---------------------------------------------------------------------------
+
+constexpr int kViewMembers = 128;
+constexpr int kViewPtrs = 2048;          // member x rank pointers per launch
+
+struct ViewBatch {
+    int32_t n;            // members in this launch
+    int32_t world;
+    int64_t clen;         // chunk length of the whole bucket, ceil(bucket_numel / N)
+    int64_t tile_end[kViewMembers];
+    int64_t numel[kViewMembers];
+    int64_t offset[kViewMembers];
+    int32_t vec[kViewMembers];
+    char* ptr[kViewPtrs];  // ptr[m * world + r]: rank r's gradient of member m
+};
+
+template <class E>
+constexpr int64_t view_tile_elems() { return (int64_t)kThreads * E::L * 4; }
+
+template <class E, int DIV, int G>
+__global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant__ ViewBatch b, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    constexpr int64_t TILE = view_tile_elems<E>();
+    const int world = b.world;
+    const int64_t tiles = b.tile_end[b.n - 1];
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        int lo = 0, hi = b.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (b.tile_end[mid] > tile) hi = mid; else lo = mid + 1;
+        }
+        const int m = lo;
+        const int64_t first = m ? b.tile_end[m - 1] : 0;
+        const int64_t e0 = (tile - first) * TILE;
+        const int64_t e1 = std::min(e0 + TILE, b.numel[m]);
+        const int64_t base = b.offset[m];          // bucket position of element 0
+        auto at = [&](int r) -> const char* { return b.ptr[m * world + r]; };
+        if (b.vec[m]) {
+            for (int64_t e = e0 + (int64_t)threadIdx.x * L; e < e1; e += (int64_t)blockDim.x * L) {
+                const int64_t q = base + e;
+                const int64_t j = q / b.clen;
+                if (e + L <= e1 && (q + L - 1) / b.clen == j) {
+                    const int start = (j + 1 == world) ? 0 : (int)j + 1;
+                    V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, e * (int64_t)sizeof(S)), dop);
+                    for (int r = 0; r < world; ++r) st_stream<V>(b.ptr[m * world + r] + e * (int64_t)sizeof(S), y);
+                } else {
+                    for (int l = 0; l < L && e + l < e1; ++l) {
+                        const int jj = (int)((q + l) / b.clen);
+                        const int start = (jj + 1 == world) ? 0 : jj + 1;
+                        S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e + l), dop);
+                        for (int r = 0; r < world; ++r) reinterpret_cast<S*>(b.ptr[m * world + r])[e + l] = y;
+                    }
+                }
+            }
+        } else {
+            for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+                const int jj = (int)((base + e) / b.clen);
+                const int start = (jj + 1 == world) ? 0 : jj + 1;
+                S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e), dop);
+                for (int r = 0; r < world; ++r) reinterpret_cast<S*>(b.ptr[m * world + r])[e] = y;
+            }
+        }
+    }
+}
+
+template <class E, int DIV, int G>
+static cudaError_t view_impl(int world, const ViewMember* members, int n, int64_t bucket_numel, float dop,
+                             cudaStream_t st) {
+    auto k = k_bucket_view<E, DIV, G>;
+    constexpr int64_t TILE = view_tile_elems<E>();
+    const int per_launch = std::min(kViewMembers, kViewPtrs / world);
+    ViewBatch b;
+    b.world = world;
+    b.clen = chunk_len(bucket_numel, world);
+    int i = 0;
+    while (i < n) {
+        b.n = 0;
+        int64_t tiles = 0;
+        for (; i < n && b.n < per_launch; ++i) {
+            if (members[i].numel <= 0) continue;
+            tiles += (members[i].numel + TILE - 1) / TILE;
+            b.tile_end[b.n] = tiles;
+            b.numel[b.n] = members[i].numel;
+            b.offset[b.n] = members[i].offset;
+            b.vec[b.n] = members[i].vec_ok ? 1 : 0;
+            for (int r = 0; r < world; ++r) b.ptr[b.n * world + r] = static_cast<char*>(members[i].ptrs[r]);
+            ++b.n;
+        }
+        if (b.n == 0) continue;
+        const int grid = grid_for((const void*)k, tiles * kThreads);
+        k<<<std::max<int64_t>(1, std::min<int64_t>(grid, tiles)), kThreads, 0, st>>>(b, dop);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <class E, int DIV>
+static cudaError_t view_g(int world, const ViewMember* m, int n, int64_t bn, float dop, cudaStream_t st) {
+    if (world <= 4) return view_impl<E, DIV, 4>(world, m, n, bn, dop, st);
+    if (world <= 8) return view_impl<E, DIV, 8>(world, m, n, bn, dop, st);
+    return view_impl<E, DIV, 16>(world, m, n, bn, dop, st);
+}
+
+template <class E>
+static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, DivSpec d, cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return view_g<E, kDivNone>(world, m, n, bn, d.operand, st);
+        case kDivPow2: return view_g<E, kDivPow2>(world, m, n, bn, d.operand, st);
+        default: return view_g<E, kDivIeee>(world, m, n, bn, d.operand, st);
+    }
+}
+
+cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
+                               DivSpec div, cudaStream_t stream) {
+    if (n == 0 || bucket_numel == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
+    return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
+}
+
+}  // namespace ddpk

@@ -1,0 +1,374 @@
+// ddp_api.cpp -- the C ABI: argument checks, launch geometry, the reducer loop.
+//
+// Every entry point validates on the host and returns a ddp_status before it
+// enqueues anything; the kernels themselves live in ring_kernels.cu and
+// bucket_kernels.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "ddp.h"
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+DivSpec make_div(int32_t divisor) {
+    DivSpec d{kDivNone, 1.0f};
+    if (divisor <= 1) return d;
+    if ((divisor & (divisor - 1)) == 0) {
+        d.mode = kDivPow2;
+        d.operand = std::ldexp(1.0f, -(int)std::log2((double)divisor));   // exact 2^-k
+    } else {
+        d.mode = kDivIeee;
+        d.operand = (float)divisor;   // exact: divisor < 2^24
+    }
+    return d;
+}
+
+bool debug_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("DDP_DEBUG");
+        return v && *v && *v != '0';
+    }();
+    return on;
+}
+
+namespace {
+std::mutex g_mu;
+std::unordered_map<int, int> g_sms;                          // device -> SM count
+std::unordered_map<unsigned long long, int> g_occ;           // (device, kernel) -> blocks per SM
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_sms[dev] = n;
+    return n;
+}
+
+// Persistent grid: SMs x resident blocks per SM, but no more blocks than the
+// work needs.
+int grid_for(const void* kernel, int64_t work_items, int threads) {
+    const int sms = sm_count();
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long key = ((unsigned long long)dev << 56) ^ (unsigned long long)(uintptr_t)kernel;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) per_sm = it->second;
+    }
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm <= 0)
+            per_sm = 1;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_occ[key] = per_sm;
+    }
+    const int64_t need = std::max<int64_t>(1, (work_items + threads - 1) / threads);
+    return (int)std::min<int64_t>((int64_t)sms * per_sm, need);
+}
+
+}  // namespace ddpk
+
+using namespace ddpk;
+
+namespace {
+
+bool valid_dtype(int32_t dtype) { return dtype == DDP_F32 || dtype == DDP_BF16; }
+
+// Rank buffers: non-null, element-aligned, pairwise disjoint.  Sets *vec_ok
+// when every buffer is 16-byte aligned.
+int32_t check_rank_buffers(int32_t world, const void* const* bufs, int64_t numel, int32_t dtype, bool* vec_ok) {
+    if (!bufs) return DDP_ERR_INVALID;
+    const uintptr_t es = (uintptr_t)elem_bytes(dtype);
+    bool v = true;
+    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+    iv.reserve(world);
+    for (int32_t r = 0; r < world; ++r) {
+        const uintptr_t p = reinterpret_cast<uintptr_t>(bufs[r]);
+        if (!p) return DDP_ERR_INVALID;
+        if (p % es) return DDP_ERR_ALIGN;
+        if (p % 16) v = false;
+        iv.emplace_back(p, p + (uintptr_t)numel * es);
+    }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
+    *vec_ok = v;
+    return DDP_OK;
+}
+
+int32_t common_checks(int32_t world, int64_t numel, int32_t dtype) {
+    if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
+    if (numel < 0 || !valid_dtype(dtype)) return DDP_ERR_INVALID;
+    if (numel > (int64_t)1 << 40) return DDP_ERR_CAPACITY;
+    return DDP_OK;
+}
+
+int32_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DDP_OK;
+    if (debug_enabled()) fprintf(stderr, "[ddp] CUDA error: %s\n", cudaGetErrorString(e));
+    return DDP_ERR_CUDA;
+}
+
+// Check one bucket's member table and build the copy items of pack/unpack.
+int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel,
+                     const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
+                     bool to_bucket, std::vector<CopyItem>* items) {
+    int32_t st = common_checks(world, 0, dtype);
+    if (st) return st;
+    if (n < 0 || bucket_numel < 0) return DDP_ERR_INVALID;
+    if (n > 0 && (!grads || !numel || !offset || !buckets)) return DDP_ERR_INVALID;
+    const int64_t es = elem_bytes(dtype);
+    // members must lie inside the bucket and not overlap each other
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    ranges.reserve(n);
+    for (int32_t i = 0; i < n; ++i) {
+        if (numel[i] < 0 || offset[i] < 0 || offset[i] > bucket_numel - numel[i]) return DDP_ERR_INVALID;
+        if (numel[i] > 0) ranges.emplace_back(offset[i], offset[i] + numel[i]);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second) return DDP_ERR_INVALID;
+    items->clear();
+    items->reserve((size_t)world * n);
+    for (int32_t r = 0; r < world; ++r) {
+        char* b = static_cast<char*>(const_cast<void*>(buckets[r]));
+        if (!b && bucket_numel > 0) return DDP_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(b) % es) return DDP_ERR_ALIGN;
+        for (int32_t i = 0; i < n; ++i) {
+            if (numel[i] == 0) continue;
+            char* g = static_cast<char*>(const_cast<void*>(grads[(int64_t)r * n + i]));
+            if (!g) return DDP_ERR_INVALID;
+            if (reinterpret_cast<uintptr_t>(g) % es) return DDP_ERR_ALIGN;
+            char* slot = b + offset[i] * es;
+            const int64_t bytes = numel[i] * es;
+            if (g < slot + bytes && slot < g + bytes) return DDP_ERR_INVALID;   // gradient overlaps its slot
+            if (to_bucket) items->push_back(CopyItem{g, slot, bytes});
+            else items->push_back(CopyItem{slot, g, bytes});
+        }
+    }
+    return DDP_OK;
+}
+
+int32_t view_members(int32_t world, int32_t n, void* const* grads, const int64_t* numel, const int64_t* offset,
+                     int64_t bucket_numel, int32_t dtype, std::vector<ViewMember>* out) {
+    int32_t st = common_checks(world, bucket_numel, dtype);
+    if (st) return st;
+    if (n < 0) return DDP_ERR_INVALID;
+    if (n > 0 && (!grads || !numel || !offset)) return DDP_ERR_INVALID;
+    const int64_t es = elem_bytes(dtype);
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    for (int32_t i = 0; i < n; ++i) {
+        if (numel[i] < 0 || offset[i] < 0 || offset[i] > bucket_numel - numel[i]) return DDP_ERR_INVALID;
+        if (numel[i] > 0) ranges.emplace_back(offset[i], offset[i] + numel[i]);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second) return DDP_ERR_INVALID;
+    // every (rank, member) gradient must be distinct memory
+    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+    out->clear();
+    for (int32_t i = 0; i < n; ++i) {
+        if (numel[i] == 0) continue;
+        bool v = true;
+        for (int32_t r = 0; r < world; ++r) {
+            const uintptr_t p = reinterpret_cast<uintptr_t>(grads[(int64_t)r * n + i]);
+            if (!p) return DDP_ERR_INVALID;
+            if (p % (uintptr_t)es) return DDP_ERR_ALIGN;
+            if (p % 16) v = false;
+            iv.emplace_back(p, p + (uintptr_t)(numel[i] * es));
+        }
+        out->push_back(ViewMember{numel[i], offset[i], nullptr, v});   // ptrs set by the caller
+    }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
+    return DDP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ddp_status_string(int32_t status) {
+    switch (status) {
+        case DDP_OK: return "DDP_OK";
+        case DDP_ERR_INVALID: return "DDP_ERR_INVALID: invalid argument";
+        case DDP_ERR_ALIGN: return "DDP_ERR_ALIGN: pointer not aligned to its element size";
+        case DDP_ERR_CUDA: return "DDP_ERR_CUDA: a CUDA call or kernel launch failed";
+        case DDP_ERR_TIMEOUT: return "DDP_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case DDP_ERR_CAPACITY: return "DDP_ERR_CAPACITY: size beyond a documented limit";
+        default: return "unknown ddp_status";
+    }
+}
+
+int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
+
+int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                             void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (divisor < 0) return DDP_ERR_INVALID;
+    if (numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
+    return cuda_status(launch_ring_fused(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
+}
+
+int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                              void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (divisor < 0) return DDP_ERR_INVALID;
+    if (numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
+    return cuda_status(launch_ring_staged(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
+}
+
+int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,
+                                       void* const* dev_bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                                       void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
+    if (numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, dev_bufs, numel, dtype, &vec))) return st;
+    for (int32_t r = 0; r < world; ++r)
+        if (!host_in[r] || !host_out[r]) return DDP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = (size_t)numel * elem_bytes(dtype);
+    for (int32_t r = 0; r < world; ++r) {
+        cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_in[r], bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if ((st = cuda_status(launch_ring_fused(world, dev_bufs, numel, dtype, make_div(divisor), vec, s)))) return st;
+    for (int32_t r = 0; r < world; ++r) {
+        cudaError_t e = cudaMemcpyAsync(host_out[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return DDP_OK;
+}
+
+int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* grads, int64_t numel,
+                            int32_t dtype, void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (numel == 0) return DDP_OK;
+    bool va = false, vg = false;
+    if ((st = check_rank_buffers(world, acc, numel, dtype, &va))) return st;
+    if ((st = check_rank_buffers(world, grads, numel, dtype, &vg))) return st;
+    return cuda_status(launch_accumulate(world, acc, grads, numel, dtype, va && vg, (cudaStream_t)stream));
+}
+
+int32_t ddp_bucket_pack(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
+                        const int64_t* offset, void* const* buckets, int64_t bucket_numel, int32_t dtype,
+                        void* stream) {
+    std::vector<CopyItem> items;
+    int32_t st = bucket_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel,
+                              dtype, true, &items);
+    if (st) return st;
+    return cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream));
+}
+
+int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                          const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
+                          void* stream) {
+    std::vector<CopyItem> items;
+    int32_t st = bucket_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel,
+                              dtype, false, &items);
+    if (st) return st;
+    return cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream));
+}
+
+int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                                  const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
+                                  void* stream) {
+    if (divisor < 0) return DDP_ERR_INVALID;
+    std::vector<ViewMember> members;
+    int32_t st = view_members(world, n_in_bucket, grads, numel, offset, bucket_numel, dtype, &members);
+    if (st) return st;
+    // per-member rank pointer tables (rank order)
+    std::vector<std::vector<void*>> tables;
+    tables.reserve(members.size());
+    size_t k = 0;
+    for (int32_t i = 0; i < n_in_bucket; ++i) {
+        if (numel[i] == 0) continue;
+        tables.emplace_back(world);
+        for (int32_t r = 0; r < world; ++r) tables.back()[r] = grads[(int64_t)r * n_in_bucket + i];
+        members[k++].ptrs = tables.back().data();
+    }
+    return cuda_status(launch_bucket_view(world, members.data(), (int)members.size(), bucket_numel, dtype,
+                                          make_div(divisor), (cudaStream_t)stream));
+}
+
+int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
+                         const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
+                         const int64_t* bucket_numel, void* const* buckets, int32_t dtype, int32_t divisor,
+                         int32_t algo, void* stream) {
+    int32_t st = common_checks(world, 0, dtype);
+    if (st) return st;
+    if (n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
+    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW) return DDP_ERR_INVALID;
+    if (n_params > 0 && (!grads || !numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
+    if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
+    if (algo != DDP_ALGO_VIEW && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
+    // members of each bucket, in bucket order
+    std::vector<std::vector<int32_t>> members(n_buckets);
+    for (int32_t p = 0; p < n_params; ++p) {
+        const int32_t k = bucket_of_param[p];
+        if (k < 0 || k >= n_buckets) return DDP_ERR_INVALID;
+        members[k].push_back(p);
+    }
+    std::vector<const void*> g;
+    std::vector<int64_t> ne, off;
+    std::vector<void*> bk(world);
+    for (int32_t k = 0; k < n_buckets; ++k) {
+        auto& m = members[k];
+        std::sort(m.begin(), m.end(), [&](int32_t a, int32_t b) { return offset_of_param[a] < offset_of_param[b]; });
+        const int32_t n = (int32_t)m.size();
+        g.assign((size_t)world * n, nullptr);
+        ne.resize(n);
+        off.resize(n);
+        for (int32_t i = 0; i < n; ++i) {
+            ne[i] = numel[m[i]];
+            off[i] = offset_of_param[m[i]];
+            for (int32_t r = 0; r < world; ++r) g[(size_t)r * n + i] = grads[(size_t)r * n_params + m[i]];
+        }
+        if (algo == DDP_ALGO_VIEW) {
+            st = ddp_bucket_allreduce_view(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
+                                           bucket_numel[k], dtype, divisor, stream);
+            if (st) return st;
+            continue;
+        }
+        for (int32_t r = 0; r < world; ++r) bk[r] = buckets[(size_t)r * n_buckets + k];
+        st = ddp_bucket_pack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], dtype, stream);
+        if (st) return st;
+        st = (algo == DDP_ALGO_FUSED)
+                 ? ring_allreduce_fused(world, bk.data(), bucket_numel[k], dtype, divisor, stream)
+                 : ring_allreduce_staged(world, bk.data(), bucket_numel[k], dtype, divisor, stream);
+        if (st) return st;
+        st = ddp_bucket_unpack(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
+                               (const void* const*)bk.data(), bucket_numel[k], dtype, stream);
+        if (st) return st;
+        if (debug_enabled())
+            fprintf(stderr, "[ddp] bucket %d: %d members, %lld elements\n", k, n, (long long)bucket_numel[k]);
+    }
+    return DDP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// ddp_device.cuh -- device-side element operations shared by the kernels.
+//
+// The reduction operator of the ring ("DDP 与 Ring-AllReduce", §1.3.2: the
+// receiver adds the incoming chunk into its own copy):
+//   fp32: one binary32 add, round to nearest even (__fadd_rn, never contracted);
+//   bf16: both operands widened exactly to binary32, one binary32 add, the sum
+//         rounded to bf16 to nearest even -- once per hop.
+// The average ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事",
+// section 05; "Day 17 · 梯度的集体行动" Reducer pseudo-code): y / divisor with
+// one IEEE division (or the exact power-of-two reciprocal, which rounds the
+// same way), bf16 results rounded once.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+template <int DIV>
+__device__ __forceinline__ float div_f32(float a, float operand) {
+    if constexpr (DIV == kDivNone) return a;
+    else if constexpr (DIV == kDivPow2) return __fmul_rn(a, operand);
+    else return __fdiv_rn(a, operand);
+}
+
+// bf16 <-> binary32.  Widening is exact: the bf16 bits are the top half of
+// the binary32 bits.  Narrowing rounds to nearest even (cvt.rn.bf16x2.f32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    __nv_bfloat162 r = __float22bfloat162_rn(make_float2(lo, hi));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    __nv_bfloat16 r = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&r);
+}
+
+// ---- fp32 ---------------------------------------------------------------
+struct EF32 {
+    using S = float;     // one element
+    using V = float4;    // one 16-byte vector
+    static constexpr int L = 4;
+    __device__ static __forceinline__ S sadd(S a, S b) { return __fadd_rn(a, b); }
+    __device__ static __forceinline__ V vadd(V a, V b) {
+        return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ S sdiv(S a, float op) { return div_f32<DIV>(a, op); }
+    template <int DIV>
+    __device__ static __forceinline__ V vdiv(V a, float op) {
+        if constexpr (DIV == kDivNone) return a;
+        return make_float4(div_f32<DIV>(a.x, op), div_f32<DIV>(a.y, op), div_f32<DIV>(a.z, op),
+                           div_f32<DIV>(a.w, op));
+    }
+};
+
+// ---- bf16 (stored as raw 16-bit patterns) -------------------------------
+struct EBF16 {
+    using S = uint16_t;
+    using V = uint4;     // 8 bf16
+    static constexpr int L = 8;
+    __device__ static __forceinline__ S sadd(S a, S b) {
+        return f32_to_bf16_rn(__fadd_rn(bf16_to_f32(a), bf16_to_f32(b)));
+    }
+    __device__ static __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        return bf16x2_rn(__fadd_rn(bf16_lo(a), bf16_lo(b)), __fadd_rn(bf16_hi(a), bf16_hi(b)));
+    }
+    __device__ static __forceinline__ V vadd(V a, V b) {
+        return make_uint4(add2(a.x, b.x), add2(a.y, b.y), add2(a.z, b.z), add2(a.w, b.w));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ S sdiv(S a, float op) {
+        if constexpr (DIV == kDivNone) return a;
+        return f32_to_bf16_rn(div_f32<DIV>(bf16_to_f32(a), op));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ uint32_t div2(uint32_t a, float op) {
+        return bf16x2_rn(div_f32<DIV>(bf16_lo(a), op), div_f32<DIV>(bf16_hi(a), op));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ V vdiv(V a, float op) {
+        if constexpr (DIV == kDivNone) return a;
+        return make_uint4(div2<DIV>(a.x, op), div2<DIV>(a.y, op), div2<DIV>(a.z, op), div2<DIV>(a.w, op));
+    }
+};
+
+// Streaming 16-byte accesses: the buffers are touched once per call, so
+// loads and stores are marked evict-first.
+template <class V>
+__device__ __forceinline__ V ld_stream(const void* p) { return __ldcs(reinterpret_cast<const V*>(p)); }
+template <class V>
+__device__ __forceinline__ void st_stream(void* p, V v) { __stcs(reinterpret_cast<V*>(p), v); }
+
+template <class V> __device__ __forceinline__ V make_zero();
+template <> __device__ __forceinline__ float4 make_zero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+template <> __device__ __forceinline__ uint4 make_zero<uint4>() { return make_uint4(0u, 0u, 0u, 0u); }
+
+// Fold the N ranks' vectors at byte offset `off` in ring order, starting at
+// rank `start` (the rank right after the chunk's owner) and wrapping around:
+// acc = x[start]; acc = acc (+) x[start+1]; ... ; acc = acc (+) x[start-1].
+// Loads are issued in groups of G before they are folded, so G 16-byte
+// requests per thread are in flight at once.
+template <class E, int G, class PtrAt>
+__device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, int start, int64_t off) {
+    using V = typename E::V;
+    V acc = make_zero<V>();
+    int r = start;
+    for (int k0 = 0; k0 < world; k0 += G) {
+        V x[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (k0 + g < world) {
+                x[g] = ld_stream<V>(ptr_at(r) + off);
+                r = (r + 1 == world) ? 0 : r + 1;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (k0 + g < world) acc = (k0 + g == 0) ? x[g] : E::vadd(acc, x[g]);
+        }
+    }
+    return acc;
+}
+
+// Scalar version of the same fold for one element at element index `e`.
+template <class E, class PtrAt>
+__device__ __forceinline__ typename E::S fold_ring_scalar(PtrAt ptr_at, int world, int start, int64_t e) {
+    using S = typename E::S;
+    int r = start;
+    S acc = reinterpret_cast<const S*>(ptr_at(r))[e];
+    for (int k = 1; k < world; ++k) {
+        r = (r + 1 == world) ? 0 : r + 1;
+        acc = E::sadd(acc, reinterpret_cast<const S*>(ptr_at(r))[e]);
+    }
+    return acc;
+}
+
+}  // namespace ddpk

@@ -1,0 +1,63 @@
+// ddp_internal.h -- declarations shared by the library's translation units.
+// Not part of the C ABI (see include/ddp.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ddp.h"
+
+namespace ddpk {
+
+constexpr int kThreads = 256;            // threads per block of every kernel
+
+// Divide modes of the average y / divisor:
+//   kDivNone  divisor 0 or 1, keep the sum
+//   kDivPow2  divisor = 2^k: multiply by the exact reciprocal 2^-k, which is
+//             the same correctly rounded value as an IEEE division
+//   kDivIeee  any other divisor: one IEEE division (round to nearest even)
+enum DivMode { kDivNone = 0, kDivPow2 = 1, kDivIeee = 2 };
+
+struct DivSpec {
+    int mode;
+    float operand;   // 2^-k for kDivPow2, (float)divisor for kDivIeee
+};
+DivSpec make_div(int32_t divisor);
+
+inline int64_t chunk_len(int64_t numel, int world) { return (numel + world - 1) / world; }
+inline int elem_bytes(int dtype) { return dtype == DDP_F32 ? 4 : 2; }
+
+// Launch geometry helpers (cached per device).
+int sm_count();
+int grid_for(const void* kernel, int64_t work_items, int threads = kThreads);
+bool debug_enabled();
+
+// ---- ring kernels (ring_kernels.cu) -----------------------------------
+// All pointers are device pointers; `ptrs` is a host array of `world` entries.
+cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                              bool vec_ok, cudaStream_t stream);
+cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                               bool vec_ok, cudaStream_t stream);
+cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,
+                              bool vec_ok, cudaStream_t stream);
+
+// ---- bucket kernels (bucket_kernels.cu) --------------------------------
+struct CopyItem {
+    const void* src;
+    void* dst;
+    int64_t bytes;
+};
+cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t stream);
+
+// One bucket member for the fused view kernel: its numel, its element offset
+// in the bucket and its `world` gradient pointers (rank order).
+struct ViewMember {
+    int64_t numel;
+    int64_t offset;
+    void* const* ptrs;   // host array of world device pointers
+    bool vec_ok;         // every pointer 16-byte aligned
+};
+cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
+                               DivSpec div, cudaStream_t stream);
+
+}  // namespace ddpk

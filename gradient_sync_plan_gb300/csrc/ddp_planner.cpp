@@ -1,0 +1,47 @@
+// ddp_planner.cpp -- bucket assignment (host only).
+//
+// Rule ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03
+// "Bucket" and "Overlap", section 05 step 2; "Day 17 · 梯度的集体行动"
+// "bucket 与 overlap"): gradients become ready roughly in reverse
+// registration order during backward, so buckets are filled walking the
+// parameters from the last registered to the first.  The first bucket has
+// its own, small cap (1 MiB by default) so that its allreduce can start
+// early; the others use the bucket cap (25 MiB by default).  A bucket is
+// closed as soon as its size reaches the cap; the trailing bucket is closed
+// at the end.
+#include <cstdint>
+
+#include "ddp.h"
+
+extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int32_t dtype,
+                                    int64_t first_bucket_bytes, int64_t bucket_cap_bytes,
+                                    int32_t* bucket_of_param, int64_t* offset_of_param, int64_t* bucket_numel,
+                                    int32_t* n_buckets) {
+    if (!n_buckets || n_params < 0) return DDP_ERR_INVALID;
+    if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
+    if (first_bucket_bytes <= 0 || bucket_cap_bytes <= 0) return DDP_ERR_INVALID;
+    if (n_params > 0 && (!numel || !bucket_of_param || !offset_of_param || !bucket_numel)) return DDP_ERR_INVALID;
+    const int64_t esize = (dtype == DDP_F32) ? 4 : 2;
+    for (int32_t p = 0; p < n_params; ++p)
+        if (numel[p] < 0 || numel[p] > (INT64_MAX / 4) / esize) return DDP_ERR_INVALID;
+
+    int32_t bucket = 0;
+    int64_t fill = 0;            // elements in the open bucket
+    bool open = false;           // the open bucket holds at least one parameter
+    int64_t cap = first_bucket_bytes;
+    for (int32_t p = n_params - 1; p >= 0; --p) {
+        bucket_of_param[p] = bucket;
+        offset_of_param[p] = fill;
+        fill += numel[p];
+        open = true;
+        if (fill * esize >= cap) {           // reached the cap: close it
+            bucket_numel[bucket++] = fill;
+            fill = 0;
+            open = false;
+            cap = bucket_cap_bytes;
+        }
+    }
+    if (open) bucket_numel[bucket++] = fill;
+    *n_buckets = bucket;
+    return DDP_OK;
+}

@@ -1,0 +1,317 @@
+// ring_kernels.cu -- ring allreduce over N logical ranks held in one GPU.
+//
+// The ring of "DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事"
+// (section 03, "两阶段：先规约，再扩散") and "DDP 与 Ring-AllReduce" (§1.3.1,
+// §1.3.2): a bucket of S elements is cut into N chunks of c = ceil(S/N);
+// rank r sends to r+1; reduce-scatter step s sends chunk (r-s) mod N and the
+// receiver adds it in, all-gather step t sends chunk (r-t+1) mod N and the
+// receiver overwrites.  Chunk j is thus summed from rank j+1 round to rank j.
+//
+// Two kernels reach that result:
+//   * k_ring_fused: one pass; every element is read once from each rank,
+//     folded in exactly that order, divided, and stored to every rank.
+//     Traffic 2*N*S elements, the minimum.
+//   * k_ring_hop: one launch per ring step, moving for every rank the chunk
+//     the ring moves in that step.  Traffic 5(N-1)*S elements.
+#include <algorithm>
+#include <cstdio>
+
+#include "ddp_device.cuh"
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+// Rank pointer table passed by value in the kernel's parameter space.
+template <int CAP>
+struct RankTable {
+    char* p[CAP];
+};
+
+// ---------------------------------------------------------------------------
+// Fused ring allreduce
+// ---------------------------------------------------------------------------
+
+// One element, any alignment: fold in ring order, divide, store to all ranks.
+template <class E, int DIV, int CAP>
+__device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world, int64_t e, int64_t clen,
+                                             float dop) {
+    using S = typename E::S;
+    const int j = (int)(e / clen);
+    const int start = (j + 1 == world) ? 0 : j + 1;
+    auto at = [&](int r) -> const char* { return t.p[r]; };
+    S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e), dop);
+    for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = y;
+}
+
+// Vectorised fused kernel: all rank buffers are 16-byte aligned.  Thread v
+// handles the 16-byte vector v of every rank.  A vector whose lanes fall in
+// two chunks (only possible when c is not a multiple of the lane count) or
+// runs past the end is done lane by lane.
+template <class E, int DIV, int CAP, int G>
+__global__ void __launch_bounds__(kThreads)
+k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+    using V = typename E::V;
+    constexpr int L = E::L;
+    const int64_t nvec = (numel + L - 1) / L;
+    const int64_t full = numel / L;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    auto at = [&](int r) -> const char* { return t.p[r]; };
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        const int64_t i = v * L;
+        const int64_t j = i / clen;
+        if (v < full && (i + L - 1) / clen == j) {
+            const int start = (j + 1 == world) ? 0 : (int)j + 1;
+            const int64_t off = v * 16;
+            V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, off), dop);
+            for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
+        } else {
+            for (int l = 0; l < L; ++l)
+                if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
+        }
+    }
+}
+
+// Element-wise fused kernel for buffers that are not 16-byte aligned.
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_ring_fused_scalar(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < numel; e += stride)
+        ring_element<E, DIV, CAP>(t, world, e, clen, dop);
+}
+
+// ---------------------------------------------------------------------------
+// Staged ring: one launch per step
+// ---------------------------------------------------------------------------
+
+// Ring step `s` of phase `phase` (0 = reduce-scatter, 1 = all-gather) for all
+// ranks at once; blockIdx.y is the receiving rank r, its left neighbour r-1
+// is the sender.
+//   reduce-scatter: chunk (r-s-1) mod N of rank r += the same chunk of rank r-1
+//   all-gather:     chunk (r-s)   mod N of rank r  = the same chunk of rank r-1
+// In one step rank r writes chunk q while its right neighbour reads chunk q+1
+// of rank r, so no element is both read and written by different ranks within
+// a step; consecutive steps are ordered by the stream.  DIV is applied only
+// in the last reduce-scatter step, by the chunk's owner, before the chunk is
+// circulated by the all-gather.
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_ring_hop(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, int phase, int s,
+           int vec_ok, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    const int r = blockIdx.y;
+    const int left = (r == 0) ? world - 1 : r - 1;
+    int c = (phase == 0) ? (r - s - 1) : (r - s);
+    c %= world;
+    if (c < 0) c += world;
+    const int64_t lo = std::min((int64_t)c * clen, numel);
+    const int64_t hi = std::min(lo + clen, numel);
+    if (lo >= hi) return;
+    char* dst = t.p[r];
+    const char* src = t.p[left];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (vec_ok) {
+        for (int64_t q = lo / L + tid; q * L < hi; q += stride) {
+            const int64_t i = q * L;
+            if (i >= lo && i + L <= hi) {
+                V m = ld_stream<V>(src + q * 16);
+                if (phase == 0) {
+                    V d = ld_stream<V>(dst + q * 16);
+                    m = E::template vdiv<DIV>(E::vadd(d, m), dop);
+                }
+                st_stream<V>(dst + q * 16, m);
+            } else {
+                for (int l = 0; l < L; ++l) {
+                    const int64_t e = i + l;
+                    if (e < lo || e >= hi) continue;
+                    S m = reinterpret_cast<const S*>(src)[e];
+                    if (phase == 0) m = E::template sdiv<DIV>(E::sadd(reinterpret_cast<S*>(dst)[e], m), dop);
+                    reinterpret_cast<S*>(dst)[e] = m;
+                }
+            }
+        }
+    } else {
+        for (int64_t e = lo + tid; e < hi; e += stride) {
+            S m = reinterpret_cast<const S*>(src)[e];
+            if (phase == 0) m = E::template sdiv<DIV>(E::sadd(reinterpret_cast<S*>(dst)[e], m), dop);
+            reinterpret_cast<S*>(dst)[e] = m;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Local accumulation (no_sync micro-batches)
+// ---------------------------------------------------------------------------
+
+template <class E, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_accumulate(const __grid_constant__ RankTable<CAP> acc, const __grid_constant__ RankTable<CAP> g, int64_t numel,
+             int vec_ok) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    const int r = blockIdx.y;
+    char* a = acc.p[r];
+    const char* b = g.p[r];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t done = 0;
+    if (vec_ok) {
+        const int64_t nv = numel / L;
+        for (int64_t q = tid; q < nv; q += stride)
+            st_stream<V>(a + q * 16, E::vadd(ld_stream<V>(a + q * 16), ld_stream<V>(b + q * 16)));
+        done = nv * L;
+    }
+    for (int64_t e = done + tid; e < numel; e += stride)
+        reinterpret_cast<S*>(a)[e] = E::sadd(reinterpret_cast<S*>(a)[e], reinterpret_cast<const S*>(b)[e]);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+
+template <int CAP>
+static RankTable<CAP> make_table(int world, void* const* ptrs) {
+    RankTable<CAP> t{};
+    for (int r = 0; r < world; ++r) t.p[r] = static_cast<char*>(ptrs[r]);
+    return t;
+}
+
+template <class E, int DIV, int CAP, int G>
+static cudaError_t fused_vec(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
+    auto k = k_ring_fused<E, DIV, CAP, G>;
+    const int64_t nvec = (numel + E::L - 1) / E::L;
+    const int grid = grid_for((const void*)k, nvec);
+    k<<<grid, kThreads, 0, st>>>(make_table<CAP>(world, ptrs), world, numel, chunk_len(numel, world), dop);
+    if (debug_enabled())
+        fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d G=%d CAP=%d\n", world, (long long)numel,
+                grid, G, CAP);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV, int CAP>
+static cudaError_t fused_scalar(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
+    auto k = k_ring_fused_scalar<E, DIV, CAP>;
+    const int grid = grid_for((const void*)k, numel);
+    k<<<grid, kThreads, 0, st>>>(make_table<CAP>(world, ptrs), world, numel, chunk_len(numel, world), dop);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV>
+static cudaError_t fused_dispatch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
+                                  cudaStream_t st) {
+    if (!vec_ok) {
+        if (world <= 16) return fused_scalar<E, DIV, 16>(world, ptrs, numel, dop, st);
+        return fused_scalar<E, DIV, DDP_MAX_WORLD>(world, ptrs, numel, dop, st);
+    }
+    if (world <= 4) return fused_vec<E, DIV, 16, 4>(world, ptrs, numel, dop, st);
+    if (world <= 8) return fused_vec<E, DIV, 16, 8>(world, ptrs, numel, dop, st);
+    if (world <= 16) return fused_vec<E, DIV, 16, 16>(world, ptrs, numel, dop, st);
+    return fused_vec<E, DIV, DDP_MAX_WORLD, 16>(world, ptrs, numel, dop, st);
+}
+
+template <class E>
+static cudaError_t fused_by_div(int world, void* const* ptrs, int64_t numel, DivSpec d, bool vec_ok,
+                                cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return fused_dispatch<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, st);
+        case kDivPow2: return fused_dispatch<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, st);
+        default: return fused_dispatch<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, st);
+    }
+}
+
+cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
+                              cudaStream_t stream) {
+    if (numel == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return fused_by_div<EF32>(world, ptrs, numel, div, vec_ok, stream);
+    return fused_by_div<EBF16>(world, ptrs, numel, div, vec_ok, stream);
+}
+
+template <class E, int DIV, int CAP>
+static cudaError_t hop(const RankTable<CAP>& t, int world, int64_t numel, int phase, int s, bool vec_ok, float dop,
+                       cudaStream_t st) {
+    auto k = k_ring_hop<E, DIV, CAP>;
+    const int64_t clen = chunk_len(numel, world);
+    const int64_t per_rank = vec_ok ? (clen + E::L - 1) / E::L + 1 : clen;
+    // blocks in x per rank: enough to fill the GPU once all ranks are counted
+    int gx = grid_for((const void*)k, per_rank * world);
+    gx = std::max(1, (gx + world - 1) / world);
+    dim3 grid(gx, world);
+    k<<<grid, kThreads, 0, st>>>(t, world, numel, clen, phase, s, vec_ok ? 1 : 0, dop);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV, int CAP>
+static cudaError_t staged_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok, cudaStream_t st) {
+    const RankTable<CAP> t = make_table<CAP>(world, ptrs);
+    for (int s = 1; s <= world - 1; ++s) {
+        cudaError_t e = (s == world - 1) ? hop<E, DIV, CAP>(t, world, numel, 0, s, vec_ok, dop, st)
+                                         : hop<E, kDivNone, CAP>(t, world, numel, 0, s, vec_ok, dop, st);
+        if (e != cudaSuccess) return e;
+    }
+    for (int s = 1; s <= world - 1; ++s) {
+        cudaError_t e = hop<E, kDivNone, CAP>(t, world, numel, 1, s, vec_ok, dop, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (debug_enabled())
+        fprintf(stderr, "[ddp] ring_staged world=%d numel=%lld launches=%d\n", world, (long long)numel,
+                2 * (world - 1));
+    return cudaSuccess;
+}
+
+template <class E, int DIV>
+static cudaError_t staged_cap(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok, cudaStream_t st) {
+    if (world <= 16) return staged_impl<E, DIV, 16>(world, ptrs, numel, dop, vec_ok, st);
+    return staged_impl<E, DIV, DDP_MAX_WORLD>(world, ptrs, numel, dop, vec_ok, st);
+}
+
+template <class E>
+static cudaError_t staged_by_div(int world, void* const* ptrs, int64_t numel, DivSpec d, bool vec_ok,
+                                 cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return staged_cap<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, st);
+        case kDivPow2: return staged_cap<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, st);
+        default: return staged_cap<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, st);
+    }
+}
+
+cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
+                               cudaStream_t stream) {
+    if (numel == 0) return cudaSuccess;
+    // One rank: there is no ring step, only the average.
+    if (world == 1) return launch_ring_fused(world, ptrs, numel, dtype, div, vec_ok, stream);
+    if (dtype == DDP_F32) return staged_by_div<EF32>(world, ptrs, numel, div, vec_ok, stream);
+    return staged_by_div<EBF16>(world, ptrs, numel, div, vec_ok, stream);
+}
+
+template <class E, int CAP>
+static cudaError_t accumulate_impl(int world, void* const* acc, const void* const* g, int64_t numel, bool vec_ok,
+                                   cudaStream_t st) {
+    auto k = k_accumulate<E, CAP>;
+    RankTable<CAP> ta{}, tg{};
+    for (int r = 0; r < world; ++r) {
+        ta.p[r] = static_cast<char*>(acc[r]);
+        tg.p[r] = static_cast<char*>(const_cast<void*>(g[r]));
+    }
+    const int64_t per_rank = vec_ok ? numel / E::L + E::L : numel;
+    int gx = grid_for((const void*)k, per_rank * world);
+    gx = std::max(1, (gx + world - 1) / world);
+    k<<<dim3(gx, world), kThreads, 0, st>>>(ta, tg, numel, vec_ok ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,
+                              bool vec_ok, cudaStream_t stream) {
+    if (numel == 0) return cudaSuccess;
+    if (dtype == DDP_F32) {
+        if (world <= 16) return accumulate_impl<EF32, 16>(world, acc, g, numel, vec_ok, stream);
+        return accumulate_impl<EF32, DDP_MAX_WORLD>(world, acc, g, numel, vec_ok, stream);
+    }
+    if (world <= 16) return accumulate_impl<EBF16, 16>(world, acc, g, numel, vec_ok, stream);
+    return accumulate_impl<EBF16, DDP_MAX_WORLD>(world, acc, g, numel, vec_ok, stream);
+}
+
+}  // namespace ddpk

@@ -1,0 +1,255 @@
+/*
+ * ddp.h -- C ABI of the GB300 DDP gradient-synchronisation library.
+ *
+ * DDP keeps one full model replica per data-parallel rank and, after every
+ * backward pass, replaces each rank's gradients by their average over the
+ * ranks.  Gradients are grouped into flat buckets, each bucket is summed by a
+ * ring allreduce, divided by the world size and copied back to the
+ * parameters' gradients.  Sources (web pages on DDP gradient sync):
+ *   [P1] "DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事"
+ *        (blog.vllbc.top): section 01 (gradient averaging), section 03
+ *        (reduce-scatter / all-gather, buckets, reverse order, caps,
+ *        gradient_as_bucket_view, no_sync), section 04 (ring traffic),
+ *        section 05 (step timeline, divide by world size).
+ *   [P2] "Day 17 · 梯度的集体行动" (blog.ans20xx.com): "bucket 与 overlap",
+ *        "梯度累积:正确使用 no_sync", and the Reducer pseudo-code
+ *        (allreduce -> wait -> div_(world_size) -> copy back).
+ *   [P3] "DDP 与 Ring-AllReduce" (xuesongtap.github.io): §1.3.1 (2(N-1)
+ *        steps), §1.3.2 (3-GPU, length-6 worked example), §1.3.3 (traffic).
+ *
+ * Model of the ranks.  The N data-parallel ranks are N logical replicas whose
+ * buffers all live in one GPU's memory; "rank r" is simply the r-th pointer
+ * of a table.  Nothing here crosses a process or a device boundary.
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every host and device buffer.  The library
+ *     allocates no device memory, keeps no pointer after a call returns and
+ *     holds no state between calls except cached device attributes.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Device work is enqueued asynchronously on it; the
+ *     host returns without waiting for the GPU.  Calls may be captured into a
+ *     CUDA graph.
+ *   - Errors: the return value is a ddp_status.  A negative status from
+ *     argument checking means that nothing was enqueued.  DDP_ERR_CUDA means
+ *     a CUDA call or launch failed; some of the call's work may have been
+ *     enqueued before the failure.
+ *   - Dtypes: DDP_F32 (IEEE binary32) or DDP_BF16 (bfloat16).  Element
+ *     pointers must be aligned to the element size (DDP_ERR_ALIGN otherwise);
+ *     16-byte aligned buffers take the vectorised paths, others a slower
+ *     element-wise path with the same results.
+ *   - Rank tables: arrays of `world` device pointers, read on the host during
+ *     the call only.
+ */
+#ifndef DDP_GB300_DDP_H
+#define DDP_GB300_DDP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDP_ABI_VERSION 1
+#define DDP_MAX_WORLD 512          /* largest supported number of logical ranks */
+
+typedef enum {
+    DDP_OK = 0,
+    DDP_ERR_INVALID = -1,    /* bad argument: null pointer, world < 1, numel < 0,
+                                unknown dtype, overlapping buffers, bad plan     */
+    DDP_ERR_ALIGN = -2,      /* a pointer is not aligned to its element size    */
+    DDP_ERR_CUDA = -3,       /* a CUDA runtime call or a kernel launch failed    */
+    DDP_ERR_TIMEOUT = -4,    /* a bounded device-side wait gave up (status word) */
+    DDP_ERR_CAPACITY = -5    /* a size exceeds a documented limit               */
+} ddp_status;
+
+typedef enum { DDP_F32 = 0, DDP_BF16 = 1 } ddp_dtype;
+
+/* Human-readable name of a ddp_status (static string, never NULL). */
+const char* ddp_status_string(int32_t status);
+
+/* DDP_ABI_VERSION of the loaded library. */
+int32_t ddp_abi_version(void);
+
+/*
+ * ddp_plan_buckets -- assign parameters to buckets ([P1] section 03 "Bucket"
+ * and "Overlap", section 05 step 2; [P2] "bucket 与 overlap").
+ *
+ * Parameters are visited in REVERSE registration order (p = n_params-1 .. 0),
+ * the order in which backward produces their gradients.  Each one is appended
+ * to the open bucket at the bucket's current element count (no padding, so
+ * in-bucket order is reverse registration order).  After an append, a bucket
+ * whose byte size is >= its cap is closed: bucket 0 uses first_bucket_bytes
+ * (DDP's default 1 MiB), every later bucket bucket_cap_bytes (default 25 MiB;
+ * the pages' "MB" is MiB).  A bucket may therefore exceed its cap by its last
+ * parameter, and a parameter larger than the cap closes its bucket at once.
+ * A bucket still open at the end is closed if it holds any parameter.
+ *
+ *   n_params                 number of parameters (>= 0)
+ *   numel[n_params]          elements of each parameter, registration order (>= 0)
+ *   dtype                    element type of every gradient (one dtype per plan)
+ *   first_bucket_bytes       cap of bucket 0, bytes (> 0)
+ *   bucket_cap_bytes         cap of the other buckets, bytes (> 0)
+ *   bucket_of_param[n_params] out: bucket index of each parameter
+ *   offset_of_param[n_params] out: element offset of each parameter in its bucket
+ *   bucket_numel[n_params]   out: elements of each bucket (room for n_params)
+ *   n_buckets                out: number of buckets
+ * Host only; no CUDA call.  DDP_ERR_INVALID on a bad argument.
+ */
+int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int32_t dtype,
+                         int64_t first_bucket_bytes, int64_t bucket_cap_bytes,
+                         int32_t* bucket_of_param, int64_t* offset_of_param,
+                         int64_t* bucket_numel, int32_t* n_buckets);
+
+/*
+ * ddp_bucket_pack -- copy gradients into each rank's flat bucket, the
+ * "gradient -> bucket" copy DDP makes when gradient_as_bucket_view is off
+ * ([P1] section 03 and section 05 step 2).
+ *
+ * For every rank r and member i:
+ *   buckets[r][offset[i] .. offset[i]+numel[i]) <- grads[r*n_in_bucket + i][0 .. numel[i])
+ *
+ *   world                 logical ranks, 1 .. DDP_MAX_WORLD
+ *   n_in_bucket           members of this bucket (>= 0)
+ *   grads[world*n_in_bucket] host table of device pointers, rank-major
+ *   numel[n_in_bucket]    elements of each member
+ *   offset[n_in_bucket]   element offset of each member inside the bucket
+ *   buckets[world]        host table of device pointers to the rank buckets
+ *   bucket_numel          elements of each rank's bucket; every member must
+ *                         satisfy offset + numel <= bucket_numel
+ * Member ranges must not overlap each other (a plan from ddp_plan_buckets
+ * never does); source and destination must not overlap.
+ */
+int32_t ddp_bucket_pack(int32_t world, int32_t n_in_bucket, const void* const* grads,
+                        const int64_t* numel, const int64_t* offset, void* const* buckets,
+                        int64_t bucket_numel, int32_t dtype, void* stream);
+
+/*
+ * ddp_bucket_unpack -- the inverse copy, bucket -> .grad, after the bucket's
+ * allreduce and average ([P1] section 05 step 3; [P2] Reducer pseudo-code,
+ * "copy back to param grads").
+ *
+ *   grads[r*n_in_bucket + i][0 .. numel[i]) <- buckets[r][offset[i] .. offset[i]+numel[i])
+ * Arguments as for ddp_bucket_pack.
+ */
+int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads,
+                          const int64_t* numel, const int64_t* offset, const void* const* buckets,
+                          int64_t bucket_numel, int32_t dtype, void* stream);
+
+/*
+ * ring_allreduce_fused -- the ring allreduce of one bucket, in one pass over
+ * memory, with the ring's exact result ([P1] section 03 "两阶段"; [P3]
+ * §1.3.1-§1.3.2).
+ *
+ * The bucket of S = numel elements is cut into N = world chunks of
+ * c = ceil(S/N) elements (chunk j = [min(jc,S), min((j+1)c,S)); trailing
+ * chunks may be short or empty).  On the ring, rank r sends to rank r+1;
+ * reduce-scatter step s (1..N-1) sends chunk (r-s) mod N and the receiver adds
+ * it into its copy, all-gather step t (1..N-1) sends chunk (r-t+1) mod N and
+ * the receiver overwrites.  Chunk j is therefore summed starting at rank
+ * (j+1) mod N and finishing at rank j:
+ *     y[i] = (((x_{j+1}[i] + x_{j+2}[i]) + ...) + x_{j+N}[i])   (ranks mod N)
+ * and then, if divisor > 1, y[i] / divisor (one IEEE division).  This kernel
+ * reads each rank's element once, folds in exactly that order and writes y to
+ * all N buffers, so its result is bit-identical to the hop-by-hop ring.
+ * fp32: binary32 adds, round to nearest even.  bf16: each add is done in
+ * binary32 and rounded to bf16 (nearest even), once per hop; the divide
+ * rounds once to bf16.
+ *
+ *   world      logical ranks N, 1 .. DDP_MAX_WORLD
+ *   bufs[world] host table of device pointers; rank r's bucket, S elements,
+ *              read and overwritten in place; buffers must not overlap
+ *   numel      S (>= 0; 0 is a no-op)
+ *   divisor    0 or 1: leave the sum; > 1: divide (DDP passes the world size)
+ */
+int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype,
+                             int32_t divisor, void* stream);
+
+/*
+ * ring_allreduce_staged -- the same allreduce reproduced hop by hop: N-1
+ * reduce-scatter kernels then N-1 all-gather kernels on `stream`, each one
+ * moving, for every rank at once, exactly the chunk the ring moves in that
+ * step ([P1] section 03; [P3] §1.3.2).  The average is folded into the last
+ * reduce-scatter step (the owner of each chunk divides it before it is
+ * circulated).  Same arguments and bit-identical results as
+ * ring_allreduce_fused; 5(N-1)/N * S elements of traffic per rank instead of 2.
+ */
+int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype,
+                              int32_t divisor, void* stream);
+
+/*
+ * ring_allreduce_fused_from_host -- ring_allreduce_fused for callers whose
+ * gradients are in host memory: per rank, host_in[r] is copied to dev_bufs[r],
+ * the fused allreduce runs, and the result is copied to host_out[r]
+ * (host_out[r] may equal host_in[r]).  All copies and the kernel are
+ * enqueued on `stream`; the caller synchronises the stream before reading
+ * host_out.  Host buffers should be pinned for the copies to be asynchronous.
+ * dev_bufs[world] is caller-provided device scratch of numel elements per rank.
+ */
+int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,
+                                       void* const* dev_bufs, int64_t numel, int32_t dtype,
+                                       int32_t divisor, void* stream);
+
+/*
+ * ddp_grad_accumulate -- one no_sync micro-batch folded into the local
+ * gradients of every rank ([P1] section 03 and section 05 step 5; [P2]
+ * "梯度累积:正确使用 no_sync"): acc[r][i] <- acc[r][i] + grads[r][i]
+ * (binary32 add; bf16: binary32 add rounded to bf16).  No communication.
+ *   acc[world], grads[world]  host tables of device pointers, numel elements each
+ */
+int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* grads, int64_t numel,
+                            int32_t dtype, void* stream);
+
+/* Allreduce algorithm used by ddp_sync_buckets for each bucket. */
+typedef enum {
+    DDP_ALGO_FUSED = 0,   /* pack -> ring_allreduce_fused -> unpack             */
+    DDP_ALGO_STAGED = 1,  /* pack -> ring_allreduce_staged -> unpack            */
+    DDP_ALGO_VIEW = 2     /* ddp_bucket_allreduce_view (no bucket copies)        */
+} ddp_algo;
+
+/*
+ * ddp_sync_buckets -- DDP's reducer step for a whole model: for every bucket
+ * k = 0 .. n_buckets-1 in order, pack the members' gradients into each rank's
+ * bucket k, ring-allreduce the bucket and divide by `divisor`, and copy the
+ * result back into the gradients ([P2] Reducer pseudo-code: allreduce, wait,
+ * div_(world_size), copy back; [P1] section 05 steps 2-3).  Bucket i+1 is
+ * never started before bucket i (same stream).
+ *
+ *   grads[world*n_params]      host table of device pointers, rank-major,
+ *                              registration order
+ *   numel[n_params], bucket_of_param[n_params], offset_of_param[n_params],
+ *   bucket_numel[n_buckets]    a plan from ddp_plan_buckets
+ *   buckets[world*n_buckets]   host table of device pointers: rank r's buffer
+ *                              for bucket k at [r*n_buckets + k], at least
+ *                              bucket_numel[k] elements (may alias across k;
+ *                              unused by DDP_ALGO_VIEW and may then be NULL)
+ *   algo                       a ddp_algo
+ * The same plan must be used on every rank (one plan is shared here by
+ * construction).  DDP_ERR_INVALID if the plan is inconsistent.
+ */
+int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
+                         const int32_t* bucket_of_param, const int64_t* offset_of_param,
+                         int32_t n_buckets, const int64_t* bucket_numel, void* const* buckets,
+                         int32_t dtype, int32_t divisor, int32_t algo, void* stream);
+
+/*
+ * ddp_bucket_allreduce_view -- pack, ring allreduce, average and unpack of one
+ * bucket fused into a single pass, as if every gradient were a view into its
+ * bucket (gradient_as_bucket_view=True, [P1] section 03 and section 05; [P2]
+ * "bucket 与 overlap"): each member's elements are read once from every
+ * rank's gradient, summed in the ring order of the chunk their BUCKET
+ * position falls in (chunk size ceil(bucket_numel/N)), divided, and written
+ * back to every rank's gradient.  Bit-identical to ddp_bucket_pack +
+ * ring_allreduce_fused + ddp_bucket_unpack on the same bucket, with a third
+ * of the memory traffic and no bucket buffer.
+ * Arguments as for ddp_bucket_pack, without the bucket buffers.
+ */
+int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads,
+                                  const int64_t* numel, const int64_t* offset, int64_t bucket_numel,
+                                  int32_t dtype, int32_t divisor, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDP_GB300_DDP_H */

@@ -1,0 +1,99 @@
+"""Helpers shared by the GPU parity tests (test code only).
+
+Expected values always come from the CPU oracle (``oracle``), computed on
+copies of the same seeded inputs; nothing the CUDA path produces is ever fed
+back as an expected value or as an oracle input.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def f32_or_bits(t: torch.Tensor) -> np.ndarray:
+    """Host numpy copy: float32 as float32, bf16 as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def from_np(a: np.ndarray, device="cuda") -> torch.Tensor:
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a.copy()).to(device)
+
+
+def ocode(t_or_a) -> int:
+    if isinstance(t_or_a, torch.Tensor):
+        return oracle.BF16 if t_or_a.dtype == torch.bfloat16 else oracle.F32
+    return oracle.BF16 if t_or_a.dtype == np.uint16 else oracle.F32
+
+
+def oracle_allreduce(x: np.ndarray, divisor: int) -> np.ndarray:
+    """Full oracle ring on a host [N, S] array (copy), returns the result."""
+    y = np.ascontiguousarray(x).copy()
+    oracle.ring_allreduce_2d(y, ocode(y), divisor)
+    return y
+
+
+def assert_bits_equal(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
+    g = got.view(np.uint32) if got.dtype == np.float32 else got
+    w = want.view(np.uint32) if want.dtype == np.float32 else want
+    if not np.array_equal(g, w):
+        bad = np.argwhere(g != w)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} mismatches; first at {i}: got {got[i]!r} want {want[i]!r}")
+
+
+def sampled_expected(samples: np.ndarray, chunk_of: np.ndarray, world: int, divisor: int) -> np.ndarray:
+    """Oracle result for individual elements of a large ring allreduce.
+
+    samples[r, k] is rank r's input at the k-th sampled element and
+    chunk_of[k] the ring chunk that element belongs to.  An element's result
+    depends only on its N inputs and its chunk, so the samples are placed in
+    a small ring problem with the same number of ranks in which chunk j has
+    one slot per sample of chunk j; the oracle runs that small ring and each
+    sample's result is read back from its slot.
+    """
+    K = samples.shape[1]
+    if K == 0:
+        return samples.copy()
+    per_chunk = np.bincount(chunk_of, minlength=world)
+    width = max(int(per_chunk.max()), 1)
+    mini = np.zeros((world, world * width), dtype=samples.dtype)
+    slot = np.zeros(K, dtype=np.int64)
+    fill = np.zeros(world, dtype=np.int64)
+    for k in range(K):
+        j = int(chunk_of[k])
+        slot[k] = j * width + fill[j]
+        fill[j] += 1
+    mini[:, slot] = samples
+    oracle.ring_allreduce_2d(mini, ocode(samples), divisor)
+    return mini[:, slot]
+
+
+def chunk_index(idx: np.ndarray, numel: int, world: int) -> np.ndarray:
+    """Ring chunk of element idx: chunks of ceil(S/N) elements."""
+    c = -(-numel // world)
+    return (idx // c).astype(np.int64)
+
+
+def sample_indices(numel: int, world: int, k_random: int, seed: int = 0) -> np.ndarray:
+    """Chunk boundaries (first/last two of every chunk), the tail, and random picks."""
+    if numel == 0:
+        return np.zeros(0, dtype=np.int64)
+    c = -(-numel // world)
+    s = set()
+    for j in range(world):
+        lo, hi = min(j * c, numel), min((j + 1) * c, numel)
+        for i in (lo, lo + 1, hi - 2, hi - 1):
+            if lo <= i < hi:
+                s.add(i)
+    for i in range(max(0, numel - 9), numel):
+        s.add(i)
+    rng = np.random.default_rng(seed)
+    s.update(int(v) for v in rng.integers(0, numel, size=k_random))
+    return np.array(sorted(s), dtype=np.int64)

@@ -1,0 +1,150 @@
+"""The C ABI on the host (no GPU needed): exports, planner, argument checks.
+
+Only calls that return before any CUDA work are made here: every rejected
+argument set below is refused by the host-side checks, so no kernel is ever
+launched with a made-up pointer.
+"""
+import ctypes
+import re
+import os
+
+import numpy as np
+import pytest
+
+import gradient_sync_plan_gb300 as ddp
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+MiB = 1 << 20
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ddp.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "ring_allreduce_fused" in names and "ddp_plan_buckets" in names
+    L = ddp.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(names) == sorted(ddp.EXPORTS)
+
+
+def test_abi_version_and_status_strings():
+    assert ddp.ddp_abi_version() == 1
+    for code, name in ddp.STATUS.items():
+        assert ddp.ddp_status_string(code).startswith(name)
+
+
+def test_library_is_the_in_tree_build():
+    L = ddp.lib()
+    assert os.path.dirname(os.path.abspath(ddp.library_path())).startswith(ROOT)
+    assert L._name == ddp.library_path()
+
+
+# --------------------------------------------------------------------------
+# planner: host C++ against the oracle's independent implementation
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(60))
+def test_planner_matches_oracle_random(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(0, 80))
+    numels = [int(v) for v in rng.integers(0, 3000, size=P)]
+    if P and seed % 3 == 0:
+        numels[int(rng.integers(0, P))] = 0
+    dtype = int(rng.integers(0, 2))
+    first_cap, cap = int(rng.integers(1, 9000)), int(rng.integers(1, 30000))
+    want = oracle.plan_buckets(numels, 4 if dtype == 0 else 2, first_cap, cap)
+    got = ddp.ddp_plan_buckets(numels, dtype, first_cap, cap)
+    for a, b in zip(got, want):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("which,dtype,cap", [("decoder", ddp.F32, 25), ("resnet", ddp.BF16, 5),
+                                             ("resnet", ddp.BF16, 10), ("resnet", ddp.BF16, 25),
+                                             ("resnet", ddp.BF16, 50)])
+def test_planner_matches_oracle_on_workloads(which, dtype, cap):
+    shapes = workloads.decoder_param_shapes() if which == "decoder" else workloads.resnet50_param_shapes()
+    numels = workloads.param_numels(shapes)
+    want = oracle.plan_buckets(numels, 4 if dtype == ddp.F32 else 2, MiB, cap * MiB)
+    got = ddp.ddp_plan_buckets(numels, dtype, MiB, cap * MiB)
+    for a, b in zip(got, want):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_planner_rejects_bad_arguments():
+    L = ddp.lib()
+    nb = ctypes.c_int32()
+    out32 = (ctypes.c_int32 * 4)()
+    out64 = (ctypes.c_int64 * 4)()
+    n = (ctypes.c_int64 * 2)(5, -1)
+    assert L.ddp_plan_buckets(2, n, 0, MiB, MiB, out32, out64, out64, ctypes.byref(nb)) == -1   # negative numel
+    n = (ctypes.c_int64 * 2)(5, 6)
+    assert L.ddp_plan_buckets(2, n, 7, MiB, MiB, out32, out64, out64, ctypes.byref(nb)) == -1   # dtype
+    assert L.ddp_plan_buckets(2, n, 0, 0, MiB, out32, out64, out64, ctypes.byref(nb)) == -1     # cap 0
+    assert L.ddp_plan_buckets(-1, n, 0, MiB, MiB, out32, out64, out64, ctypes.byref(nb)) == -1
+    assert L.ddp_plan_buckets(2, n, 0, MiB, MiB, out32, out64, out64, None) == -1
+
+
+# --------------------------------------------------------------------------
+# argument checks that return before any CUDA call
+# --------------------------------------------------------------------------
+
+def _vp(*p):
+    return (ctypes.c_void_p * max(len(p), 1))(*p)
+
+
+def test_ring_rejects_bad_arguments_on_host():
+    L = ddp.lib()
+    A, B = 0x7f0000000000, 0x7f0000100000       # never dereferenced: every call below is refused
+    for fn in (L.ring_allreduce_fused, L.ring_allreduce_staged):
+        assert fn(0, _vp(A), 8, 0, 0, None) == -1                 # world < 1
+        assert fn(DDP_MAX := 513, _vp(A), 8, 0, 0, None) == -5    # world > DDP_MAX_WORLD
+        assert fn(2, _vp(A, B), -1, 0, 0, None) == -1             # numel < 0
+        assert fn(2, _vp(A, B), 8, 9, 0, None) == -1              # dtype
+        assert fn(2, _vp(A, B), 8, 0, -2, None) == -1             # divisor < 0
+        assert fn(2, None, 8, 0, 0, None) == -1                   # null table
+        assert fn(2, _vp(A, 0), 8, 0, 0, None) == -1              # null rank buffer
+        assert fn(2, _vp(A, A + 16), 8, 0, 0, None) == -1         # overlapping ranks (8 fp32 = 32 B)
+        assert fn(2, _vp(A, B + 2), 8, 0, 0, None) == -2          # fp32 pointer not 4-byte aligned
+        assert fn(2, _vp(A, B + 1), 8, 1, 0, None) == -2          # bf16 pointer not 2-byte aligned
+        assert fn(2, _vp(A, B), 0, 0, 0, None) == 0               # empty bucket: no-op, no CUDA call
+
+
+def test_accumulate_and_host_variant_reject_bad_arguments():
+    L = ddp.lib()
+    A, B, C, D = 0x7f0000000000, 0x7f0000100000, 0x7f0000200000, 0x7f0000300000
+    assert L.ddp_grad_accumulate(2, _vp(A, B), _vp(C, C), 8, 0, None) == -1    # grads overlap each other
+    assert L.ddp_grad_accumulate(2, _vp(A, B), _vp(C, D + 1), 8, 0, None) == -2
+    assert L.ring_allreduce_fused_from_host(2, None, _vp(C, D), _vp(A, B), 8, 0, 0, None) == -1
+    assert L.ring_allreduce_fused_from_host(2, _vp(C, 0), _vp(C, D), _vp(A, B), 8, 0, 0, None) == -1
+
+
+def test_pack_unpack_view_reject_bad_plans():
+    L = ddp.lib()
+    A, B = 0x7f0000000000, 0x7f0000100000
+    G0, G1 = 0x7f0000200000, 0x7f0000300000
+    i64 = lambda *v: (ctypes.c_int64 * max(len(v), 1))(*v)
+    # member beyond the bucket end
+    assert L.ddp_bucket_pack(2, 1, _vp(G0, G1), i64(10), i64(5), _vp(A, B), 12, 0, None) == -1
+    # two members overlapping inside the bucket
+    assert L.ddp_bucket_pack(1, 2, _vp(G0, G1), i64(4, 4), i64(0, 2), _vp(A), 16, 0, None) == -1
+    # negative offset
+    assert L.ddp_bucket_unpack(1, 1, _vp(G0), i64(4), i64(-1), _vp(A), 16, 0, None) == -1
+    # misaligned gradient
+    assert L.ddp_bucket_pack(1, 1, _vp(G0 + 2), i64(4), i64(0), _vp(A), 16, 0, None) == -2
+    # gradient aliasing its own slot
+    assert L.ddp_bucket_pack(1, 1, _vp(A + 8), i64(4), i64(0), _vp(A), 16, 0, None) == -1
+    # view: same memory used for two ranks
+    assert L.ddp_bucket_allreduce_view(2, 1, _vp(G0, G0), i64(4), i64(0), 4, 0, 2, None) == -1
+    assert L.ddp_bucket_allreduce_view(2, 1, _vp(G0, G1), i64(4), i64(1), 4, 0, 2, None) == -1   # past the end
+    # sync_buckets: a parameter pointing at a bucket that does not exist
+    b_of = (ctypes.c_int32 * 1)(3)
+    assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), b_of, i64(0), 1, i64(4), _vp(A), 0, 1, 0, None) == -1
+    assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), (ctypes.c_int32 * 1)(0), i64(0), 1, i64(4), _vp(A), 0, 1,
+                              7, None) == -1      # unknown algorithm

@@ -1,0 +1,242 @@
+"""GPU parity of the bucket path: plan -> pack -> ring allreduce / N -> unpack.
+
+Against the oracle's own composition of the same steps (``oracle.ddp_sync``,
+``oracle.no_sync_then_sync``), bit-exact, through the C ABI:
+  * pack/unpack of random member lists with odd sizes and offsets (so slots
+    are often not 16-byte aligned), both dtypes;
+  * ddp_sync_buckets with each algorithm (fused, staged, fused view) on a
+    small decoder with many buckets, and the view kernel against
+    pack + fused + unpack;
+  * the ResNet-50 parameter list in bf16, N = 16, caps 5/10/25/50 MiB (full
+    comparison);
+  * the 355M-parameter decoder, N = 8, 25 MiB / 1 MiB caps, with and without
+    no_sync accumulation of 4 micro-batches (sampled comparison: inputs made
+    on the device, sampled inputs snapshot before the sync).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_plan_gb300 as ddp
+import oracle
+import workloads
+from gpu_util import assert_bits_equal, f32_or_bits, sampled_expected
+
+pytestmark = pytest.mark.gpu
+MiB = 1 << 20
+
+
+def _host_grads(numels, world, dtype, seed0, kind="randn", std=1e-2):
+    """grads[r][p] host arrays (float32 or uint16 bf16 bits), rank r from seed seed0+r."""
+    total = sum(numels)
+    flat = workloads.rank_vectors(world, total, kind, std=std, dtype=dtype, seed0=seed0)
+    flat_h = f32_or_bits(flat)
+    out, o = [], 0
+    offs = np.cumsum([0] + list(numels))
+    return flat, [[flat_h[r, offs[p]:offs[p + 1]].copy() for p in range(len(numels))] for r in range(world)]
+
+
+def _device_views(flat_dev, numels):
+    offs = np.cumsum([0] + list(numels))
+    return [[flat_dev[r, int(offs[p]):int(offs[p + 1])] for p in range(len(numels))]
+            for r in range(flat_dev.shape[0])]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pack_unpack_random_members(dtype):
+    rng = np.random.default_rng(1)
+    for trial in range(20):
+        world = int(rng.integers(1, 9))
+        n = int(rng.integers(1, 30))
+        numels = [int(v) for v in rng.integers(0, 5000, size=n)]
+        code = oracle.BF16 if dtype == "bf16" else oracle.F32
+        order = list(rng.permutation(n))
+        offsets, pos = [0] * n, int(rng.integers(0, 7))
+        for i in order:
+            offsets[i] = pos
+            pos += numels[i] + int(rng.integers(0, 3))
+        bucket_numel = pos + int(rng.integers(0, 5))
+        flat, grads_h = _host_grads(numels, world, dtype, seed0=trial * 10)
+        gdev = _device_views(flat.cuda(), numels)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        buckets = torch.zeros((world, bucket_numel), dtype=tdt, device="cuda")
+        ddp.ddp_bucket_pack(gdev, offsets, buckets)
+        torch.cuda.synchronize()
+        want = np.zeros((world, bucket_numel), dtype=np.uint16 if dtype == "bf16" else np.float32)
+        for r in range(world):
+            oracle.bucket_pack(grads_h[r], offsets, want[r], code)
+        assert_bits_equal(f32_or_bits(buckets), want, f"pack trial {trial}")
+        # unpack a different bucket content back into zeroed gradients
+        src = workloads.rank_vectors(world, bucket_numel, "uniform", dtype=dtype, seed0=99 + trial)
+        src_h = f32_or_bits(src)
+        out = [[torch.zeros_like(g) for g in gdev[r]] for r in range(world)]
+        ddp.ddp_bucket_unpack(out, offsets, src.cuda())
+        torch.cuda.synchronize()
+        for r in range(world):
+            exp = [np.zeros_like(g) for g in grads_h[r]]
+            oracle.bucket_unpack(exp, offsets, src_h[r], code)
+            for i in range(n):
+                assert_bits_equal(f32_or_bits(out[r][i]), exp[i], f"unpack trial {trial} r{r} m{i}")
+
+
+def _small_decoder():
+    return workloads.param_numels(workloads.decoder_param_shapes(n_layer=3, d_model=64, d_ff=256, vocab=1000,
+                                                                 n_pos=64))
+
+
+@pytest.mark.parametrize("algo", [ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_STAGED, ddp.DDP_ALGO_VIEW])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sync_buckets_small_decoder(algo, dtype):
+    numels = _small_decoder()
+    world = 8
+    es = 2 if dtype == "bf16" else 4
+    first, cap = 4096, 40000
+    plan = ddp.ddp_plan_buckets(numels, ddp.BF16 if dtype == "bf16" else ddp.F32, first, cap)
+    assert len(plan[2]) > 5
+    flat, grads_h = _host_grads(numels, world, dtype, seed0=0)
+    gdev_flat = flat.cuda()
+    gdev = _device_views(gdev_flat, numels)
+    bk = None
+    if algo != ddp.DDP_ALGO_VIEW:
+        bk = [[torch.empty(int(n), dtype=flat.dtype, device="cuda") for n in plan[2]] for _ in range(world)]
+    ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
+    torch.cuda.synchronize()
+    oracle.ddp_sync(grads_h, oracle.BF16 if dtype == "bf16" else oracle.F32, first, cap)
+    got = f32_or_bits(gdev_flat)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(got, want, f"sync algo={algo} {dtype}")
+    assert es in (2, 4)
+
+
+def test_view_equals_pack_fused_unpack_bitwise():
+    rng = np.random.default_rng(3)
+    for trial in range(12):
+        world = int(rng.integers(1, 17))
+        n = int(rng.integers(1, 12))
+        numels = [int(v) for v in rng.integers(1, 20000, size=n)]
+        dtype = "bf16" if trial % 2 else "f32"
+        b_of, off, bn = ddp.ddp_plan_buckets(numels, ddp.BF16 if dtype == "bf16" else ddp.F32, 10 ** 9, 10 ** 9)
+        assert len(bn) == 1
+        flat = workloads.rank_vectors(world, sum(numels), "randn", dtype=dtype, seed0=trial).cuda()
+        a, b = flat.clone(), flat.clone()
+        ga, gb = _device_views(a, numels), _device_views(b, numels)
+        offsets = [int(o) for o in off]
+        ddp.ddp_bucket_allreduce_view(ga, offsets, int(bn[0]), world)
+        bucket = torch.empty((world, int(bn[0])), dtype=flat.dtype, device="cuda")
+        ddp.ddp_bucket_pack(gb, offsets, bucket)
+        ddp.ring_allreduce_fused(bucket, world)
+        ddp.ddp_bucket_unpack(gb, offsets, bucket)
+        torch.cuda.synchronize()
+        iv = torch.int16 if dtype == "bf16" else torch.int32
+        assert torch.equal(a.view(iv), b.view(iv)), f"trial {trial}"
+
+
+@pytest.mark.parametrize("cap_mib,count", [(5, 9), (10, 6), (25, 3), (50, 2)])
+def test_resnet50_bf16_n16_cap_sweep_full(cap_mib, count):
+    numels = workloads.param_numels(workloads.resnet50_param_shapes())
+    world = 16
+    plan = ddp.ddp_plan_buckets(numels, ddp.BF16, MiB, cap_mib * MiB)
+    assert len(plan[2]) == count
+    flat, grads_h = _host_grads(numels, world, "bf16", seed0=0)
+    gdev_flat = flat.cuda()
+    gdev = _device_views(gdev_flat, numels)
+    bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
+    ddp.ddp_sync_buckets(gdev, plan, bk, algo=ddp.DDP_ALGO_FUSED)
+    torch.cuda.synchronize()
+    ref64 = np.zeros(sum(numels))
+    for r in range(world):
+        ref64 += oracle.bf16_to_f32(np.concatenate(grads_h[r])).astype(np.float64)
+    ref64 /= world
+    oracle.ddp_sync(grads_h, oracle.BF16, MiB, cap_mib * MiB)
+    got = f32_or_bits(gdev_flat)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(got, want, f"resnet50 cap {cap_mib}")
+    y = oracle.bf16_to_f32(got[0]).astype(np.float64)
+    assert np.linalg.norm(y - ref64) / np.linalg.norm(ref64) <= 2e-2
+
+
+def _decoder_sampled(algo, no_sync):
+    numels = workloads.param_numels(workloads.decoder_param_shapes())
+    world, total = 8, sum(numels)
+    b_of, off, bn = plan = ddp.ddp_plan_buckets(numels, ddp.F32, MiB, 25 * MiB)
+    assert len(bn) == 37
+    pstart = np.cumsum([0] + numels)
+    g = torch.empty((world, total), dtype=torch.float32, device="cuda")
+    rng = np.random.default_rng(7)
+    # sampled elements: both ends of every parameter plus random ones
+    picks = []
+    for p in range(len(numels)):
+        for e in (0, numels[p] - 1):
+            picks.append((p, e))
+    for p in rng.integers(0, len(numels), size=3000):
+        picks.append((int(p), int(rng.integers(0, numels[int(p)]))))
+    flat_idx = torch.tensor([int(pstart[p] + e) for p, e in picks], device="cuda")
+    M = 4 if no_sync else 1
+    samples = None
+    code = oracle.F32
+    scratch = torch.empty_like(g) if no_sync else None
+    for m in range(M):
+        dst = g if m == 0 else scratch
+        for r in range(world):
+            dst[r].copy_(workloads.randn_f32(total, workloads.microbatch_seed(r, world, m), 1e-2, device="cuda"))
+        s = f32_or_bits(dst[:, flat_idx])
+        if m == 0:
+            samples = s
+        else:
+            for r in range(world):
+                oracle.accumulate(samples[r], s[r], code)
+            ddp.ddp_grad_accumulate(g, scratch)
+    gdev = _device_views(g, numels)
+    bk = None
+    if algo != ddp.DDP_ALGO_VIEW:
+        bk = [[torch.empty(int(n), dtype=torch.float32, device="cuda") for n in bn] for _ in range(world)]
+    ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
+    torch.cuda.synchronize()
+    got = f32_or_bits(g[:, flat_idx])
+    # expected: each sample's bucket position decides its chunk; samples of
+    # one bucket go through one small oracle ring
+    want = np.empty_like(got)
+    picks_arr = np.array(picks)
+    for k in range(len(bn)):
+        sel = np.nonzero(b_of[picks_arr[:, 0]] == k)[0]
+        if len(sel) == 0:
+            continue
+        q = off[picks_arr[sel, 0]] + picks_arr[sel, 1]
+        c = -(-int(bn[k]) // world)
+        want[:, sel] = sampled_expected(samples[:, sel], (q // c).astype(np.int64), world, world)
+    assert_bits_equal(got, want, f"decoder algo={algo} no_sync={no_sync}")
+    for r in range(1, world):
+        assert torch.equal(g[r].view(torch.int32), g[0].view(torch.int32))
+
+
+@pytest.mark.parametrize("algo", [ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_VIEW])
+def test_decoder_355m_n8_sampled(algo):
+    _decoder_sampled(algo, no_sync=False)
+    torch.cuda.empty_cache()
+
+
+def test_decoder_355m_n8_no_sync_sampled():
+    _decoder_sampled(ddp.DDP_ALGO_FUSED, no_sync=True)
+    torch.cuda.empty_cache()
+
+
+def test_no_sync_small_decoder_full():
+    numels = _small_decoder()
+    world, M = 4, 4
+    micro_h, micro_d = [], []
+    for m in range(M):
+        rows = [workloads.randn_f32(sum(numels), workloads.microbatch_seed(r, world, m), 1e-2) for r in range(world)]
+        flat = torch.stack(rows)
+        offs = np.cumsum([0] + numels)
+        micro_h.append([[flat[r, offs[p]:offs[p + 1]].numpy().copy() for p in range(len(numels))]
+                        for r in range(world)])
+        micro_d.append(flat.cuda())
+    acc = micro_d[0].clone()
+    for m in range(1, M):
+        ddp.ddp_grad_accumulate(acc, micro_d[m])
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, 4096, 40000)
+    gdev = _device_views(acc, numels)
+    ddp.ddp_sync_buckets(gdev, plan, None, algo=ddp.DDP_ALGO_VIEW)
+    torch.cuda.synchronize()
+    want = oracle.no_sync_then_sync(micro_h, oracle.F32, 4096, 40000)
+    assert_bits_equal(f32_or_bits(acc), np.stack([np.concatenate(want[r]) for r in range(world)]), "no_sync")

@@ -1,0 +1,231 @@
+"""GPU parity of the ring allreduce kernels against the CPU oracle.
+
+Bit-exact comparison (the summation order is fixed, so any difference is a
+bug) of ring_allreduce_fused and ring_allreduce_staged, called through the C
+ABI, with the oracle's ring simulation on the same seeded inputs:
+  * the pages' 3-rank, length-6 example and the order pins;
+  * every N in 1..9 with every S in 0..70 (ragged chunks, empty chunks);
+  * sizes spanning many tiles with ragged tails, both dtypes, several divisors;
+  * buffers that are not 16-byte aligned (element-wise path);
+  * the N=4, 1 Mi-element fp32 bucket (full comparison) and the N=8, 1 GiB
+    bucket and N=64 sweep points (sampled comparison + properties at any size).
+Tolerance against float64: normwise 1e-5 (fp32) and 2e-2 (bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_plan_gb300 as ddp
+import oracle
+import workloads
+from gpu_util import (assert_bits_equal, chunk_index, f32_or_bits, from_np, oracle_allreduce, sample_indices,
+                      sampled_expected)
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"fused": ddp.ring_allreduce_fused, "staged": ddp.ring_allreduce_staged}
+
+
+def run_gpu(kernel: str, x_host: np.ndarray, divisor: int) -> np.ndarray:
+    x = from_np(x_host)
+    KERNELS[kernel](x, divisor)
+    torch.cuda.synchronize()
+    return f32_or_bits(x)
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_worked_example(kernel):
+    k = np.arange(6, dtype=np.float32)
+    x = np.stack([k + 1, 10 * (k + 1), 100 * (k + 1)]).astype(np.float32)
+    got = run_gpu(kernel, x, 3)
+    want = np.tile((37 * (k + 1)).astype(np.float32), (3, 1))
+    assert_bits_equal(got, want, kernel)
+    assert_bits_equal(got, oracle_allreduce(x, 3), kernel)
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_order_pins(kernel):
+    for N in (3, 4):
+        x = np.zeros((N, N), dtype=np.float32)
+        for j in range(N):
+            x[(j + 1) % N, j] = 2.0 ** 24
+            x[(j + 2) % N, j] = 1.0
+            if N == 4:
+                x[(j + 3) % N, j] = 1.0
+            x[j, j] = -(2.0 ** 24)
+        assert np.all(run_gpu(kernel, x, 0) == 0.0)
+    f = np.zeros((3, 3), dtype=np.float32)
+    for j in range(3):
+        f[(j + 1) % 3, j], f[(j + 2) % 3, j], f[j, j] = 256.0, 3.0, -256.0
+    got = run_gpu(kernel, oracle.bf16_rne(f), 0)
+    assert np.all(oracle.bf16_to_f32(got) == 4.0)
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_exhaustive_small(kernel, dtype):
+    for N in range(1, 10):
+        for S in range(0, 71):
+            x = workloads.rank_vectors(N, S, "randn", dtype=dtype, seed0=N * 1000 + S)
+            xh = f32_or_bits(x)
+            for div in (0, N):
+                assert_bits_equal(run_gpu(kernel, xh, div), oracle_allreduce(xh, div), f"{kernel} N={N} S={S}")
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,S,div", [(2, 1_000_003, 2), (3, 3 * 65536 + 5, 3), (5, 777_777, 5), (7, 1 << 20, 7),
+                                     (8, (1 << 21) + 13, 8), (16, 1_048_583, 16), (6, 99_991, 0), (4, 4096, 1)])
+def test_many_tiles_ragged(kernel, dtype, N, S, div):
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=17)
+    xh = f32_or_bits(x)
+    assert_bits_equal(run_gpu(kernel, xh, div), oracle_allreduce(xh, div), f"{kernel} {dtype} N={N} S={S}")
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_buffers_take_elementwise_path(kernel, dtype):
+    # rank rows start 1 element into 16-byte-aligned storage: element aligned
+    # but not 16-byte aligned, so the library takes its element-wise kernels
+    N, S = 5, 12_345
+    x = workloads.rank_vectors(N, S, "randn", dtype=dtype, seed0=3)
+    xh = f32_or_bits(x)
+    store = torch.zeros((N, S + 8), dtype=x.dtype, device="cuda")
+    rows = [store[r, 1:1 + S] for r in range(N)]
+    for r in range(N):
+        rows[r].copy_(x[r].cuda())
+    KERNELS[kernel](rows, N)
+    torch.cuda.synchronize()
+    got = np.stack([f32_or_bits(r) for r in rows])
+    assert_bits_equal(got, oracle_allreduce(xh, N), kernel)
+
+
+def test_staged_equals_fused_bitwise_random_shapes():
+    rng = np.random.default_rng(0)
+    for _ in range(25):
+        N = int(rng.integers(1, 20))
+        S = int(rng.integers(0, 200_000))
+        dtype = "bf16" if rng.integers(0, 2) else "f32"
+        x = workloads.rank_vectors(N, S, "uniform", dtype=dtype, seed0=int(rng.integers(0, 1000))).cuda()
+        a, b = x.clone(), x.clone()
+        ddp.ring_allreduce_fused(a, N)
+        ddp.ring_allreduce_staged(b, N)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16) if dtype == "bf16" else a.view(torch.int32),
+                           b.view(torch.int16) if dtype == "bf16" else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_config_n4_one_mi_fp32_full(kernel):
+    # one bucket of 1,048,576 fp32 per rank, N(0,1) from seed r, divide by 4
+    N, S = 4, 1 << 20
+    x = workloads.rank_vectors(N, S, "randn")
+    xh = x.numpy()
+    got = run_gpu(kernel, xh, 4)
+    want = oracle_allreduce(xh, 4)
+    assert_bits_equal(got, want, kernel)
+    s64 = xh.astype(np.float64).sum(0) / 4
+    assert np.linalg.norm(got[0] - s64) / np.linalg.norm(s64) <= 1e-5
+
+
+def _sampled_check(kernel, N, S, dtype, kind, std, divisor, k_random=4000):
+    """Large bucket: inputs generated on the device, sampled inputs snapshot
+    before the kernel, sampled outputs compared with the oracle; at every
+    element all ranks must agree and the normwise error vs float64 holds."""
+    torch_dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.empty((N, S), dtype=torch_dtype, device="cuda")
+    for r in range(N):
+        if kind == "randn":
+            v = workloads.randn_f32(S, r, std, device="cuda")
+        else:
+            v = workloads.uniform_pm1_f32(S, r, device="cuda")
+        x[r].copy_(v)
+        del v
+    idx = sample_indices(S, N, k_random, seed=S % 1000 + N)
+    idx_t = torch.from_numpy(idx).cuda()
+    samples = f32_or_bits(x[:, idx_t])
+    ref64 = torch.zeros(S, dtype=torch.float64, device="cuda")
+    for r in range(N):
+        ref64 += x[r].to(torch.float64)
+    ref64 /= max(divisor, 1)
+    KERNELS[kernel](x, divisor)
+    torch.cuda.synchronize()
+    got = f32_or_bits(x[:, idx_t])
+    want = sampled_expected(samples, chunk_index(idx, S, N), N, divisor)
+    assert_bits_equal(got, want, f"{kernel} N={N} S={S}")
+    for r in range(1, N):
+        assert torch.equal(x[r].view(torch.int16 if dtype == "bf16" else torch.int32),
+                           x[0].view(torch.int16 if dtype == "bf16" else torch.int32))
+    err = torch.linalg.vector_norm(x[0].to(torch.float64) - ref64) / torch.linalg.vector_norm(ref64)
+    assert float(err) <= (2e-2 if dtype == "bf16" else 1e-5)
+    del x, ref64
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_config_n8_one_gib_fp32_sampled(kernel):
+    # N = 8, 268,435,456 fp32 per rank, N(0, 1e-2^2), divide by 8
+    _sampled_check(kernel, 8, 1 << 28, "f32", "randn", 1e-2, 8)
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("N", [8, 64])
+@pytest.mark.parametrize("kb", [4, 64, 1024, 16384, 262144])
+def test_message_size_sweep(N, kb):
+    # uniform(-1,1) fp32, S_b = kb KiB per rank; full comparison up to 1 MiB,
+    # sampled above
+    S = kb * 1024 // 4
+    if kb <= 1024:
+        x = workloads.rank_vectors(N, S, "uniform").numpy()
+        for kernel in ("fused", "staged"):
+            assert_bits_equal(run_gpu(kernel, x, N), oracle_allreduce(x, N), f"{kernel} N={N} {kb}KiB")
+    else:
+        for kernel in ("fused", "staged"):
+            _sampled_check(kernel, N, S, "f32", "uniform", 1.0, N, k_random=2000)
+            torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_bf16_n16_large_sampled(kernel):
+    _sampled_check(kernel, 16, 25_557_032 // 2 + 3, "bf16", "randn", 1e-2, 16)
+
+
+def test_accumulate_matches_oracle():
+    for dtype in ("f32", "bf16"):
+        for N, S in ((1, 5), (3, 1001), (8, 1 << 20)):
+            a = workloads.rank_vectors(N, S, "randn", dtype=dtype, seed0=1)
+            g = workloads.rank_vectors(N, S, "randn", dtype=dtype, seed0=100)
+            ah, gh = f32_or_bits(a), f32_or_bits(g)
+            ad, gd = a.cuda(), g.cuda()
+            ddp.ddp_grad_accumulate(ad, gd)
+            torch.cuda.synchronize()
+            want = ah.copy()
+            code = oracle.BF16 if dtype == "bf16" else oracle.F32
+            for r in range(N):
+                oracle.accumulate(want[r], gh[r], code)
+            assert_bits_equal(f32_or_bits(ad), want, f"accumulate {dtype} N={N} S={S}")
+
+
+def test_from_host_matches_oracle():
+    N, S = 8, 1_000_001
+    x = workloads.rank_vectors(N, S, "randn", seed0=5)
+    want = oracle_allreduce(x.numpy(), 8)
+    host_in = x.pin_memory()
+    host_out = torch.empty_like(host_in).pin_memory()
+    dev = torch.empty((N, S), dtype=torch.float32, device="cuda")
+    ddp.ring_allreduce_fused_from_host(host_in, host_out, dev, 8)
+    torch.cuda.synchronize()
+    assert_bits_equal(host_out.numpy(), want, "from_host")
+
+
+def test_empty_bucket_is_noop():
+    x = torch.zeros((4, 0), device="cuda")
+    ddp.ring_allreduce_fused(x, 4)
+    ddp.ring_allreduce_staged(x, 4)
+    torch.cuda.synchronize()
+
+
+def test_single_rank_divides_only():
+    x = workloads.rank_vectors(1, 1003, "randn").numpy()
+    for kernel in ("fused", "staged"):
+        assert_bits_equal(run_gpu(kernel, x, 3), oracle_allreduce(x, 3), kernel)
+        assert_bits_equal(run_gpu(kernel, x, 0), x, kernel)

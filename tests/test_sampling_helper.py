@@ -1,0 +1,29 @@
+"""The sampled-expectation helper used by the large GPU parity tests must give
+exactly the full oracle's values at the sampled elements (CPU only)."""
+import numpy as np
+import torch
+import pytest
+
+import oracle
+import workloads
+from gpu_util import chunk_index, oracle_allreduce, sample_indices, sampled_expected
+
+
+@pytest.mark.parametrize("N,S,dtype,div", [(2, 1001, "f32", 2), (5, 10_007, "f32", 5), (8, 65_536, "f32", 8),
+                                           (3, 999, "bf16", 3), (16, 40_009, "bf16", 16), (7, 13, "f32", 0)])
+def test_sampled_expected_equals_full_oracle(N, S, dtype, div):
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N)
+    xh = x.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else x.numpy()
+    full = oracle_allreduce(xh, div)
+    idx = sample_indices(S, N, 500, seed=1)
+    got = sampled_expected(xh[:, idx].copy(), chunk_index(idx, S, N), N, div)
+    assert np.array_equal(got.view(np.uint16 if dtype == "bf16" else np.uint32),
+                          full[:, idx].view(np.uint16 if dtype == "bf16" else np.uint32))
+
+
+def test_sample_indices_cover_every_chunk_boundary():
+    S, N = 1000, 7
+    idx = set(sample_indices(S, N, 0).tolist())
+    c = -(-S // N)
+    for j in range(N):
+        assert j * c in idx and min((j + 1) * c, S) - 1 in idx
