@@ -33,7 +33,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
           -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY"}
 
 # every symbol include/ddp.h declares
-EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_plan_buckets", "ddp_bucket_pack", "ddp_bucket_unpack",
+EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_device_status", "ddp_plan_buckets", "ddp_bucket_pack", "ddp_bucket_unpack",
            "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
 
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.ddp_status_string.restype = ctypes.c_char_p
             L.ddp_abi_version.argtypes = []
             L.ddp_abi_version.restype = i32
+            L.ddp_device_status.argtypes = [P(i32), i32]
+            L.ddp_device_status.restype = i32
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
@@ -77,7 +79,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_sync_buckets.argtypes = [i32, i32, P(vp), P(i64), P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                            i32, vp]
             L.ddp_bucket_allreduce_view.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, i32, vp]
-            for name in EXPORTS[2:]:
+            for name in EXPORTS[3:]:
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -159,6 +161,13 @@ def ddp_status_string(status: int) -> str:
 
 def ddp_abi_version() -> int:
     return int(lib().ddp_abi_version())
+
+
+def ddp_device_status(clear: bool = True) -> int:
+    """The sticky device status word (0, or DDP_ERR_TIMEOUT); synchronise first."""
+    v = ctypes.c_int32(0)
+    _check("ddp_device_status", lib().ddp_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
 
 
 def ddp_plan_buckets(numels: Sequence[int], dtype: int = F32, first_bucket_bytes: int = FIRST_BUCKET_BYTES,

@@ -217,6 +217,11 @@ const char* ddp_status_string(int32_t status) {
 
 int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
 
+int32_t ddp_device_status(int32_t* status, int32_t clear) {
+    if (!status) return DDP_ERR_INVALID;
+    return cuda_status(read_device_status(status, clear != 0));
+}
+
 int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                              void* stream) {
     int32_t st = common_checks(world, numel, dtype);

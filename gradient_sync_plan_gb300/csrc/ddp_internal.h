@@ -41,6 +41,15 @@ cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int 
 cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,
                               bool vec_ok, cudaStream_t stream);
 
+// ---- TMA-staged fused ring (ring_tma.cu) --------------------------------
+// Usable when every buffer is 16-byte aligned, chunk and bucket byte sizes
+// are multiples of 16, world <= 128 and the bucket is large enough.
+bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok);
+int64_t tma_tile_bytes(int world);
+cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                                  cudaStream_t stream);
+cudaError_t read_device_status(int32_t* out, bool clear);
+
 // ---- bucket kernels (bucket_kernels.cu) --------------------------------
 struct CopyItem {
     const void* src;

@@ -226,6 +226,7 @@ static cudaError_t fused_by_div(int world, void* const* ptrs, int64_t numel, Div
 cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
                               cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
+    if (tma_usable(world, numel, dtype, vec_ok)) return launch_ring_fused_tma(world, ptrs, numel, dtype, div, stream);
     if (dtype == DDP_F32) return fused_by_div<EF32>(world, ptrs, numel, div, vec_ok, stream);
     return fused_by_div<EBF16>(world, ptrs, numel, div, vec_ok, stream);
 }

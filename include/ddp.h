@@ -72,6 +72,16 @@ const char* ddp_status_string(int32_t status);
 int32_t ddp_abi_version(void);
 
 /*
+ * ddp_device_status -- the library's sticky device-side status word on the
+ * current device: DDP_OK, or DDP_ERR_TIMEOUT if a kernel's bounded wait on an
+ * asynchronous copy gave up (the kernel then stopped early, so the buffers
+ * of that call hold partial results).  Synchronous: call it after the
+ * stream of interest has been synchronised.  clear != 0 resets the word.
+ * Returns DDP_OK, DDP_ERR_INVALID (status NULL) or DDP_ERR_CUDA.
+ */
+int32_t ddp_device_status(int32_t* status, int32_t clear);
+
+/*
  * ddp_plan_buckets -- assign parameters to buckets ([P1] section 03 "Bucket"
  * and "Overlap", section 05 step 2; [P2] "bucket 与 overlap").
  *

@@ -100,6 +100,28 @@ def test_unaligned_buffers_take_elementwise_path(kernel, dtype):
     assert_bits_equal(got, oracle_allreduce(xh, N), kernel)
 
 
+@pytest.mark.parametrize("N,S,dtype", [
+    (5, 5 * 262144 - 4, "f32"),      # chunks of 262144, last chunk 4 shorter
+    (9, 9 * 131072 - 8, "bf16"),     # chunks of 131072, last chunk 8 shorter
+    (64, 64 * 16384 - 60, "f32"),    # 64 ranks, last chunk 60 shorter
+    (2, 1 << 22, "bf16"),            # two ranks, equal chunks
+    (1, 1 << 21, "f32"),             # one rank: divide only
+])
+def test_tma_staged_path_ragged_last_chunk(N, S, dtype):
+    # 16-byte aligned chunks and bucket, more than 4 MiB over all ranks: the
+    # fused call streams tiles through shared memory with bulk copies; tiles
+    # stop at chunk ends, so chunk ends that are not tile multiples are hit
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + 40)
+    xh = f32_or_bits(x)
+    es = 2 if dtype == "bf16" else 4
+    clen = -(-S // N)
+    assert (clen * es) % 16 == 0 and (S * es) % 16 == 0 and S * es * N >= 4 << 20
+    for div in (N, 0):
+        got = run_gpu("fused", xh, div)
+        assert_bits_equal(got, oracle_allreduce(xh, div), f"tma N={N} S={S} {dtype} div={div}")
+    assert ddp.ddp_device_status() == 0
+
+
 def test_staged_equals_fused_bitwise_random_shapes():
     rng = np.random.default_rng(0)
     for _ in range(25):
