@@ -33,8 +33,8 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
           -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY"}
 
 # every symbol include/ddp.h declares
-EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_device_status", "ddp_plan_buckets", "ddp_bucket_pack", "ddp_bucket_unpack",
-           "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
+EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_plan_buckets",
+           "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
 
 
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.ddp_status_string.restype = ctypes.c_char_p
             L.ddp_abi_version.argtypes = []
             L.ddp_abi_version.restype = i32
+            L.ddp_last_cuda_error.argtypes = []
+            L.ddp_last_cuda_error.restype = ctypes.c_char_p
             L.ddp_device_status.argtypes = [P(i32), i32]
             L.ddp_device_status.restype = i32
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
@@ -79,7 +81,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_sync_buckets.argtypes = [i32, i32, P(vp), P(i64), P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                            i32, vp]
             L.ddp_bucket_allreduce_view.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, i32, vp]
-            for name in EXPORTS[3:]:
+            for name in EXPORTS[4:]:
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -87,7 +89,10 @@ def lib() -> ctypes.CDLL:
 
 def _check(fn: str, status: int) -> None:
     if status != 0:
-        raise DDPError(fn, status)
+        err = DDPError(fn, status)
+        if status == -3:
+            err.args = (f"{err.args[0]} ({_lib.ddp_last_cuda_error().decode()})",)
+        raise err
 
 
 # --------------------------------------------------------------------------

@@ -9,8 +9,9 @@
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "ddp.h"
@@ -41,8 +42,8 @@ bool debug_enabled() {
 
 namespace {
 std::mutex g_mu;
-std::unordered_map<int, int> g_sms;                          // device -> SM count
-std::unordered_map<unsigned long long, int> g_occ;           // (device, kernel) -> blocks per SM
+std::map<int, int> g_sms;                                    // device -> SM count
+std::map<std::pair<int, const void*>, int> g_occ;            // (device, kernel) -> blocks per SM
 }  // namespace
 
 int sm_count() {
@@ -63,7 +64,7 @@ int grid_for(const void* kernel, int64_t work_items, int threads) {
     const int sms = sm_count();
     int dev = 0;
     cudaGetDevice(&dev);
-    const unsigned long long key = ((unsigned long long)dev << 56) ^ (unsigned long long)(uintptr_t)kernel;
+    const auto key = std::make_pair(dev, kernel);
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -117,9 +118,12 @@ int32_t common_checks(int32_t world, int64_t numel, int32_t dtype) {
     return DDP_OK;
 }
 
+thread_local const char* t_last_cuda_error = "no error";
+
 int32_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DDP_OK;
-    if (debug_enabled()) fprintf(stderr, "[ddp] CUDA error: %s\n", cudaGetErrorString(e));
+    t_last_cuda_error = cudaGetErrorString(e);
+    if (debug_enabled()) fprintf(stderr, "[ddp] CUDA error: %s\n", t_last_cuda_error);
     return DDP_ERR_CUDA;
 }
 
@@ -216,6 +220,8 @@ const char* ddp_status_string(int32_t status) {
 }
 
 int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
+
+const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
 
 int32_t ddp_device_status(int32_t* status, int32_t clear) {
     if (!status) return DDP_ERR_INVALID;

@@ -18,8 +18,9 @@
 // the CTA's copies still in flight, and the CTA returns.
 #include <algorithm>
 #include <cstdio>
+#include <map>
 #include <mutex>
-#include <unordered_map>
+#include <tuple>
 
 #include "ddp_device.cuh"
 #include "ddp_internal.h"
@@ -28,7 +29,7 @@ namespace ddpk {
 
 __device__ int32_t g_device_status = 0;     // sticky DDP_ERR_TIMEOUT flag, read by ddp_device_status()
 
-constexpr int kTmaStages = 2;
+constexpr int kTmaStages = 3;
 constexpr int kTmaThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
@@ -229,16 +230,18 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 
 namespace {
 std::mutex g_tma_mu;
-std::unordered_map<unsigned long long, int> g_tma_occ;     // (device, kernel, smem) -> CTAs per SM
+std::map<std::tuple<int, const void*, size_t>, int> g_tma_occ;   // (device, kernel, smem) -> CTAs per SM
 }  // namespace
 
 // Bytes of one rank's tile: two CTAs per SM share ~220 KB, each CTA holds
-// kTmaStages x world input tiles and two result tiles.  0 = path not usable.
+// kTmaStages x world input tiles and two result tiles.  Tiles are powers of
+// two (4 KB for eight ranks): tiles that start on page-sized boundaries
+// stream measurably faster than odd sizes.  0 = path not usable.
 int64_t tma_tile_bytes(int world) {
     const int64_t budget = 110 * 1024 - 64;
-    int64_t tb = budget / ((int64_t)kTmaStages * world + 2);
-    tb = std::min<int64_t>(tb, 16384);
-    tb &= ~(int64_t)511;
+    const int64_t fit = budget / ((int64_t)kTmaStages * world + 2);
+    int64_t tb = 16384;
+    while (tb > fit) tb >>= 1;
     return tb >= 512 ? tb : 0;
 }
 
@@ -259,7 +262,7 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
     const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * tile_bytes + kTmaStages * sizeof(uint64_t);
     int dev = 0;
     cudaGetDevice(&dev);
-    const unsigned long long key = ((unsigned long long)dev << 56) ^ ((unsigned long long)(uintptr_t)k << 8) ^ smem;
+    const auto key = std::make_tuple(dev, (const void*)k, smem);
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lk(g_tma_mu);

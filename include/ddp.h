@@ -71,6 +71,10 @@ const char* ddp_status_string(int32_t status);
 /* DDP_ABI_VERSION of the loaded library. */
 int32_t ddp_abi_version(void);
 
+/* Text of the last CUDA error that made a call on this host thread return
+ * DDP_ERR_CUDA ("no error" if none); a static string, never NULL. */
+const char* ddp_last_cuda_error(void);
+
 /*
  * ddp_device_status -- the library's sticky device-side status word on the
  * current device: DDP_OK, or DDP_ERR_TIMEOUT if a kernel's bounded wait on an
