@@ -20,7 +20,7 @@
 #include <cstdio>
 #include <map>
 #include <mutex>
-#include <tuple>
+#include <utility>
 
 #include "ddp_device.cuh"
 #include "ddp_internal.h"
@@ -229,8 +229,16 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 // ---------------------------------------------------------------------------
 
 namespace {
+// Per (device, kernel): the dynamic shared-memory limit set on the function so
+// far (a function attribute: it is only ever raised, never lowered, so a
+// launch with less shared memory stays valid) and the CTAs per SM measured
+// for each shared-memory size.
+struct FnState {
+    size_t smem_attr = 0;
+    std::map<size_t, int> per_sm;
+};
 std::mutex g_tma_mu;
-std::map<std::tuple<int, const void*, size_t>, int> g_tma_occ;   // (device, kernel, smem) -> CTAs per SM
+std::map<std::pair<int, const void*>, FnState> g_tma_fn;
 }  // namespace
 
 // Bytes of one rank's tile: two CTAs per SM share ~220 KB, each CTA holds
@@ -262,21 +270,25 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
     const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * tile_bytes + kTmaStages * sizeof(uint64_t);
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, (const void*)k, smem);
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lk(g_tma_mu);
-        auto it = g_tma_occ.find(key);
-        if (it != g_tma_occ.end()) per_sm = it->second;
-    }
-    if (per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTmaThreads, smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm <= 0) per_sm = 1;
-        std::lock_guard<std::mutex> lk(g_tma_mu);
-        g_tma_occ[key] = per_sm;
+        FnState& fs = g_tma_fn[std::make_pair(dev, (const void*)k)];
+        if (smem > fs.smem_attr) {
+            cudaError_t e =
+                cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            fs.smem_attr = smem;
+        }
+        auto it = fs.per_sm.find(smem);
+        if (it != fs.per_sm.end()) {
+            per_sm = it->second;
+        } else {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTmaThreads, smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm <= 0) per_sm = 1;
+            fs.per_sm[smem] = per_sm;
+        }
     }
     TileMap map;
     map.init(numel, chunk_len(numel, world), tile);

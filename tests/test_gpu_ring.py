@@ -122,6 +122,15 @@ def test_tma_staged_path_ragged_last_chunk(N, S, dtype):
     assert ddp.ddp_device_status() == 0
 
 
+def test_tma_alternating_world_sizes():
+    # the staged path needs a different amount of shared memory per world
+    # size; calls that alternate between larger and smaller needs on the same
+    # kernel must all launch and stay exact
+    for N, S in ((8, 1 << 20), (4, 1 << 20), (8, 1 << 20), (2, 1 << 21), (16, 1 << 19), (8, 1 << 20)):
+        x = workloads.rank_vectors(N, S, "randn", seed0=N).numpy()
+        assert_bits_equal(run_gpu("fused", x, N), oracle_allreduce(x, N), f"N={N}")
+
+
 def test_staged_equals_fused_bitwise_random_shapes():
     rng = np.random.default_rng(0)
     for _ in range(25):
