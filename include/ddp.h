@@ -205,6 +205,38 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
                                        int32_t divisor, void* stream);
 
 /*
+ * ring_allreduce_fused_from_host_noalloc -- ring_allreduce_fused_from_host for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * to this entry point; it exists for callers whose gradients sit in host
+ * memory and who have no device allocator of their own to hand over scratch
+ * buffers (for example a host-side loop inside a framework that owns all of
+ * the device's memory, or a tool that links only this library).
+ *
+ * Instead of caller-provided device buffers, the ranks' copies live in one
+ * array of DDP_STATIC_SCRATCH_BYTES bytes that the library reserves in its own
+ * module: every GPU that loads the library holds that memory until the
+ * process exits.  The call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).  Each rank's copy starts on a 256-byte
+ * boundary, so world * round_up(numel * element size, 256) must not exceed
+ * DDP_STATIC_SCRATCH_BYTES; larger requests return DDP_ERR_CAPACITY before
+ * any CUDA work.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current) and caches it; make
+ * that first call before any stream capture.  All calls on a device share
+ * the array: calls that overlap on the GPU (different streams, or host
+ * threads without ordering) race and corrupt each other's results.  The
+ * array keeps the last call's contents; no clearing is needed, since a call
+ * overwrites every byte it uses before reading it.
+ *
+ * Arguments, copies, results and synchronisation as for
+ * ring_allreduce_fused_from_host, without dev_bufs.
+ */
+#define DDP_STATIC_SCRATCH_BYTES (64ll << 20)   /* 64 MiB per GPU */
+int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const void* const* host_in, void* const* host_out,
+                                               int64_t numel, int32_t dtype, int32_t divisor, void* stream);
+
+/*
  * ddp_grad_accumulate -- one no_sync micro-batch folded into the local
  * gradients of every rank ([P1] section 03 and section 05 step 5; [P2]
  * "梯度累积:正确使用 no_sync"): acc[r][i] <- acc[r][i] + grads[r][i]
