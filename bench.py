@@ -61,7 +61,7 @@ def measured_peak():
 
 def kernel_sources_digest() -> str:
     h = hashlib.sha256()
-    for f in ("ring_kernels.cu", "ddp_device.cuh", "ddp_internal.h"):
+    for f in ("ring_kernels.cu", "ring_tma.cu", "ddp_device.cuh", "ddp_internal.h"):
         with open(os.path.join(ROOT, "gradient_sync_plan_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -323,7 +323,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
            "roofline": {"bound": "hbm", "achieved": hbm, "peak": peak, "unit": "GB/s", "frac": hbm / peak,
                         "traffic": traffic, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                        "kernel": "k_ring_fused", "algorithmic_bytes_per_launch": 2 * N * s_bytes},
+                        "kernel": "k_ring_fused_tma", "algorithmic_bytes_per_launch": 2 * N * s_bytes},
            "gpu_launches": args.steps}
     if sampler:
         out["clocks"] = sampler.summary()
