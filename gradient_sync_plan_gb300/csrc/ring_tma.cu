@@ -1,21 +1,26 @@
-// ring_tma.cu -- fused ring allreduce with TMA bulk copies through shared memory.
+// ring_tma.cu -- fused ring allreduce with TMA bulk copies into shared memory.
 //
 // Same result as k_ring_fused (ring_kernels.cu): element i of chunk j is
 // folded over the ranks starting at rank j+1 ("DDP 与 Ring-AllReduce", §1.3.2;
 // "DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03),
 // divided by the divisor and written to every rank.  What differs is how the
-// bytes move: the bucket is cut into tiles that never cross a chunk boundary;
-// a persistent CTA streams its tiles through a ring of shared-memory stages.
-// For every tile one thread issues N bulk copies (cp.async.bulk, one per
-// rank) that complete on the stage's mbarrier; the CTA folds the N staged
-// copies into one result tile in shared memory; the same thread then issues N
-// bulk stores of that single result tile, one to each rank.  Per tile the
-// threads execute no global load or store instruction at all, which removes
-// the memory-instruction queue pressure of the register path.
+// bytes move.  The bucket is cut into tiles that never cross a chunk
+// boundary; one persistent CTA per SM streams its tiles through a ring of
+// shared-memory stages, with its warps split by role:
+//   * a producer warp: one thread issues, for every tile, N bulk copies
+//     (cp.async.bulk, one per rank) that complete on the stage's "full"
+//     mbarrier, as soon as the consumers have released that stage;
+//   * eight consumer warps: wait for a full stage, fold the N staged copies
+//     in ring order, release the stage on its "empty" mbarrier, and store the
+//     result vector from registers to every rank.
+// No CTA-wide barrier sits in the loop: the producer refills a stage the
+// moment the last consumer warp has read it, which keeps the copy engine's
+// queue full.
 //
 // Waits are bounded: an mbarrier wait that exceeds kWaitLimitNs sets the
-// library's device status word to DDP_ERR_TIMEOUT, waits (again bounded) for
-// the CTA's copies still in flight, and the CTA returns.
+// library's device status word to DDP_ERR_TIMEOUT and the thread stops; the
+// producer then waits (again bounded) for the copies it issued before it
+// returns.
 #include <algorithm>
 #include <cstdio>
 #include <map>
@@ -29,8 +34,10 @@ namespace ddpk {
 
 __device__ int32_t g_device_status = 0;     // sticky DDP_ERR_TIMEOUT flag, read by ddp_device_status()
 
-constexpr int kTmaStages = 3;
-constexpr int kTmaThreads = 256;
+constexpr int kTmaStages = 2;
+constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaThreads = 32 * (kTmaConsumerWarps + 1);    // + one producer warp
+constexpr int kTmaMaxVec = 4;        // 16-byte vectors per consumer thread per tile (tile <= 16 KB)
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <int CAP>
@@ -49,6 +56,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx_bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(tx_bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -88,35 +99,14 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
         : "memory");
 }
 
-// Bulk copy shared -> global, tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Shared-memory writes by the threads must be visible to the async proxy
-// before a bulk store reads them.
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
 // Tiles never cross a chunk boundary: chunk j (length clen, the last one
 // shorter) holds ceil(len / tile) tiles; empty trailing chunks hold none.
+// Tile k is tile q = k mod per_chunk of chunk j = k / per_chunk (the last
+// chunk's tiles are a prefix of that numbering).
 struct TileMap {
     int64_t numel, clen, tile, per_chunk, last_chunk, total;
     __host__ __device__ void init(int64_t n, int64_t c, int64_t t) {
@@ -128,100 +118,132 @@ struct TileMap {
         const int64_t last_len = n - last_chunk * c;
         total = last_chunk * per_chunk + (last_len + t - 1) / t;
     }
-    __device__ void at(int64_t k, int64_t& e0, int64_t& n, int& j) const {
-        j = (int)(k / per_chunk);
-        const int64_t cs = (int64_t)j * clen;
-        const int64_t ce = (cs + clen < numel) ? cs + clen : numel;
-        e0 = cs + (k - (int64_t)j * per_chunk) * tile;
-        n = (ce - e0 < tile) ? ce - e0 : tile;
+};
+
+// A CTA visits tiles k, k + G, k + 2G, ... (G = gridDim.x).  The cursor keeps
+// (j, q) for its current tile and advances by G with adds and one compare:
+// integer division on this path measurably delayed the refills.
+struct TileCursor {
+    int64_t k, j, q;          // tile index, its chunk, its tile within the chunk
+    int64_t step_j, step_q;   // G / per_chunk, G % per_chunk
+    __device__ void start(const TileMap& m, int64_t k0, int64_t g) {
+        k = k0;
+        j = k0 / m.per_chunk;
+        q = k0 - j * m.per_chunk;
+        step_j = g / m.per_chunk;
+        step_q = g - step_j * m.per_chunk;
+    }
+    __device__ void advance(const TileMap& m, int64_t g) {
+        k += g;
+        j += step_j;
+        q += step_q;
+        if (q >= m.per_chunk) {
+            q -= m.per_chunk;
+            ++j;
+        }
+    }
+    // first element and length of the current tile
+    __device__ void range(const TileMap& m, int64_t& e0, int64_t& n) const {
+        const int64_t cs = j * m.clen;
+        const int64_t ce = (cs + m.clen < m.numel) ? cs + m.clen : m.numel;
+        e0 = cs + q * m.tile;
+        n = (ce - e0 < m.tile) ? ce - e0 : m.tile;
     }
 };
 
 template <class E, int DIV, int CAP>
-__global__ void __launch_bounds__(kTmaThreads)
+__global__ void __launch_bounds__(kTmaThreads, 1)
 k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map, float dop) {
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
+    constexpr int kConsumers = 32 * kTmaConsumerWarps;
     extern __shared__ __align__(128) unsigned char smem[];
     const int64_t tile_bytes = map.tile * (int64_t)sizeof(S);
-    unsigned char* stages = smem;                                           // [stages][world][tile]
-    unsigned char* results = smem + (size_t)kTmaStages * world * tile_bytes;  // [2][tile]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(results + 2 * tile_bytes);  // [stages]
-    const bool leader = threadIdx.x == 0;
+    unsigned char* stages = smem;                                                    // [stages][world][tile]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTmaStages * world * tile_bytes);
+    uint64_t* empty = full + kTmaStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
 
-    if (leader) {
-        for (int s = 0; s < kTmaStages; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(&full[s], 1);                     // the producer's expect_tx arrival + bytes
+            mbar_init(&empty[s], kTmaConsumerWarps);    // one arrival per consumer warp
+        }
         fence_barrier_init();
     }
     __syncthreads();
 
-    auto issue = [&](int64_t tile_idx, int s) {
-        int64_t e0, n;
-        int j;
-        map.at(tile_idx, e0, n, j);
-        const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
-        mbar_arrive_expect_tx(&bars[s], bytes * (uint32_t)world);
-        unsigned char* dst = stages + (size_t)s * world * tile_bytes;
-        for (int r = 0; r < world; ++r)
-            bulk_load(dst + (size_t)r * tile_bytes, t.p[r] + e0 * (int64_t)sizeof(S), bytes, &bars[s]);
-    };
-
-    if (leader)
-        for (int s = 0; s < kTmaStages; ++s) {
-            const int64_t k = blockIdx.x + (int64_t)s * gridDim.x;
-            if (k < map.total) issue(k, s);
+    if (warp == kTmaConsumerWarps) {
+        // ---- producer ----
+        if (lane != 0) return;
+        TileCursor ic;
+        ic.start(map, blockIdx.x, G);
+        int it = 0;
+        for (; ic.k < map.total; ic.advance(map, G), ++it) {
+            const int s = it % kTmaStages;
+            // the stage's previous tile (it - kTmaStages) must have been read
+            if (it >= kTmaStages && !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u)) {
+                atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
+                break;
+            }
+            int64_t e0, n;
+            ic.range(map, e0, n);
+            const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
+            mbar_arrive_expect_tx(&full[s], bytes * (uint32_t)world);
+            unsigned char* dst = stages + (size_t)s * world * tile_bytes;
+            for (int r = 0; r < world; ++r)
+                bulk_load(dst + (size_t)r * tile_bytes, t.p[r] + e0 * (int64_t)sizeof(S), bytes, &full[s]);
         }
+        // do not leave while copies into this CTA's shared memory may still
+        // be landing: wait until the consumers have drained the last stages
+        for (int q = 1; q <= kTmaStages && it - q >= 0; ++q) {
+            const int i2 = it - q;
+            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u);
+        }
+        return;
+    }
 
-    int it = 0;
-    bool failed = false;
-    for (int64_t k = blockIdx.x; k < map.total; k += gridDim.x, ++it) {
+    // ---- consumers ----
+    TileCursor cc;
+    cc.start(map, blockIdx.x, G);
+    for (int it = 0; cc.k < map.total; cc.advance(map, G), ++it) {
         const int s = it % kTmaStages;
-        const uint32_t parity = (uint32_t)(it / kTmaStages) & 1u;
         int64_t e0, n;
-        int j;
-        map.at(k, e0, n, j);
-        const bool ok = mbar_wait_bounded(&bars[s], parity);
-        if (!__syncthreads_and(ok)) {
-            failed = true;
+        cc.range(map, e0, n);
+        const int j = (int)cc.j;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u)) {
+            atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
             break;
         }
-        const int rb = it & 1;
-        if (leader) bulk_wait_read<1>();      // result buffer rb was last stored two tiles ago
-        __syncthreads();
         const int start = (j + 1 == world) ? 0 : j + 1;
         const int nv = (int)(n / L);
         const unsigned char* sb = stages + (size_t)s * world * tile_bytes;
-        V* res = reinterpret_cast<V*>(results + rb * tile_bytes);
-        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-            int r = start;
-            V acc = reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v];
-            for (int q = 1; q < world; ++q) {
-                r = (r + 1 == world) ? 0 : r + 1;
-                acc = E::vadd(acc, reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]);
+        V y[kTmaMaxVec];
+#pragma unroll
+        for (int u = 0; u < kTmaMaxVec; ++u) {
+            const int v = threadIdx.x + u * kConsumers;
+            if (v < nv) {
+                int r = start;
+                V acc = reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v];
+                for (int q = 1; q < world; ++q) {
+                    r = (r + 1 == world) ? 0 : r + 1;
+                    acc = E::vadd(acc, reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]);
+                }
+                y[u] = E::template vdiv<DIV>(acc, dop);
             }
-            res[v] = E::template vdiv<DIV>(acc, dop);
         }
-        fence_async_smem();
-        __syncthreads();
-        if (leader) {
-            const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
-            for (int r = 0; r < world; ++r) bulk_store(t.p[r] + e0 * (int64_t)sizeof(S), res, bytes);
-            bulk_commit();
-            const int64_t next = k + (int64_t)kTmaStages * gridDim.x;
-            if (next < map.total) issue(next, s);
-        }
-    }
-    if (failed && leader) {
-        atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
-        // let the loads already issued for this CTA land before it exits
-        for (int q = 0; q < kTmaStages; ++q) {
-            const int it2 = it + q;
-            const int64_t k2 = blockIdx.x + (int64_t)it2 * gridDim.x;
-            if (k2 < map.total) mbar_wait_bounded(&bars[it2 % kTmaStages], (uint32_t)(it2 / kTmaStages) & 1u);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);      // this warp has read stage s
+#pragma unroll
+        for (int u = 0; u < kTmaMaxVec; ++u) {
+            const int v = threadIdx.x + u * kConsumers;
+            if (v < nv)
+                for (int r = 0; r < world; ++r)
+                    st_stream<V>(t.p[r] + e0 * (int64_t)sizeof(S) + (int64_t)v * 16, y[u]);
         }
     }
-    if (leader) bulk_wait_all<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -241,13 +263,13 @@ std::mutex g_tma_mu;
 std::map<std::pair<int, const void*>, FnState> g_tma_fn;
 }  // namespace
 
-// Bytes of one rank's tile: two CTAs per SM share ~220 KB, each CTA holds
-// kTmaStages x world input tiles and two result tiles.  Tiles are powers of
-// two (4 KB for eight ranks): tiles that start on page-sized boundaries
-// stream measurably faster than odd sizes.  0 = path not usable.
+// Bytes of one rank's tile: one CTA per SM holds kTmaStages x world tiles
+// in about 200 KB of shared memory.  Tiles are powers of two (8 KB for eight
+// ranks, at most 16 KB): tiles that start on page-sized boundaries stream
+// measurably faster than odd sizes.  0 = path not usable.
 int64_t tma_tile_bytes(int world) {
-    const int64_t budget = 110 * 1024 - 64;
-    const int64_t fit = budget / ((int64_t)kTmaStages * world + 2);
+    const int64_t budget = 200 * 1024;
+    const int64_t fit = budget / ((int64_t)kTmaStages * world);
     int64_t tb = 16384;
     while (tb > fit) tb >>= 1;
     return tb >= 512 ? tb : 0;
@@ -267,7 +289,7 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
     auto k = k_ring_fused_tma<E, DIV, CAP>;
     const int64_t tile_bytes = tma_tile_bytes(world);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
-    const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * tile_bytes + kTmaStages * sizeof(uint64_t);
+    const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
     int dev = 0;
     cudaGetDevice(&dev);
     int per_sm = 0;
