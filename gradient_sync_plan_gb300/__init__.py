@@ -35,7 +35,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_plan_buckets",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
-           "ring_allreduce_fused_from_host_noalloc",
+           "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
 
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             L.ring_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_fused_from_host.argtypes = [i32, P(vp), P(vp), P(vp), i64, i32, i32, vp]
             L.ring_allreduce_fused_from_host_noalloc.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp]
+            L.ring_allreduce_fused_host_direct.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp]
             L.ddp_grad_accumulate.argtypes = [i32, P(vp), P(vp), i64, i32, vp]
             L.ddp_sync_buckets.argtypes = [i32, i32, P(vp), P(i64), P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                            i32, vp]
@@ -216,6 +217,19 @@ def ring_allreduce_fused_from_host(host_in, host_out, dev_bufs, divisor: int = 0
     _check("ring_allreduce_fused_from_host",
            lib().ring_allreduce_fused_from_host(len(hi), _vp_array(hi), _vp_array(ho), _vp_array(dv), numel, code,
                                                 divisor, _stream(stream)))
+
+
+def ring_allreduce_fused_host_direct(host_in, host_out, divisor: int = 0, stream=None) -> None:
+    """Fused allreduce read from and written to host buffers directly by the
+    kernel (no device copies).  The buffers must be GPU-reachable, e.g.
+    pinned (``tensor.pin_memory()``); host_out may be host_in."""
+    hi, numel, code = _rank_ptrs(host_in)
+    ho, n2, c2 = _rank_ptrs(host_out)
+    if not (numel == n2 and code == c2 and len(hi) == len(ho)):
+        raise ValueError("host_in and host_out must match")
+    _check("ring_allreduce_fused_host_direct",
+           lib().ring_allreduce_fused_host_direct(len(hi), _vp_array(hi), _vp_array(ho), numel, code, divisor,
+                                                  _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 64 << 20     # DDP_STATIC_SCRATCH_BYTES

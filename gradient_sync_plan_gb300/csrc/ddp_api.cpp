@@ -275,6 +275,67 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
     return DDP_OK;
 }
 
+// Device address through which the GPU reaches host buffer p, or nullptr
+// if it cannot reach it: pinned (page-locked, mapped) memory, managed or
+// device memory, and plain pageable memory on systems where the GPU reads
+// pageable memory through the host page tables (coherent CPU-GPU nodes).
+static void* device_view_of(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return const_cast<void*>(p);
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) return nullptr;
+    return pageable ? const_cast<void*>(p) : nullptr;
+}
+
+int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_in, void* const* host_out,
+                                         int64_t numel, int32_t dtype, int32_t divisor, void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
+    if (numel == 0) return DDP_OK;
+    const uintptr_t es = (uintptr_t)elem_bytes(dtype);
+    const uintptr_t bytes = (uintptr_t)numel * es;
+    // inputs pairwise disjoint; each output either is its own input (in
+    // place) or overlaps no input and no other output
+    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+    bool same = true;
+    for (int32_t r = 0; r < world; ++r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(host_in[r]), b = reinterpret_cast<uintptr_t>(host_out[r]);
+        if (!a || !b) return DDP_ERR_INVALID;
+        if (a % es || b % es) return DDP_ERR_ALIGN;
+        if (a != b) same = false;
+        iv.emplace_back(a, a + bytes);
+    }
+    if (!same)
+        for (int32_t r = 0; r < world; ++r) {
+            const uintptr_t b = reinterpret_cast<uintptr_t>(host_out[r]);
+            if (b == reinterpret_cast<uintptr_t>(host_in[r])) {
+                // in place for this rank: nothing else may overlap it (checked via the input ranges)
+                continue;
+            }
+            iv.emplace_back(b, b + bytes);
+        }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
+    std::vector<void*> din(world), dout(world);
+    bool vec = true;
+    for (int32_t r = 0; r < world; ++r) {
+        din[r] = device_view_of(host_in[r]);
+        dout[r] = (host_out[r] == host_in[r]) ? din[r] : device_view_of(host_out[r]);
+        if (!din[r] || !dout[r]) return DDP_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(din[r]) % 16 || reinterpret_cast<uintptr_t>(dout[r]) % 16) vec = false;
+    }
+    return cuda_status(launch_ring_fused_io(world, din.data(), dout.data(), numel, dtype, make_div(divisor), vec,
+                                            (cudaStream_t)stream));
+}
+
 int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* grads, int64_t numel,
                             int32_t dtype, void* stream) {
     int32_t st = common_checks(world, numel, dtype);

@@ -36,6 +36,11 @@ bool debug_enabled();
 // All pointers are device pointers; `ptrs` is a host array of `world` entries.
 cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                               bool vec_ok, cudaStream_t stream);
+// Register path only, out of place: reads in[r], writes the result to out[r]
+// (out[r] == in[r] for in place).  Used for buffers the copy engine must not
+// stage, e.g. host memory the GPU reads directly.
+cudaError_t launch_ring_fused_io(int world, void* const* in, void* const* out, int64_t numel, int dtype, DivSpec div,
+                                 bool vec_ok, cudaStream_t stream);
 cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                bool vec_ok, cudaStream_t stream);
 cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,

@@ -31,6 +31,10 @@ struct RankTable {
 // Fused ring allreduce
 // ---------------------------------------------------------------------------
 
+// The fused kernels read rank r from t.p[r] and write it to t.p[world + r]:
+// an in-place call passes the same pointer twice, an out-of-place call (host
+// buffers read and written directly) two.  The table holds 2 * world entries.
+
 // One element, any alignment: fold in ring order, divide, store to all ranks.
 template <class E, int DIV, int CAP>
 __device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world, int64_t e, int64_t clen,
@@ -40,7 +44,7 @@ __device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world,
     const int start = (j + 1 == world) ? 0 : j + 1;
     auto at = [&](int r) -> const char* { return t.p[r]; };
     S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e), dop);
-    for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = y;
+    for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[world + r])[e] = y;
 }
 
 // Vectorised fused kernel: all rank buffers are 16-byte aligned.  Thread v
@@ -63,7 +67,7 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
             const int start = (j + 1 == world) ? 0 : (int)j + 1;
             const int64_t off = v * 16;
             V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, off), dop);
-            for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
+            for (int r = 0; r < world; ++r) st_stream<V>(t.p[world + r] + off, y);
         } else {
             for (int l = 0; l < L; ++l)
                 if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
@@ -180,12 +184,24 @@ static RankTable<CAP> make_table(int world, void* const* ptrs) {
     return t;
 }
 
+// in + out pointer table of 2 * world entries (see the fused kernels)
+template <int CAP>
+static RankTable<CAP> make_io_table(int world, void* const* in, void* const* out) {
+    RankTable<CAP> t{};
+    for (int r = 0; r < world; ++r) {
+        t.p[r] = static_cast<char*>(in[r]);
+        t.p[world + r] = static_cast<char*>(out[r]);
+    }
+    return t;
+}
+
 template <class E, int DIV, int CAP, int G>
-static cudaError_t fused_vec(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
-    auto k = k_ring_fused<E, DIV, CAP, G>;
+static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64_t numel, float dop,
+                             cudaStream_t st) {
+    auto k = k_ring_fused<E, DIV, 2 * CAP, G>;
     const int64_t nvec = (numel + E::L - 1) / E::L;
     const int grid = grid_for((const void*)k, nvec);
-    k<<<grid, kThreads, 0, st>>>(make_table<CAP>(world, ptrs), world, numel, chunk_len(numel, world), dop);
+    k<<<grid, kThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
     if (debug_enabled())
         fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d G=%d CAP=%d\n", world, (long long)numel,
                 grid, G, CAP);
@@ -193,33 +209,34 @@ static cudaError_t fused_vec(int world, void* const* ptrs, int64_t numel, float 
 }
 
 template <class E, int DIV, int CAP>
-static cudaError_t fused_scalar(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
-    auto k = k_ring_fused_scalar<E, DIV, CAP>;
+static cudaError_t fused_scalar(int world, void* const* in, void* const* out, int64_t numel, float dop,
+                                cudaStream_t st) {
+    auto k = k_ring_fused_scalar<E, DIV, 2 * CAP>;
     const int grid = grid_for((const void*)k, numel);
-    k<<<grid, kThreads, 0, st>>>(make_table<CAP>(world, ptrs), world, numel, chunk_len(numel, world), dop);
+    k<<<grid, kThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
     return cudaGetLastError();
 }
 
 template <class E, int DIV>
-static cudaError_t fused_dispatch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
-                                  cudaStream_t st) {
+static cudaError_t fused_dispatch(int world, void* const* in, void* const* out, int64_t numel, float dop,
+                                  bool vec_ok, cudaStream_t st) {
     if (!vec_ok) {
-        if (world <= 16) return fused_scalar<E, DIV, 16>(world, ptrs, numel, dop, st);
-        return fused_scalar<E, DIV, DDP_MAX_WORLD>(world, ptrs, numel, dop, st);
+        if (world <= 16) return fused_scalar<E, DIV, 16>(world, in, out, numel, dop, st);
+        return fused_scalar<E, DIV, DDP_MAX_WORLD>(world, in, out, numel, dop, st);
     }
-    if (world <= 4) return fused_vec<E, DIV, 16, 4>(world, ptrs, numel, dop, st);
-    if (world <= 8) return fused_vec<E, DIV, 16, 8>(world, ptrs, numel, dop, st);
-    if (world <= 16) return fused_vec<E, DIV, 16, 16>(world, ptrs, numel, dop, st);
-    return fused_vec<E, DIV, DDP_MAX_WORLD, 16>(world, ptrs, numel, dop, st);
+    if (world <= 4) return fused_vec<E, DIV, 16, 4>(world, in, out, numel, dop, st);
+    if (world <= 8) return fused_vec<E, DIV, 16, 8>(world, in, out, numel, dop, st);
+    if (world <= 16) return fused_vec<E, DIV, 16, 16>(world, in, out, numel, dop, st);
+    return fused_vec<E, DIV, DDP_MAX_WORLD, 16>(world, in, out, numel, dop, st);
 }
 
 template <class E>
-static cudaError_t fused_by_div(int world, void* const* ptrs, int64_t numel, DivSpec d, bool vec_ok,
-                                cudaStream_t st) {
+static cudaError_t fused_by_div(int world, void* const* in, void* const* out, int64_t numel, DivSpec d,
+                                bool vec_ok, cudaStream_t st) {
     switch (d.mode) {
-        case kDivNone: return fused_dispatch<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, st);
-        case kDivPow2: return fused_dispatch<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, st);
-        default: return fused_dispatch<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, st);
+        case kDivNone: return fused_dispatch<E, kDivNone>(world, in, out, numel, d.operand, vec_ok, st);
+        case kDivPow2: return fused_dispatch<E, kDivPow2>(world, in, out, numel, d.operand, vec_ok, st);
+        default: return fused_dispatch<E, kDivIeee>(world, in, out, numel, d.operand, vec_ok, st);
     }
 }
 
@@ -227,8 +244,15 @@ cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int d
                               cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
     if (tma_usable(world, numel, dtype, vec_ok)) return launch_ring_fused_tma(world, ptrs, numel, dtype, div, stream);
-    if (dtype == DDP_F32) return fused_by_div<EF32>(world, ptrs, numel, div, vec_ok, stream);
-    return fused_by_div<EBF16>(world, ptrs, numel, div, vec_ok, stream);
+    if (dtype == DDP_F32) return fused_by_div<EF32>(world, ptrs, ptrs, numel, div, vec_ok, stream);
+    return fused_by_div<EBF16>(world, ptrs, ptrs, numel, div, vec_ok, stream);
+}
+
+cudaError_t launch_ring_fused_io(int world, void* const* in, void* const* out, int64_t numel, int dtype, DivSpec div,
+                                 bool vec_ok, cudaStream_t stream) {
+    if (numel == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return fused_by_div<EF32>(world, in, out, numel, div, vec_ok, stream);
+    return fused_by_div<EBF16>(world, in, out, numel, div, vec_ok, stream);
 }
 
 template <class E, int DIV, int CAP>

@@ -205,6 +205,26 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
                                        int32_t divisor, void* stream);
 
 /*
+ * ring_allreduce_fused_host_direct -- the fused allreduce run directly on
+ * host buffers, without device copies: the kernel reads every rank's
+ * elements from host_in[r] over the CPU-GPU link and writes the averaged
+ * result to host_out[r] (host_out[r] may equal host_in[r]).  Result and order
+ * as ring_allreduce_fused ([P1] section 03; [P3] §1.3.2).  Host traffic per
+ * call: world * numel elements read, the same written, in one pass -- both
+ * directions of the link at once, where a copy-based path moves them one
+ * after the other.
+ *
+ * Every buffer must be reachable by the GPU: page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister), managed or device memory, or pageable
+ * memory on systems whose GPU reads pageable memory directly; otherwise
+ * DDP_ERR_INVALID before any work.  Inputs must not overlap; an output must
+ * either be its own input or overlap no input and no other output.
+ * Asynchronous on `stream`: synchronise before reading host_out.
+ */
+int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_in, void* const* host_out,
+                                         int64_t numel, int32_t dtype, int32_t divisor, void* stream);
+
+/*
  * ring_allreduce_fused_from_host_noalloc -- ring_allreduce_fused_from_host for
  * callers that cannot allocate device memory.  The pages have no counterpart
  * to this entry point; it exists for callers whose gradients sit in host

@@ -148,3 +148,16 @@ def test_pack_unpack_view_reject_bad_plans():
     assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), b_of, i64(0), 1, i64(4), _vp(A), 0, 1, 0, None) == -1
     assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), (ctypes.c_int32 * 1)(0), i64(0), 1, i64(4), _vp(A), 0, 1,
                               7, None) == -1      # unknown algorithm
+
+
+def test_host_direct_rejects_aliasing_on_host():
+    L = ddp.lib()
+    A, B, C = 0x7f0000000000, 0x7f0000100000, 0x7f0000200000
+    f = L.ring_allreduce_fused_host_direct
+    assert f(2, _vp(A, B), _vp(B, A), 8, 0, 2, None) == -1        # rank 0 writes rank 1's input
+    assert f(2, _vp(A, B), _vp(C, C), 8, 0, 2, None) == -1        # two outputs on the same memory
+    assert f(2, _vp(A, A + 8), _vp(A, A + 8), 8, 0, 2, None) == -1    # inputs overlap
+    assert f(2, _vp(A, B), _vp(C, C + 2), 8, 0, 2, None) == -2    # fp32 output not 4-byte aligned
+    assert f(2, None, _vp(C, B), 8, 0, 2, None) == -1
+    assert f(2, _vp(A, B), _vp(A, B), 0, 0, 2, None) == 0          # empty: no CUDA work
+

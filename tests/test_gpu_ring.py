@@ -248,6 +248,45 @@ def test_from_host_matches_oracle():
     assert_bits_equal(host_out.numpy(), want, "from_host")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,S", [(3, 6), (8, 1_000_001), (4, 1 << 20), (16, 77_777)])
+def test_host_direct_matches_oracle(dtype, N, S):
+    # the kernel reads pinned host memory and writes the result back to it
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + 7)
+    xh = f32_or_bits(x)
+    want = oracle_allreduce(xh, N)
+    src = x.pin_memory()
+    out = torch.zeros_like(src).pin_memory()
+    ddp.ring_allreduce_fused_host_direct(src, out, N)           # out of place
+    torch.cuda.synchronize()
+    assert_bits_equal(f32_or_bits(out), want, "host direct out of place")
+    assert_bits_equal(f32_or_bits(src), xh, "host direct input untouched")
+    ddp.ring_allreduce_fused_host_direct(src, src, N)           # in place
+    torch.cuda.synchronize()
+    assert_bits_equal(f32_or_bits(src), want, "host direct in place")
+
+
+def test_host_direct_unaligned_and_pageable():
+    N, S = 5, 10_001
+    x = workloads.rank_vectors(N, S, "randn", seed0=2)
+    want = oracle_allreduce(x.numpy(), N)
+    store = torch.zeros((N, S + 4)).pin_memory()
+    rows = [store[r, 1:1 + S] for r in range(N)]                # 4-byte but not 16-byte aligned
+    for r in range(N):
+        rows[r].copy_(x[r])
+    ddp.ring_allreduce_fused_host_direct(rows, rows, N)
+    torch.cuda.synchronize()
+    assert_bits_equal(np.stack([r.numpy() for r in rows]), want, "unaligned pinned")
+    pageable = x.clone()
+    try:
+        ddp.ring_allreduce_fused_host_direct(pageable, pageable, N)
+    except ddp.DDPError as e:
+        assert e.status == -1                                    # this GPU cannot read pageable memory
+    else:
+        torch.cuda.synchronize()
+        assert_bits_equal(pageable.numpy(), want, "pageable")
+
+
 def test_empty_bucket_is_noop():
     x = torch.zeros((4, 0), device="cuda")
     ddp.ring_allreduce_fused(x, 4)
