@@ -365,7 +365,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                    "ms_per_step": c_ms, "steps": e2e_steps,
                                    "api": "ring_allreduce_fused_from_host (cudaMemcpyAsync in, kernel, "
                                           "cudaMemcpyAsync out, one stream)"}
-        out["gpu_launches"] += 2 * (e2e_steps + 1)
+        out["e2e"]["gpu_launches"] = e2e_steps          # one fused kernel per direct call
         del host
 
     # ---- extra measurements ------------------------------------------------
@@ -450,6 +450,63 @@ def ddp_step_bench(ddp, workloads, torch, dev, stream, steps):
     return res
 
 
+def run_sweep(args):
+    """Message-size sweep: 4 KiB .. 256 MiB per rank, fp32 U[-1,1), N = 8 and 64,
+    fused vs staged.  Each point replays a CUDA graph of R back-to-back calls
+    (so the host's call overhead is not timed); buffers below the L2 size stay
+    resident between calls, which is the latency regime the sweep exposes.
+    One JSON line per point."""
+    import torch
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ddp.lib()
+    for N in (8, 64):
+        for k in range(17):
+            S = 1024 << k
+            s_bytes = S * 4
+            x = torch.empty((N, S), dtype=torch.float32, device=dev)
+            for r in range(N):
+                x[r].copy_(workloads.uniform_pm1_f32(S, r, device=str(dev)))
+            reps = int(max(2, min(200, (1 << 28) // (N * S))))
+            row = {"sweep": "message size", "ranks": N, "bytes_per_rank": s_bytes, "reps_per_graph": reps}
+            status = torch.zeros(2, dtype=torch.int32, device=dev)
+            persistent = lambda b, d: ddp.ring_allreduce_persistent(b, d, status=status)   # noqa: E731
+            for name, fn in (("fused", ddp.ring_allreduce_fused), ("staged", ddp.ring_allreduce_staged),
+                             ("persistent", persistent)):
+                s = torch.cuda.Stream()
+                with torch.cuda.stream(s):
+                    for _ in range(3):
+                        fn(x, N)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    for _ in range(reps):
+                        fn(x, N)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                best = None
+                for _ in range(3):
+                    e0.record()
+                    g.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    t = e0.elapsed_time(e1) / reps
+                    best = t if best is None else min(best, t)
+                alg = (2 * N * s_bytes) if name == "fused" else (5 * (N - 1) * s_bytes)
+                row[name] = {"us_per_call": best * 1e3, "busbw_gbs": 2 * (N - 1) / N * s_bytes / (best / 1e3) / 1e9,
+                             "hbm_alg_gbs": alg / (best / 1e3) / 1e9,
+                             "launches_per_call": 2 * (N - 1) if name == "staged" else 1}
+                if name == "persistent":
+                    assert int(status[0]) == 0, "persistent ring reported a barrier timeout"
+                del g
+            print(json.dumps(row), flush=True)
+            del x
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,6 +520,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.steps >= 10:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -478,6 +536,9 @@ def main():
             dist.init_process_group("nccl")
         else:
             dist.init_process_group("gloo")
+    if args.sweep:
+        run_sweep(args)
+        return
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)

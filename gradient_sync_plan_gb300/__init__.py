@@ -34,7 +34,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_plan_buckets",
-           "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_fused_from_host",
+           "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
 
@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ring_allreduce_fused.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
+            L.ring_allreduce_persistent.argtypes = [i32, P(vp), i64, i32, i32, vp, i32, i32, vp]
             L.ring_allreduce_fused_from_host.argtypes = [i32, P(vp), P(vp), P(vp), i64, i32, i32, vp]
             L.ring_allreduce_fused_from_host_noalloc.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp]
             L.ring_allreduce_fused_host_direct.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp]
@@ -205,6 +206,23 @@ def ring_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
     ptrs, numel, code = _rank_ptrs(bufs)
     _check("ring_allreduce_staged", lib().ring_allreduce_staged(len(ptrs), _vp_array(ptrs), numel, code, divisor,
                                                                 _stream(stream)))
+
+
+def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step: int = -1, wait_limit_ms: int = 0,
+                              stream=None):
+    """Staged ring in one cooperative launch with bounded barriers.
+
+    status: a device int32 tensor of >= 2 elements (allocated here if None and
+    returned); status[0] holds DDP_OK (0) or DDP_ERR_TIMEOUT (-4) once the
+    stream has run the kernel."""
+    ptrs, numel, code = _rank_ptrs(bufs)
+    torch = _torch()
+    if status is None:
+        status = torch.zeros(2, dtype=torch.int32, device=_rank_tensors(bufs)[0].device)
+    _check("ring_allreduce_persistent",
+           lib().ring_allreduce_persistent(len(ptrs), _vp_array(ptrs), numel, code, divisor, status.data_ptr(),
+                                           fail_at_step, wait_limit_ms, _stream(stream)))
+    return status
 
 
 def ring_allreduce_fused_from_host(host_in, host_out, dev_bufs, divisor: int = 0, stream=None) -> None:

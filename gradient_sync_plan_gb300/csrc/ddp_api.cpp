@@ -250,6 +250,28 @@ int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, i
     return cuda_status(launch_ring_staged(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
 }
 
+int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                                  int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (divisor < 0 || !dev_status || wait_limit_ms < 0) return DDP_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(dev_status) % 8) return DDP_ERR_ALIGN;
+    if (fail_at_step < -1 || (fail_at_step >= 0 && fail_at_step > 2 * (world - 1) - 2)) return DDP_ERR_INVALID;
+    cudaStream_t s = (cudaStream_t)stream;
+    bool vec = false;
+    if (numel > 0 && (st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
+    if (numel == 0 || world == 1) {
+        // no ring step to wait on: clear the status word, and for one rank divide
+        cudaError_t e = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (numel == 0) return DDP_OK;
+        return cuda_status(launch_ring_fused(world, bufs, numel, dtype, make_div(divisor), vec, s));
+    }
+    const unsigned long long limit = (unsigned long long)(wait_limit_ms ? wait_limit_ms : 2000) * 1000000ull;
+    return cuda_status(launch_ring_persistent(world, bufs, numel, dtype, make_div(divisor), vec, dev_status,
+                                              fail_at_step, limit, s));
+}
+
 int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,
                                        void* const* dev_bufs, int64_t numel, int32_t dtype, int32_t divisor,
                                        void* stream) {

@@ -43,6 +43,10 @@ cudaError_t launch_ring_fused_io(int world, void* const* in, void* const* out, i
                                  bool vec_ok, cudaStream_t stream);
 cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                bool vec_ok, cudaStream_t stream);
+// Staged ring in one cooperative launch with bounded grid barriers
+// (ring_persistent.cu).  ws: device int32[2] = {status, arrivals}.
+cudaError_t launch_ring_persistent(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
+                                   int32_t* ws, int skip_step, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,
                               bool vec_ok, cudaStream_t stream);
 

@@ -1,0 +1,220 @@
+// ring_persistent.cu -- the staged ring in one persistent, cooperative launch.
+//
+// Same steps as k_ring_hop ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce
+// 就完事", section 03; "DDP 与 Ring-AllReduce", §1.3.2): N-1 reduce-scatter
+// steps then N-1 all-gather steps, each moving for every rank the chunk the
+// ring moves in that step.  Instead of one launch per step, one cooperative
+// launch runs all 2(N-1) steps, separated by grid-wide barriers.  This removes
+// the per-step launch latency that dominates small buckets.
+//
+// The barrier is where a real ring hangs when a rank never joins a collective
+// ("Day 17 · 梯度的集体行动", "为什么 DDP 会卡住不报错").  Here every wait is
+// bounded: a block that has waited longer than the limit writes
+// DDP_ERR_TIMEOUT into the caller's device status word and returns, and the
+// context stays usable.  `skip_step` plants exactly that failure for tests:
+// block 0 does not arrive at the barrier that ends step skip_step.
+#include <algorithm>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "ddp_device.cuh"
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+template <int CAP>
+struct PTable {
+    char* p[CAP];
+};
+
+__device__ __forceinline__ unsigned long long pers_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// L2-coherent loads: a value written by another SM in an earlier step must
+// not come from this SM's L1.
+template <class V>
+__device__ __forceinline__ V ld_l2(const void* p) { return __ldcg(reinterpret_cast<const V*>(p)); }
+template <class S>
+__device__ __forceinline__ S ld_l2_scalar(const S* p);
+template <>
+__device__ __forceinline__ float ld_l2_scalar<float>(const float* p) { return __ldcg(p); }
+template <>
+__device__ __forceinline__ uint16_t ld_l2_scalar<uint16_t>(const uint16_t* p) {
+    return (uint16_t)__ldcg(reinterpret_cast<const unsigned short*>(p));
+}
+
+// Grid barrier number `k` (0-based): every block adds one arrival to
+// *counter and waits until all gridDim.x * (k + 1) arrivals are in.  False if
+// the wait ran past limit_ns.
+__device__ __forceinline__ bool grid_barrier(unsigned int* counter, unsigned int k, bool arrive,
+                                             unsigned long long limit_ns) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (arrive) atomicAdd(counter, 1u);
+        const unsigned int target = gridDim.x * (k + 1);
+        const unsigned long long t0 = pers_ns();
+        int ok = 1;
+        while (*reinterpret_cast<volatile unsigned int*>(counter) < target) {
+            if (pers_ns() - t0 > limit_ns) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+template <class E, int DIV, int CAP>
+__device__ __forceinline__ void hop_all_ranks(const PTable<CAP>& t, int world, int64_t numel, int64_t clen, int phase,
+                                              int s, bool divide, bool vec_ok, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int r = 0; r < world; ++r) {
+        const int left = (r == 0) ? world - 1 : r - 1;
+        int c = (phase == 0) ? (r - s - 1) : (r - s);
+        c %= world;
+        if (c < 0) c += world;
+        const int64_t lo = min((int64_t)c * clen, numel);
+        const int64_t hi = min(lo + clen, numel);
+        char* dst = t.p[r];
+        const char* src = t.p[left];
+        if (vec_ok) {
+            for (int64_t q = lo / L + tid; q * L < hi; q += stride) {
+                const int64_t i = q * L;
+                if (i >= lo && i + L <= hi) {
+                    V m = ld_l2<V>(src + q * 16);
+                    if (phase == 0) {
+                        m = E::vadd(ld_l2<V>(dst + q * 16), m);
+                        if (divide) m = E::template vdiv<DIV>(m, dop);
+                    }
+                    *reinterpret_cast<V*>(dst + q * 16) = m;
+                } else {
+                    for (int l = 0; l < L; ++l) {
+                        const int64_t e = i + l;
+                        if (e < lo || e >= hi) continue;
+                        S m = ld_l2_scalar<S>(reinterpret_cast<const S*>(src) + e);
+                        if (phase == 0) {
+                            m = E::sadd(ld_l2_scalar<S>(reinterpret_cast<const S*>(dst) + e), m);
+                            if (divide) m = E::template sdiv<DIV>(m, dop);
+                        }
+                        reinterpret_cast<S*>(dst)[e] = m;
+                    }
+                }
+            }
+        } else {
+            for (int64_t e = lo + tid; e < hi; e += stride) {
+                S m = ld_l2_scalar<S>(reinterpret_cast<const S*>(src) + e);
+                if (phase == 0) {
+                    m = E::sadd(ld_l2_scalar<S>(reinterpret_cast<const S*>(dst) + e), m);
+                    if (divide) m = E::template sdiv<DIV>(m, dop);
+                }
+                reinterpret_cast<S*>(dst)[e] = m;
+            }
+        }
+    }
+}
+
+// ws[0]: status word (DDP_OK / DDP_ERR_TIMEOUT), ws[1]: barrier arrivals.
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_ring_persistent(const __grid_constant__ PTable<CAP> t, int world, int64_t numel, int64_t clen, int vec_ok,
+                  float dop, int32_t* ws, int skip_step, unsigned long long limit_ns) {
+    unsigned int* counter = reinterpret_cast<unsigned int*>(ws + 1);
+    const int steps = 2 * (world - 1);
+    for (int step = 0; step < steps; ++step) {
+        const int phase = step < world - 1 ? 0 : 1;
+        const int s = phase == 0 ? step + 1 : step - (world - 1) + 1;
+        const bool divide = (DIV != kDivNone) && phase == 0 && s == world - 1;
+        hop_all_ranks<E, DIV, CAP>(t, world, numel, clen, phase, s, divide, vec_ok != 0, dop);
+        if (step + 1 == steps) break;                 // the kernel's end orders the last step
+        const bool arrive = !(blockIdx.x == 0 && step == skip_step);
+        if (!grid_barrier(counter, (unsigned int)step, arrive, limit_ns)) {
+            if (threadIdx.x == 0) atomicExch(ws, (int32_t)DDP_ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+namespace {
+std::mutex g_pers_mu;
+std::map<std::pair<int, const void*>, int> g_pers_occ;
+}  // namespace
+
+template <class E, int DIV, int CAP>
+static cudaError_t pers_launch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok, int32_t* ws,
+                               int skip_step, unsigned long long limit_ns, cudaStream_t st) {
+    auto k = k_ring_persistent<E, DIV, CAP>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_pers_mu);
+        auto it = g_pers_occ.find(std::make_pair(dev, (const void*)k));
+        if (it != g_pers_occ.end()) per_sm = it->second;
+    }
+    if (per_sm == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (per_sm <= 0) per_sm = 1;
+        std::lock_guard<std::mutex> lk(g_pers_mu);
+        g_pers_occ[std::make_pair(dev, (const void*)k)] = per_sm;
+    }
+    // every block must be resident at once (cooperative launch); no more
+    // blocks than one step's widest chunk needs
+    const int64_t clen = chunk_len(numel, world);
+    const int64_t per_step = world * ((clen + E::L - 1) / E::L + 1);
+    const int64_t need = std::max<int64_t>(1, (per_step + kThreads - 1) / kThreads);
+    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * std::min(per_sm, 2), need);
+    // zero the status word and the arrival counter before the launch
+    cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+    PTable<CAP> tab{};
+    for (int r = 0; r < world; ++r) tab.p[r] = static_cast<char*>(ptrs[r]);
+    int vec = vec_ok ? 1 : 0;
+    void* args[] = {(void*)&tab, (void*)&world, (void*)&numel, (void*)&clen, (void*)&vec,
+                    (void*)&dop,  (void*)&ws,   (void*)&skip_step, (void*)&limit_ns};
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kThreads), args, 0, st);
+    if (debug_enabled())
+        fprintf(stderr, "[ddp] ring_persistent world=%d numel=%lld grid=%d steps=%d\n", world, (long long)numel,
+                grid, 2 * (world - 1));
+    return e;
+}
+
+template <class E, int DIV>
+static cudaError_t pers_cap(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok, int32_t* ws,
+                            int skip, unsigned long long lim, cudaStream_t st) {
+    if (world <= 16) return pers_launch<E, DIV, 16>(world, ptrs, numel, dop, vec_ok, ws, skip, lim, st);
+    return pers_launch<E, DIV, DDP_MAX_WORLD>(world, ptrs, numel, dop, vec_ok, ws, skip, lim, st);
+}
+
+template <class E>
+static cudaError_t pers_div(int world, void* const* ptrs, int64_t numel, DivSpec d, bool vec_ok, int32_t* ws,
+                            int skip, unsigned long long lim, cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return pers_cap<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, ws, skip, lim, st);
+        case kDivPow2: return pers_cap<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, ws, skip, lim, st);
+        default: return pers_cap<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, ws, skip, lim, st);
+    }
+}
+
+cudaError_t launch_ring_persistent(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
+                                   int32_t* ws, int skip_step, unsigned long long limit_ns, cudaStream_t stream) {
+    if (dtype == DDP_F32) return pers_div<EF32>(world, ptrs, numel, div, vec_ok, ws, skip_step, limit_ns, stream);
+    return pers_div<EBF16>(world, ptrs, numel, div, vec_ok, ws, skip_step, limit_ns, stream);
+}
+
+}  // namespace ddpk

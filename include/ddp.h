@@ -192,6 +192,31 @@ int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, i
                               int32_t divisor, void* stream);
 
 /*
+ * ring_allreduce_persistent -- ring_allreduce_staged in ONE cooperative
+ * launch: the same 2(N-1) steps and the same bit-identical result ([P1]
+ * section 03; [P3] §1.3.2), with the steps separated by grid-wide barriers
+ * instead of kernel launches, which removes the per-step launch latency on
+ * small buckets.
+ *
+ * A real ring hangs when one rank never joins a step ([P2] "常见疑问", on why
+ * DDP can hang without an error).  Here every barrier wait is bounded by
+ * wait_limit_ms (0 = 2000 ms): a block that waits longer writes
+ * DDP_ERR_TIMEOUT to dev_status[0] and returns, so the context stays usable
+ * and the buffers hold a partial result.
+ *
+ *   dev_status   device int32[2], 8-byte aligned, caller-owned: [0] status
+ *                (DDP_OK or DDP_ERR_TIMEOUT after the kernel), [1] barrier
+ *                arrivals.  Both are zeroed on `stream` before the launch; read
+ *                [0] after synchronising.  Concurrent calls need separate words.
+ *   fail_at_step -1 for normal use.  k in [0, 2(N-1)-2] plants a failure for
+ *                testing: one block never arrives at the barrier that ends
+ *                step k, so every block times out there.
+ * Other arguments as for ring_allreduce_fused.
+ */
+int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                                  int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream);
+
+/*
  * ring_allreduce_fused_from_host -- ring_allreduce_fused for callers whose
  * gradients are in host memory: per rank, host_in[r] is copied to dev_bufs[r],
  * the fused allreduce runs, and the result is copied to host_out[r]

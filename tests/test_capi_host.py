@@ -161,3 +161,16 @@ def test_host_direct_rejects_aliasing_on_host():
     assert f(2, None, _vp(C, B), 8, 0, 2, None) == -1
     assert f(2, _vp(A, B), _vp(A, B), 0, 0, 2, None) == 0          # empty: no CUDA work
 
+
+def test_persistent_rejects_bad_arguments_on_host():
+    L = ddp.lib()
+    A, B, W = 0x7f0000000000, 0x7f0000100000, 0x7f0000200000
+    f = L.ring_allreduce_persistent
+    i32p = ctypes.c_void_p(W)
+    assert f(2, _vp(A, B), 8, 0, 2, None, -1, 0, None) == -1                       # no status word
+    assert f(2, _vp(A, B), 8, 0, 2, ctypes.c_void_p(W + 4), -1, 0, None) == -2     # status not 8-byte aligned
+    assert f(3, _vp(A, B, A + 4096), 8, 0, 3, i32p, 4, 0, None) == -1             # step 4 > 2(N-1)-2 = 2
+    assert f(3, _vp(A, B, A + 4096), 8, 0, 3, i32p, -2, 0, None) == -1
+    assert f(2, _vp(A, B), 8, 0, 2, i32p, -1, -5, None) == -1                      # negative wait limit
+    assert f(2, _vp(A, A + 4), 8, 0, 2, i32p, -1, 0, None) == -1                   # overlapping ranks
+

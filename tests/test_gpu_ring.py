@@ -23,7 +23,13 @@ from gpu_util import (assert_bits_equal, chunk_index, f32_or_bits, from_np, orac
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = {"fused": ddp.ring_allreduce_fused, "staged": ddp.ring_allreduce_staged}
+def _persistent(x, divisor):
+    st = ddp.ring_allreduce_persistent(x, divisor)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0, f"persistent ring status {int(st[0])}"
+
+
+KERNELS = {"fused": ddp.ring_allreduce_fused, "staged": ddp.ring_allreduce_staged, "persistent": _persistent}
 
 
 def run_gpu(kernel: str, x_host: np.ndarray, divisor: int) -> np.ndarray:
@@ -33,7 +39,7 @@ def run_gpu(kernel: str, x_host: np.ndarray, divisor: int) -> np.ndarray:
     return f32_or_bits(x)
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_worked_example(kernel):
     k = np.arange(6, dtype=np.float32)
     x = np.stack([k + 1, 10 * (k + 1), 100 * (k + 1)]).astype(np.float32)
@@ -43,7 +49,7 @@ def test_worked_example(kernel):
     assert_bits_equal(got, oracle_allreduce(x, 3), kernel)
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_order_pins(kernel):
     for N in (3, 4):
         x = np.zeros((N, N), dtype=np.float32)
@@ -61,7 +67,7 @@ def test_order_pins(kernel):
     assert np.all(oracle.bf16_to_f32(got) == 4.0)
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_exhaustive_small(kernel, dtype):
     for N in range(1, 10):
@@ -72,7 +78,7 @@ def test_exhaustive_small(kernel, dtype):
                 assert_bits_equal(run_gpu(kernel, xh, div), oracle_allreduce(xh, div), f"{kernel} N={N} S={S}")
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("N,S,div", [(2, 1_000_003, 2), (3, 3 * 65536 + 5, 3), (5, 777_777, 5), (7, 1 << 20, 7),
                                      (8, (1 << 21) + 13, 8), (16, 1_048_583, 16), (6, 99_991, 0), (4, 4096, 1)])
@@ -82,7 +88,7 @@ def test_many_tiles_ragged(kernel, dtype, N, S, div):
     assert_bits_equal(run_gpu(kernel, xh, div), oracle_allreduce(xh, div), f"{kernel} {dtype} N={N} S={S}")
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_unaligned_buffers_take_elementwise_path(kernel, dtype):
     # rank rows start 1 element into 16-byte-aligned storage: element aligned
@@ -146,7 +152,7 @@ def test_staged_equals_fused_bitwise_random_shapes():
                            b.view(torch.int16) if dtype == "bf16" else b.view(torch.int32))
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_config_n4_one_mi_fp32_full(kernel):
     # one bucket of 1,048,576 fp32 per rank, N(0,1) from seed r, divide by 4
     N, S = 4, 1 << 20
@@ -192,7 +198,7 @@ def _sampled_check(kernel, N, S, dtype, kind, std, divisor, k_random=4000):
     del x, ref64
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_config_n8_one_gib_fp32_sampled(kernel):
     # N = 8, 268,435,456 fp32 per rank, N(0, 1e-2^2), divide by 8
     _sampled_check(kernel, 8, 1 << 28, "f32", "randn", 1e-2, 8)
@@ -207,15 +213,15 @@ def test_message_size_sweep(N, kb):
     S = kb * 1024 // 4
     if kb <= 1024:
         x = workloads.rank_vectors(N, S, "uniform").numpy()
-        for kernel in ("fused", "staged"):
+        for kernel in ("fused", "staged", "persistent"):
             assert_bits_equal(run_gpu(kernel, x, N), oracle_allreduce(x, N), f"{kernel} N={N} {kb}KiB")
     else:
-        for kernel in ("fused", "staged"):
+        for kernel in ("fused", "staged", "persistent"):
             _sampled_check(kernel, N, S, "f32", "uniform", 1.0, N, k_random=2000)
             torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_bf16_n16_large_sampled(kernel):
     _sampled_check(kernel, 16, 25_557_032 // 2 + 3, "bf16", "randn", 1e-2, 16)
 
@@ -287,11 +293,41 @@ def test_host_direct_unaligned_and_pageable():
         assert_bits_equal(pageable.numpy(), want, "pageable")
 
 
+def test_persistent_barrier_timeout_is_reported_and_context_survives():
+    # a planted missing arrival at the barrier ending step 1: every block
+    # waits 200 ms, reports DDP_ERR_TIMEOUT and returns
+    import time
+    N, S = 4, 1 << 16
+    x = workloads.rank_vectors(N, S, "randn", seed0=9).cuda()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = ddp.ring_allreduce_persistent(x, N, fail_at_step=1, wait_limit_ms=200)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st[0]) == -4
+    assert 0.15 < dt < 5.0
+    # the context is still usable and exact afterwards
+    y = workloads.rank_vectors(N, S, "randn", seed0=10).numpy()
+    for kernel in ("fused", "persistent"):
+        assert_bits_equal(run_gpu(kernel, y, N), oracle_allreduce(y, N), f"after timeout: {kernel}")
+
+
+def test_persistent_status_word_is_cleared_on_each_call():
+    N, S = 3, 1000
+    x = workloads.rank_vectors(N, S, "randn", seed0=1).cuda()
+    st = torch.full((2,), -4, dtype=torch.int32, device="cuda")
+    ddp.ring_allreduce_persistent(x, N, status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+
+
 def test_empty_bucket_is_noop():
     x = torch.zeros((4, 0), device="cuda")
     ddp.ring_allreduce_fused(x, 4)
     ddp.ring_allreduce_staged(x, 4)
+    st = ddp.ring_allreduce_persistent(x, 4)
     torch.cuda.synchronize()
+    assert int(st[0]) == 0
 
 
 def test_single_rank_divides_only():
