@@ -75,54 +75,145 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, unsigned int
     return s_ok != 0;
 }
 
+// Chunk range of rank r's receive in step s of `phase`.
+__device__ __forceinline__ void hop_range(int world, int64_t numel, int64_t clen, int phase, int s, int r,
+                                          int64_t& lo, int64_t& hi) {
+    int c = (phase == 0) ? (r - s - 1) : (r - s);
+    c %= world;
+    if (c < 0) c += world;
+    lo = min((int64_t)c * clen, numel);
+    hi = min(lo + clen, numel);
+}
+
+// One element of one rank's step (any alignment).
+template <class E, int DIV>
+__device__ __forceinline__ void hop_element(char* dst, const char* src, int64_t e, int phase, bool divide,
+                                            float dop) {
+    using S = typename E::S;
+    S m = ld_l2_scalar<S>(reinterpret_cast<const S*>(src) + e);
+    if (phase == 0) {
+        m = E::sadd(ld_l2_scalar<S>(reinterpret_cast<const S*>(dst) + e), m);
+        if (divide) m = E::template sdiv<DIV>(m, dop);
+    }
+    reinterpret_cast<S*>(dst)[e] = m;
+}
+
+// One ring step for every rank at once.  The work items are (rank, 16-byte
+// slot) pairs numbered rank-major, spread over all threads of the grid, so
+// that the ranks are processed side by side; each thread takes kPersUnroll
+// items per round and issues all their loads before any store.
+constexpr int kPersUnroll = 4;
+
 template <class E, int DIV, int CAP>
 __device__ __forceinline__ void hop_all_ranks(const PTable<CAP>& t, int world, int64_t numel, int64_t clen, int phase,
                                               int s, bool divide, bool vec_ok, float dop) {
     using V = typename E::V;
-    using S = typename E::S;
     constexpr int L = E::L;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (int r = 0; r < world; ++r) {
-        const int left = (r == 0) ? world - 1 : r - 1;
-        int c = (phase == 0) ? (r - s - 1) : (r - s);
-        c %= world;
-        if (c < 0) c += world;
-        const int64_t lo = min((int64_t)c * clen, numel);
-        const int64_t hi = min(lo + clen, numel);
+    if (!vec_ok) {
+        const int64_t items = (int64_t)world * clen;
+        for (int64_t idx = tid; idx < items; idx += nthreads) {
+            const int r = (int)(idx / clen);
+            int64_t lo, hi;
+            hop_range(world, numel, clen, phase, s, r, lo, hi);
+            const int64_t e = lo + (idx - (int64_t)r * clen);
+            if (e < hi) hop_element<E, DIV>(t.p[r], t.p[r == 0 ? world - 1 : r - 1], e, phase, divide, dop);
+        }
+        return;
+    }
+    if (gridDim.x >= (unsigned)world) {
+        // enough blocks: rank r gets blocks [r*bpr, (r+1)*bpr) and strides over
+        // its chunk with no per-item division
+        const int bpr = gridDim.x / world;
+        const int r = blockIdx.x / bpr;
+        if (r >= world) return;
+        int64_t lo, hi;
+        hop_range(world, numel, clen, phase, s, r, lo, hi);
+        if (lo >= hi) return;
         char* dst = t.p[r];
-        const char* src = t.p[left];
-        if (vec_ok) {
-            for (int64_t q = lo / L + tid; q * L < hi; q += stride) {
+        const char* src = t.p[r == 0 ? world - 1 : r - 1];
+        const int64_t lt = (int64_t)(blockIdx.x - r * bpr) * blockDim.x + threadIdx.x;
+        const int64_t gstride = (int64_t)bpr * blockDim.x;
+        const int64_t q0 = lo / L, q1 = (hi - 1) / L;          // slots touching [lo, hi)
+        for (int64_t qb = q0 + lt; qb <= q1; qb += gstride * kPersUnroll) {
+            V m[kPersUnroll], d[kPersUnroll];
+            int kind[kPersUnroll];
+#pragma unroll
+            for (int u = 0; u < kPersUnroll; ++u) {
+                const int64_t q = qb + (int64_t)u * gstride;
                 const int64_t i = q * L;
-                if (i >= lo && i + L <= hi) {
-                    V m = ld_l2<V>(src + q * 16);
+                kind[u] = (q > q1) ? 0 : ((i >= lo && i + L <= hi) ? 1 : 2);
+                if (kind[u] == 1) {
+                    m[u] = ld_l2<V>(src + q * 16);
+                    if (phase == 0) d[u] = ld_l2<V>(dst + q * 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPersUnroll; ++u) {
+                const int64_t q = qb + (int64_t)u * gstride;
+                if (kind[u] == 1) {
+                    V v = m[u];
                     if (phase == 0) {
-                        m = E::vadd(ld_l2<V>(dst + q * 16), m);
-                        if (divide) m = E::template vdiv<DIV>(m, dop);
+                        v = E::vadd(d[u], v);
+                        if (divide) v = E::template vdiv<DIV>(v, dop);
                     }
-                    *reinterpret_cast<V*>(dst + q * 16) = m;
-                } else {
+                    *reinterpret_cast<V*>(dst + q * 16) = v;
+                } else if (kind[u] == 2) {
                     for (int l = 0; l < L; ++l) {
-                        const int64_t e = i + l;
-                        if (e < lo || e >= hi) continue;
-                        S m = ld_l2_scalar<S>(reinterpret_cast<const S*>(src) + e);
-                        if (phase == 0) {
-                            m = E::sadd(ld_l2_scalar<S>(reinterpret_cast<const S*>(dst) + e), m);
-                            if (divide) m = E::template sdiv<DIV>(m, dop);
-                        }
-                        reinterpret_cast<S*>(dst)[e] = m;
+                        const int64_t e = q * L + l;
+                        if (e >= lo && e < hi) hop_element<E, DIV>(dst, src, e, phase, divide, dop);
                     }
                 }
             }
-        } else {
-            for (int64_t e = lo + tid; e < hi; e += stride) {
-                S m = ld_l2_scalar<S>(reinterpret_cast<const S*>(src) + e);
+        }
+        return;
+    }
+    const int64_t spr = (clen + L - 1) / L + 1;          // slots that can touch one chunk
+    const int64_t items = (int64_t)world * spr;
+    for (int64_t base = tid; base < items; base += nthreads * kPersUnroll) {
+        V m[kPersUnroll], d[kPersUnroll];
+        int64_t q[kPersUnroll], lo[kPersUnroll], hi[kPersUnroll];
+        int rk[kPersUnroll];
+        int kind[kPersUnroll];                          // 0 none, 1 full vector, 2 partial
+#pragma unroll
+        for (int u = 0; u < kPersUnroll; ++u) {
+            const int64_t idx = base + (int64_t)u * nthreads;
+            kind[u] = 0;
+            if (idx >= items) continue;
+            const int r = (int)(idx / spr);
+            rk[u] = r;
+            hop_range(world, numel, clen, phase, s, r, lo[u], hi[u]);
+            q[u] = lo[u] / L + (idx - (int64_t)r * spr);
+            const int64_t i = q[u] * L;
+            if (lo[u] >= hi[u] || i >= hi[u]) continue;
+            if (i >= lo[u] && i + L <= hi[u]) {
+                kind[u] = 1;
+                const char* src = t.p[r == 0 ? world - 1 : r - 1];
+                m[u] = ld_l2<V>(src + q[u] * 16);
+                if (phase == 0) d[u] = ld_l2<V>(t.p[r] + q[u] * 16);
+            } else {
+                kind[u] = 2;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPersUnroll; ++u) {
+            if (kind[u] == 0) continue;
+            const int r = rk[u];
+            char* dst = t.p[r];
+            if (kind[u] == 1) {
+                V v = m[u];
                 if (phase == 0) {
-                    m = E::sadd(ld_l2_scalar<S>(reinterpret_cast<const S*>(dst) + e), m);
-                    if (divide) m = E::template sdiv<DIV>(m, dop);
+                    v = E::vadd(d[u], v);
+                    if (divide) v = E::template vdiv<DIV>(v, dop);
                 }
-                reinterpret_cast<S*>(dst)[e] = m;
+                *reinterpret_cast<V*>(dst + q[u] * 16) = v;
+            } else {
+                const char* src = t.p[r == 0 ? world - 1 : r - 1];
+                for (int l = 0; l < L; ++l) {
+                    const int64_t e = q[u] * L + l;
+                    if (e >= lo[u] && e < hi[u]) hop_element<E, DIV>(dst, src, e, phase, divide, dop);
+                }
             }
         }
     }
@@ -174,11 +265,11 @@ static cudaError_t pers_launch(int world, void* const* ptrs, int64_t numel, floa
         g_pers_occ[std::make_pair(dev, (const void*)k)] = per_sm;
     }
     // every block must be resident at once (cooperative launch); no more
-    // blocks than one step's widest chunk needs
+    // blocks than one step's items need
     const int64_t clen = chunk_len(numel, world);
-    const int64_t per_step = world * ((clen + E::L - 1) / E::L + 1);
+    const int64_t per_step = vec_ok ? world * ((clen + E::L - 1) / E::L + 1) : world * clen;
     const int64_t need = std::max<int64_t>(1, (per_step + kThreads - 1) / kThreads);
-    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * std::min(per_sm, 2), need);
+    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * per_sm, need);
     // zero the status word and the arrival counter before the launch
     cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
