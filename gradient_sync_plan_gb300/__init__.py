@@ -25,6 +25,7 @@ BF16 = 1
 DDP_ALGO_FUSED = 0
 DDP_ALGO_STAGED = 1
 DDP_ALGO_VIEW = 2
+DDP_ALGO_DRYRUN = 3
 DDP_MAX_WORLD = 512
 FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
 BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
@@ -36,7 +37,9 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_plan_buckets",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
-           "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view"]
+           "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view",
+           "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
+           "ddp_reducer_launch_order", "ddp_reducer_destroy"]
 
 
 class DDPError(RuntimeError):
@@ -85,6 +88,13 @@ def lib() -> ctypes.CDLL:
             L.ddp_sync_buckets.argtypes = [i32, i32, P(vp), P(i64), P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                            i32, vp]
             L.ddp_bucket_allreduce_view.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, i32, vp]
+            L.ddp_reducer_create.argtypes = [i32, i32, P(vp), P(i64), i32, P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
+                                             vp, P(vp)]
+            L.ddp_reducer_prepare.argtypes = [vp]
+            L.ddp_reducer_mark_ready.argtypes = [vp, i32, vp]
+            L.ddp_reducer_finalize.argtypes = [vp, vp]
+            L.ddp_reducer_launch_order.argtypes = [vp, P(i32), i32, P(i32)]
+            L.ddp_reducer_destroy.argtypes = [vp]
             for name in EXPORTS[4:]:
                 getattr(L, name).restype = i32
             _lib = L
@@ -387,3 +397,78 @@ class SyncCall:
                lib().ddp_sync_buckets(self.world, self.n_params, self._grads, self._numel, self._b_of, self._off,
                                       self.K, self._bn, self._buckets, self.dtype, self.divisor, self.algo,
                                       _stream(stream)))
+
+
+class Reducer:
+    """DDP's reducer over the C ABI (ddp_reducer_*): buckets are launched on
+    `comm_stream` as soon as their gradients are marked ready, in bucket order.
+
+    grads[r][p]: rank r's gradient tensors (registration order); plan from
+    ddp_plan_buckets; buckets[r][k] needed for DDP_ALGO_FUSED / _STAGED.
+    For DDP_ALGO_DRYRUN pass grads=None and numels= the parameter sizes."""
+
+    def __init__(self, grads, plan, buckets=None, divisor=None, algo=DDP_ALGO_VIEW, comm_stream=None,
+                 world=None, numels=None, dtype=F32):
+        b_of, off, bn = plan
+        if grads is not None:
+            world = len(grads)
+            flat, numels, code = [], [], None
+            for r in range(world):
+                for p, g in enumerate(grads[r]):
+                    c = dtype_code(g)
+                    code = c if code is None else code
+                    if c != code or not g.is_contiguous():
+                        raise ValueError("gradients must be contiguous and of one dtype")
+                    flat.append(g.data_ptr())
+                    if r == 0:
+                        numels.append(g.numel())
+            dtype = F32 if code is None else code
+            gtab = _vp_array(flat)
+        else:
+            if algo != DDP_ALGO_DRYRUN:
+                raise ValueError("gradients are required unless algo is DDP_ALGO_DRYRUN")
+            gtab = None
+        btab = None
+        if buckets is not None:
+            btab = _vp_array([buckets[r][k].data_ptr() for r in range(world) for k in range(len(bn))])
+        self.world = world
+        self.n_params = len(b_of)
+        self.n_buckets = len(bn)
+        self._keep = (grads, buckets, gtab, btab)
+        h = ctypes.c_void_p()
+        comm = 0 if algo == DDP_ALGO_DRYRUN else _stream(comm_stream)
+        _check("ddp_reducer_create",
+               lib().ddp_reducer_create(world, self.n_params, gtab, _i64_array(numels), dtype, _i32_array(b_of),
+                                        _i64_array(off), self.n_buckets, _i64_array(bn), btab, int(algo),
+                                        world if divisor is None else int(divisor), comm, ctypes.byref(h)))
+        self._h = h
+
+    def prepare(self):
+        _check("ddp_reducer_prepare", lib().ddp_reducer_prepare(self._h))
+
+    def mark_ready(self, param: int, stream=None):
+        s = 0 if stream == 0 else _stream(stream)
+        _check("ddp_reducer_mark_ready", lib().ddp_reducer_mark_ready(self._h, int(param), s))
+
+    def finalize(self, stream=None):
+        s = 0 if stream == 0 else _stream(stream)
+        _check("ddp_reducer_finalize", lib().ddp_reducer_finalize(self._h, s))
+
+    def launch_order(self):
+        buf = (ctypes.c_int32 * max(self.n_buckets, 1))()
+        n = ctypes.c_int32(0)
+        _check("ddp_reducer_launch_order",
+               lib().ddp_reducer_launch_order(self._h, buf, self.n_buckets, ctypes.byref(n)))
+        return [int(v) for v in buf[:n.value]]
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().ddp_reducer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+

@@ -295,7 +295,9 @@ int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* 
 typedef enum {
     DDP_ALGO_FUSED = 0,   /* pack -> ring_allreduce_fused -> unpack             */
     DDP_ALGO_STAGED = 1,  /* pack -> ring_allreduce_staged -> unpack            */
-    DDP_ALGO_VIEW = 2     /* ddp_bucket_allreduce_view (no bucket copies)        */
+    DDP_ALGO_VIEW = 2,    /* ddp_bucket_allreduce_view (no bucket copies)        */
+    DDP_ALGO_DRYRUN = 3   /* ddp_reducer only: track readiness and launch order,
+                             make no CUDA call (for checking a plan's order)    */
 } ddp_algo;
 
 /*
@@ -338,6 +340,52 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
 int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads,
                                   const int64_t* numel, const int64_t* offset, int64_t bucket_numel,
                                   int32_t dtype, int32_t divisor, void* stream);
+
+/*
+ * ddp_reducer -- DDP's reducer: each bucket's allreduce starts as soon as its
+ * gradients are ready, in bucket order, overlapping the rest of backward
+ * ([P1] section 03 "Overlap", section 05 steps 2 and 5; [P2] "梯度同步时机"
+ * and the Reducer pseudo-code).
+ *
+ * A reducer is created once per model and plan.  For every backward pass:
+ *   ddp_reducer_prepare   forget the previous pass's readiness;
+ *   ddp_reducer_mark_ready(p, compute_stream)
+ *                         call after the producer of parameter p's gradient
+ *                         (on every rank) has been enqueued on compute_stream;
+ *                         when p completes its bucket, an event is recorded on
+ *                         compute_stream, and every bucket of the ready prefix
+ *                         (bucket 0, 1, ... not launched yet and complete) is
+ *                         launched on comm_stream after its event -- bucket i+1
+ *                         never before bucket i;
+ *   ddp_reducer_finalize(stream)
+ *                         the point before the optimizer step: `stream` waits
+ *                         for every bucket's sync.  DDP_ERR_INVALID if some
+ *                         bucket never became ready (a parameter that got no
+ *                         gradient, the case DDP needs find_unused_parameters
+ *                         for).
+ * Marking a parameter twice in one pass is DDP_ERR_INVALID.
+ *
+ *   grads[world*n_params], numel, bucket_of_param, offset_of_param,
+ *   bucket_numel, buckets[world*n_buckets]  as for ddp_sync_buckets (buckets may
+ *                         be NULL for DDP_ALGO_VIEW and DDP_ALGO_DRYRUN, grads
+ *                         for DDP_ALGO_DRYRUN); the reducer keeps these pointers
+ *                         until it is destroyed, the caller keeps the memory
+ *   algo                  DDP_ALGO_FUSED, _STAGED, _VIEW or _DRYRUN
+ *   comm_stream           cudaStream_t on which the buckets' syncs run
+ * The reducer owns host memory and one CUDA event per bucket (created here,
+ * destroyed by ddp_reducer_destroy); it allocates no device memory.
+ */
+typedef struct ddp_reducer ddp_reducer;
+int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel, int32_t dtype,
+                           const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
+                           const int64_t* bucket_numel, void* const* buckets, int32_t algo, int32_t divisor,
+                           void* comm_stream, ddp_reducer** out);
+int32_t ddp_reducer_prepare(ddp_reducer* reducer);
+int32_t ddp_reducer_mark_ready(ddp_reducer* reducer, int32_t param, void* compute_stream);
+int32_t ddp_reducer_finalize(ddp_reducer* reducer, void* stream);
+/* Buckets launched in the current pass, in launch order (up to capacity). */
+int32_t ddp_reducer_launch_order(ddp_reducer* reducer, int32_t* order, int32_t capacity, int32_t* n);
+int32_t ddp_reducer_destroy(ddp_reducer* reducer);
 
 #ifdef __cplusplus
 }
