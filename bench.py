@@ -385,6 +385,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         del a, x
         torch.cuda.empty_cache()
         out["ddp_step"] = ddp_step_bench(ddp, workloads, torch, dev, stream, extra_steps)
+        out["ddp_step"]["overlap"] = overlap_bench(ddp, workloads, torch, dev, 5)
 
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_oracle_run(N, args.cpu_budget, NUMEL)
@@ -505,6 +506,92 @@ def run_sweep(args):
             print(json.dumps(row), flush=True)
             del x
             torch.cuda.empty_cache()
+
+
+def overlap_bench(ddp, workloads, torch, dev, steps):
+    """Backward/communication overlap on the decoder DDP step (N = 8, fp32).
+
+    A synthetic backward walks the layers in reverse: per transformer block two
+    bf16 GEMMs of 4096^3 on a compute stream (emulated layer backward), then
+    the block's gradients are written on every rank.  Three timings:
+      backward      -- the synthetic backward alone
+      serial        -- backward, then ddp_sync_buckets (view fusion) on the same stream
+      overlapped    -- backward with a ddp_reducer that syncs each bucket on a comm
+                       stream as soon as its gradients are ready
+    exposed_comm_ms = overlapped - backward (the communication tail left after overlap)."""
+    shapes = workloads.decoder_param_shapes()
+    numels = workloads.param_numels(shapes)
+    N, total = N_RANKS, sum(numels)
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, MiB, 25 * MiB)
+    src = torch.empty((N, total), dtype=torch.float32, device=dev)
+    for r in range(N):
+        src[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)))
+    g = torch.empty_like(src)
+    offs = [0]
+    for n in numels:
+        offs.append(offs[-1] + n)
+    views = [[g[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+    A = torch.randn(4096, 4096, dtype=torch.bfloat16, device=dev)
+    B = torch.randn(4096, 4096, dtype=torch.bfloat16, device=dev)
+    C = torch.empty(4096, 4096, dtype=torch.bfloat16, device=dev)
+    # parameters grouped by block, in backward order: lnf, block 23 .. block 0, wpe+wte
+    groups = [[len(numels) - 1, len(numels) - 2]]
+    for blk in range(23, -1, -1):
+        first = 2 + 12 * blk
+        groups.append(list(range(first + 11, first - 1, -1)))
+    groups.append([1, 0])
+    compute, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    red = ddp.Reducer(views, plan, None, N, ddp.DDP_ALGO_VIEW, comm_stream=comm)
+    sync = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW)
+
+    def backward(reducer):
+        with torch.cuda.stream(compute):
+            for gi, grp in enumerate(groups):
+                if 0 < gi <= 24:
+                    torch.mm(A, B, out=C)
+                    torch.mm(C, B, out=C)
+                for p in grp:
+                    g[:, offs[p]:offs[p + 1]].copy_(src[:, offs[p]:offs[p + 1]])
+                    if reducer is not None:
+                        reducer.mark_ready(p, compute)
+
+    def timed(fn):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(steps):
+            torch.cuda.synchronize()
+            ev0.record(compute)
+            fn()
+            ev1.record(compute)
+            torch.cuda.synchronize()
+            t = ev0.elapsed_time(ev1)
+            best = t if best is None else min(best, t)
+        return best
+
+    def run_backward():
+        backward(None)
+
+    def run_serial():
+        backward(None)
+        sync(compute)
+
+    def run_overlapped():
+        red.prepare()
+        backward(red)
+        red.finalize(compute)
+
+    t_b, t_s, t_o = timed(run_backward), timed(run_serial), timed(run_overlapped)
+    red.close()
+    del g, src, views
+    torch.cuda.empty_cache()
+    comm_ms = t_s - t_b
+    return {"backward_ms": t_b, "serial_ms": t_s, "overlapped_ms": t_o, "comm_ms": comm_ms,
+            "exposed_comm_ms": t_o - t_b,
+            "hidden_fraction": (t_s - t_o) / comm_ms if comm_ms > 0 else None,
+            "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block on a compute stream; view-fusion sync; "
+                    "best of %d" % steps}
 
 
 def main():
