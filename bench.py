@@ -556,18 +556,27 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
                         reducer.mark_ready(p, compute)
 
     def timed(fn):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # capture the whole pass (both streams) into a CUDA graph so that the
+        # host's per-op launch cost is not what gets measured
         fn()
         torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=compute):
+            fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         best = None
+        replay_stream = torch.cuda.current_stream()      # graph.replay() runs here
         for _ in range(steps):
             torch.cuda.synchronize()
-            ev0.record(compute)
-            fn()
-            ev1.record(compute)
+            ev0.record(replay_stream)
+            graph.replay()
+            ev1.record(replay_stream)
             torch.cuda.synchronize()
             t = ev0.elapsed_time(ev1)
             best = t if best is None else min(best, t)
+        del graph
         return best
 
     def run_backward():
@@ -582,16 +591,26 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
         backward(red)
         red.finalize(compute)
 
-    t_b, t_s, t_o = timed(run_backward), timed(run_serial), timed(run_overlapped)
+    t_b = timed(run_backward)
+    res = {"backward_ms": t_b,
+           "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block on a compute stream; view-fusion sync; "
+                   "each pass captured as one CUDA graph (both streams) and replayed; best of %d; "
+                   "max_ctas = CTA cap of the sync kernels (0 = fill the GPU)" % steps, "by_max_ctas": {}}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for cap in (0, sms // 2, sms // 4):
+        prev = ddp.ddp_set_max_ctas(cap)
+        try:
+            t_s, t_o = timed(run_serial), timed(run_overlapped)
+        finally:
+            ddp.ddp_set_max_ctas(prev)
+        comm_ms = t_s - t_b
+        res["by_max_ctas"][str(cap)] = {"serial_ms": t_s, "overlapped_ms": t_o, "comm_ms": comm_ms,
+                                        "exposed_comm_ms": t_o - t_b,
+                                        "hidden_fraction": (t_s - t_o) / comm_ms if comm_ms > 0 else None}
     red.close()
     del g, src, views
     torch.cuda.empty_cache()
-    comm_ms = t_s - t_b
-    return {"backward_ms": t_b, "serial_ms": t_s, "overlapped_ms": t_o, "comm_ms": comm_ms,
-            "exposed_comm_ms": t_o - t_b,
-            "hidden_fraction": (t_s - t_o) / comm_ms if comm_ms > 0 else None,
-            "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block on a compute stream; view-fusion sync; "
-                    "best of %d" % steps}
+    return res
 
 
 def main():

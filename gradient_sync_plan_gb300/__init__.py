@@ -34,7 +34,8 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
           -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY"}
 
 # every symbol include/ddp.h declares
-EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_plan_buckets",
+EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
+           "ddp_plan_buckets",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view",
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_last_cuda_error.restype = ctypes.c_char_p
             L.ddp_device_status.argtypes = [P(i32), i32]
             L.ddp_device_status.restype = i32
+            L.ddp_set_max_ctas.argtypes = [i32, P(i32)]
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
@@ -95,7 +97,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_reducer_finalize.argtypes = [vp, vp]
             L.ddp_reducer_launch_order.argtypes = [vp, P(i32), i32, P(i32)]
             L.ddp_reducer_destroy.argtypes = [vp]
-            for name in EXPORTS[4:]:
+            for name in EXPORTS[4:]:   # every entry point from ddp_set_max_ctas on returns a status
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -187,6 +189,13 @@ def ddp_device_status(clear: bool = True) -> int:
     v = ctypes.c_int32(0)
     _check("ddp_device_status", lib().ddp_device_status(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def ddp_set_max_ctas(max_ctas: int) -> int:
+    """Cap the CTAs of every library kernel (0 = no cap); returns the previous cap."""
+    prev = ctypes.c_int32(0)
+    _check("ddp_set_max_ctas", lib().ddp_set_max_ctas(int(max_ctas), ctypes.byref(prev)))
+    return int(prev.value)
 
 
 def ddp_plan_buckets(numels: Sequence[int], dtype: int = F32, first_bucket_bytes: int = FIRST_BUCKET_BYTES,

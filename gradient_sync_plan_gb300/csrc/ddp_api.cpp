@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -38,6 +39,16 @@ bool debug_enabled() {
         return v && *v && *v != '0';
     }();
     return on;
+}
+
+namespace {
+std::atomic<int> g_max_ctas{0};                              // 0 = no cap (ddp_set_max_ctas)
+}  // namespace
+
+int cap_ctas(int64_t grid) {
+    const int cap = g_max_ctas.load(std::memory_order_relaxed);
+    if (cap > 0 && grid > cap) grid = cap;
+    return (int)std::max<int64_t>(1, grid);
 }
 
 namespace {
@@ -78,7 +89,7 @@ int grid_for(const void* kernel, int64_t work_items, int threads) {
         g_occ[key] = per_sm;
     }
     const int64_t need = std::max<int64_t>(1, (work_items + threads - 1) / threads);
-    return (int)std::min<int64_t>((int64_t)sms * per_sm, need);
+    return cap_ctas(std::min<int64_t>((int64_t)sms * per_sm, need));
 }
 
 }  // namespace ddpk
@@ -222,6 +233,13 @@ const char* ddp_status_string(int32_t status) {
 int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
 
 const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
+
+int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) {
+    if (max_ctas < 0) return DDP_ERR_INVALID;
+    const int prev = g_max_ctas.exchange(max_ctas);
+    if (previous) *previous = prev;
+    return DDP_OK;
+}
 
 int32_t ddp_device_status(int32_t* status, int32_t clear) {
     if (!status) return DDP_ERR_INVALID;

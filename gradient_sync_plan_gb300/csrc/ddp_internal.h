@@ -30,6 +30,8 @@ inline int elem_bytes(int dtype) { return dtype == DDP_F32 ? 4 : 2; }
 // Launch geometry helpers (cached per device).
 int sm_count();
 int grid_for(const void* kernel, int64_t work_items, int threads = kThreads);
+// grid clamped to the process-wide CTA cap of ddp_set_max_ctas (0 = none), at least 1
+int cap_ctas(int64_t grid);
 bool debug_enabled();
 
 // ---- ring kernels (ring_kernels.cu) -----------------------------------

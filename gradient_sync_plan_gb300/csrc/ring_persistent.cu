@@ -269,7 +269,7 @@ static cudaError_t pers_launch(int world, void* const* ptrs, int64_t numel, floa
     const int64_t clen = chunk_len(numel, world);
     const int64_t per_step = vec_ok ? world * ((clen + E::L - 1) / E::L + 1) : world * clen;
     const int64_t need = std::max<int64_t>(1, (per_step + kThreads - 1) / kThreads);
-    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * per_sm, need);
+    const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, need));
     // zero the status word and the arrival counter before the launch
     cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;

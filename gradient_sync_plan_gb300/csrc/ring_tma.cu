@@ -314,7 +314,7 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
     }
     TileMap map;
     map.init(numel, chunk_len(numel, world), tile);
-    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * per_sm, map.total);
+    const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, map.total));
     TmaTable<CAP> tab{};
     for (int r = 0; r < world; ++r) tab.p[r] = static_cast<char*>(ptrs[r]);
     k<<<std::max(grid, 1), kTmaThreads, smem, st>>>(tab, world, map, dop);

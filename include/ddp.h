@@ -76,6 +76,17 @@ int32_t ddp_abi_version(void);
 const char* ddp_last_cuda_error(void);
 
 /*
+ * ddp_set_max_ctas -- upper bound on the thread blocks (CTAs) of every kernel
+ * this library launches in this process from now on; 0 removes the bound
+ * (the default: every kernel fills the GPU).  A bound leaves SMs to compute
+ * that runs at the same time, e.g. backward kernels overlapping the bucket
+ * syncs of ddp_reducer, at the price of less bandwidth for the sync itself.
+ * Results do not depend on it.  *previous (if not NULL) receives the old
+ * value.  DDP_ERR_INVALID for a negative bound.
+ */
+int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
+
+/*
  * ddp_device_status -- the library's sticky device-side status word on the
  * current device: DDP_OK, or DDP_ERR_TIMEOUT if a kernel's bounded wait on an
  * asynchronous copy gave up (the kernel then stopped early, so the buffers

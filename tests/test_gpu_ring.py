@@ -321,6 +321,23 @@ def test_persistent_status_word_is_cleared_on_each_call():
     assert int(st[0]) == 0
 
 
+@pytest.mark.parametrize("cap", [1, 7, 40])
+def test_cta_cap_does_not_change_results(cap):
+    # every kernel family under a CTA cap: TMA fused (large aligned), register
+    # fused (ragged), staged, persistent -- all must stay exact
+    cases = [(8, 1 << 20, "f32"), (5, 77_777, "bf16"), (3, 1000, "f32")]
+    prev = ddp.ddp_set_max_ctas(cap)
+    try:
+        for N, S, dtype in cases:
+            x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=cap + N)
+            xh = f32_or_bits(x)
+            want = oracle_allreduce(xh, N)
+            for kernel in ("fused", "staged", "persistent"):
+                assert_bits_equal(run_gpu(kernel, xh, N), want, f"cap={cap} {kernel} N={N} S={S}")
+    finally:
+        ddp.ddp_set_max_ctas(prev)
+
+
 def test_empty_bucket_is_noop():
     x = torch.zeros((4, 0), device="cuda")
     ddp.ring_allreduce_fused(x, 4)
