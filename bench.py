@@ -431,6 +431,22 @@ def ddp_step_bench(ddp, workloads, torch, dev, stream, steps):
         ms = ev0.elapsed_time(ev1) / steps
         res[name] = {"ms_per_step": ms, "hbm_alg_gbs": bytes_alg / (ms / 1e3) / 1e9,
                      "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
+    # bf16 compression hook: float32 grads -> bf16 buckets -> bf16 ring -> float32
+    bk16 = [[torch.empty(int(n), dtype=torch.bfloat16, device=dev) for n in plan[2]] for _ in range(N)]
+    call = ddp.SyncCall(views, plan, bk16, N, ddp.DDP_ALGO_BF16_HOOK)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    # pack: read 4 + write 2, ring: 2 + 2, unpack: read 2 + write 4 bytes per element and rank
+    res["bf16_hook"] = {"ms_per_step": ms, "hbm_alg_gbs": 16 * N * total / (ms / 1e3) / 1e9,
+                        "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
+    del bk16
     # no_sync: 3 local accumulations of a micro-batch, then one sync (view)
     scratch = torch.empty_like(g)
     scratch.copy_(g)

@@ -26,6 +26,7 @@ DDP_ALGO_FUSED = 0
 DDP_ALGO_STAGED = 1
 DDP_ALGO_VIEW = 2
 DDP_ALGO_DRYRUN = 3
+DDP_ALGO_BF16_HOOK = 4
 DDP_MAX_WORLD = 512
 FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
 BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
@@ -36,7 +37,8 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
            "ddp_plan_buckets",
-           "ddp_bucket_pack", "ddp_bucket_unpack", "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
+           "ddp_bucket_pack", "ddp_bucket_unpack", "ddp_bucket_pack_bf16", "ddp_bucket_unpack_bf16",
+           "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view",
            "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
@@ -80,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
+            L.ddp_bucket_pack_bf16.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, vp]
+            L.ddp_bucket_unpack_bf16.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, vp]
             L.ring_allreduce_fused.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_persistent.argtypes = [i32, P(vp), i64, i32, i32, vp, i32, i32, vp]
@@ -339,6 +343,28 @@ def ddp_bucket_unpack(grads: Sequence[Sequence], offsets: Sequence[int], buckets
     _check("ddp_bucket_unpack", lib().ddp_bucket_unpack(world, n, _vp_array(ptrs), _i64_array(numels),
                                                         _i64_array(offsets), _vp_array(bp), bnumel, bcode,
                                                         _stream(stream)))
+
+
+def ddp_bucket_pack_bf16(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
+    """bf16 compression hook: float32 gradients rounded into bf16 buckets."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    bp, bnumel, bcode = _rank_ptrs(buckets)
+    if (n and code != F32) or bcode != BF16:
+        raise ValueError("float32 gradients and bf16 buckets expected")
+    _check("ddp_bucket_pack_bf16", lib().ddp_bucket_pack_bf16(world, n, _vp_array(ptrs), _i64_array(numels),
+                                                              _i64_array(offsets), _vp_array(bp), bnumel,
+                                                              _stream(stream)))
+
+
+def ddp_bucket_unpack_bf16(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
+    """bf16 compression hook: bf16 buckets widened back into float32 gradients."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    bp, bnumel, bcode = _rank_ptrs(buckets)
+    if (n and code != F32) or bcode != BF16:
+        raise ValueError("float32 gradients and bf16 buckets expected")
+    _check("ddp_bucket_unpack_bf16", lib().ddp_bucket_unpack_bf16(world, n, _vp_array(ptrs), _i64_array(numels),
+                                                                  _i64_array(offsets), _vp_array(bp), bnumel,
+                                                                  _stream(stream)))
 
 
 def ddp_bucket_allreduce_view(grads: Sequence[Sequence], offsets: Sequence[int], bucket_numel: int,

@@ -117,6 +117,105 @@ cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t str
 }
 
 // ---------------------------------------------------------------------------
+// Converting copies for the bf16 compression hook
+// ---------------------------------------------------------------------------
+//
+// DDP's communication hooks ("Day 17 · 梯度的集体行动", reading list on DDP
+// communication hooks: fp16/bf16 compression) let the bucket travel in a
+// narrower type: fp32 gradients are rounded to bf16 (nearest even) on the way
+// into the bucket and widened back (exactly) on the way out.
+
+constexpr int kConvItems = 256;
+constexpr int64_t kConvTile = 8192;      // elements per tile
+
+struct ConvBatch {
+    int32_t n;
+    int32_t pad_;
+    int64_t tile_end[kConvItems];
+    const char* src[kConvItems];
+    char* dst[kConvItems];
+    int64_t numel[kConvItems];
+    int32_t vec[kConvItems];
+};
+
+// MODE 0: float32 -> bf16 (round to nearest even); MODE 1: bf16 -> float32 (exact)
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) k_convert_items(const __grid_constant__ ConvBatch b) {
+    const int64_t tiles = b.tile_end[b.n - 1];
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        int lo = 0, hi = b.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (b.tile_end[mid] > tile) hi = mid; else lo = mid + 1;
+        }
+        const int64_t first = lo ? b.tile_end[lo - 1] : 0;
+        const int64_t e0 = (tile - first) * kConvTile;
+        const int64_t e1 = std::min(e0 + kConvTile, b.numel[lo]);
+        const char* src = b.src[lo];
+        char* dst = b.dst[lo];
+        int64_t done = e0;
+        if (b.vec[lo]) {
+            // 8 elements per step: 32 bytes of fp32 <-> 16 bytes of bf16
+            const int64_t nv = (e1 - e0) / 8;
+            for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+                const int64_t e = e0 + v * 8;
+                if (MODE == 0) {
+                    const float4 a = reinterpret_cast<const float4*>(src + e * 4)[0];
+                    const float4 c = reinterpret_cast<const float4*>(src + e * 4)[1];
+                    uint4 o;
+                    o.x = bf16x2_rn(a.x, a.y);
+                    o.y = bf16x2_rn(a.z, a.w);
+                    o.z = bf16x2_rn(c.x, c.y);
+                    o.w = bf16x2_rn(c.z, c.w);
+                    *reinterpret_cast<uint4*>(dst + e * 2) = o;
+                } else {
+                    const uint4 w = *reinterpret_cast<const uint4*>(src + e * 2);
+                    reinterpret_cast<float4*>(dst + e * 4)[0] =
+                        make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                    reinterpret_cast<float4*>(dst + e * 4)[1] =
+                        make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                }
+            }
+            done = e0 + nv * 8;
+        }
+        for (int64_t e = done + threadIdx.x; e < e1; e += blockDim.x) {
+            if (MODE == 0)
+                reinterpret_cast<uint16_t*>(dst)[e] = f32_to_bf16_rn(reinterpret_cast<const float*>(src)[e]);
+            else
+                reinterpret_cast<float*>(dst)[e] = bf16_to_f32(reinterpret_cast<const uint16_t*>(src)[e]);
+        }
+    }
+}
+
+cudaError_t launch_convert_items(const ConvItem* items, int64_t n, int to_bf16, cudaStream_t stream) {
+    ConvBatch b;
+    int64_t i = 0;
+    while (i < n) {
+        b.n = 0;
+        b.pad_ = 0;
+        int64_t tiles = 0;
+        for (; i < n && b.n < kConvItems; ++i) {
+            if (items[i].numel <= 0) continue;
+            tiles += (items[i].numel + kConvTile - 1) / kConvTile;
+            b.tile_end[b.n] = tiles;
+            b.src[b.n] = static_cast<const char*>(items[i].src);
+            b.dst[b.n] = static_cast<char*>(items[i].dst);
+            b.numel[b.n] = items[i].numel;
+            b.vec[b.n] = ((reinterpret_cast<uintptr_t>(items[i].src) | reinterpret_cast<uintptr_t>(items[i].dst)) % 16) == 0;
+            ++b.n;
+        }
+        if (b.n == 0) continue;
+        const void* k = to_bf16 ? (const void*)k_convert_items<0> : (const void*)k_convert_items<1>;
+        const int grid = std::max<int64_t>(1, std::min<int64_t>(grid_for(k, tiles * kThreads), tiles));
+        if (to_bf16) k_convert_items<0><<<grid, kThreads, 0, stream>>>(b);
+        else k_convert_items<1><<<grid, kThreads, 0, stream>>>(b);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
 // Fused view: pack + ring allreduce + average + unpack of one bucket
 // ---------------------------------------------------------------------------
 

@@ -178,6 +178,39 @@ int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const i
     return DDP_OK;
 }
 
+// Members of one bucket for the bf16 hook: float32 gradients, bf16 bucket.
+int32_t hook_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel, const int64_t* offset,
+                   const void* const* buckets, int64_t bucket_numel, bool to_bucket, std::vector<ConvItem>* items) {
+    if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
+    if (n < 0 || bucket_numel < 0) return DDP_ERR_INVALID;
+    if (n > 0 && (!grads || !numel || !offset || !buckets)) return DDP_ERR_INVALID;
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    for (int32_t i = 0; i < n; ++i) {
+        if (numel[i] < 0 || offset[i] < 0 || offset[i] > bucket_numel - numel[i]) return DDP_ERR_INVALID;
+        if (numel[i] > 0) ranges.emplace_back(offset[i], offset[i] + numel[i]);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second) return DDP_ERR_INVALID;
+    items->clear();
+    for (int32_t r = 0; r < world; ++r) {
+        char* b = static_cast<char*>(const_cast<void*>(buckets[r]));
+        if (!b && bucket_numel > 0) return DDP_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(b) % 2) return DDP_ERR_ALIGN;
+        for (int32_t i = 0; i < n; ++i) {
+            if (numel[i] == 0) continue;
+            char* g = static_cast<char*>(const_cast<void*>(grads[(int64_t)r * n + i]));
+            if (!g) return DDP_ERR_INVALID;
+            if (reinterpret_cast<uintptr_t>(g) % 4) return DDP_ERR_ALIGN;
+            char* slot = b + offset[i] * 2;
+            if (g < slot + numel[i] * 2 && slot < g + numel[i] * 4) return DDP_ERR_INVALID;
+            if (to_bucket) items->push_back(ConvItem{g, slot, numel[i]});
+            else items->push_back(ConvItem{slot, g, numel[i]});
+        }
+    }
+    return DDP_OK;
+}
+
 int32_t view_members(int32_t world, int32_t n, void* const* grads, const int64_t* numel, const int64_t* offset,
                      int64_t bucket_numel, int32_t dtype, std::vector<ViewMember>* out) {
     int32_t st = common_checks(world, bucket_numel, dtype);
@@ -407,6 +440,24 @@ int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads
     return cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream));
 }
 
+int32_t ddp_bucket_pack_bf16(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
+                             const int64_t* offset, void* const* buckets, int64_t bucket_numel, void* stream) {
+    std::vector<ConvItem> items;
+    int32_t st = hook_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel, true,
+                            &items);
+    if (st) return st;
+    return cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 1, (cudaStream_t)stream));
+}
+
+int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                               const int64_t* offset, const void* const* buckets, int64_t bucket_numel, void* stream) {
+    std::vector<ConvItem> items;
+    int32_t st = hook_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel, false,
+                            &items);
+    if (st) return st;
+    return cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 0, (cudaStream_t)stream));
+}
+
 int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                                   const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
                                   void* stream) {
@@ -435,7 +486,9 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
     int32_t st = common_checks(world, 0, dtype);
     if (st) return st;
     if (n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
-    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW) return DDP_ERR_INVALID;
+    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_BF16_HOOK)
+        return DDP_ERR_INVALID;
+    if (algo == DDP_ALGO_BF16_HOOK && dtype != DDP_F32) return DDP_ERR_INVALID;
     if (n_params > 0 && (!grads || !numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
     if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
     if (algo != DDP_ALGO_VIEW && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
@@ -468,6 +521,16 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             continue;
         }
         for (int32_t r = 0; r < world; ++r) bk[r] = buckets[(size_t)r * n_buckets + k];
+        if (algo == DDP_ALGO_BF16_HOOK) {
+            st = ddp_bucket_pack_bf16(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], stream);
+            if (st) return st;
+            st = ring_allreduce_fused(world, bk.data(), bucket_numel[k], DDP_BF16, divisor, stream);
+            if (st) return st;
+            st = ddp_bucket_unpack_bf16(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
+                                        (const void* const*)bk.data(), bucket_numel[k], stream);
+            if (st) return st;
+            continue;
+        }
         st = ddp_bucket_pack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], dtype, stream);
         if (st) return st;
         st = (algo == DDP_ALGO_FUSED)

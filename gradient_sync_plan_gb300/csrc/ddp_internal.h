@@ -69,6 +69,15 @@ struct CopyItem {
 };
 cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t stream);
 
+// Converting copies (bf16 compression hook): float32 -> bf16 (to_bf16 = 1,
+// round to nearest even) or bf16 -> float32 (to_bf16 = 0, exact).
+struct ConvItem {
+    const void* src;
+    void* dst;
+    int64_t numel;
+};
+cudaError_t launch_convert_items(const ConvItem* items, int64_t n, int to_bf16, cudaStream_t stream);
+
 // One bucket member for the fused view kernel: its numel, its element offset
 // in the bucket and its `world` gradient pointers (rank order).
 struct ViewMember {

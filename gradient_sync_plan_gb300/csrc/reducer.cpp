@@ -55,6 +55,13 @@ int32_t sync_bucket(ddp_reducer* r, int32_t k) {
     if (r->algo == DDP_ALGO_VIEW)
         return ddp_bucket_allreduce_view(r->world, n, g, ne, off, r->bucket_numel[k], r->dtype, r->divisor, r->comm);
     void* const* b = r->bucket_bufs[k].data();
+    if (r->algo == DDP_ALGO_BF16_HOOK) {
+        int32_t st = ddp_bucket_pack_bf16(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->comm);
+        if (st) return st;
+        st = ring_allreduce_fused(r->world, b, r->bucket_numel[k], DDP_BF16, r->divisor, r->comm);
+        if (st) return st;
+        return ddp_bucket_unpack_bf16(r->world, n, g, ne, off, (const void* const*)b, r->bucket_numel[k], r->comm);
+    }
     int32_t st = ddp_bucket_pack(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->dtype, r->comm);
     if (st) return st;
     st = (r->algo == DDP_ALGO_STAGED)
@@ -108,12 +115,15 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     *out = nullptr;
     if (world < 1 || world > DDP_MAX_WORLD || n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
-    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_DRYRUN)
+    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_DRYRUN &&
+        algo != DDP_ALGO_BF16_HOOK)
         return DDP_ERR_INVALID;
+    if (algo == DDP_ALGO_BF16_HOOK && dtype != DDP_F32) return DDP_ERR_INVALID;
     if (n_params > 0 && (!numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
     if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
     if (algo != DDP_ALGO_DRYRUN && n_params > 0 && !grads) return DDP_ERR_INVALID;
-    if ((algo == DDP_ALGO_FUSED || algo == DDP_ALGO_STAGED) && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
+    const bool needs_buckets = algo == DDP_ALGO_FUSED || algo == DDP_ALGO_STAGED || algo == DDP_ALGO_BF16_HOOK;
+    if (needs_buckets && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
 
     ddp_reducer* r = new (std::nothrow) ddp_reducer();
     if (!r) return DDP_ERR_CAPACITY;
@@ -155,7 +165,7 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
             for (int32_t w = 0; w < world; ++w)
                 for (int32_t i = 0; i < n; ++i) r->member_grads[k][(size_t)w * n + i] = grads[(size_t)w * n_params + m[i]];
         }
-        if (algo == DDP_ALGO_FUSED || algo == DDP_ALGO_STAGED) {
+        if (needs_buckets) {
             r->bucket_bufs[k].resize(world);
             for (int32_t w = 0; w < world; ++w) r->bucket_bufs[k][w] = buckets[(size_t)w * n_buckets + k];
         }

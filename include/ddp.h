@@ -162,6 +162,23 @@ int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads
                           int64_t bucket_numel, int32_t dtype, void* stream);
 
 /*
+ * ddp_bucket_pack_bf16 / ddp_bucket_unpack_bf16 -- the copies of the bf16
+ * compression communication hook ([P2] reading list, "PyTorch DDP
+ * Communication Hooks": fp16/bf16 compression): float32 gradients are rounded
+ * to bf16 (nearest even) as they are packed into a bf16 bucket, the bucket is
+ * reduced in bf16 (per-hop rounding, see ring_allreduce_fused), and the
+ * averaged bf16 values are widened exactly to float32 as they are unpacked.
+ * The pages do not say where the hook divides; like every other path here,
+ * the division by the world size happens once, after the reduction.
+ * Arguments as for ddp_bucket_pack / ddp_bucket_unpack, with float32 `grads`,
+ * bf16 `buckets` (bucket_numel elements each) and no dtype argument.
+ */
+int32_t ddp_bucket_pack_bf16(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
+                             const int64_t* offset, void* const* buckets, int64_t bucket_numel, void* stream);
+int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                               const int64_t* offset, const void* const* buckets, int64_t bucket_numel, void* stream);
+
+/*
  * ring_allreduce_fused -- the ring allreduce of one bucket, in one pass over
  * memory, with the ring's exact result ([P1] section 03 "两阶段"; [P3]
  * §1.3.1-§1.3.2).
@@ -307,8 +324,10 @@ typedef enum {
     DDP_ALGO_FUSED = 0,   /* pack -> ring_allreduce_fused -> unpack             */
     DDP_ALGO_STAGED = 1,  /* pack -> ring_allreduce_staged -> unpack            */
     DDP_ALGO_VIEW = 2,    /* ddp_bucket_allreduce_view (no bucket copies)        */
-    DDP_ALGO_DRYRUN = 3   /* ddp_reducer only: track readiness and launch order,
+    DDP_ALGO_DRYRUN = 3,  /* ddp_reducer only: track readiness and launch order,
                              make no CUDA call (for checking a plan's order)    */
+    DDP_ALGO_BF16_HOOK = 4 /* float32 gradients, bf16 buckets: ddp_bucket_pack_bf16
+                             -> ring_allreduce_fused in bf16 -> ddp_bucket_unpack_bf16 */
 } ddp_algo;
 
 /*
@@ -327,7 +346,8 @@ typedef enum {
  *                              for bucket k at [r*n_buckets + k], at least
  *                              bucket_numel[k] elements (may alias across k;
  *                              unused by DDP_ALGO_VIEW and may then be NULL)
- *   algo                       a ddp_algo
+ *   algo                       a ddp_algo (DDP_ALGO_BF16_HOOK: float32 `grads` and
+ *                              dtype, bf16 `buckets`)
  * The same plan must be used on every rank (one plan is shared here by
  * construction).  DDP_ERR_INVALID if the plan is inconsistent.
  */

@@ -234,3 +234,33 @@ def no_sync_then_sync(micro: Sequence[Sequence[Sequence[np.ndarray]]], dtype: in
                 accumulate(acc[r][p], micro[m][r][p], dtype)
     ddp_sync(acc, dtype, first_cap_bytes, cap_bytes)
     return acc
+
+
+def ddp_sync_bf16_hook(grads: Sequence[Sequence[np.ndarray]], first_cap_bytes: int = FIRST_BUCKET_BYTES,
+                       cap_bytes: int = BUCKET_CAP_BYTES, divisor: Optional[int] = None):
+    """DDP step with the bf16 compression communication hook, in place.
+
+    grads[r][p] are float32.  Buckets are planned on the float32 sizes, as DDP
+    builds them before any hook runs; each bucket is packed, every element
+    rounded to bf16 (nearest even), the bf16 bucket ring-reduced (one bf16
+    rounding per hop) and divided, and the result widened back to float32 and
+    unpacked.  ("Day 17 · 梯度的集体行动", reading list: DDP communication hooks,
+    fp16/bf16 compression; the division after the reduction is this build's
+    reading, as everywhere else.)
+    """
+    world = len(grads)
+    numels = [int(a.size) for a in grads[0]]
+    b_of, off, bn = plan_buckets(numels, 4, first_cap_bytes, cap_bytes)
+    div = world if divisor is None else divisor
+    for k in range(len(bn)):
+        members = bucket_members(b_of, off, k)
+        bufs = []
+        for r in range(world):
+            b32 = np.zeros(int(bn[k]), dtype=np.float32)
+            bucket_pack([grads[r][p] for p in members], [off[p] for p in members], b32, F32)
+            bufs.append(bf16_rne(b32))
+        ring_allreduce(bufs, BF16, div)
+        for r in range(world):
+            bucket_unpack([grads[r][p] for p in members], [off[p] for p in members], bf16_to_f32(bufs[r]), F32)
+    return b_of, off, bn
+

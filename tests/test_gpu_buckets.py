@@ -240,3 +240,50 @@ def test_no_sync_small_decoder_full():
     torch.cuda.synchronize()
     want = oracle.no_sync_then_sync(micro_h, oracle.F32, 4096, 40000)
     assert_bits_equal(f32_or_bits(acc), np.stack([np.concatenate(want[r]) for r in range(world)]), "no_sync")
+
+
+@pytest.mark.parametrize("via", ["sync_buckets", "reducer"])
+def test_bf16_hook_matches_oracle(via):
+    numels = _small_decoder()
+    world, first, cap = 8, 4096, 40000
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=4)
+    x64 = flat.numpy().astype(np.float64)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
+    if via == "sync_buckets":
+        ddp.ddp_sync_buckets(views, plan, bk, algo=ddp.DDP_ALGO_BF16_HOOK)
+    else:
+        red = ddp.Reducer(views, plan, bk, algo=ddp.DDP_ALGO_BF16_HOOK, comm_stream=torch.cuda.Stream())
+        for p in range(len(numels) - 1, -1, -1):
+            red.mark_ready(p, torch.cuda.current_stream())
+        red.finalize(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    oracle.ddp_sync_bf16_hook(grads_h, first, cap)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    got = f32_or_bits(g)
+    assert_bits_equal(got, want, f"bf16 hook via {via}")
+    ref = x64.sum(0) / world
+    assert np.linalg.norm(got[0] - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def test_bf16_pack_unpack_round_trip_matches_oracle_rounding():
+    rng = np.random.default_rng(8)
+    world, numels = 3, [1001, 16, 5, 4096]
+    offsets = [0, 1001, 1017, 1022]             # odd offsets: element-wise conversion paths too
+    bucket_numel = 1022 + 4096
+    grads = [[torch.from_numpy(rng.standard_normal(n).astype(np.float32)).cuda() for n in numels] for _ in range(world)]
+    buckets = torch.zeros((world, bucket_numel), dtype=torch.bfloat16, device="cuda")
+    ddp.ddp_bucket_pack_bf16(grads, offsets, buckets)
+    out = [[torch.zeros_like(t) for t in grads[r]] for r in range(world)]
+    ddp.ddp_bucket_unpack_bf16(out, offsets, buckets)
+    torch.cuda.synchronize()
+    for r in range(world):
+        for i in range(len(numels)):
+            src = grads[r][i].cpu().numpy()
+            want_bits = oracle.bf16_rne(src)
+            got_bits = f32_or_bits(buckets[r, offsets[i]:offsets[i] + numels[i]])
+            assert_bits_equal(got_bits, want_bits, f"pack r{r} m{i}")
+            assert_bits_equal(f32_or_bits(out[r][i]), oracle.bf16_to_f32(want_bits), f"unpack r{r} m{i}")
+

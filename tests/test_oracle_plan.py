@@ -192,3 +192,26 @@ def test_bf16_widening_exact():
     t = torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).to(torch.float32).numpy()
     same = (f.view(np.uint32) == t.view(np.uint32)) | (np.isnan(f) & np.isnan(t))
     assert np.all(same)
+
+
+def test_bf16_hook_exact_on_small_integers_and_bounded_on_random():
+    # small integers survive the rounding to bf16 and every hop exactly, and
+    # the mean over 4 ranks is a multiple of 1/4: the hook must give it exactly
+    rng = np.random.default_rng(21)
+    N, numels = 4, [33, 7, 64, 5]
+    grads = [[rng.integers(-8, 9, size=n).astype(np.float32) for n in numels] for _ in range(N)]
+    exact = [sum(grads[r][p].astype(np.float64) for r in range(N)) / N for p in range(len(numels))]
+    oracle.ddp_sync_bf16_hook(grads, 64, 128)
+    for r in range(N):
+        for p in range(len(numels)):
+            np.testing.assert_array_equal(grads[r][p], exact[p].astype(np.float32))
+    # random values: within the input rounding plus the per-hop bf16 bound
+    u = 2.0 ** -8
+    g = [[rng.standard_normal(n).astype(np.float32) * 1e-2 for n in numels] for _ in range(N)]
+    x64 = [np.stack([g[r][p].astype(np.float64) for r in range(N)]) for p in range(len(numels))]
+    oracle.ddp_sync_bf16_hook(g, 64, 128)
+    for p in range(len(numels)):
+        s_abs = np.abs(x64[p]).sum(0)
+        bound = (u * s_abs + (N - 1) * u * s_abs * (1 + u)) / N + u * np.abs(x64[p].sum(0) / N) * 1.01
+        assert np.all(np.abs(g[0][p].astype(np.float64) - x64[p].sum(0) / N) <= bound + 1e-12)
+
