@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
             L.oracle_ring_allreduce.argtypes = [i32, i64, i32, ctypes.POINTER(vp), i32, i32, ctypes.POINTER(i64)]
             L.oracle_ring_allreduce.restype = ctypes.c_int
+            L.oracle_tree_allreduce.argtypes = [i32, i64, i32, ctypes.POINTER(vp), i32, i32, ctypes.POINTER(i64)]
+            L.oracle_tree_allreduce.restype = ctypes.c_int
             L.oracle_plan_buckets.argtypes = [i32, ctypes.POINTER(i64), i64, i64, i64,
                                               ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(i64),
                                               ctypes.POINTER(i32)]
@@ -116,6 +118,27 @@ def ring_allreduce(bufs: Sequence[np.ndarray], dtype: int = F32, divisor: int = 
     sent = (ctypes.c_int64 * max(world, 1))()
     _check(lib().oracle_ring_allreduce(world, numel, dtype, ptrs, divisor, n_steps, sent), "ring_allreduce")
     return np.array(sent[:world], dtype=np.int64)
+
+
+def tree_allreduce(bufs: Sequence[np.ndarray], dtype: int = F32, divisor: int = 0, n_steps: int = -1) -> np.ndarray:
+    """Binomial-tree allreduce of the rank buffers in place (reduce to rank 0,
+    divide, broadcast); returns elements sent per rank."""
+    world = len(bufs)
+    numel = int(bufs[0].size) if world else 0
+    want = _np_dtype(dtype)
+    for b in bufs:
+        if b.dtype != want or not b.flags["C_CONTIGUOUS"] or b.size != numel:
+            raise ValueError("rank buffers must be contiguous, same size and dtype")
+    ptrs = (ctypes.c_void_p * max(world, 1))(*[b.ctypes.data for b in bufs])
+    sent = (ctypes.c_int64 * max(world, 1))()
+    _check(lib().oracle_tree_allreduce(world, numel, dtype, ptrs, divisor, n_steps, sent), "tree_allreduce")
+    return np.array(sent[:world], dtype=np.int64)
+
+
+def tree_allreduce_2d(x: np.ndarray, dtype: int = F32, divisor: int = 0, n_steps: int = -1) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    tree_allreduce([x[r] for r in range(x.shape[0])], dtype, divisor, n_steps)
+    return x
 
 
 def ring_allreduce_2d(x: np.ndarray, dtype: int = F32, divisor: int = 0, n_steps: int = -1) -> np.ndarray:

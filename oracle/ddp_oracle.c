@@ -201,6 +201,80 @@ int oracle_ring_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bu
 }
 
 /* ------------------------------------------------------------------------ */
+/* Tree allreduce: binomial-tree reduce to rank 0, divide, broadcast back.    */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name a tree-based allreduce as the alternative to the ring for
+ * small messages ([P1] section 02 and section 07, NCCL's Tree algorithm and
+ * its small-message threshold) without spelling it out.  Reading taken: a
+ * binomial tree over the whole vector.  Reduce steps use distances
+ * d = 1, 2, 4, ... < N: every rank r with r mod 2d == d sends its buffer to
+ * rank r - d, which adds it into its own (receiver's value first).  After the
+ * last reduce step rank 0 holds the sum and divides it.  Broadcast steps use
+ * the same distances in reverse: every rank r with r mod 2d == 0 and
+ * r + d < N sends its buffer to r + d, which stores it.  Each step is again
+ * "all send, then all receive".
+ *
+ * n_steps: -1 = everything (reduce, divide, broadcast); k = stop after the
+ * first k of the 2 * ceil(log2 N) steps, no divide. */
+static int32_t tree_depth(int32_t N)
+{
+    int32_t L = 0;
+    while ((1 << L) < N) ++L;
+    return L;
+}
+
+int oracle_tree_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bufs, int32_t divisor,
+                          int32_t n_steps, int64_t* sent)
+{
+    if (world < 1 || numel < 0 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16) || divisor < 0 || !bufs)
+        return ORACLE_EINVAL;
+    for (int32_t r = 0; r < world; ++r)
+        if (!bufs[r] && numel > 0) return ORACLE_EINVAL;
+    const int32_t depth = tree_depth(world);
+    const int32_t total_steps = 2 * depth;
+    if (n_steps < -1 || n_steps > total_steps) return ORACLE_EINVAL;
+    const int32_t run = n_steps < 0 ? total_steps : n_steps;
+    const size_t es = elem_size(dtype);
+    const size_t bytes = (size_t)numel * es;
+    char** msg = (char**)calloc((size_t)world, sizeof(char*));
+    if (!msg) return ORACLE_ENOMEM;
+    for (int32_t r = 0; r < world; ++r) {
+        msg[r] = (char*)malloc(bytes ? bytes : 1u);
+        if (!msg[r]) {
+            for (int32_t q = 0; q < r; ++q) free(msg[q]);
+            free(msg);
+            return ORACLE_ENOMEM;
+        }
+    }
+    for (int32_t step = 0; step < run; ++step) {
+        const int reduce = step < depth;
+        const int32_t d = reduce ? (1 << step) : (1 << (total_steps - 1 - step));
+        /* send half */
+        for (int32_t r = 0; r < world; ++r) {
+            const int sends = reduce ? (r % (2 * d) == d) : (r % (2 * d) == 0 && r + d < world);
+            if (!sends) continue;
+            memcpy(msg[r], bufs[r], bytes);
+            if (sent) sent[r] += numel;
+        }
+        /* receive half */
+        for (int32_t r = 0; r < world; ++r) {
+            if (reduce) {
+                if (r % (2 * d) == 0 && r + d < world) add_into(dtype, bufs[r], msg[r + d], numel);
+            } else {
+                if (r % (2 * d) == d) memcpy(bufs[r], msg[r - d], bytes);
+            }
+        }
+        if (n_steps < 0 && reduce && step == depth - 1 && divisor > 1)
+            divide_all(dtype, bufs[0], numel, divisor);
+    }
+    if (n_steps < 0 && depth == 0 && divisor > 1) divide_all(dtype, bufs[0], numel, divisor);
+    for (int32_t r = 0; r < world; ++r) free(msg[r]);
+    free(msg);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Bucket plan: reverse registration order, first-bucket cap then bucket cap. */
 /* ------------------------------------------------------------------------ */
 

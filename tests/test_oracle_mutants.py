@@ -14,7 +14,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ddp_oracle.c")
-PINS = ["tests/test_oracle_ring.py", "tests/test_oracle_plan.py"]
+PINS = ["tests/test_oracle_ring.py", "tests/test_oracle_plan.py", "tests/test_oracle_tree.py"]
 
 MUTANTS = {
     "rs_send_chunk_off_by_one": ("? mod((int64_t)r - s, world) :", "? mod((int64_t)r - s - 1, world) :"),
@@ -35,6 +35,11 @@ MUTANTS = {
                            "for (int32_t p = 0; p < n_params; ++p) {"),
     "plan_first_cap_everywhere": ("int64_t cap = (k == 0) ? first_cap_bytes : cap_bytes;",
                                   "int64_t cap = first_cap_bytes;"),
+    "tree_reduce_distances_reversed": ("const int32_t d = reduce ? (1 << step) : (1 << (total_steps - 1 - step));",
+                                       "const int32_t d = reduce ? (1 << (depth - 1 - step)) : (1 << (total_steps - 1 - step));"),
+    "tree_broadcast_wrong_sender": ("if (r % (2 * d) == d) memcpy(bufs[r], msg[r - d], bytes);",
+                                    "if (r % (2 * d) == d) memcpy(bufs[r], msg[r], bytes);"),
+    "tree_divide_dropped": ("if (n_steps < 0 && reduce && step == depth - 1 && divisor > 1)", "if (0)"),
     "plan_drops_trailing_bucket": ("    if (members > 0) {\n        bucket_numel[k] = elems;",
                                    "    if (0) {\n        bucket_numel[k] = elems;"),
 }
