@@ -491,7 +491,8 @@ def run_sweep(args):
             status = torch.zeros(2, dtype=torch.int32, device=dev)
             persistent = lambda b, d: ddp.ring_allreduce_persistent(b, d, status=status)   # noqa: E731
             for name, fn in (("fused", ddp.ring_allreduce_fused), ("staged", ddp.ring_allreduce_staged),
-                             ("persistent", persistent)):
+                             ("persistent", persistent), ("tree_fused", ddp.tree_allreduce_fused),
+                             ("tree_staged", ddp.tree_allreduce_staged)):
                 s = torch.cuda.Stream()
                 with torch.cuda.stream(s):
                     for _ in range(3):
@@ -512,10 +513,12 @@ def run_sweep(args):
                     torch.cuda.synchronize()
                     t = e0.elapsed_time(e1) / reps
                     best = t if best is None else min(best, t)
-                alg = (2 * N * s_bytes) if name == "fused" else (5 * (N - 1) * s_bytes)
+                depth = (N - 1).bit_length()
+                alg = {"fused": 2 * N * s_bytes, "tree_fused": 2 * N * s_bytes,
+                       "tree_staged": 5 * (N - 1) * s_bytes}.get(name, 5 * (N - 1) * s_bytes)
                 row[name] = {"us_per_call": best * 1e3, "busbw_gbs": 2 * (N - 1) / N * s_bytes / (best / 1e3) / 1e9,
                              "hbm_alg_gbs": alg / (best / 1e3) / 1e9,
-                             "launches_per_call": 2 * (N - 1) if name == "staged" else 1}
+                             "launches_per_call": {"staged": 2 * (N - 1), "tree_staged": 2 * depth}.get(name, 1)}
                 if name == "persistent":
                     assert int(status[0]) == 0, "persistent ring reported a barrier timeout"
                 del g

@@ -38,7 +38,8 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
            "ddp_plan_buckets",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ddp_bucket_pack_bf16", "ddp_bucket_unpack_bf16",
-           "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "ring_allreduce_fused_from_host",
+           "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "tree_allreduce_fused",
+           "tree_allreduce_staged", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view",
            "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.ddp_bucket_unpack_bf16.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, vp]
             L.ring_allreduce_fused.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
+            L.tree_allreduce_fused.argtypes = [i32, P(vp), i64, i32, i32, vp]
+            L.tree_allreduce_staged.argtypes = [i32, P(vp), i64, i32, i32, vp]
             L.ring_allreduce_persistent.argtypes = [i32, P(vp), i64, i32, i32, vp, i32, i32, vp]
             L.ring_allreduce_fused_from_host.argtypes = [i32, P(vp), P(vp), P(vp), i64, i32, i32, vp]
             L.ring_allreduce_fused_from_host_noalloc.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp]
@@ -231,6 +234,20 @@ def ring_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
                                                                 _stream(stream)))
 
 
+def tree_allreduce_fused(bufs, divisor: int = 0, stream=None) -> None:
+    """In-place binomial-tree allreduce (+ divide), one pass; world <= 64."""
+    ptrs, numel, code = _rank_ptrs(bufs)
+    _check("tree_allreduce_fused", lib().tree_allreduce_fused(len(ptrs), _vp_array(ptrs), numel, code, divisor,
+                                                              _stream(stream)))
+
+
+def tree_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
+    """In-place binomial-tree allreduce, one launch per tree step (2 ceil(log2 N))."""
+    ptrs, numel, code = _rank_ptrs(bufs)
+    _check("tree_allreduce_staged", lib().tree_allreduce_staged(len(ptrs), _vp_array(ptrs), numel, code, divisor,
+                                                                _stream(stream)))
+
+
 def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step: int = -1, wait_limit_ms: int = 0,
                               stream=None):
     """Staged ring in one cooperative launch with bounded barriers.
@@ -242,7 +259,8 @@ def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step:
     torch = _torch()
     if status is None:
         status = torch.zeros(2, dtype=torch.int32, device=_rank_tensors(bufs)[0].device)
-    _check("ring_allreduce_persistent",
+    _check("ring_allreduce_persistent", "tree_allreduce_fused",
+           "tree_allreduce_staged",
            lib().ring_allreduce_persistent(len(ptrs), _vp_array(ptrs), numel, code, divisor, status.data_ptr(),
                                            fail_at_step, wait_limit_ms, _stream(stream)))
     return status

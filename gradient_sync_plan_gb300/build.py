@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libddp_gb300.so")
 
-SOURCES = ["ring_kernels.cu", "ring_tma.cu", "ring_static.cu", "ring_persistent.cu", "bucket_kernels.cu", "ddp_api.cpp", "ddp_planner.cpp", "reducer.cpp"]
+SOURCES = ["ring_kernels.cu", "ring_tma.cu", "ring_static.cu", "ring_persistent.cu", "tree_kernels.cu", "bucket_kernels.cu", "ddp_api.cpp", "ddp_planner.cpp", "reducer.cpp"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

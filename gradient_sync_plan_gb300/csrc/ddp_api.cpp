@@ -301,6 +301,29 @@ int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, i
     return cuda_status(launch_ring_staged(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
 }
 
+static int32_t tree_common(bool staged, int32_t world, void* const* bufs, int64_t numel, int32_t dtype,
+                           int32_t divisor, void* stream) {
+    int32_t st = common_checks(world, numel, dtype);
+    if (st) return st;
+    if (!staged && world > 64) return DDP_ERR_CAPACITY;
+    if (divisor < 0) return DDP_ERR_INVALID;
+    if (numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
+    return cuda_status(launch_tree_allreduce(staged, world, bufs, numel, dtype, make_div(divisor), vec,
+                                             (cudaStream_t)stream));
+}
+
+int32_t tree_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                             void* stream) {
+    return tree_common(false, world, bufs, numel, dtype, divisor, stream);
+}
+
+int32_t tree_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                              void* stream) {
+    return tree_common(true, world, bufs, numel, dtype, divisor, stream);
+}
+
 int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                                   int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream) {
     int32_t st = common_checks(world, numel, dtype);

@@ -49,6 +49,9 @@ cudaError_t launch_ring_staged(int world, void* const* ptrs, int64_t numel, int 
 // (ring_persistent.cu).  ws: device int32[2] = {status, arrivals}.
 cudaError_t launch_ring_persistent(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
                                    int32_t* ws, int skip_step, unsigned long long limit_ns, cudaStream_t stream);
+// Binomial-tree allreduce (tree_kernels.cu): fused (world <= 64) or one launch per step.
+cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                                  bool vec_ok, cudaStream_t stream);
 cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,
                               bool vec_ok, cudaStream_t stream);
 

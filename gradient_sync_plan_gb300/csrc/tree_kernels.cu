@@ -1,0 +1,202 @@
+// tree_kernels.cu -- binomial-tree allreduce over N logical ranks.
+//
+// The pages name a tree-based allreduce as the alternative to the ring when
+// messages are small ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事",
+// section 02 and section 07: NCCL's Tree algorithm and its small-message
+// threshold).  Reading taken (the pages give no definition): a binomial tree
+// over the whole vector.  Reduce steps d = 1, 2, 4, ... < N: rank r with
+// r mod 2d == 0 adds the buffer of rank r + d into its own; rank 0 then holds
+// the sum and divides it; broadcast steps run the distances in reverse and
+// copy rank r's buffer to rank r + d.  Every element is therefore summed in
+// the binomial pairwise order ((x0 + x1) + (x2 + x3)) + ..., the same for all
+// elements, in 2 ceil(log2 N) steps instead of the ring's 2(N-1).
+//
+//   k_tree_fused  one pass: every element folded in that order, divided,
+//                 written to every rank (N <= 64)
+//   k_tree_hop    one launch per tree step, moving exactly what the step moves
+#include <algorithm>
+#include <cstdio>
+
+#include "ddp_device.cuh"
+#include "ddp_internal.h"
+
+namespace ddpk {
+
+template <int CAP>
+struct TreeTable {
+    char* p[CAP];
+};
+
+constexpr int kTreeGroup = 16;
+constexpr int kTreeMaxWorld = 4 * kTreeGroup;   // 64
+
+// Binomial pairwise sum of load(0) .. load(world - 1), world <= 64.  Ranks are
+// folded in groups of 16 (levels 1, 2, 4, 8 inside a group), then the group
+// sums at levels 16 and 32 -- exactly the tree's additions, in its order.
+template <class T, class Add, class Load>
+__device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
+    T gs[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (kTreeGroup * g < world) {
+            T v[kTreeGroup];
+#pragma unroll
+            for (int i = 0; i < kTreeGroup; ++i)
+                if (kTreeGroup * g + i < world) v[i] = load(kTreeGroup * g + i);
+#pragma unroll
+            for (int d = 1; d < kTreeGroup; d <<= 1)
+#pragma unroll
+                for (int i = 0; i < kTreeGroup; i += 2 * d)
+                    if (kTreeGroup * g + i + d < world) v[i] = add(v[i], v[i + d]);
+            gs[g] = v[0];
+        }
+    }
+    if (16 < world) gs[0] = add(gs[0], gs[1]);
+    if (48 < world) gs[2] = add(gs[2], gs[3]);
+    if (32 < world) gs[0] = add(gs[0], gs[2]);
+    return gs[0];
+}
+
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel, int vec_ok, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t done = 0;
+    if (vec_ok) {
+        const int64_t nv = numel / L;
+        for (int64_t v = tid; v < nv; v += stride) {
+            const int64_t off = v * 16;
+            V y = tree_fold<V>(world, [](V a, V b) { return E::vadd(a, b); },
+                               [&](int r) { return ld_stream<V>(t.p[r] + off); });
+            y = E::template vdiv<DIV>(y, dop);
+            for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
+        }
+        done = nv * L;
+    }
+    for (int64_t e = done + tid; e < numel; e += stride) {
+        S y = tree_fold<S>(world, [](S a, S b) { return E::sadd(a, b); },
+                           [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
+        y = E::template sdiv<DIV>(y, dop);
+        for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = y;
+    }
+}
+
+// One tree step for every pair at once; blockIdx.y is the pair index, its
+// lower rank is r = blockIdx.y * 2d and its upper rank r + d.
+//   phase 0 (reduce):    buf[r]     = buf[r] (+) buf[r + d]   (divided if `divide`)
+//   phase 1 (broadcast): buf[r + d] = buf[r]
+// Within a step, the ranks written and the ranks read are disjoint sets.
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kThreads)
+k_tree_hop(const __grid_constant__ TreeTable<CAP> t, int64_t numel, int d, int phase, int divide, int vec_ok,
+           float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    const int r = blockIdx.y * 2 * d;
+    char* lo_buf = t.p[r];
+    char* hi_buf = t.p[r + d];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t done = 0;
+    if (vec_ok) {
+        const int64_t nv = numel / L;
+        for (int64_t v = tid; v < nv; v += stride) {
+            const int64_t off = v * 16;
+            if (phase == 0) {
+                V y = E::vadd(ld_stream<V>(lo_buf + off), ld_stream<V>(hi_buf + off));
+                if (DIV != kDivNone && divide) y = E::template vdiv<DIV>(y, dop);
+                st_stream<V>(lo_buf + off, y);
+            } else {
+                st_stream<V>(hi_buf + off, ld_stream<V>(lo_buf + off));
+            }
+        }
+        done = nv * L;
+    }
+    for (int64_t e = done + tid; e < numel; e += stride) {
+        S* a = reinterpret_cast<S*>(lo_buf);
+        S* b = reinterpret_cast<S*>(hi_buf);
+        if (phase == 0) {
+            S y = E::sadd(a[e], b[e]);
+            if (DIV != kDivNone && divide) y = E::template sdiv<DIV>(y, dop);
+            a[e] = y;
+        } else {
+            b[e] = a[e];
+        }
+    }
+}
+
+template <int CAP>
+static TreeTable<CAP> tree_table(int world, void* const* ptrs) {
+    TreeTable<CAP> t{};
+    for (int r = 0; r < world; ++r) t.p[r] = static_cast<char*>(ptrs[r]);
+    return t;
+}
+
+template <class E, int DIV>
+static cudaError_t tree_fused_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
+                                   cudaStream_t st) {
+    auto k = k_tree_fused<E, DIV, kTreeMaxWorld>;
+    const int64_t work = vec_ok ? (numel + E::L - 1) / E::L : numel;
+    const int grid = grid_for((const void*)k, work);
+    k<<<grid, kThreads, 0, st>>>(tree_table<kTreeMaxWorld>(world, ptrs), world, numel, vec_ok ? 1 : 0, dop);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV>
+static cudaError_t tree_staged_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
+                                    cudaStream_t st) {
+    int depth = 0;
+    while ((1 << depth) < world) ++depth;
+    const TreeTable<DDP_MAX_WORLD> t = tree_table<DDP_MAX_WORLD>(world, ptrs);
+    auto launch = [&](int d, int phase, bool divide) -> cudaError_t {
+        const int pairs = (world - d - 1) / (2 * d) + 1;       // r = 0, 2d, ... with r + d < world
+        auto kd = k_tree_hop<E, DIV, DDP_MAX_WORLD>;
+        const int64_t per_pair = vec_ok ? numel / E::L + E::L : numel;
+        int gx = grid_for((const void*)kd, per_pair * pairs);
+        gx = std::max(1, (gx + pairs - 1) / pairs);
+        kd<<<dim3(gx, pairs), kThreads, 0, st>>>(t, numel, d, phase, divide ? 1 : 0, vec_ok ? 1 : 0, dop);
+        return cudaGetLastError();
+    };
+    for (int k = 0; k < depth; ++k) {
+        cudaError_t e = launch(1 << k, 0, k == depth - 1);
+        if (e != cudaSuccess) return e;
+    }
+    for (int k = depth - 1; k >= 0; --k) {
+        cudaError_t e = launch(1 << k, 1, false);
+        if (e != cudaSuccess) return e;
+    }
+    if (debug_enabled())
+        fprintf(stderr, "[ddp] tree_staged world=%d numel=%lld launches=%d\n", world, (long long)numel, 2 * depth);
+    return cudaSuccess;
+}
+
+template <class E>
+static cudaError_t tree_by_div(bool staged, int world, void* const* ptrs, int64_t numel, DivSpec d, bool vec_ok,
+                               cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone:
+            return staged ? tree_staged_impl<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, st)
+                          : tree_fused_impl<E, kDivNone>(world, ptrs, numel, d.operand, vec_ok, st);
+        case kDivPow2:
+            return staged ? tree_staged_impl<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, st)
+                          : tree_fused_impl<E, kDivPow2>(world, ptrs, numel, d.operand, vec_ok, st);
+        default:
+            return staged ? tree_staged_impl<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, st)
+                          : tree_fused_impl<E, kDivIeee>(world, ptrs, numel, d.operand, vec_ok, st);
+    }
+}
+
+cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                                  bool vec_ok, cudaStream_t stream) {
+    if (numel == 0) return cudaSuccess;
+    if (staged && world == 1) staged = false;                 // no step: the divide only
+    if (dtype == DDP_F32) return tree_by_div<EF32>(staged, world, ptrs, numel, div, vec_ok, stream);
+    return tree_by_div<EBF16>(staged, world, ptrs, numel, div, vec_ok, stream);
+}
+
+}  // namespace ddpk

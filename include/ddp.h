@@ -220,6 +220,27 @@ int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, i
                               int32_t divisor, void* stream);
 
 /*
+ * tree_allreduce_fused / tree_allreduce_staged -- the latency-oriented
+ * alternative to the ring for small buckets ([P1] section 02 and section 07:
+ * a tree-based allreduce, NCCL's Tree algorithm below a message-size
+ * threshold).  The pages do not define the tree; this library uses the
+ * binomial tree over the whole vector: reduce steps d = 1, 2, 4, ... < N in
+ * which rank r (r mod 2d == 0) adds rank r+d's buffer into its own, the root
+ * divides, and broadcast steps in reverse order copy rank r's buffer to rank
+ * r+d.  Every element is summed in the pairwise order ((x0+x1)+(x2+x3))+...,
+ * which differs from the ring's, so tree and ring results differ in the last
+ * bits; both are reproducible.  2*ceil(log2 N) steps instead of 2(N-1).
+ *   tree_allreduce_fused   one pass over memory; world <= 64 (DDP_ERR_CAPACITY)
+ *   tree_allreduce_staged  one launch per tree step; world <= DDP_MAX_WORLD
+ * Arguments, dtypes, rounding (bf16: one rounding per addition) and the
+ * divide as for ring_allreduce_fused.
+ */
+int32_t tree_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                             void* stream);
+int32_t tree_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
+                              void* stream);
+
+/*
  * ring_allreduce_persistent -- ring_allreduce_staged in ONE cooperative
  * launch: the same 2(N-1) steps and the same bit-identical result ([P1]
  * section 03; [P3] §1.3.2), with the steps separated by grid-wide barriers

@@ -174,3 +174,12 @@ def test_persistent_rejects_bad_arguments_on_host():
     assert f(2, _vp(A, B), 8, 0, 2, i32p, -1, -5, None) == -1                      # negative wait limit
     assert f(2, _vp(A, A + 4), 8, 0, 2, i32p, -1, 0, None) == -1                   # overlapping ranks
 
+
+def test_tree_rejects_bad_arguments_on_host():
+    L = ddp.lib()
+    tab = (ctypes.c_void_p * 65)(*[0x7f0000000000 + r * (1 << 20) for r in range(65)])
+    assert L.tree_allreduce_fused(65, tab, 8, 0, 65, None) == -5     # fused tree: at most 64 ranks
+    assert L.tree_allreduce_staged(0, tab, 8, 0, 1, None) == -1
+    assert L.tree_allreduce_staged(2, tab, 8, 5, 2, None) == -1      # dtype
+    assert L.tree_allreduce_fused(2, _vp(0x7f0000000000, 0x7f0000000004), 8, 0, 2, None) == -1   # overlap
+

@@ -1,0 +1,90 @@
+"""GPU parity of the tree allreduce kernels against the oracle's binomial tree.
+
+tree_allreduce_fused and tree_allreduce_staged, through the C ABI, bit-exact
+against oracle.tree_allreduce on the same seeded inputs: every N in 1..9 with
+every S in 0..70, larger N (fused up to 64, staged beyond), ragged multi-tile
+sizes, buffers that are not 16-byte aligned, and a sampled check on an
+8 x 1 GiB bucket (the tree folds every element in the same order, so sampled
+columns go straight through the oracle).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_plan_gb300 as ddp
+import oracle
+import workloads
+from gpu_util import assert_bits_equal, f32_or_bits, from_np
+
+pytestmark = pytest.mark.gpu
+
+TREE = {"fused": ddp.tree_allreduce_fused, "staged": ddp.tree_allreduce_staged}
+
+
+def oracle_tree(x, divisor):
+    y = np.ascontiguousarray(x).copy()
+    oracle.tree_allreduce_2d(y, oracle.BF16 if y.dtype == np.uint16 else oracle.F32, divisor)
+    return y
+
+
+def run(kernel, xh, divisor):
+    x = from_np(xh)
+    TREE[kernel](x, divisor)
+    torch.cuda.synchronize()
+    return f32_or_bits(x)
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_exhaustive_small(kernel, dtype):
+    for N in range(1, 10):
+        for S in range(0, 71):
+            xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", dtype=dtype, seed0=N * 77 + S))
+            for div in (0, N):
+                assert_bits_equal(run(kernel, xh, div), oracle_tree(xh, div), f"tree {kernel} N={N} S={S}")
+
+
+@pytest.mark.parametrize("kernel,N", [("fused", 16), ("fused", 17), ("fused", 33), ("fused", 48), ("fused", 49),
+                                      ("fused", 64), ("staged", 64), ("staged", 100)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_many_ranks(kernel, N, dtype):
+    xh = f32_or_bits(workloads.rank_vectors(N, 1029, "randn", std=1e-2, dtype=dtype, seed0=N))
+    assert_bits_equal(run(kernel, xh, N), oracle_tree(xh, N), f"tree {kernel} N={N}")
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+@pytest.mark.parametrize("N,S", [(3, 1_000_003), (8, (1 << 20) + 5), (5, 777_777)])
+def test_many_tiles_ragged(kernel, N, S):
+    for dtype in ("f32", "bf16"):
+        xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=1))
+        assert_bits_equal(run(kernel, xh, N), oracle_tree(xh, N), f"tree {kernel} N={N} S={S} {dtype}")
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_unaligned(kernel):
+    N, S = 6, 5000
+    x = workloads.rank_vectors(N, S, "randn", seed0=2)
+    store = torch.zeros((N, S + 8), device="cuda")
+    rows = [store[r, 3:3 + S] for r in range(N)]
+    for r in range(N):
+        rows[r].copy_(x[r].cuda())
+    TREE[kernel](rows, N)
+    torch.cuda.synchronize()
+    assert_bits_equal(np.stack([f32_or_bits(r) for r in rows]), oracle_tree(x.numpy(), N), f"unaligned {kernel}")
+
+
+@pytest.mark.parametrize("kernel", ["fused", "staged"])
+def test_one_gib_buckets_sampled(kernel):
+    N, S = 8, 1 << 28
+    x = torch.empty((N, S), device="cuda")
+    for r in range(N):
+        x[r].copy_(workloads.randn_f32(S, r, 1e-2, device="cuda"))
+    idx = torch.from_numpy(np.random.default_rng(0).integers(0, S, size=5000)).cuda()
+    samples = f32_or_bits(x[:, idx])
+    TREE[kernel](x, N)
+    torch.cuda.synchronize()
+    assert_bits_equal(f32_or_bits(x[:, idx]), oracle_tree(samples, N), f"1 GiB {kernel}")
+    for r in range(1, N):
+        assert torch.equal(x[r].view(torch.int32), x[0].view(torch.int32))
+    del x
+    torch.cuda.empty_cache()
