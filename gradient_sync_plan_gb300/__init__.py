@@ -259,8 +259,7 @@ def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step:
     torch = _torch()
     if status is None:
         status = torch.zeros(2, dtype=torch.int32, device=_rank_tensors(bufs)[0].device)
-    _check("ring_allreduce_persistent", "tree_allreduce_fused",
-           "tree_allreduce_staged",
+    _check("ring_allreduce_persistent",
            lib().ring_allreduce_persistent(len(ptrs), _vp_array(ptrs), numel, code, divisor, status.data_ptr(),
                                            fail_at_step, wait_limit_ms, _stream(stream)))
     return status
