@@ -187,6 +187,17 @@ def cpu_oracle_run(n_ranks: int, budget_s: float, max_numel: int, reps_cap: int 
             "hbm_equiv_gbs": 2 * n_ranks * s_bytes / tm / 1e9}
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -212,7 +223,7 @@ def run_reference(args, rank: int, world: int):
     t = time.perf_counter()
     oracle.ring_allreduce(rows, oracle.F32, N_RANKS)
     per_elem = max((time.perf_counter() - t) / cal, 1e-10)
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     numel = int(min(NUMEL, max(1 << 12, budget / per_elem)))
     numel = 1 << int(math.log2(numel))
     x = workloads.rank_vectors(N_RANKS, numel, "randn", std=1e-2).numpy()
@@ -294,11 +305,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if sampler:
         sampler.mark_end()
     barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     if sampler:
         sampler.stop()
     ms_step = ms / args.steps
@@ -343,12 +350,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 fn()
             ev1.record(stream)
             torch.cuda.synchronize()
-            t_ms = ev0.elapsed_time(ev1)
-            if world > 1:
-                tt = torch.tensor([t_ms], device=dev)
-                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-                t_ms = float(tt.item())
-            return t_ms / steps
+            return max_over_ranks(ev0.elapsed_time(ev1), world, dev) / steps
 
         # the kernel reads the pinned host buffers and writes the result back
         # to them over the CPU-GPU link: both directions at once, no device copy
@@ -645,6 +647,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle work to size the per-step sample for")
     ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.steps >= 10:
