@@ -257,10 +257,25 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
         const int64_t base = b.offset[m];          // bucket position of element 0
         auto at = [&](int r) -> const char* { return b.ptr[m * world + r]; };
         if (b.vec[m]) {
+            // chunk of the tile's first element and where (member-relative)
+            // the next chunk starts: most vectors are placed by one compare
+            const int64_t j_first = (base + e0) / b.clen;
+            const int64_t next_start = (j_first + 1) * b.clen - base;
             for (int64_t e = e0 + (int64_t)threadIdx.x * L; e < e1; e += (int64_t)blockDim.x * L) {
                 const int64_t q = base + e;
-                const int64_t j = q / b.clen;
-                if (e + L <= e1 && (q + L - 1) / b.clen == j) {
+                int64_t j;
+                bool whole;
+                if (e + L <= next_start) {
+                    j = j_first;
+                    whole = e + L <= e1;
+                } else if (e >= next_start && e + L <= next_start + b.clen) {
+                    j = j_first + 1;
+                    whole = e + L <= e1;
+                } else {
+                    j = q / b.clen;
+                    whole = e + L <= e1 && (q + L - 1) / b.clen == j;
+                }
+                if (whole) {
                     const int start = (j + 1 == world) ? 0 : (int)j + 1;
                     V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, e * (int64_t)sizeof(S)), dop);
                     for (int r = 0; r < world; ++r) st_stream<V>(b.ptr[m * world + r] + e * (int64_t)sizeof(S), y);
