@@ -347,9 +347,40 @@ static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, D
     }
 }
 
+// Cut every member at the bucket's chunk boundaries; true if the TMA-staged
+// kernel can take the bucket (16-byte aligned pointers, segment starts and
+// lengths, a world size the tiles fit, enough bytes to be worth it).
+static bool view_segments(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
+                          std::vector<ViewSegment>* segs) {
+    const int64_t es = elem_bytes(dtype);
+    if (world > 128 || tma_tile_bytes(world) == 0 || bucket_numel * es * world < ((int64_t)4 << 20)) return false;
+    const int64_t clen = chunk_len(bucket_numel, world);
+    segs->clear();
+    for (int i = 0; i < n; ++i) {
+        const ViewMember& m = members[i];
+        if (!m.vec_ok) return false;
+        int64_t a = m.offset;
+        const int64_t end = m.offset + m.numel;
+        while (a < end) {
+            const int64_t j = a / clen;
+            const int64_t b = std::min(end, (j + 1) * clen);
+            const ViewSegment g{i, (int32_t)j, a - m.offset, b - a};
+            if ((g.start * es) % 16 || (g.len * es) % 16) return false;
+            segs->push_back(g);
+            a = b;
+        }
+    }
+    return true;
+}
+
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                DivSpec div, cudaStream_t stream) {
     if (n == 0 || bucket_numel == 0) return cudaSuccess;
+    {
+        std::vector<ViewSegment> segs;
+        if (view_segments(world, members, n, bucket_numel, dtype, &segs))
+            return launch_bucket_view_tma(world, members, n, segs.data(), (int)segs.size(), dtype, div, stream);
+    }
     if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
     return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
 }

@@ -92,4 +92,17 @@ struct ViewMember {
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                DivSpec div, cudaStream_t stream);
 
+// A piece of one member that lies inside one ring chunk of its bucket:
+// elements [start, start + len) of member `member`, summed from rank j + 1.
+struct ViewSegment {
+    int32_t member;
+    int32_t j;
+    int64_t start;
+    int64_t len;
+};
+// TMA-staged view kernel (ring_tma.cu): members' pointers 16-byte aligned,
+// every segment's start and length multiples of 16 bytes.
+cudaError_t launch_bucket_view_tma(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
+                                   int n_segs, int dtype, DivSpec div, cudaStream_t stream);
+
 }  // namespace ddpk

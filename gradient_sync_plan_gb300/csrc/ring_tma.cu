@@ -247,6 +247,138 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 }
 
 // ---------------------------------------------------------------------------
+// The fused view path (pack + ring + average + unpack of one bucket) with the
+// same producer / consumer structure.  The host cuts every member of the
+// bucket at the bucket's chunk boundaries into segments; a segment has one
+// ring start rank, and tiles are cut inside segments, so a tile never crosses
+// a chunk.  Tiles are numbered segment after segment; each CTA walks its
+// tiles k, k + G, ... and finds their segment by scanning forward.
+// ---------------------------------------------------------------------------
+
+constexpr int kViewSegs = 160;
+constexpr int kViewPtrCap = 2048;
+
+struct ViewTmaBatch {
+    int32_t n_seg;
+    int32_t world;
+    int64_t tile;                    // elements per tile
+    int64_t tile_end[kViewSegs];     // inclusive prefix of tiles per segment
+    int64_t start[kViewSegs];        // first element of the segment in its member
+    int64_t len[kViewSegs];
+    int32_t j[kViewSegs];            // ring chunk of the segment
+    int32_t mem[kViewSegs];          // member slot: its rank pointers are ptr[mem * world ..]
+    char* ptr[kViewPtrCap];
+};
+
+struct SegCursor {
+    int seg;
+    __device__ void seek(const ViewTmaBatch& b, int64_t k) {
+        while (b.tile_end[seg] <= k) ++seg;
+    }
+    __device__ void range(const ViewTmaBatch& b, int64_t k, int64_t& e0, int64_t& n) const {
+        const int64_t first = seg ? b.tile_end[seg - 1] : 0;
+        const int64_t off = (k - first) * b.tile;
+        e0 = b.start[seg] + off;
+        n = (b.len[seg] - off < b.tile) ? b.len[seg] - off : b.tile;
+    }
+};
+
+template <class E, int DIV>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    constexpr int kConsumers = 32 * kTmaConsumerWarps;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int world = b.world;
+    const int64_t tile_bytes = b.tile * (int64_t)sizeof(S);
+    unsigned char* stages = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTmaStages * world * tile_bytes);
+    uint64_t* empty = full + kTmaStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
+    const int64_t total = b.tile_end[b.n_seg - 1];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kTmaConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kTmaConsumerWarps) {
+        if (lane != 0) return;
+        SegCursor sc{0};
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < total; k += G, ++it) {
+            const int s = it % kTmaStages;
+            if (it >= kTmaStages && !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u)) {
+                atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
+                break;
+            }
+            sc.seek(b, k);
+            int64_t e0, n;
+            sc.range(b, k, e0, n);
+            const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(S));
+            mbar_arrive_expect_tx(&full[s], bytes * (uint32_t)world);
+            unsigned char* dst = stages + (size_t)s * world * tile_bytes;
+            char* const* pp = b.ptr + (size_t)b.mem[sc.seg] * world;
+            for (int r = 0; r < world; ++r)
+                bulk_load(dst + (size_t)r * tile_bytes, pp[r] + e0 * (int64_t)sizeof(S), bytes, &full[s]);
+        }
+        for (int q = 1; q <= kTmaStages && it - q >= 0; ++q) {
+            const int i2 = it - q;
+            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u);
+        }
+        return;
+    }
+
+    SegCursor sc{0};
+    int it = 0;
+    for (int64_t k = blockIdx.x; k < total; k += G, ++it) {
+        const int s = it % kTmaStages;
+        sc.seek(b, k);
+        int64_t e0, n;
+        sc.range(b, k, e0, n);
+        const int j = b.j[sc.seg];
+        char* const* pp = b.ptr + (size_t)b.mem[sc.seg] * world;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u)) {
+            atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
+            break;
+        }
+        const int start = (j + 1 == world) ? 0 : j + 1;
+        const int nv = (int)(n / L);
+        const unsigned char* sb = stages + (size_t)s * world * tile_bytes;
+        V y[kTmaMaxVec];
+#pragma unroll
+        for (int u = 0; u < kTmaMaxVec; ++u) {
+            const int v = threadIdx.x + u * kConsumers;
+            if (v < nv) {
+                int r = start;
+                V acc = reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v];
+                for (int q = 1; q < world; ++q) {
+                    r = (r + 1 == world) ? 0 : r + 1;
+                    acc = E::vadd(acc, reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]);
+                }
+                y[u] = E::template vdiv<DIV>(acc, dop);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+        for (int u = 0; u < kTmaMaxVec; ++u) {
+            const int v = threadIdx.x + u * kConsumers;
+            if (v < nv)
+                for (int r = 0; r < world; ++r)
+                    st_stream<V>(pp[r] + e0 * (int64_t)sizeof(S) + (int64_t)v * 16, y[u]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -343,6 +475,91 @@ cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, i
                                   cudaStream_t stream) {
     if (dtype == DDP_F32) return tma_div<EF32>(world, ptrs, numel, div, stream);
     return tma_div<EBF16>(world, ptrs, numel, div, stream);
+}
+
+template <class E, int DIV>
+static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
+                                   int n_segs, float dop, cudaStream_t st) {
+    auto k = k_bucket_view_tma<E, DIV>;
+    const int64_t tile_bytes = tma_tile_bytes(world);
+    const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
+    const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_tma_mu);
+        FnState& fs = g_tma_fn[std::make_pair(dev, (const void*)k)];
+        if (smem > fs.smem_attr) {
+            cudaError_t e =
+                cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            fs.smem_attr = smem;
+        }
+        auto it = fs.per_sm.find(smem);
+        if (it != fs.per_sm.end()) {
+            per_sm = it->second;
+        } else {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTmaThreads, smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm <= 0) per_sm = 1;
+            fs.per_sm[smem] = per_sm;
+        }
+    }
+    // launches take consecutive members (and all their segments) while the
+    // pointer and segment tables have room
+    const int max_members = kViewPtrCap / world;
+    ViewTmaBatch b;
+    b.world = world;
+    b.tile = tile;
+    int si = 0;
+    while (si < n_segs) {
+        b.n_seg = 0;
+        int64_t tiles = 0;
+        int first_member = segs[si].member, slots = 0, last_member = -1;
+        while (si < n_segs && b.n_seg < kViewSegs) {
+            const ViewSegment& g = segs[si];
+            if (g.member != last_member) {
+                if (slots == max_members) break;
+                const ViewMember& m = members[g.member];
+                for (int r = 0; r < world; ++r) b.ptr[(size_t)slots * world + r] = static_cast<char*>(m.ptrs[r]);
+                last_member = g.member;
+                ++slots;
+            }
+            tiles += (g.len + tile - 1) / tile;
+            b.tile_end[b.n_seg] = tiles;
+            b.start[b.n_seg] = g.start;
+            b.len[b.n_seg] = g.len;
+            b.j[b.n_seg] = g.j;
+            b.mem[b.n_seg] = slots - 1;
+            ++b.n_seg;
+            ++si;
+        }
+        (void)first_member;
+        if (b.n_seg == 0) break;
+        const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, tiles));
+        k<<<grid, kTmaThreads, smem, st>>>(b, dop);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <class E>
+static cudaError_t view_tma_div(int world, const ViewMember* m, int nm, const ViewSegment* sg, int ns, DivSpec d,
+                                cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return view_tma_launch<E, kDivNone>(world, m, nm, sg, ns, d.operand, st);
+        case kDivPow2: return view_tma_launch<E, kDivPow2>(world, m, nm, sg, ns, d.operand, st);
+        default: return view_tma_launch<E, kDivIeee>(world, m, nm, sg, ns, d.operand, st);
+    }
+}
+
+cudaError_t launch_bucket_view_tma(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
+                                   int n_segs, int dtype, DivSpec div, cudaStream_t stream) {
+    if (n_segs == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return view_tma_div<EF32>(world, members, n_members, segs, n_segs, div, stream);
+    return view_tma_div<EBF16>(world, members, n_members, segs, n_segs, div, stream);
 }
 
 cudaError_t read_device_status(int32_t* out, bool clear) {

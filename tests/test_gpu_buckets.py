@@ -287,3 +287,28 @@ def test_bf16_pack_unpack_round_trip_matches_oracle_rounding():
             assert_bits_equal(got_bits, want_bits, f"pack r{r} m{i}")
             assert_bits_equal(f32_or_bits(out[r][i]), oracle.bf16_to_f32(want_bits), f"unpack r{r} m{i}")
 
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_view_tma_path_matches_oracle(dtype):
+    # one bucket of ~1.2M elements over 8 ranks (> 4 MiB): member sizes and the
+    # chunk length are multiples of 16 elements, so the view path streams
+    # chunk-aligned segments through shared memory; one member spans several
+    # chunks, others end inside a chunk
+    world = 8
+    numels = [16 * 7, 16 * 40000, 16 * 3, 16 * 25000, 16 * 1000, 16 * 9001]
+    total = sum(numels)
+    assert (-(-total // world)) % 16 == 0
+    code = ddp.BF16 if dtype == "bf16" else ddp.F32
+    es = 2 if dtype == "bf16" else 4
+    assert total * es * world >= 4 << 20
+    plan = ddp.ddp_plan_buckets(numels, code, 1 << 40, 1 << 40)
+    assert len(plan[2]) == 1
+    flat, grads_h = _host_grads(numels, world, dtype, seed0=6)
+    g = flat.cuda()
+    ddp.ddp_sync_buckets(_device_views(g, numels), plan, None, algo=ddp.DDP_ALGO_VIEW)
+    torch.cuda.synchronize()
+    oracle.ddp_sync(grads_h, code, 1 << 40, 1 << 40)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"view tma {dtype}")
+    assert ddp.ddp_device_status() == 0
+
