@@ -295,7 +295,7 @@ def test_view_tma_path_matches_oracle(dtype):
     # chunk-aligned segments through shared memory; one member spans several
     # chunks, others end inside a chunk
     world = 8
-    numels = [16 * 7, 16 * 40000, 16 * 3, 16 * 25000, 16 * 1000, 16 * 9001]
+    numels = [16 * 7, 16 * 40000, 16 * 3, 16 * 25000, 16 * 1000, 16 * 9006]
     total = sum(numels)
     assert (-(-total // world)) % 16 == 0
     code = ddp.BF16 if dtype == "bf16" else ddp.F32
