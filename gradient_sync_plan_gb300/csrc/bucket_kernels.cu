@@ -347,16 +347,14 @@ static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, D
     }
 }
 
-// Cut every member at the bucket's chunk boundaries; true if the TMA-staged
-// kernel can take the bucket (16-byte aligned pointers, segment starts and
-// lengths, a world size the tiles fit, enough bytes to be worth it).
-static bool view_segments(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
-                          std::vector<ViewSegment>* segs) {
+// Cut members [first, first + n) of one bucket at the bucket's chunk
+// boundaries into segments (member indices are global); false if a pointer,
+// a segment start or a segment length is not 16-byte aligned.
+static bool append_segments(int world, const ViewMember* members, int first, int n, int64_t bucket_numel, int dtype,
+                            std::vector<ViewSegment>* segs) {
     const int64_t es = elem_bytes(dtype);
-    if (world > 128 || tma_tile_bytes(world) == 0 || bucket_numel * es * world < ((int64_t)4 << 20)) return false;
     const int64_t clen = chunk_len(bucket_numel, world);
-    segs->clear();
-    for (int i = 0; i < n; ++i) {
+    for (int i = first; i < first + n; ++i) {
         const ViewMember& m = members[i];
         if (!m.vec_ok) return false;
         int64_t a = m.offset;
@@ -371,6 +369,43 @@ static bool view_segments(int world, const ViewMember* members, int n, int64_t b
         }
     }
     return true;
+}
+
+// The TMA-staged kernel takes a set of segments when the tiles fit the world
+// size and the bytes moved are worth its set-up.
+static bool view_tma_worth(int world, int64_t elems, int dtype) {
+    return world <= 128 && tma_tile_bytes(world) > 0 && elems * elem_bytes(dtype) * world >= ((int64_t)4 << 20);
+}
+
+static bool view_segments(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
+                          std::vector<ViewSegment>* segs) {
+    if (!view_tma_worth(world, bucket_numel, dtype)) return false;
+    segs->clear();
+    return append_segments(world, members, 0, n, bucket_numel, dtype, segs);
+}
+
+cudaError_t launch_buckets_view(int world, const ViewMember* members, const int* bucket_first, const int* bucket_count,
+                                const int64_t* bucket_numel, int n_buckets, int dtype, DivSpec div,
+                                cudaStream_t stream) {
+    // every bucket's segments in one set of launches when all of them are
+    // aligned; otherwise bucket by bucket
+    std::vector<ViewSegment> segs;
+    int64_t elems = 0;
+    bool ok = true;
+    for (int k = 0; k < n_buckets && ok; ++k) {
+        ok = append_segments(world, members, bucket_first[k], bucket_count[k], bucket_numel[k], dtype, &segs);
+        elems += bucket_numel[k];
+    }
+    int n_members = 0;
+    for (int k = 0; k < n_buckets; ++k) n_members = std::max(n_members, bucket_first[k] + bucket_count[k]);
+    if (ok && view_tma_worth(world, elems, dtype))
+        return launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(), dtype, div, stream);
+    for (int k = 0; k < n_buckets; ++k) {
+        cudaError_t e = launch_bucket_view(world, members + bucket_first[k], bucket_count[k], bucket_numel[k], dtype,
+                                           div, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,

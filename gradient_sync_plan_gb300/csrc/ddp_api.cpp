@@ -522,6 +522,41 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
         if (k < 0 || k >= n_buckets) return DDP_ERR_INVALID;
         members[k].push_back(p);
     }
+    if (algo == DDP_ALGO_VIEW) {
+        // validate every bucket, then sync all of them together
+        std::vector<ViewMember> all;
+        std::vector<std::vector<void*>> tables;
+        std::vector<int> first(n_buckets), count(n_buckets);
+        tables.reserve(n_params);
+        for (int32_t k = 0; k < n_buckets; ++k) {
+            auto& m = members[k];
+            std::sort(m.begin(), m.end(),
+                      [&](int32_t a, int32_t b) { return offset_of_param[a] < offset_of_param[b]; });
+            const int32_t n = (int32_t)m.size();
+            std::vector<void*> g((size_t)world * n);
+            std::vector<int64_t> ne(n), off(n);
+            for (int32_t i = 0; i < n; ++i) {
+                ne[i] = numel[m[i]];
+                off[i] = offset_of_param[m[i]];
+                for (int32_t r = 0; r < world; ++r) g[(size_t)r * n + i] = grads[(size_t)r * n_params + m[i]];
+            }
+            std::vector<ViewMember> vm;
+            st = view_members(world, n, g.data(), ne.data(), off.data(), bucket_numel[k], dtype, &vm);
+            if (st) return st;
+            first[k] = (int)all.size();
+            size_t q = 0;
+            for (int32_t i = 0; i < n; ++i) {
+                if (ne[i] == 0) continue;
+                tables.emplace_back(world);
+                for (int32_t r = 0; r < world; ++r) tables.back()[r] = g[(size_t)r * n + i];
+                vm[q].ptrs = tables.back().data();
+                all.push_back(vm[q++]);
+            }
+            count[k] = (int)all.size() - first[k];
+        }
+        return cuda_status(launch_buckets_view(world, all.data(), first.data(), count.data(), bucket_numel, n_buckets,
+                                               dtype, make_div(divisor), (cudaStream_t)stream));
+    }
     std::vector<const void*> g;
     std::vector<int64_t> ne, off;
     std::vector<void*> bk(world);

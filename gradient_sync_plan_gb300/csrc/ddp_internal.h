@@ -92,6 +92,12 @@ struct ViewMember {
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                DivSpec div, cudaStream_t stream);
 
+// Several buckets' view syncs at once: bucket k is members
+// [bucket_first[k], bucket_first[k] + bucket_count[k]) of `members`.
+cudaError_t launch_buckets_view(int world, const ViewMember* members, const int* bucket_first, const int* bucket_count,
+                                const int64_t* bucket_numel, int n_buckets, int dtype, DivSpec div,
+                                cudaStream_t stream);
+
 // A piece of one member that lies inside one ring chunk of its bucket:
 // elements [start, start + len) of member `member`, summed from rank j + 1.
 struct ViewSegment {
