@@ -634,6 +634,66 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
     return res
 
 
+def run_cap_sweep(args):
+    """Bucket-cap sweep (survey config C4 and the pages' 6/12/25/50 MB sweep):
+    the DDP step for ResNet-50 in bf16 at N = 16 (caps 5, 10, 25, 50 MiB) and
+    for the 355M decoder in fp32 at N = 8 (caps 6, 12, 25, 50 MiB), first
+    bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  One
+    JSON line per point."""
+    import torch
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ddp.lib()
+    for model, shapes, N, dtype, caps in (
+            ("resnet50", workloads.resnet50_param_shapes(), 16, "bf16", (5, 10, 25, 50)),
+            ("decoder355m", workloads.decoder_param_shapes(), 8, "f32", (6, 12, 25, 50))):
+        numels = workloads.param_numels(shapes)
+        total = sum(numels)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        es = 2 if dtype == "bf16" else 4
+        g = torch.empty((N, total), dtype=tdt, device=dev)
+        for r in range(N):
+            g[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)).to(tdt))
+        offs = [0]
+        for n in numels:
+            offs.append(offs[-1] + n)
+        views = [[g[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+        for cap in caps:
+            plan = ddp.ddp_plan_buckets(numels, ddp.BF16 if dtype == "bf16" else ddp.F32, MiB, cap * MiB)
+            buckets = [[torch.empty(int(n), dtype=tdt, device=dev) for n in plan[2]] for _ in range(N)]
+            row = {"sweep": "bucket cap", "model": model, "ranks": N, "dtype": dtype, "cap_mib": cap,
+                   "buckets": int(len(plan[2])), "grad_bytes_per_rank": total * es}
+            for name, algo, per_elem in (("pack_fused_unpack", ddp.DDP_ALGO_FUSED, 6), ("view", ddp.DDP_ALGO_VIEW, 2)):
+                call = ddp.SyncCall(views, plan, buckets if algo != ddp.DDP_ALGO_VIEW else None, N, algo)
+                s = torch.cuda.Stream(device=dev)
+                with torch.cuda.stream(s):
+                    for _ in range(3):
+                        call(s)
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=s):
+                    call(s)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                best = None
+                for _ in range(5):
+                    torch.cuda.synchronize()
+                    e0.record()
+                    graph.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    t = e0.elapsed_time(e1)
+                    best = t if best is None else min(best, t)
+                row[name] = {"ms_per_step": best, "hbm_alg_gbs": per_elem * N * total * es / (best / 1e3) / 1e9}
+                del graph
+            print(json.dumps(row), flush=True)
+            del buckets
+            torch.cuda.empty_cache()
+        del g, views
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -649,6 +709,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work to size the per-step sample for")
+    ap.add_argument("--cap-sweep", action="store_true", help="bucket-cap sweep (one JSON line per point) instead")
     ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.steps >= 10:
@@ -667,6 +728,9 @@ def main():
             dist.init_process_group("gloo")
     if args.sweep:
         run_sweep(args)
+        return
+    if args.cap_sweep:
+        run_cap_sweep(args)
         return
     try:
         if args.impl == "reference":
