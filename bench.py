@@ -694,6 +694,42 @@ def run_cap_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_profile_view(args):
+    """A small DDP step for profiling the fused view kernel: a decoder with
+    --profile-layers blocks (d = 1024), N = 8 ranks, fp32, caps 1 / 25 MiB,
+    ddp_sync_buckets with the view algorithm, --steps times.  Prints one JSON
+    line (not a bench result)."""
+    import torch
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    numels = workloads.param_numels(workloads.decoder_param_shapes(n_layer=args.profile_layers))
+    N, total = N_RANKS, sum(numels)
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, MiB, 25 * MiB)
+    g = torch.empty((N, total), dtype=torch.float32, device=dev)
+    for r in range(N):
+        g[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)))
+    offs = [0]
+    for n in numels:
+        offs.append(offs[-1] + n)
+    views = [[g[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+    call = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    print(json.dumps({"profile": "view sync", "layers": args.profile_layers, "params": total, "ranks": N,
+                      "buckets": int(len(plan[2])), "ms_per_step": ms,
+                      "hbm_alg_gbs": 2 * N * total * 4 / (ms / 1e3) / 1e9}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -709,6 +745,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work to size the per-step sample for")
+    ap.add_argument("--profile-view", action="store_true", help="small view-sync run for profiling instead")
+    ap.add_argument("--profile-layers", type=int, default=2)
     ap.add_argument("--cap-sweep", action="store_true", help="bucket-cap sweep (one JSON line per point) instead")
     ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
     args = ap.parse_args()
@@ -731,6 +769,9 @@ def main():
         return
     if args.cap_sweep:
         run_cap_sweep(args)
+        return
+    if args.profile_view:
+        run_profile_view(args)
         return
     try:
         if args.impl == "reference":
