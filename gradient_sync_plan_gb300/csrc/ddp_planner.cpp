@@ -10,6 +10,8 @@
 // closed as soon as its size reaches the cap; the trailing bucket is closed
 // at the end.
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 
 #include "ddp.h"
 
@@ -43,5 +45,13 @@ extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int3
     }
     if (open) bucket_numel[bucket++] = fill;
     *n_buckets = bucket;
+    const char* dbg = std::getenv("DDP_DEBUG");
+    if (dbg && *dbg && *dbg != '0') {
+        std::fprintf(stderr, "[ddp] plan: %d parameters -> %d buckets (first cap %lld B, cap %lld B)\n", n_params,
+                     bucket, (long long)first_bucket_bytes, (long long)bucket_cap_bytes);
+        for (int32_t k = 0; k < bucket; ++k)
+            std::fprintf(stderr, "[ddp]   bucket %d: %lld elements (%lld B)\n", k, (long long)bucket_numel[k],
+                         (long long)(bucket_numel[k] * esize));
+    }
     return DDP_OK;
 }

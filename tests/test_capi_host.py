@@ -183,3 +183,30 @@ def test_tree_rejects_bad_arguments_on_host():
     assert L.tree_allreduce_staged(2, tab, 8, 5, 2, None) == -1      # dtype
     assert L.tree_allreduce_fused(2, _vp(0x7f0000000000, 0x7f0000000004), 8, 0, 2, None) == -1   # overlap
 
+
+def test_header_is_plain_c_and_cxx(tmp_path):
+    # include/ddp.h is a C ABI: it must compile as pedantic C99 and as C++
+    import shutil
+    import subprocess
+    src = tmp_path / "use_ddp.c"
+    src.write_text('#include "ddp.h"\nint main(void) { ddp_reducer* r = 0; (void)r;\n'
+                   '  return ddp_abi_version() == DDP_ABI_VERSION ? 0 : 1; }\n')
+    inc = os.path.join(ROOT, "include")
+    if shutil.which("gcc"):
+        subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, "-c",
+                               str(src), "-o", str(tmp_path / "a.o")])
+    if shutil.which("g++"):
+        subprocess.check_call(["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-I", inc, "-x", "c++", "-c",
+                               str(src), "-o", str(tmp_path / "b.o")])
+
+
+def test_oracle_compiles_without_warnings(tmp_path):
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        return
+    r = subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror", "-ffp-contract=off",
+                        "-fno-fast-math", "-fPIC", "-shared", "-o", str(tmp_path / "o.so"),
+                        os.path.join(ROOT, "oracle", "ddp_oracle.c")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
