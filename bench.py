@@ -481,7 +481,7 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     ddp.lib()
-    for N in (8, 64):
+    for N in (4, 8, 64):
         for k in range(17):
             S = 1024 << k
             s_bytes = S * 4
@@ -730,6 +730,74 @@ def run_profile_view(args):
                       "hbm_alg_gbs": 2 * N * total * 4 / (ms / 1e3) / 1e9}), flush=True)
 
 
+def run_cpu_table(args):
+    """The CPU oracle (single-threaded C, this host) on every survey config,
+    for the comparison table: one JSON line per measurement."""
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+
+    def timed(fn, reps=1):
+        best = None
+        for _ in range(reps):
+            t = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t
+            best = dt if best is None else min(best, dt)
+        return best
+
+    def emit(**kw):
+        kw["cores"] = 1
+        kw["host_cores_present"] = host_cores()
+        print(json.dumps(kw), flush=True)
+
+    # C1 and C2 and the C5 sweep: one bucket, ring allreduce / N
+    for cfg, N, S, reps in (("C1", 4, 1 << 20, 3), ("C2", 8, 1 << 28, 1)):
+        x = workloads.rank_vectors(N, S, "randn", std=1.0 if cfg == "C1" else 1e-2).numpy()
+        rows = [x[r] for r in range(N)]
+        t = timed(lambda: oracle.ring_allreduce(rows, oracle.F32, N), reps)
+        emit(config=cfg, ranks=N, bytes_per_rank=S * 4, seconds=t,
+             busbw_gbs=2 * (N - 1) / N * S * 4 / t / 1e9)
+        del x, rows
+    for N, kmax in ((8, 16), (64, 14)):
+        for k in range(0, kmax + 1, 2):
+            S = 1024 << k
+            x = workloads.rank_vectors(N, S, "uniform").numpy()
+            rows = [x[r] for r in range(N)]
+            t = timed(lambda: oracle.ring_allreduce(rows, oracle.F32, N), 3 if S < (1 << 22) else 1)
+            emit(config="C5", ranks=N, bytes_per_rank=S * 4, seconds=t,
+                 busbw_gbs=2 * (N - 1) / N * S * 4 / t / 1e9)
+            del x, rows
+    # C3: the decoder DDP step (plan, pack, ring / 8, unpack), and no_sync's accumulation
+    numels = workloads.param_numels(workloads.decoder_param_shapes())
+    N, total = 8, sum(numels)
+    offs = np.cumsum([0] + numels)
+    flat = workloads.rank_vectors(N, total, "randn", std=1e-2).numpy()
+    grads = [[flat[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+    t = timed(lambda: oracle.ddp_sync(grads, oracle.F32))
+    emit(config="C3", step="pack + ring / 8 + unpack, 37 buckets", ranks=N, grad_bytes_per_rank=total * 4, seconds=t)
+    t = timed(lambda: oracle.accumulate(flat.reshape(-1), flat.reshape(-1).copy(), oracle.F32))
+    emit(config="C3", step="one no_sync accumulation of all gradients, all ranks", ranks=N,
+         grad_bytes_per_rank=total * 4, seconds=t)
+    del flat, grads
+    # C4: ResNet-50 bf16, N = 16, caps 5/10/25/50 MiB
+    numels = workloads.param_numels(workloads.resnet50_param_shapes())
+    N, total = 16, sum(numels)
+    offs = np.cumsum([0] + numels)
+    base = workloads.rank_vectors(N, total, "randn", std=1e-2, dtype="bf16").view(torch_int16()).numpy()
+    for cap in (5, 10, 25, 50):
+        flat = base.view(np.uint16).copy()
+        grads = [[flat[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+        t = timed(lambda: oracle.ddp_sync(grads, oracle.BF16, MiB, cap * MiB))
+        emit(config="C4", cap_mib=cap, ranks=N, grad_bytes_per_rank=total * 2, seconds=t)
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -745,6 +813,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work to size the per-step sample for")
+    ap.add_argument("--cpu-table", action="store_true", help="time the CPU oracle on every config instead")
     ap.add_argument("--profile-view", action="store_true", help="small view-sync run for profiling instead")
     ap.add_argument("--profile-layers", type=int, default=2)
     ap.add_argument("--cap-sweep", action="store_true", help="bucket-cap sweep (one JSON line per point) instead")
@@ -772,6 +841,9 @@ def main():
         return
     if args.profile_view:
         run_profile_view(args)
+        return
+    if args.cpu_table:
+        run_cpu_table(args)
         return
     try:
         if args.impl == "reference":
