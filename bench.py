@@ -449,6 +449,19 @@ def ddp_step_bench(ddp, workloads, torch, dev, stream, steps):
     res["bf16_hook"] = {"ms_per_step": ms, "hbm_alg_gbs": 16 * N * total / (ms / 1e3) / 1e9,
                         "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
     del bk16
+    # the same hook fused into one pass over the float32 gradients
+    call = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_BF16_HOOK_VIEW)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    res["bf16_hook_view"] = {"ms_per_step": ms, "hbm_alg_gbs": 2 * N * p_bytes / (ms / 1e3) / 1e9,
+                             "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
     # no_sync: 3 local accumulations of a micro-batch, then one sync (view)
     scratch = torch.empty_like(g)
     scratch.copy_(g)
@@ -635,7 +648,7 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
 
 
 def run_cap_sweep(args):
-    """Bucket-cap sweep (survey config C4 and the pages' 6/12/25/50 MB sweep):
+    """Bucket-cap sweep (the pages' 6/12/25/50 MB bucket-size sweep):
     the DDP step for ResNet-50 in bf16 at N = 16 (caps 5, 10, 25, 50 MiB) and
     for the 355M decoder in fp32 at N = 8 (caps 6, 12, 25, 50 MiB), first
     bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  One
@@ -731,7 +744,7 @@ def run_profile_view(args):
 
 
 def run_cpu_table(args):
-    """The CPU oracle (single-threaded C, this host) on every survey config,
+    """The CPU oracle (single-threaded C, this host) on every workload,
     for the comparison table: one JSON line per measurement."""
     import numpy as np
     import oracle

@@ -417,6 +417,7 @@ cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int6
             return launch_bucket_view_tma(world, members, n, segs.data(), (int)segs.size(), dtype, div, stream);
     }
     if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
+    if (dtype == kDtypeHook) return view_div<EHOOK>(world, members, n, bucket_numel, div, stream);
     return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
 }
 

@@ -481,9 +481,9 @@ int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* 
     return cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 0, (cudaStream_t)stream));
 }
 
-int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
-                                  const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
-                                  void* stream) {
+static int32_t view_one(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                        const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t launch_dtype,
+                        int32_t divisor, void* stream) {
     if (divisor < 0) return DDP_ERR_INVALID;
     std::vector<ViewMember> members;
     int32_t st = view_members(world, n_in_bucket, grads, numel, offset, bucket_numel, dtype, &members);
@@ -498,8 +498,19 @@ int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* cons
         for (int32_t r = 0; r < world; ++r) tables.back()[r] = grads[(int64_t)r * n_in_bucket + i];
         members[k++].ptrs = tables.back().data();
     }
-    return cuda_status(launch_bucket_view(world, members.data(), (int)members.size(), bucket_numel, dtype,
+    return cuda_status(launch_bucket_view(world, members.data(), (int)members.size(), bucket_numel, launch_dtype,
                                           make_div(divisor), (cudaStream_t)stream));
+}
+
+int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                                  const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
+                                  void* stream) {
+    return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, dtype, dtype, divisor, stream);
+}
+
+int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) {
+    return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook, divisor, stream);
 }
 
 int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
@@ -509,12 +520,14 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
     int32_t st = common_checks(world, 0, dtype);
     if (st) return st;
     if (n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
-    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_BF16_HOOK)
+    if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_BF16_HOOK &&
+        algo != DDP_ALGO_BF16_HOOK_VIEW)
         return DDP_ERR_INVALID;
-    if (algo == DDP_ALGO_BF16_HOOK && dtype != DDP_F32) return DDP_ERR_INVALID;
+    if ((algo == DDP_ALGO_BF16_HOOK || algo == DDP_ALGO_BF16_HOOK_VIEW) && dtype != DDP_F32) return DDP_ERR_INVALID;
+    const bool view = algo == DDP_ALGO_VIEW || algo == DDP_ALGO_BF16_HOOK_VIEW;
     if (n_params > 0 && (!grads || !numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
     if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
-    if (algo != DDP_ALGO_VIEW && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
+    if (!view && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
     // members of each bucket, in bucket order
     std::vector<std::vector<int32_t>> members(n_buckets);
     for (int32_t p = 0; p < n_params; ++p) {
@@ -522,7 +535,7 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
         if (k < 0 || k >= n_buckets) return DDP_ERR_INVALID;
         members[k].push_back(p);
     }
-    if (algo == DDP_ALGO_VIEW) {
+    if (view) {
         // validate every bucket, then sync all of them together
         std::vector<ViewMember> all;
         std::vector<std::vector<void*>> tables;
@@ -554,8 +567,9 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             }
             count[k] = (int)all.size() - first[k];
         }
+        const int32_t launch_dtype = (algo == DDP_ALGO_BF16_HOOK_VIEW) ? kDtypeHook : dtype;
         return cuda_status(launch_buckets_view(world, all.data(), first.data(), count.data(), bucket_numel, n_buckets,
-                                               dtype, make_div(divisor), (cudaStream_t)stream));
+                                               launch_dtype, make_div(divisor), (cudaStream_t)stream));
     }
     std::vector<const void*> g;
     std::vector<int64_t> ne, off;
@@ -571,12 +585,6 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             ne[i] = numel[m[i]];
             off[i] = offset_of_param[m[i]];
             for (int32_t r = 0; r < world; ++r) g[(size_t)r * n + i] = grads[(size_t)r * n_params + m[i]];
-        }
-        if (algo == DDP_ALGO_VIEW) {
-            st = ddp_bucket_allreduce_view(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
-                                           bucket_numel[k], dtype, divisor, stream);
-            if (st) return st;
-            continue;
         }
         for (int32_t r = 0; r < world; ++r) bk[r] = buckets[(size_t)r * n_buckets + k];
         if (algo == DDP_ALGO_BF16_HOOK) {

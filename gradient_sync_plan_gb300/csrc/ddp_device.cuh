@@ -89,6 +89,36 @@ struct EBF16 {
     }
 };
 
+// ---- float32 storage, bf16 arithmetic (the bf16 compression hook, fused) --
+// Every input is rounded to bf16 before it is used, every sum and the
+// quotient are rounded to bf16, and the result is stored widened back to
+// float32 -- exactly what packing into a bf16 bucket, a bf16 ring and
+// unpacking produce.  Rounding is idempotent, so re-rounding a running sum
+// that is already a bf16 value changes nothing.
+struct EHOOK {
+    using S = float;
+    using V = float4;
+    static constexpr int L = 4;
+    __device__ static __forceinline__ float rt(float x) { return bf16_to_f32(f32_to_bf16_rn(x)); }
+    __device__ static __forceinline__ float4 rt4(float4 a) {
+        const uint32_t lo = bf16x2_rn(a.x, a.y), hi = bf16x2_rn(a.z, a.w);
+        return make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));
+    }
+    __device__ static __forceinline__ S sadd(S a, S b) { return rt(__fadd_rn(rt(a), rt(b))); }
+    __device__ static __forceinline__ V vadd(V a, V b) {
+        const float4 x = rt4(a), y = rt4(b);
+        return rt4(make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w)));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ S sdiv(S a, float op) { return rt(div_f32<DIV>(rt(a), op)); }
+    template <int DIV>
+    __device__ static __forceinline__ V vdiv(V a, float op) {
+        const float4 x = rt4(a);
+        return rt4(make_float4(div_f32<DIV>(x.x, op), div_f32<DIV>(x.y, op), div_f32<DIV>(x.z, op),
+                               div_f32<DIV>(x.w, op)));
+    }
+};
+
 // Streaming 16-byte accesses: the buffers are touched once per call, so
 // loads and stores are marked evict-first.
 template <class V>

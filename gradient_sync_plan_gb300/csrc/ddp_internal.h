@@ -24,8 +24,11 @@ struct DivSpec {
 };
 DivSpec make_div(int32_t divisor);
 
+// Internal element type of the fused bf16 hook: float32 storage, bf16 arithmetic.
+constexpr int kDtypeHook = 100;
+
 inline int64_t chunk_len(int64_t numel, int world) { return (numel + world - 1) / world; }
-inline int elem_bytes(int dtype) { return dtype == DDP_F32 ? 4 : 2; }
+inline int elem_bytes(int dtype) { return dtype == DDP_BF16 ? 2 : 4; }
 
 // Launch geometry helpers (cached per device).
 int sm_count();

@@ -347,8 +347,10 @@ typedef enum {
     DDP_ALGO_VIEW = 2,    /* ddp_bucket_allreduce_view (no bucket copies)        */
     DDP_ALGO_DRYRUN = 3,  /* ddp_reducer only: track readiness and launch order,
                              make no CUDA call (for checking a plan's order)    */
-    DDP_ALGO_BF16_HOOK = 4 /* float32 gradients, bf16 buckets: ddp_bucket_pack_bf16
+    DDP_ALGO_BF16_HOOK = 4, /* float32 gradients, bf16 buckets: ddp_bucket_pack_bf16
                              -> ring_allreduce_fused in bf16 -> ddp_bucket_unpack_bf16 */
+    DDP_ALGO_BF16_HOOK_VIEW = 5 /* the same result in one pass, no bucket buffers:
+                             ddp_bucket_allreduce_view_bf16                         */
 } ddp_algo;
 
 /*
@@ -438,6 +440,21 @@ int32_t ddp_reducer_finalize(ddp_reducer* reducer, void* stream);
 /* Buckets launched in the current pass, in launch order (up to capacity). */
 int32_t ddp_reducer_launch_order(ddp_reducer* reducer, int32_t* order, int32_t capacity, int32_t* n);
 int32_t ddp_reducer_destroy(ddp_reducer* reducer);
+
+/*
+ * ddp_bucket_allreduce_view_bf16 -- the bf16 compression hook fused like
+ * ddp_bucket_allreduce_view: float32 gradients are read once from every
+ * rank, each value is rounded to bf16, the values are summed in the ring
+ * order of their bucket chunk with one bf16 rounding per hop, divided
+ * (rounded to bf16), and the bf16 result is written back widened to float32.
+ * Bit-identical to ddp_bucket_pack_bf16 + ring_allreduce_fused (bf16) +
+ * ddp_bucket_unpack_bf16 on the same bucket, without the bucket buffers.
+ * Arguments as for ddp_bucket_allreduce_view, with float32 gradients and no
+ * dtype argument.
+ */
+int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void* const* grads,
+                                       const int64_t* numel, const int64_t* offset, int64_t bucket_numel,
+                                       int32_t divisor, void* stream);
 
 #ifdef __cplusplus
 }

@@ -268,8 +268,8 @@ def ddp_sync_bf16_hook(grads: Sequence[Sequence[np.ndarray]], first_cap_bytes: i
     rounded to bf16 (nearest even), the bf16 bucket ring-reduced (one bf16
     rounding per hop) and divided, and the result widened back to float32 and
     unpacked.  ("Day 17 · 梯度的集体行动", reading list: DDP communication hooks,
-    fp16/bf16 compression; the division after the reduction is this build's
-    reading, as everywhere else.)
+    fp16/bf16 compression; dividing after the reduction is the reading taken
+    for every sync here.)
     """
     world = len(grads)
     numels = [int(a.size) for a in grads[0]]

@@ -242,8 +242,9 @@ def test_no_sync_small_decoder_full():
     assert_bits_equal(f32_or_bits(acc), np.stack([np.concatenate(want[r]) for r in range(world)]), "no_sync")
 
 
+@pytest.mark.parametrize("algo", ["hook", "hook_view"])
 @pytest.mark.parametrize("via", ["sync_buckets", "reducer"])
-def test_bf16_hook_matches_oracle(via):
+def test_bf16_hook_matches_oracle(via, algo):
     numels = _small_decoder()
     world, first, cap = 8, 4096, 40000
     plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
@@ -251,11 +252,14 @@ def test_bf16_hook_matches_oracle(via):
     x64 = flat.numpy().astype(np.float64)
     g = flat.cuda()
     views = _device_views(g, numels)
-    bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
+    code = ddp.DDP_ALGO_BF16_HOOK if algo == "hook" else ddp.DDP_ALGO_BF16_HOOK_VIEW
+    bk = None
+    if algo == "hook":
+        bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
     if via == "sync_buckets":
-        ddp.ddp_sync_buckets(views, plan, bk, algo=ddp.DDP_ALGO_BF16_HOOK)
+        ddp.ddp_sync_buckets(views, plan, bk, algo=code)
     else:
-        red = ddp.Reducer(views, plan, bk, algo=ddp.DDP_ALGO_BF16_HOOK, comm_stream=torch.cuda.Stream())
+        red = ddp.Reducer(views, plan, bk, algo=code, comm_stream=torch.cuda.Stream())
         for p in range(len(numels) - 1, -1, -1):
             red.mark_ready(p, torch.cuda.current_stream())
         red.finalize(torch.cuda.current_stream())
@@ -263,7 +267,7 @@ def test_bf16_hook_matches_oracle(via):
     oracle.ddp_sync_bf16_hook(grads_h, first, cap)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
     got = f32_or_bits(g)
-    assert_bits_equal(got, want, f"bf16 hook via {via}")
+    assert_bits_equal(got, want, f"bf16 {algo} via {via}")
     ref = x64.sum(0) / world
     assert np.linalg.norm(got[0] - ref) / np.linalg.norm(ref) <= 2e-2
 
@@ -312,3 +316,45 @@ def test_view_tma_path_matches_oracle(dtype):
     assert_bits_equal(f32_or_bits(g), want, f"view tma {dtype}")
     assert ddp.ddp_device_status() == 0
 
+
+
+@pytest.mark.parametrize("divisor", [None, 0, 3])
+def test_bf16_hook_view_tma_path_matches_oracle(divisor):
+    # the fused hook on one TMA-sized bucket (> 4 MiB of float32 over 8 ranks,
+    # chunk-aligned segments), plus the world-size, no-divide and
+    # non-power-of-two divisors; the second call on a ragged single member
+    # takes the register path
+    world = 8
+    numels = [16 * 7, 16 * 40000, 16 * 3, 16 * 25000, 16 * 1000, 16 * 9006]
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, 1 << 40, 1 << 40)
+    assert len(plan[2]) == 1
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=9)
+    g = flat.cuda()
+    div = world if divisor is None else divisor
+    offsets = [int(o) for o in plan[1]]
+    ddp.ddp_bucket_allreduce_view_bf16(_device_views(g, numels), offsets, int(plan[2][0]), div)
+    torch.cuda.synchronize()
+    oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=div)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"hook view tma div={div}")
+    assert ddp.ddp_device_status() == 0
+
+    numels = [1001]
+    flat, grads_h = _host_grads(numels, 3, "f32", seed0=10)
+    g = flat.cuda()
+    ddp.ddp_bucket_allreduce_view_bf16(_device_views(g, numels), [0], 1001, div)
+    torch.cuda.synchronize()
+    oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=div)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(3)])
+    assert_bits_equal(f32_or_bits(g), want, f"hook view ragged div={div}")
+
+
+def test_bf16_hook_view_world_one_rounds():
+    # one rank: no hop, but the hook still rounds every value to bf16
+    numels = [4096 + 5]
+    flat, grads_h = _host_grads(numels, 1, "f32", seed0=11)
+    g = flat.cuda()
+    ddp.ddp_bucket_allreduce_view_bf16(_device_views(g, numels), [0], numels[0], 1)
+    torch.cuda.synchronize()
+    oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=1)
+    assert_bits_equal(f32_or_bits(g), np.stack([grads_h[0][0]]), "hook view world 1")
