@@ -28,6 +28,7 @@ DDP_ALGO_VIEW = 2
 DDP_ALGO_DRYRUN = 3
 DDP_ALGO_BF16_HOOK = 4
 DDP_ALGO_BF16_HOOK_VIEW = 5
+DDP_FUSED_AUTO, DDP_FUSED_VECTOR, DDP_FUSED_GROUP, DDP_FUSED_TMA = 0, 1, 2, 3
 DDP_MAX_WORLD = 512
 FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
 BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
@@ -37,7 +38,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
-           "ddp_plan_buckets",
+           "ddp_set_fused_kernel", "ddp_plan_buckets",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ddp_bucket_pack_bf16", "ddp_bucket_unpack_bf16",
            "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "tree_allreduce_fused",
            "tree_allreduce_staged", "ring_allreduce_fused_from_host",
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_device_status.argtypes = [P(i32), i32]
             L.ddp_device_status.restype = i32
             L.ddp_set_max_ctas.argtypes = [i32, P(i32)]
+            L.ddp_set_fused_kernel.argtypes = [i32, P(i32)]
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
@@ -204,6 +206,14 @@ def ddp_set_max_ctas(max_ctas: int) -> int:
     """Cap the CTAs of every library kernel (0 = no cap); returns the previous cap."""
     prev = ctypes.c_int32(0)
     _check("ddp_set_max_ctas", lib().ddp_set_max_ctas(int(max_ctas), ctypes.byref(prev)))
+    return int(prev.value)
+
+
+def ddp_set_fused_kernel(kind: int) -> int:
+    """Choose the fused-ring kernel (DDP_FUSED_*; results are identical);
+    returns the previous choice."""
+    prev = ctypes.c_int32(0)
+    _check("ddp_set_fused_kernel", lib().ddp_set_fused_kernel(int(kind), ctypes.byref(prev)))
     return int(prev.value)
 
 

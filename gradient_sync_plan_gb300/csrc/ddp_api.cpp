@@ -43,7 +43,10 @@ bool debug_enabled() {
 
 namespace {
 std::atomic<int> g_max_ctas{0};                              // 0 = no cap (ddp_set_max_ctas)
+std::atomic<int> g_fused_kernel{DDP_FUSED_AUTO};             // ddp_set_fused_kernel
 }  // namespace
+
+int fused_kernel_override() { return g_fused_kernel.load(std::memory_order_relaxed); }
 
 int cap_ctas(int64_t grid) {
     const int cap = g_max_ctas.load(std::memory_order_relaxed);
@@ -270,6 +273,13 @@ const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
 int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) {
     if (max_ctas < 0) return DDP_ERR_INVALID;
     const int prev = g_max_ctas.exchange(max_ctas);
+    if (previous) *previous = prev;
+    return DDP_OK;
+}
+
+int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) {
+    if (kind < DDP_FUSED_AUTO || kind > DDP_FUSED_TMA) return DDP_ERR_INVALID;
+    const int prev = g_fused_kernel.exchange(kind);
     if (previous) *previous = prev;
     return DDP_OK;
 }

@@ -130,6 +130,17 @@ template <class V> __device__ __forceinline__ V make_zero();
 template <> __device__ __forceinline__ float4 make_zero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 template <> __device__ __forceinline__ uint4 make_zero<uint4>() { return make_uint4(0u, 0u, 0u, 0u); }
 
+// Warp shuffle of a 16-byte vector from lane `src` of the caller's `width`-lane
+// segment (all 32 lanes must call it).
+__device__ __forceinline__ float4 shfl_vec(float4 a, int src, int width) {
+    return make_float4(__shfl_sync(0xffffffffu, a.x, src, width), __shfl_sync(0xffffffffu, a.y, src, width),
+                       __shfl_sync(0xffffffffu, a.z, src, width), __shfl_sync(0xffffffffu, a.w, src, width));
+}
+__device__ __forceinline__ uint4 shfl_vec(uint4 a, int src, int width) {
+    return make_uint4(__shfl_sync(0xffffffffu, a.x, src, width), __shfl_sync(0xffffffffu, a.y, src, width),
+                      __shfl_sync(0xffffffffu, a.z, src, width), __shfl_sync(0xffffffffu, a.w, src, width));
+}
+
 // Fold the N ranks' vectors at byte offset `off` in ring order, starting at
 // rank `start` (the rank right after the chunk's owner) and wrapping around:
 // acc = x[start]; acc = acc (+) x[start+1]; ... ; acc = acc (+) x[start-1].

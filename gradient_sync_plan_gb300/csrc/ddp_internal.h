@@ -33,6 +33,13 @@ inline int elem_bytes(int dtype) { return dtype == DDP_BF16 ? 2 : 4; }
 // Launch geometry helpers (cached per device).
 int sm_count();
 int grid_for(const void* kernel, int64_t work_items, int threads = kThreads);
+// Fused-ring kernel chosen by ddp_set_fused_kernel (DDP_FUSED_AUTO = by size).
+int fused_kernel_override();
+
+// Kernel that runs one in-place fused ring call.
+enum class FusedPath { kScalar, kVector, kGroup, kTma };
+constexpr int kGroupMaxWorld = 128;
+FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok);
 // grid clamped to the process-wide CTA cap of ddp_set_max_ctas (0 = none), at least 1
 int cap_ctas(int64_t grid);
 bool debug_enabled();
@@ -59,8 +66,9 @@ cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g,
                               bool vec_ok, cudaStream_t stream);
 
 // ---- TMA-staged fused ring (ring_tma.cu) --------------------------------
-// Usable when every buffer is 16-byte aligned, chunk and bucket byte sizes
-// are multiples of 16, world <= 128 and the bucket is large enough.
+// The TMA fused kernel can run this call: every buffer 16-byte aligned,
+// chunk and bucket byte sizes multiples of 16, world <= 128 (any size; the
+// size decision is the caller's).
 bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok);
 int64_t tma_tile_bytes(int world);
 cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,

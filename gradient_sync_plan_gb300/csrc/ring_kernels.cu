@@ -75,6 +75,72 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
     }
 }
 
+// Group fused kernel, for buckets too small to fill the GPU with one thread
+// per vector.  P lanes of a warp (a group) share one 16-byte vector: lane q
+// loads the ranks at ring positions q, q + P, ... (position k is rank
+// (start + k) mod N), and every lane of the group folds the N values in
+// ring order, taking each from its owner lane by a warp shuffle -- the adds
+// of k_ring_fused in the same order, on P times as many threads, each with
+// ceil(N / P) = R loads in flight instead of N.  Vectors that straddle a
+// chunk boundary or the end are done element-wise by the group's lane 0.
+template <class E, int DIV, int CAP, int P, int R>
+__global__ void __launch_bounds__(kThreads)
+k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+    using V = typename E::V;
+    constexpr int L = E::L;
+    constexpr int kGroups = 32 / P;                     // vectors per warp and pass
+    const int lane = threadIdx.x & 31;
+    const int q = lane & (P - 1);
+    const int64_t nvec = (numel + L - 1) / L;
+    const int64_t full = numel / L;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    // the loop bounds are the same for every lane of a warp, so every lane
+    // reaches every shuffle
+    for (int64_t base = warp * kGroups; base < nvec; base += n_warps * kGroups) {
+        const int64_t v = base + lane / P;
+        const int64_t i = v * L;
+        const bool valid = v < nvec;
+        const int64_t j = valid ? i / clen : 0;
+        const bool clean = valid && v < full && (i + L - 1) / clen == j;
+        const int start = (j + 1 == world) ? 0 : (int)j + 1;
+        const int64_t off = v * 16;
+        V x[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const int k = m * P + q;
+            x[m] = make_zero<V>();
+            if (clean && k < world) {
+                const int r = (start + k >= world) ? start + k - world : start + k;
+                x[m] = ld_stream<V>(t.p[r] + off);
+            }
+        }
+        V acc = shfl_vec(x[0], 0, P);
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+#pragma unroll
+            for (int qq = 0; qq < P; ++qq) {
+                const int k = m * P + qq;
+                if (k > 0 && k < world) acc = E::vadd(acc, shfl_vec(x[m], qq, P));
+            }
+        }
+        if (clean) {
+            const V y = E::template vdiv<DIV>(acc, dop);
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                const int k = m * P + q;
+                if (k < world) {
+                    const int r = (start + k >= world) ? start + k - world : start + k;
+                    st_stream<V>(t.p[world + r] + off, y);
+                }
+            }
+        } else if (valid && q == 0) {
+            for (int l = 0; l < L; ++l)
+                if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
+        }
+    }
+}
+
 // Element-wise fused kernel for buffers that are not 16-byte aligned.
 template <class E, int DIV, int CAP>
 __global__ void __launch_bounds__(kThreads)
@@ -208,6 +274,35 @@ static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64
     return cudaGetLastError();
 }
 
+constexpr int kGroupThreads = 128;     // small blocks spread a small bucket over more SMs
+
+template <class E, int DIV, int CAP, int P, int R>
+static cudaError_t fused_group(int world, void* const* in, void* const* out, int64_t numel, float dop,
+                               cudaStream_t st) {
+    auto k = k_ring_fused_group<E, DIV, 2 * CAP, P, R>;
+    const int64_t nvec = (numel + E::L - 1) / E::L;
+    const int64_t lanes = (nvec + 32 / P - 1) / (32 / P) * 32;
+    const int grid = grid_for((const void*)k, lanes, kGroupThreads);
+    k<<<grid, kGroupThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world),
+                                      dop);
+    if (debug_enabled())
+        fprintf(stderr, "[ddp] ring_fused_group world=%d numel=%lld grid=%d P=%d R=%d\n", world, (long long)numel,
+                grid, P, R);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV>
+static cudaError_t group_dispatch(int world, void* const* in, void* const* out, int64_t numel, float dop,
+                                  cudaStream_t st) {
+    if (world <= 2) return fused_group<E, DIV, 16, 2, 1>(world, in, out, numel, dop, st);
+    if (world <= 4) return fused_group<E, DIV, 16, 4, 1>(world, in, out, numel, dop, st);
+    if (world <= 8) return fused_group<E, DIV, 16, 8, 1>(world, in, out, numel, dop, st);
+    if (world <= 16) return fused_group<E, DIV, 16, 16, 1>(world, in, out, numel, dop, st);
+    if (world <= 32) return fused_group<E, DIV, 64, 32, 1>(world, in, out, numel, dop, st);
+    if (world <= 64) return fused_group<E, DIV, 64, 32, 2>(world, in, out, numel, dop, st);
+    return fused_group<E, DIV, kGroupMaxWorld, 32, 4>(world, in, out, numel, dop, st);
+}
+
 template <class E, int DIV, int CAP>
 static cudaError_t fused_scalar(int world, void* const* in, void* const* out, int64_t numel, float dop,
                                 cudaStream_t st) {
@@ -218,41 +313,76 @@ static cudaError_t fused_scalar(int world, void* const* in, void* const* out, in
 }
 
 template <class E, int DIV>
-static cudaError_t fused_dispatch(int world, void* const* in, void* const* out, int64_t numel, float dop,
-                                  bool vec_ok, cudaStream_t st) {
-    if (!vec_ok) {
+static cudaError_t fused_dispatch(FusedPath path, int world, void* const* in, void* const* out, int64_t numel,
+                                  float dop, cudaStream_t st) {
+    if (path == FusedPath::kScalar) {
         if (world <= 16) return fused_scalar<E, DIV, 16>(world, in, out, numel, dop, st);
         return fused_scalar<E, DIV, DDP_MAX_WORLD>(world, in, out, numel, dop, st);
     }
+    if (path == FusedPath::kGroup) return group_dispatch<E, DIV>(world, in, out, numel, dop, st);
     if (world <= 4) return fused_vec<E, DIV, 16, 4>(world, in, out, numel, dop, st);
     if (world <= 8) return fused_vec<E, DIV, 16, 8>(world, in, out, numel, dop, st);
     if (world <= 16) return fused_vec<E, DIV, 16, 16>(world, in, out, numel, dop, st);
+    if (world <= 64) return fused_vec<E, DIV, 64, 16>(world, in, out, numel, dop, st);
     return fused_vec<E, DIV, DDP_MAX_WORLD, 16>(world, in, out, numel, dop, st);
 }
 
 template <class E>
-static cudaError_t fused_by_div(int world, void* const* in, void* const* out, int64_t numel, DivSpec d,
-                                bool vec_ok, cudaStream_t st) {
+static cudaError_t fused_by_div(FusedPath path, int world, void* const* in, void* const* out, int64_t numel,
+                                DivSpec d, cudaStream_t st) {
     switch (d.mode) {
-        case kDivNone: return fused_dispatch<E, kDivNone>(world, in, out, numel, d.operand, vec_ok, st);
-        case kDivPow2: return fused_dispatch<E, kDivPow2>(world, in, out, numel, d.operand, vec_ok, st);
-        default: return fused_dispatch<E, kDivIeee>(world, in, out, numel, d.operand, vec_ok, st);
+        case kDivNone: return fused_dispatch<E, kDivNone>(path, world, in, out, numel, d.operand, st);
+        case kDivPow2: return fused_dispatch<E, kDivPow2>(path, world, in, out, numel, d.operand, st);
+        default: return fused_dispatch<E, kDivIeee>(path, world, in, out, numel, d.operand, st);
     }
+}
+
+FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
+    if (!vec_ok) return FusedPath::kScalar;
+    const bool tma_ok = tma_usable(world, numel, dtype, vec_ok);
+    const bool group_ok = world >= 2 && world <= kGroupMaxWorld;
+    switch (fused_kernel_override()) {
+        case DDP_FUSED_VECTOR: return FusedPath::kVector;
+        case DDP_FUSED_GROUP: return group_ok ? FusedPath::kGroup : FusedPath::kVector;
+        case DDP_FUSED_TMA: return tma_ok ? FusedPath::kTma : FusedPath::kVector;
+        default: break;
+    }
+    // Crossovers measured on GB300 (CUDA-graph replay of back-to-back calls,
+    // fp32 and bf16, N = 2 .. 128, 4 KiB .. 64 MiB per rank):
+    //  * a few KiB per rank: one thread per vector leaves most SMs idle and
+    //    waits on N loads; the group kernel spreads the ranks over lanes;
+    //  * while the whole bucket sits in L2 the vector kernel is fastest;
+    //  * from HBM, the TMA kernel streams best for up to 8 ranks (16 in
+    //    bf16), and for many ranks with short chunks its one-CTA-per-tile
+    //    grid reaches more SMs than one thread per vector.
+    constexpr int64_t KiB = 1024, MiB = 1024 * 1024;
+    const int64_t per_rank = numel * elem_bytes(dtype);
+    const int64_t total = per_rank * world;
+    if (group_ok && (per_rank <= 16 * KiB || (world <= 16 && per_rank <= 64 * KiB))) return FusedPath::kGroup;
+    if (tma_ok) {
+        if (world == 2 && per_rank >= 16 * MiB) return FusedPath::kTma;
+        if (world <= 8 && total > 128 * MiB) return FusedPath::kTma;
+        if (world <= 16 && dtype == DDP_BF16 && total >= 64 * MiB) return FusedPath::kTma;
+        if (world > 16 && per_rank >= 32 * KiB && per_rank <= 128 * KiB) return FusedPath::kTma;
+    }
+    return FusedPath::kVector;
 }
 
 cudaError_t launch_ring_fused(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div, bool vec_ok,
                               cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
-    if (tma_usable(world, numel, dtype, vec_ok)) return launch_ring_fused_tma(world, ptrs, numel, dtype, div, stream);
-    if (dtype == DDP_F32) return fused_by_div<EF32>(world, ptrs, ptrs, numel, div, vec_ok, stream);
-    return fused_by_div<EBF16>(world, ptrs, ptrs, numel, div, vec_ok, stream);
+    const FusedPath path = choose_fused_path(world, numel, dtype, vec_ok);
+    if (path == FusedPath::kTma) return launch_ring_fused_tma(world, ptrs, numel, dtype, div, stream);
+    if (dtype == DDP_F32) return fused_by_div<EF32>(path, world, ptrs, ptrs, numel, div, stream);
+    return fused_by_div<EBF16>(path, world, ptrs, ptrs, numel, div, stream);
 }
 
 cudaError_t launch_ring_fused_io(int world, void* const* in, void* const* out, int64_t numel, int dtype, DivSpec div,
                                  bool vec_ok, cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
-    if (dtype == DDP_F32) return fused_by_div<EF32>(world, in, out, numel, div, vec_ok, stream);
-    return fused_by_div<EBF16>(world, in, out, numel, div, vec_ok, stream);
+    const FusedPath path = vec_ok ? FusedPath::kVector : FusedPath::kScalar;
+    if (dtype == DDP_F32) return fused_by_div<EF32>(path, world, in, out, numel, div, stream);
+    return fused_by_div<EBF16>(path, world, in, out, numel, div, stream);
 }
 
 template <class E, int DIV, int CAP>

@@ -412,7 +412,6 @@ bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok) {
     const int64_t es = elem_bytes(dtype);
     const int64_t clen = chunk_len(numel, world);
     if ((clen * es) % 16 != 0 || (numel * es) % 16 != 0) return false;
-    if (numel * es * world < (int64_t)4 << 20) return false;     // small buckets: register path
     return tma_tile_bytes(world) > 0;
 }
 

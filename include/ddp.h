@@ -87,6 +87,37 @@ const char* ddp_last_cuda_error(void);
 int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
 
 /*
+ * ddp_set_fused_kernel -- which kernel ring_allreduce_fused (and every call
+ * that runs it on one buffer per rank: ddp_sync_buckets with
+ * DDP_ALGO_FUSED / DDP_ALGO_BF16_HOOK, the reducer) uses from now on in this
+ * process.  All of them compute the same fold in the same order, so results
+ * are bit-identical whichever runs; the choice only changes speed.
+ *   DDP_FUSED_AUTO   by size (the default): buckets of a few KiB per rank
+ *                    take the group kernel; buckets that fit in L2 the
+ *                    vector kernel; buckets streamed from HBM over up to 8
+ *                    ranks (16 in bf16), and 32-128 KiB per rank over more
+ *                    than 16 ranks, the TMA kernel;
+ *   DDP_FUSED_VECTOR one thread per 16-byte vector, folding all N ranks;
+ *   DDP_FUSED_GROUP  a group of lanes per vector, one rank (or a few) per
+ *                    lane, the fold done on values passed by warp shuffles
+ *                    (N <= 128);
+ *   DDP_FUSED_TMA    tiles of every rank staged in shared memory by bulk
+ *                    copies (N <= 128, 16-byte-aligned chunks).
+ * A kernel that cannot run a call (alignment, world size) is replaced by
+ * the vector kernel, or the element-wise one for unaligned buffers.
+ * *previous (if not NULL) receives the old choice.  DDP_ERR_INVALID for an
+ * unknown kind.
+ */
+typedef enum {
+    DDP_FUSED_AUTO = 0,
+    DDP_FUSED_VECTOR = 1,
+    DDP_FUSED_GROUP = 2,
+    DDP_FUSED_TMA = 3
+} ddp_fused_kernel;
+
+int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous);
+
+/*
  * ddp_device_status -- the library's sticky device-side status word on the
  * current device: DDP_OK, or DDP_ERR_TIMEOUT if a kernel's bounded wait on an
  * asynchronous copy gave up (the kernel then stopped early, so the buffers
@@ -193,7 +224,8 @@ int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* 
  *     y[i] = (((x_{j+1}[i] + x_{j+2}[i]) + ...) + x_{j+N}[i])   (ranks mod N)
  * and then, if divisor > 1, y[i] / divisor (one IEEE division).  This kernel
  * reads each rank's element once, folds in exactly that order and writes y to
- * all N buffers, so its result is bit-identical to the hop-by-hop ring.
+ * all N buffers, so its result is bit-identical to the hop-by-hop ring
+ * (which of its kernels runs: ddp_set_fused_kernel).
  * fp32: binary32 adds, round to nearest even.  bf16: each add is done in
  * binary32 and rounded to bf16 (nearest even), once per hop; the divide
  * rounds once to bf16.

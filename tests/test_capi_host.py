@@ -210,3 +210,18 @@ def test_oracle_compiles_without_warnings(tmp_path):
                         os.path.join(ROOT, "oracle", "ddp_oracle.c")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
 
+
+
+def test_process_wide_knobs_validate_and_return_previous():
+    L = ddp.lib()
+    prev = ctypes.c_int32(-7)
+    assert L.ddp_set_max_ctas(-1, ctypes.byref(prev)) == -1
+    assert prev.value == -7                          # untouched on error
+    for bad in (-1, 4, 100):
+        assert L.ddp_set_fused_kernel(bad, ctypes.byref(prev)) == -1
+    assert prev.value == -7
+    assert ddp.ddp_set_fused_kernel(ddp.DDP_FUSED_GROUP) == ddp.DDP_FUSED_AUTO
+    assert ddp.ddp_set_fused_kernel(ddp.DDP_FUSED_TMA) == ddp.DDP_FUSED_GROUP
+    assert L.ddp_set_fused_kernel(ddp.DDP_FUSED_AUTO, None) == 0      # previous may be NULL
+    assert ddp.ddp_set_max_ctas(5) == 0
+    assert ddp.ddp_set_max_ctas(0) == 5

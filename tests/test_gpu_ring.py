@@ -39,6 +39,18 @@ def run_gpu(kernel: str, x_host: np.ndarray, divisor: int) -> np.ndarray:
     return f32_or_bits(x)
 
 
+FUSED_KINDS = {"auto": ddp.DDP_FUSED_AUTO, "vector": ddp.DDP_FUSED_VECTOR, "group": ddp.DDP_FUSED_GROUP,
+               "tma": ddp.DDP_FUSED_TMA}
+
+
+def _with_fused_kernel(kind, fn):
+    prev = ddp.ddp_set_fused_kernel(FUSED_KINDS[kind])
+    try:
+        return fn()
+    finally:
+        ddp.ddp_set_fused_kernel(prev)
+
+
 @pytest.mark.parametrize("kernel", ["fused", "staged", "persistent"])
 def test_worked_example(kernel):
     k = np.arange(6, dtype=np.float32)
@@ -114,27 +126,31 @@ def test_unaligned_buffers_take_elementwise_path(kernel, dtype):
     (1, 1 << 21, "f32"),             # one rank: divide only
 ])
 def test_tma_staged_path_ragged_last_chunk(N, S, dtype):
-    # 16-byte aligned chunks and bucket, more than 4 MiB over all ranks: the
-    # fused call streams tiles through shared memory with bulk copies; tiles
-    # stop at chunk ends, so chunk ends that are not tile multiples are hit
+    # 16-byte aligned chunks and bucket, several MiB over all ranks: the TMA
+    # kernel streams tiles through shared memory with bulk copies; tiles stop
+    # at chunk ends, so chunk ends that are not tile multiples are hit.  The
+    # size-based choice runs the same call too.
     x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + 40)
     xh = f32_or_bits(x)
     es = 2 if dtype == "bf16" else 4
     clen = -(-S // N)
     assert (clen * es) % 16 == 0 and (S * es) % 16 == 0 and S * es * N >= 4 << 20
     for div in (N, 0):
-        got = run_gpu("fused", xh, div)
-        assert_bits_equal(got, oracle_allreduce(xh, div), f"tma N={N} S={S} {dtype} div={div}")
+        want = oracle_allreduce(xh, div)
+        for kind in ("tma", "auto"):
+            got = _with_fused_kernel(kind, lambda: run_gpu("fused", xh, div))
+            assert_bits_equal(got, want, f"{kind} N={N} S={S} {dtype} div={div}")
     assert ddp.ddp_device_status() == 0
 
 
 def test_tma_alternating_world_sizes():
-    # the staged path needs a different amount of shared memory per world
+    # the TMA kernel needs a different amount of shared memory per world
     # size; calls that alternate between larger and smaller needs on the same
     # kernel must all launch and stay exact
     for N, S in ((8, 1 << 20), (4, 1 << 20), (8, 1 << 20), (2, 1 << 21), (16, 1 << 19), (8, 1 << 20)):
         x = workloads.rank_vectors(N, S, "randn", seed0=N).numpy()
-        assert_bits_equal(run_gpu("fused", x, N), oracle_allreduce(x, N), f"N={N}")
+        got = _with_fused_kernel("tma", lambda: run_gpu("fused", x, N))
+        assert_bits_equal(got, oracle_allreduce(x, N), f"N={N}")
 
 
 def test_staged_equals_fused_bitwise_random_shapes():
@@ -323,8 +339,9 @@ def test_persistent_status_word_is_cleared_on_each_call():
 
 @pytest.mark.parametrize("cap", [1, 7, 40])
 def test_cta_cap_does_not_change_results(cap):
-    # every kernel family under a CTA cap: TMA fused (large aligned), register
-    # fused (ragged), staged, persistent -- all must stay exact
+    # every kernel family under a CTA cap: each fused kernel (TMA, group and
+    # vector on aligned buckets, element-wise on ragged ones), staged,
+    # persistent -- all must stay exact
     cases = [(8, 1 << 20, "f32"), (5, 77_777, "bf16"), (3, 1000, "f32")]
     prev = ddp.ddp_set_max_ctas(cap)
     try:
@@ -332,7 +349,10 @@ def test_cta_cap_does_not_change_results(cap):
             x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=cap + N)
             xh = f32_or_bits(x)
             want = oracle_allreduce(xh, N)
-            for kernel in ("fused", "staged", "persistent"):
+            for kind in ("tma", "group", "vector"):
+                got = _with_fused_kernel(kind, lambda: run_gpu("fused", xh, N))
+                assert_bits_equal(got, want, f"cap={cap} fused/{kind} N={N} S={S}")
+            for kernel in ("staged", "persistent"):
                 assert_bits_equal(run_gpu(kernel, xh, N), want, f"cap={cap} {kernel} N={N} S={S}")
     finally:
         ddp.ddp_set_max_ctas(prev)
@@ -352,3 +372,60 @@ def test_single_rank_divides_only():
     for kernel in ("fused", "staged"):
         assert_bits_equal(run_gpu(kernel, x, 3), oracle_allreduce(x, 3), kernel)
         assert_bits_equal(run_gpu(kernel, x, 0), x, kernel)
+
+
+@pytest.mark.parametrize("kind", ["vector", "group", "tma", "auto"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_every_fused_kernel_matches_oracle(kind, dtype):
+    # each fused kernel forced on world sizes that exercise every lane split
+    # of the group kernel (P = 2 .. 32 lanes per vector, 1, 2 or 4 vectors
+    # per lane) and the fallbacks (N = 1, N > 128); sizes with straddling
+    # vectors (chunk not a multiple of the vector), ragged tails, chunk
+    # multiples of 16 bytes (TMA-eligible) and several tiles
+    es = 2 if dtype == "bf16" else 4
+    per16 = 16 // es
+    cases = []
+    for N in (1, 2, 3, 4, 5, 8, 9, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 130):
+        cases += [(N, 7 * N + 3), (N, N * per16 * 37), (N, N * per16 * 1024 + 5 * per16)]
+    cases += [(8, 8 * per16 * 5000), (64, 64 * per16 * 300 + 11), (3, 1_000_003)]
+    for i, (N, S) in enumerate(cases):
+        x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=100 + i)
+        xh = f32_or_bits(x)
+        for div in ((N, 0, 3) if i % 3 == 0 else (N,)):
+            got = _with_fused_kernel(kind, lambda: run_gpu("fused", xh, div))
+            assert_bits_equal(got, oracle_allreduce(xh, div), f"{kind} {dtype} N={N} S={S} div={div}")
+
+
+@pytest.mark.parametrize("kind", ["vector", "group", "tma"])
+def test_forced_fused_kernel_on_unaligned_buffers_falls_back(kind):
+    # a forced kernel that cannot run the call (rows not 16-byte aligned)
+    # gives way to the element-wise kernel, with the same result
+    N, S = 6, 4099
+    x = workloads.rank_vectors(N, S, "randn", seed0=5)
+    xh = f32_or_bits(x)
+    store = torch.zeros((N, S + 8), dtype=x.dtype, device="cuda")
+    rows = [store[r, 1:1 + S] for r in range(N)]
+    for r in range(N):
+        rows[r].copy_(x[r].cuda())
+    _with_fused_kernel(kind, lambda: ddp.ring_allreduce_fused(rows, N))
+    torch.cuda.synchronize()
+    assert_bits_equal(np.stack([f32_or_bits(r) for r in rows]), oracle_allreduce(xh, N), kind)
+
+
+@pytest.mark.parametrize("kind", ["vector", "group", "tma"])
+def test_forced_fused_kernel_in_bucketed_sync(kind):
+    # the bucketed DDP step (pack + fused ring + unpack) is the same whichever
+    # kernel reduces the buckets
+    from test_gpu_buckets import _device_views, _host_grads, _small_decoder
+    numels = _small_decoder()
+    world, first, cap = 8, 4096, 40000
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=21)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    bk = [[torch.empty(int(n), dtype=torch.float32, device="cuda") for n in plan[2]] for _ in range(world)]
+    _with_fused_kernel(kind, lambda: ddp.ddp_sync_buckets(views, plan, bk, algo=ddp.DDP_ALGO_FUSED))
+    torch.cuda.synchronize()
+    oracle.ddp_sync(grads_h, oracle.F32, first, cap)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"bucketed sync with {kind}")
