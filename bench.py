@@ -575,7 +575,12 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
         groups.append(list(range(first + 11, first - 1, -1)))
     groups.append([1, 0])
     compute, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # the same reducer on a high-priority stream: its CTAs are dispatched
+    # ahead of queued backward CTAs whenever an SM frees up
+    lo_prio, hi_prio = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, -1)
+    comm_hi = torch.cuda.Stream(device=dev, priority=hi_prio)
     red = ddp.Reducer(views, plan, None, N, ddp.DDP_ALGO_VIEW, comm_stream=comm)
+    red_hi = ddp.Reducer(views, plan, None, N, ddp.DDP_ALGO_VIEW, comm_stream=comm_hi)
     sync = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW)
 
     def backward(reducer):
@@ -625,6 +630,11 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
         backward(red)
         red.finalize(compute)
 
+    def run_overlapped_hi():
+        red_hi.prepare()
+        backward(red_hi)
+        red_hi.finalize(compute)
+
     t_b = timed(run_backward)
     res = {"backward_ms": t_b,
            "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block on a compute stream; view-fusion sync; "
@@ -634,14 +644,18 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
     for cap in (0, sms // 2, sms // 4):
         prev = ddp.ddp_set_max_ctas(cap)
         try:
-            t_s, t_o = timed(run_serial), timed(run_overlapped)
+            t_s, t_o, t_h = timed(run_serial), timed(run_overlapped), timed(run_overlapped_hi)
         finally:
             ddp.ddp_set_max_ctas(prev)
         comm_ms = t_s - t_b
         res["by_max_ctas"][str(cap)] = {"serial_ms": t_s, "overlapped_ms": t_o, "comm_ms": comm_ms,
                                         "exposed_comm_ms": t_o - t_b,
-                                        "hidden_fraction": (t_s - t_o) / comm_ms if comm_ms > 0 else None}
+                                        "hidden_fraction": (t_s - t_o) / comm_ms if comm_ms > 0 else None,
+                                        "high_priority_comm": {
+                                            "overlapped_ms": t_h, "exposed_comm_ms": t_h - t_b,
+                                            "hidden_fraction": (t_s - t_h) / comm_ms if comm_ms > 0 else None}}
     red.close()
+    red_hi.close()
     del g, src, views
     torch.cuda.empty_cache()
     return res
@@ -743,6 +757,43 @@ def run_profile_view(args):
                       "hbm_alg_gbs": 2 * N * total * 4 / (ms / 1e3) / 1e9}), flush=True)
 
 
+def run_profile_resnet(args):
+    """The ResNet-50 DDP step in bf16 at N = 16 with the 25 MiB cap (first
+    bucket 1 MiB), for profiling: --steps times pack + fused ring + unpack,
+    then --steps times the fused view sync.  Prints one JSON line (not a
+    bench result)."""
+    import torch
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    numels = workloads.param_numels(workloads.resnet50_param_shapes())
+    N, total = 16, sum(numels)
+    plan = ddp.ddp_plan_buckets(numels, ddp.BF16, MiB, 25 * MiB)
+    g = torch.empty((N, total), dtype=torch.bfloat16, device=dev)
+    for r in range(N):
+        g[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)).to(torch.bfloat16))
+    offs = [0]
+    for n in numels:
+        offs.append(offs[-1] + n)
+    views = [[g[r, offs[p]:offs[p + 1]] for p in range(len(numels))] for r in range(N)]
+    buckets = [[torch.empty(int(n), dtype=torch.bfloat16, device=dev) for n in plan[2]] for _ in range(N)]
+    out = {"profile": "resnet50 bf16 sync", "params": total, "ranks": N, "buckets": int(len(plan[2]))}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, call in (("pack_fused_unpack", ddp.SyncCall(views, plan, buckets, N, ddp.DDP_ALGO_FUSED)),
+                       ("view", ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW))):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name + "_ms"] = e0.elapsed_time(e1) / max(1, args.steps)
+    print(json.dumps(out), flush=True)
+
+
 def run_cpu_table(args):
     """The CPU oracle (single-threaded C, this host) on every workload,
     for the comparison table: one JSON line per measurement."""
@@ -828,6 +879,8 @@ def main():
                     help="--impl reference: seconds of oracle work to size the per-step sample for")
     ap.add_argument("--cpu-table", action="store_true", help="time the CPU oracle on every config instead")
     ap.add_argument("--profile-view", action="store_true", help="small view-sync run for profiling instead")
+    ap.add_argument("--profile-resnet", action="store_true",
+                    help="ResNet-50 bf16 N=16 sync (25 MiB cap) for profiling instead")
     ap.add_argument("--profile-layers", type=int, default=2)
     ap.add_argument("--cap-sweep", action="store_true", help="bucket-cap sweep (one JSON line per point) instead")
     ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
@@ -854,6 +907,9 @@ def main():
         return
     if args.profile_view:
         run_profile_view(args)
+        return
+    if args.profile_resnet:
+        run_profile_resnet(args)
         return
     if args.cpu_table:
         run_cpu_table(args)

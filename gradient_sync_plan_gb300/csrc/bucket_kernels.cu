@@ -27,7 +27,7 @@ namespace ddpk {
 // Multi-tensor copy
 // ---------------------------------------------------------------------------
 
-constexpr int kCopyItems = 256;          // items per launch (8 KB of parameters)
+constexpr int kCopyItems = 768;          // items per launch (24 KB of parameters)
 constexpr int64_t kCopyTile = 32768;     // bytes per tile
 
 struct CopyBatch {
@@ -38,6 +38,7 @@ struct CopyBatch {
     char* dst[kCopyItems];
     int64_t bytes[kCopyItems];
 };
+static_assert(sizeof(CopyBatch) <= kMaxParamBytes, "copy batch exceeds the kernel parameter limit");
 
 // Copy [b0, b1) bytes from src to dst with the whole block.  Element pointers
 // are at least 2-byte aligned; when src and dst agree modulo 16 the middle is
@@ -125,7 +126,7 @@ cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t str
 // narrower type: fp32 gradients are rounded to bf16 (nearest even) on the way
 // into the bucket and widened back (exactly) on the way out.
 
-constexpr int kConvItems = 256;
+constexpr int kConvItems = 704;
 constexpr int64_t kConvTile = 8192;      // elements per tile
 
 struct ConvBatch {
@@ -137,6 +138,7 @@ struct ConvBatch {
     int64_t numel[kConvItems];
     int32_t vec[kConvItems];
 };
+static_assert(sizeof(ConvBatch) <= kMaxParamBytes, "convert batch exceeds the kernel parameter limit");
 
 // MODE 0: float32 -> bf16 (round to nearest even); MODE 1: bf16 -> float32 (exact)
 template <int MODE>
@@ -219,19 +221,20 @@ cudaError_t launch_convert_items(const ConvItem* items, int64_t n, int to_bf16, 
 // Fused view: pack + ring allreduce + average + unpack of one bucket
 // ---------------------------------------------------------------------------
 
-constexpr int kViewMembers = 128;
-constexpr int kViewPtrs = 2048;          // member x rank pointers per launch
+constexpr int kViewMembers = 192;
+constexpr int kViewPtrs = 3072;          // member x rank pointers per launch
 
 struct ViewBatch {
     int32_t n;            // members in this launch
     int32_t world;
-    int64_t clen;         // chunk length of the whole bucket, ceil(bucket_numel / N)
+    int64_t clen[kViewMembers];   // chunk length of the member's bucket, ceil(bucket_numel / N)
     int64_t tile_end[kViewMembers];
     int64_t numel[kViewMembers];
     int64_t offset[kViewMembers];
     int32_t vec[kViewMembers];
     char* ptr[kViewPtrs];  // ptr[m * world + r]: rank r's gradient of member m
 };
+static_assert(sizeof(ViewBatch) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
 
 template <class E>
 constexpr int64_t view_tile_elems() { return (int64_t)kThreads * E::L * 4; }
@@ -255,12 +258,13 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
         const int64_t e0 = (tile - first) * TILE;
         const int64_t e1 = std::min(e0 + TILE, b.numel[m]);
         const int64_t base = b.offset[m];          // bucket position of element 0
+        const int64_t clen = b.clen[m];
         auto at = [&](int r) -> const char* { return b.ptr[m * world + r]; };
         if (b.vec[m]) {
             // chunk of the tile's first element and where (member-relative)
             // the next chunk starts: most vectors are placed by one compare
-            const int64_t j_first = (base + e0) / b.clen;
-            const int64_t next_start = (j_first + 1) * b.clen - base;
+            const int64_t j_first = (base + e0) / clen;
+            const int64_t next_start = (j_first + 1) * clen - base;
             for (int64_t e = e0 + (int64_t)threadIdx.x * L; e < e1; e += (int64_t)blockDim.x * L) {
                 const int64_t q = base + e;
                 int64_t j;
@@ -268,12 +272,12 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
                 if (e + L <= next_start) {
                     j = j_first;
                     whole = e + L <= e1;
-                } else if (e >= next_start && e + L <= next_start + b.clen) {
+                } else if (e >= next_start && e + L <= next_start + clen) {
                     j = j_first + 1;
                     whole = e + L <= e1;
                 } else {
-                    j = q / b.clen;
-                    whole = e + L <= e1 && (q + L - 1) / b.clen == j;
+                    j = q / clen;
+                    whole = e + L <= e1 && (q + L - 1) / clen == j;
                 }
                 if (whole) {
                     const int start = (j + 1 == world) ? 0 : (int)j + 1;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
                     for (int r = 0; r < world; ++r) st_stream<V>(b.ptr[m * world + r] + e * (int64_t)sizeof(S), y);
                 } else {
                     for (int l = 0; l < L && e + l < e1; ++l) {
-                        const int jj = (int)((q + l) / b.clen);
+                        const int jj = (int)((q + l) / clen);
                         const int start = (jj + 1 == world) ? 0 : jj + 1;
                         S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e + l), dop);
                         for (int r = 0; r < world; ++r) reinterpret_cast<S*>(b.ptr[m * world + r])[e + l] = y;
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
             }
         } else {
             for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-                const int jj = (int)((base + e) / b.clen);
+                const int jj = (int)((base + e) / clen);
                 const int start = (jj + 1 == world) ? 0 : jj + 1;
                 S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, e), dop);
                 for (int r = 0; r < world; ++r) reinterpret_cast<S*>(b.ptr[m * world + r])[e] = y;
@@ -305,9 +309,9 @@ static cudaError_t view_impl(int world, const ViewMember* members, int n, int64_
     auto k = k_bucket_view<E, DIV, G>;
     constexpr int64_t TILE = view_tile_elems<E>();
     const int per_launch = std::min(kViewMembers, kViewPtrs / world);
+    const int64_t bucket_clen = chunk_len(bucket_numel, world);
     ViewBatch b;
     b.world = world;
-    b.clen = chunk_len(bucket_numel, world);
     int i = 0;
     while (i < n) {
         b.n = 0;
@@ -319,6 +323,7 @@ static cudaError_t view_impl(int world, const ViewMember* members, int n, int64_
             b.numel[b.n] = members[i].numel;
             b.offset[b.n] = members[i].offset;
             b.vec[b.n] = members[i].vec_ok ? 1 : 0;
+            b.clen[b.n] = members[i].clen > 0 ? members[i].clen : bucket_clen;
             for (int r = 0; r < world; ++r) b.ptr[b.n * world + r] = static_cast<char*>(members[i].ptrs[r]);
             ++b.n;
         }
@@ -347,28 +352,69 @@ static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, D
     }
 }
 
+// Elements of a member that the TMA view kernel cannot take: the pieces
+// before and after each segment's 16-byte-aligned body (fewer than 16 bytes
+// each side of a chunk boundary that is not 16-byte aligned), or the whole
+// member if its pointers are not 16-byte aligned.  Done by the register view
+// kernel, one rank-pointer table per piece.
+struct ViewEdges {
+    std::vector<ViewMember> pieces;
+    std::vector<std::vector<void*>> tables;
+    void add(int world, const ViewMember& m, int64_t start, int64_t len, int64_t es, int64_t clen) {
+        if (len <= 0) return;
+        tables.emplace_back(world);
+        for (int r = 0; r < world; ++r) tables.back()[r] = static_cast<char*>(m.ptrs[r]) + start * es;
+        pieces.push_back(ViewMember{len, m.offset + start, nullptr, false, clen});
+    }
+    void bind() {       // the tables no longer move
+        for (size_t i = 0; i < pieces.size(); ++i) pieces[i].ptrs = tables[i].data();
+    }
+};
+
 // Cut members [first, first + n) of one bucket at the bucket's chunk
-// boundaries into segments (member indices are global); false if a pointer,
-// a segment start or a segment length is not 16-byte aligned.
-static bool append_segments(int world, const ViewMember* members, int first, int n, int64_t bucket_numel, int dtype,
-                            std::vector<ViewSegment>* segs) {
+// boundaries into segments (member indices are global).  A segment's
+// 16-byte-aligned body goes to `segs`; what is left of it, and every member
+// whose pointers are not 16-byte aligned, goes to `edges`.
+static void split_segments(int world, const ViewMember* members, int first, int n, int64_t bucket_numel, int dtype,
+                           std::vector<ViewSegment>* segs, ViewEdges* edges) {
     const int64_t es = elem_bytes(dtype);
+    const int64_t lanes = 16 / es;                       // elements per 16 bytes
     const int64_t clen = chunk_len(bucket_numel, world);
     for (int i = first; i < first + n; ++i) {
         const ViewMember& m = members[i];
-        if (!m.vec_ok) return false;
+        if (!m.vec_ok) {
+            edges->add(world, m, 0, m.numel, es, clen);
+            continue;
+        }
         int64_t a = m.offset;
         const int64_t end = m.offset + m.numel;
+        int64_t pending = 0, pending_len = 0;             // edge piece still open (member-relative)
         while (a < end) {
             const int64_t j = a / clen;
             const int64_t b = std::min(end, (j + 1) * clen);
-            const ViewSegment g{i, (int32_t)j, a - m.offset, b - a};
-            if ((g.start * es) % 16 || (g.len * es) % 16) return false;
-            segs->push_back(g);
+            const int64_t s0 = a - m.offset, s1 = b - m.offset;
+            const int64_t body0 = (s0 + lanes - 1) / lanes * lanes, body1 = s1 / lanes * lanes;
+            if (body1 > body0) {
+                // the head joins the piece left open at the previous boundary
+                if (body0 > s0) {
+                    if (pending_len == 0) pending = s0;
+                    pending_len = body0 - pending;
+                }
+                edges->add(world, m, pending, pending_len, es, clen);
+                pending_len = 0;
+                segs->push_back(ViewSegment{i, (int32_t)j, body0, body1 - body0});
+                if (s1 > body1) {
+                    pending = body1;
+                    pending_len = s1 - body1;
+                }
+            } else {
+                if (pending_len == 0) pending = s0;
+                pending_len = s1 - pending;
+            }
             a = b;
         }
+        edges->add(world, m, pending, pending_len, es, clen);
     }
-    return true;
 }
 
 // The TMA-staged kernel takes a set of segments when the tiles fit the world
@@ -377,32 +423,41 @@ static bool view_tma_worth(int world, int64_t elems, int dtype) {
     return world <= 128 && tma_tile_bytes(world) > 0 && elems * elem_bytes(dtype) * world >= ((int64_t)4 << 20);
 }
 
-static bool view_segments(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
-                          std::vector<ViewSegment>* segs) {
-    if (!view_tma_worth(world, bucket_numel, dtype)) return false;
-    segs->clear();
-    return append_segments(world, members, 0, n, bucket_numel, dtype, segs);
+static cudaError_t view_register(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
+                                 DivSpec div, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
+    if (dtype == kDtypeHook) return view_div<EHOOK>(world, members, n, bucket_numel, div, stream);
+    return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
 }
 
 cudaError_t launch_buckets_view(int world, const ViewMember* members, const int* bucket_first, const int* bucket_count,
                                 const int64_t* bucket_numel, int n_buckets, int dtype, DivSpec div,
                                 cudaStream_t stream) {
-    // every bucket's segments in one set of launches when all of them are
-    // aligned; otherwise bucket by bucket
+    // the aligned bodies of every bucket in one set of TMA launches, the
+    // edges in one register launch; buckets too small for the TMA kernel all
+    // go to the register kernel
     std::vector<ViewSegment> segs;
-    int64_t elems = 0;
-    bool ok = true;
-    for (int k = 0; k < n_buckets && ok; ++k) {
-        ok = append_segments(world, members, bucket_first[k], bucket_count[k], bucket_numel[k], dtype, &segs);
-        elems += bucket_numel[k];
+    ViewEdges edges;
+    int64_t body = 0;
+    for (int k = 0; k < n_buckets; ++k)
+        split_segments(world, members, bucket_first[k], bucket_count[k], bucket_numel[k], dtype, &segs, &edges);
+    for (const ViewSegment& g : segs) body += g.len;
+    if (view_tma_worth(world, body, dtype)) {
+        int n_members = 0;
+        for (int k = 0; k < n_buckets; ++k) n_members = std::max(n_members, bucket_first[k] + bucket_count[k]);
+        cudaError_t e = launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(), dtype, div,
+                                               stream);
+        if (e != cudaSuccess) return e;
+        edges.bind();
+        if (debug_enabled())
+            fprintf(stderr, "[ddp] bucket_view edges=%zu\n", edges.pieces.size());
+        // every edge piece carries its own bucket's chunk length
+        return view_register(world, edges.pieces.data(), (int)edges.pieces.size(), 1, dtype, div, stream);
     }
-    int n_members = 0;
-    for (int k = 0; k < n_buckets; ++k) n_members = std::max(n_members, bucket_first[k] + bucket_count[k]);
-    if (ok && view_tma_worth(world, elems, dtype))
-        return launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(), dtype, div, stream);
     for (int k = 0; k < n_buckets; ++k) {
-        cudaError_t e = launch_bucket_view(world, members + bucket_first[k], bucket_count[k], bucket_numel[k], dtype,
-                                           div, stream);
+        cudaError_t e = view_register(world, members + bucket_first[k], bucket_count[k], bucket_numel[k], dtype, div,
+                                      stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -411,14 +466,8 @@ cudaError_t launch_buckets_view(int world, const ViewMember* members, const int*
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                DivSpec div, cudaStream_t stream) {
     if (n == 0 || bucket_numel == 0) return cudaSuccess;
-    {
-        std::vector<ViewSegment> segs;
-        if (view_segments(world, members, n, bucket_numel, dtype, &segs))
-            return launch_bucket_view_tma(world, members, n, segs.data(), (int)segs.size(), dtype, div, stream);
-    }
-    if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
-    if (dtype == kDtypeHook) return view_div<EHOOK>(world, members, n, bucket_numel, div, stream);
-    return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
+    const int first = 0;
+    return launch_buckets_view(world, members, &first, &n, &bucket_numel, 1, dtype, div, stream);
 }
 
 }  // namespace ddpk

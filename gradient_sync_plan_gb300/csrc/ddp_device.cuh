@@ -168,15 +168,27 @@ __device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, 
     return acc;
 }
 
-// Scalar version of the same fold for one element at element index `e`.
+// Scalar version of the same fold for one element at element index `e`,
+// its loads issued eight at a time.
 template <class E, class PtrAt>
 __device__ __forceinline__ typename E::S fold_ring_scalar(PtrAt ptr_at, int world, int start, int64_t e) {
     using S = typename E::S;
+    constexpr int G = 8;
+    S acc{};
     int r = start;
-    S acc = reinterpret_cast<const S*>(ptr_at(r))[e];
-    for (int k = 1; k < world; ++k) {
-        r = (r + 1 == world) ? 0 : r + 1;
-        acc = E::sadd(acc, reinterpret_cast<const S*>(ptr_at(r))[e]);
+    for (int k0 = 0; k0 < world; k0 += G) {
+        S x[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (k0 + g < world) {
+                x[g] = reinterpret_cast<const S*>(ptr_at(r))[e];
+                r = (r + 1 == world) ? 0 : r + 1;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (k0 + g < world) acc = (k0 + g == 0) ? x[g] : E::sadd(acc, x[g]);
+        }
     }
     return acc;
 }

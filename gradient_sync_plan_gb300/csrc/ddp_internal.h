@@ -10,6 +10,7 @@
 namespace ddpk {
 
 constexpr int kThreads = 256;            // threads per block of every kernel
+constexpr size_t kMaxParamBytes = 32764;  // kernel parameter space per launch (CUDA 12.1+)
 
 // Divide modes of the average y / divisor:
 //   kDivNone  divisor 0 or 1, keep the sum
@@ -99,6 +100,7 @@ struct ViewMember {
     int64_t offset;
     void* const* ptrs;   // host array of world device pointers
     bool vec_ok;         // every pointer 16-byte aligned
+    int64_t clen = 0;    // chunk length of the member's bucket (0: the bucket passed with it)
 };
 cudaError_t launch_bucket_view(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                DivSpec div, cudaStream_t stream);

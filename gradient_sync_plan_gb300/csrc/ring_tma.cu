@@ -255,8 +255,8 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 // tiles k, k + G, ... and finds their segment by scanning forward.
 // ---------------------------------------------------------------------------
 
-constexpr int kViewSegs = 160;
-constexpr int kViewPtrCap = 2048;
+constexpr int kViewSegs = 224;
+constexpr int kViewPtrCap = 2816;
 
 struct ViewTmaBatch {
     int32_t n_seg;
@@ -269,6 +269,7 @@ struct ViewTmaBatch {
     int32_t mem[kViewSegs];          // member slot: its rank pointers are ptr[mem * world ..]
     char* ptr[kViewPtrCap];
 };
+static_assert(sizeof(ViewTmaBatch) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
 
 struct SegCursor {
     int seg;
@@ -540,6 +541,9 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
         k<<<grid, kTmaThreads, smem, st>>>(b, dop);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        if (debug_enabled())
+            fprintf(stderr, "[ddp] bucket_view_tma world=%d segments=%d members=%d tiles=%lld grid=%d\n", world,
+                    b.n_seg, slots, (long long)tiles, grid);
     }
     return cudaSuccess;
 }

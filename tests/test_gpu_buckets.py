@@ -358,3 +358,93 @@ def test_bf16_hook_view_world_one_rounds():
     torch.cuda.synchronize()
     oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=1)
     assert_bits_equal(f32_or_bits(g), np.stack([grads_h[0][0]]), "hook view world 1")
+
+
+@pytest.mark.parametrize("layout", ["decoder", "aligned"])
+@pytest.mark.parametrize("algo", ["fused", "view", "hook", "hook_view"])
+def test_many_ranks_split_into_several_launches(algo, layout):
+    # 128 ranks x ~40 members: the pack / unpack / convert item tables and
+    # the view pointer tables overflow one launch's parameter space, so each
+    # bucket is done in several launches; the result must not change.  The
+    # small decoder's chunks are not 16-byte aligned (register view kernel);
+    # the "aligned" list's are (TMA view kernel).
+    if layout == "decoder":
+        numels = _small_decoder()
+    else:
+        numels = [512 * (i % 7 + 1) for i in range(40)]
+    world, first, cap = 128, 4096, 1 << 30
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=31)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    code = {"fused": ddp.DDP_ALGO_FUSED, "view": ddp.DDP_ALGO_VIEW, "hook": ddp.DDP_ALGO_BF16_HOOK,
+            "hook_view": ddp.DDP_ALGO_BF16_HOOK_VIEW}[algo]
+    bk = None
+    if algo in ("fused", "hook"):
+        bdt = torch.float32 if algo == "fused" else torch.bfloat16
+        bk = [[torch.empty(int(n), dtype=bdt, device="cuda") for n in plan[2]] for _ in range(world)]
+    ddp.ddp_sync_buckets(views, plan, bk, algo=code)
+    torch.cuda.synchronize()
+    if algo in ("hook", "hook_view"):
+        oracle.ddp_sync_bf16_hook(grads_h, first, cap)
+    else:
+        oracle.ddp_sync(grads_h, oracle.F32, first, cap)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"{algo} {layout} at N={world}")
+
+
+def _oracle_view(grads_h, offsets, bucket_numel, code, divisor):
+    """Oracle pack -> ring -> unpack of one bucket (in place on grads_h)."""
+    world = len(grads_h)
+    dt = np.uint16 if code == oracle.BF16 else np.float32
+    bufs = []
+    for r in range(world):
+        b = np.zeros(bucket_numel, dtype=dt)
+        oracle.bucket_pack(grads_h[r], offsets, b, code)
+        bufs.append(b)
+    oracle.ring_allreduce(bufs, code, divisor)
+    for r in range(world):
+        oracle.bucket_unpack(grads_h[r], offsets, bufs[r], code)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", ["boundaries", "pointers"])
+def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
+    # a TMA-sized bucket (8 ranks) whose chunk boundaries are not 16-byte
+    # aligned ("boundaries": every member 16-byte aligned in memory, the
+    # chunk length odd), or whose members' pointers are not ("pointers":
+    # members packed back to back at odd offsets in one arena).  The aligned
+    # bodies go to the TMA kernel, the few elements around each boundary and
+    # the misaligned members to the register kernel.
+    world = 8
+    es = 2 if dtype == "bf16" else 4
+    lanes = 16 // es
+    if layout == "boundaries":
+        numels = [lanes * 100_000, lanes * 1_000_001, 3 * lanes, lanes * 150_000]
+    else:
+        numels = [5, 1_000_003, 17, 1, 700_001, 6]
+    total = sum(numels)
+    offsets = list(np.cumsum([0] + numels[:-1]))
+    if layout == "boundaries":
+        assert (-(-total // world) * es) % 16 != 0
+    host = []
+    for r in range(world):
+        xs = workloads.rank_vectors(1, total, "randn", std=1e-2, dtype=dtype, seed0=50 + r)[0]
+        host.append(xs)
+    if layout == "boundaries":
+        dev = [[host[r][offsets[i]:offsets[i] + numels[i]].clone().to("cuda") for i in range(len(numels))]
+               for r in range(world)]
+    else:
+        arenas = [h.to("cuda") for h in host]
+        dev = [[arenas[r][offsets[i]:offsets[i] + numels[i]] for i in range(len(numels))] for r in range(world)]
+        assert any(t.data_ptr() % 16 for t in dev[0])
+    code = oracle.BF16 if dtype == "bf16" else oracle.F32
+    for div in (world, 3):
+        grads_h = [[f32_or_bits(t) for t in dev[r]] for r in range(world)]
+        ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
+        torch.cuda.synchronize()
+        _oracle_view(grads_h, offsets, total, code, div)
+        for r in range(world):
+            for i in range(len(numels)):
+                assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i], f"{layout} {dtype} div={div} r{r} m{i}")
+    assert ddp.ddp_device_status() == 0
