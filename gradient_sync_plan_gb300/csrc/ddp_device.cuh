@@ -140,6 +140,20 @@ __device__ __forceinline__ uint4 shfl_vec(uint4 a, int src, int width) {
     return make_uint4(__shfl_sync(0xffffffffu, a.x, src, width), __shfl_sync(0xffffffffu, a.y, src, width),
                       __shfl_sync(0xffffffffu, a.z, src, width), __shfl_sync(0xffffffffu, a.w, src, width));
 }
+// The same, from lane (caller + delta) of the segment (the caller's own value
+// where that lane is past the segment's end).
+__device__ __forceinline__ float4 shfl_down_vec(float4 a, int delta, int width) {
+    return make_float4(__shfl_down_sync(0xffffffffu, a.x, delta, width),
+                       __shfl_down_sync(0xffffffffu, a.y, delta, width),
+                       __shfl_down_sync(0xffffffffu, a.z, delta, width),
+                       __shfl_down_sync(0xffffffffu, a.w, delta, width));
+}
+__device__ __forceinline__ uint4 shfl_down_vec(uint4 a, int delta, int width) {
+    return make_uint4(__shfl_down_sync(0xffffffffu, a.x, delta, width),
+                      __shfl_down_sync(0xffffffffu, a.y, delta, width),
+                      __shfl_down_sync(0xffffffffu, a.z, delta, width),
+                      __shfl_down_sync(0xffffffffu, a.w, delta, width));
+}
 
 // Fold the N ranks' vectors at byte offset `off` in ring order, starting at
 // rank `start` (the rank right after the chunk's owner) and wrapping around:

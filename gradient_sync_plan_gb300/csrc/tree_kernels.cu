@@ -13,6 +13,8 @@
 //
 //   k_tree_fused  one pass: every element folded in that order, divided,
 //                 written to every rank (N <= 64)
+//   k_tree_fused_group  the same for buckets of a few KiB per rank, the
+//                 ranks spread over the lanes of a warp
 //   k_tree_hop    one launch per tree step, moving exactly what the step moves
 #include <algorithm>
 #include <cstdio>
@@ -85,6 +87,69 @@ k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel,
     }
 }
 
+// Group fused tree for small buckets: P lanes share one 16-byte vector, lane
+// q holding ranks q, q + P, ... (R = ceil(N / P) of them).  Tree levels
+// d < P are warp shuffles (lane q, q a multiple of 2d, adds lane q + d's
+// value), levels d >= P add a lane's own registers -- the binomial tree's
+// additions in its order, as in tree_fold.  Lane 0 of the group ends with
+// the sum, which every lane then takes and stores to its ranks.  Vectors
+// that run past the end are done element-wise by the group's lane 0.
+template <class E, int DIV, int CAP, int P, int R>
+__global__ void __launch_bounds__(kThreads)
+k_tree_fused_group(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    constexpr int kGroups = 32 / P;
+    const int lane = threadIdx.x & 31;
+    const int q = lane & (P - 1);
+    const int64_t nvec = (numel + L - 1) / L;
+    const int64_t full = numel / L;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t base = warp * kGroups; base < nvec; base += n_warps * kGroups) {    // warp-uniform bounds
+        const int64_t v = base + lane / P;
+        const bool valid = v < nvec;
+        const bool whole = v < full;
+        const int64_t off = v * 16;
+        V x[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const int r = m * P + q;
+            x[m] = (whole && r < world) ? ld_stream<V>(t.p[r] + off) : make_zero<V>();
+        }
+#pragma unroll
+        for (int d = 1; d < P; d <<= 1) {
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                const V o = shfl_down_vec(x[m], d, P);
+                if ((q & (2 * d - 1)) == 0 && m * P + q + d < world) x[m] = E::vadd(x[m], o);
+            }
+        }
+#pragma unroll
+        for (int dm = 1; dm < R; dm <<= 1) {               // d = dm * P
+#pragma unroll
+            for (int m = 0; m + dm < R; m += 2 * dm)
+                if (m * P + dm * P < world) x[m] = E::vadd(x[m], x[m + dm]);
+        }
+        const V y = E::template vdiv<DIV>(shfl_vec(x[0], 0, P), dop);
+        if (whole) {
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                const int r = m * P + q;
+                if (r < world) st_stream<V>(t.p[r] + off, y);
+            }
+        } else if (valid && q == 0) {
+            for (int64_t e = v * L; e < numel; ++e) {
+                S z = tree_fold<S>(world, [](S a, S b) { return E::sadd(a, b); },
+                                   [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
+                z = E::template sdiv<DIV>(z, dop);
+                for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = z;
+            }
+        }
+    }
+}
+
 // One tree step for every pair at once; blockIdx.y is the pair index, its
 // lower rank is r = blockIdx.y * 2d and its upper rank r + d.
 //   phase 0 (reduce):    buf[r]     = buf[r] (+) buf[r + d]   (divided if `divide`)
@@ -147,6 +212,46 @@ static cudaError_t tree_fused_impl(int world, void* const* ptrs, int64_t numel, 
     return cudaGetLastError();
 }
 
+constexpr int kTreeGroupThreads = 128;
+
+template <class E, int DIV, int P, int R>
+static cudaError_t tree_group_launch(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
+    auto k = k_tree_fused_group<E, DIV, kTreeMaxWorld, P, R>;
+    const int64_t nvec = (numel + E::L - 1) / E::L;
+    const int64_t lanes = (nvec + 32 / P - 1) / (32 / P) * 32;
+    const int grid = grid_for((const void*)k, lanes, kTreeGroupThreads);
+    k<<<grid, kTreeGroupThreads, 0, st>>>(tree_table<kTreeMaxWorld>(world, ptrs), world, numel, dop);
+    return cudaGetLastError();
+}
+
+template <class E, int DIV>
+static cudaError_t tree_group_impl(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
+    if (world <= 2) return tree_group_launch<E, DIV, 2, 1>(world, ptrs, numel, dop, st);
+    if (world <= 4) return tree_group_launch<E, DIV, 4, 1>(world, ptrs, numel, dop, st);
+    if (world <= 8) return tree_group_launch<E, DIV, 8, 1>(world, ptrs, numel, dop, st);
+    if (world <= 16) return tree_group_launch<E, DIV, 16, 1>(world, ptrs, numel, dop, st);
+    if (world <= 32) return tree_group_launch<E, DIV, 32, 1>(world, ptrs, numel, dop, st);
+    return tree_group_launch<E, DIV, 32, 2>(world, ptrs, numel, dop, st);
+}
+
+// The group kernel for buckets of a few KiB per rank, one thread per vector
+// above that (ddp_set_fused_kernel can force either).
+static bool tree_use_group(int world, int64_t numel, int dtype, bool vec_ok) {
+    if (!vec_ok || world < 2) return false;
+    switch (fused_kernel_override()) {
+        case DDP_FUSED_GROUP: return true;
+        case DDP_FUSED_VECTOR:
+        case DDP_FUSED_TMA: return false;
+        default: break;
+    }
+    // crossovers measured on GB300 (fp32 and bf16, N = 2 .. 64): the group
+    // kernel needs log2(P) shuffle levels per vector, so it stays ahead up to
+    // larger buckets than the ring's group kernel, the more so the fewer ranks
+    const int64_t KiB = 1024;
+    const int64_t limit = world == 2 ? 4096 * KiB : world <= 4 ? 512 * KiB : world <= 16 ? 128 * KiB : 64 * KiB;
+    return numel * elem_bytes(dtype) <= limit;
+}
+
 template <class E, int DIV>
 static cudaError_t tree_staged_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                     cudaStream_t st) {
@@ -191,10 +296,23 @@ static cudaError_t tree_by_div(bool staged, int world, void* const* ptrs, int64_
     }
 }
 
+template <class E>
+static cudaError_t tree_group_by_div(int world, void* const* ptrs, int64_t numel, DivSpec d, cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return tree_group_impl<E, kDivNone>(world, ptrs, numel, d.operand, st);
+        case kDivPow2: return tree_group_impl<E, kDivPow2>(world, ptrs, numel, d.operand, st);
+        default: return tree_group_impl<E, kDivIeee>(world, ptrs, numel, d.operand, st);
+    }
+}
+
 cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                   bool vec_ok, cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
     if (staged && world == 1) staged = false;                 // no step: the divide only
+    if (!staged && tree_use_group(world, numel, dtype, vec_ok)) {
+        if (dtype == DDP_F32) return tree_group_by_div<EF32>(world, ptrs, numel, div, stream);
+        return tree_group_by_div<EBF16>(world, ptrs, numel, div, stream);
+    }
     if (dtype == DDP_F32) return tree_by_div<EF32>(staged, world, ptrs, numel, div, vec_ok, stream);
     return tree_by_div<EBF16>(staged, world, ptrs, numel, div, vec_ok, stream);
 }

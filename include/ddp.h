@@ -105,6 +105,8 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  *                    copies (N <= 128, 16-byte-aligned chunks).
  * A kernel that cannot run a call (alignment, world size) is replaced by
  * the vector kernel, or the element-wise one for unaligned buffers.
+ * tree_allreduce_fused follows the same choice between its group and vector
+ * kernels (DDP_FUSED_TMA selects its vector kernel: the tree has no TMA one).
  * *previous (if not NULL) receives the old choice.  DDP_ERR_INVALID for an
  * unknown kind.
  */

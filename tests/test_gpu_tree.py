@@ -88,3 +88,29 @@ def test_one_gib_buckets_sampled(kernel):
         assert torch.equal(x[r].view(torch.int32), x[0].view(torch.int32))
     del x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_both_kernels_around_the_size_switch(dtype):
+    # small buckets take the lane-group kernel, larger ones one thread per
+    # vector; sizes on both sides of the switches (64, 128 and 512 KiB per
+    # rank) with ragged tails, every lane split (P = 2 .. 32 lanes per
+    # vector, one or two vectors per lane); then each kernel forced
+    es = 2 if dtype == "bf16" else 4
+    for N in (2, 3, 5, 8, 16, 17, 31, 33, 64):
+        for kib in ((16, 64, 128, 512) if N <= 8 else (16, 64, 128)):
+            for delta in (-3, 0, 5):
+                S = kib * 1024 // es + delta
+                xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + kib + delta))
+                for div in (N, 3):
+                    assert_bits_equal(run("fused", xh, div), oracle_tree(xh, div), f"tree N={N} S={S} div={div}")
+
+    for kind in (ddp.DDP_FUSED_GROUP, ddp.DDP_FUSED_VECTOR):
+        for N, S in ((2, 3 * 1024 * 1024 // es + 7), (7, 99_999), (64, 40_000 + 3)):
+            xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + kind))
+            prev = ddp.ddp_set_fused_kernel(kind)
+            try:
+                got = run("fused", xh, N)
+            finally:
+                ddp.ddp_set_fused_kernel(prev)
+            assert_bits_equal(got, oracle_tree(xh, N), f"tree forced kernel {kind} N={N} S={S}")
