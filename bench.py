@@ -794,6 +794,62 @@ def run_profile_resnet(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_kernels(args):
+    """Every kernel family once on one workload larger than L2, for a
+    per-kernel ncu DRAM capture: N = 8 ranks x 2^25 fp32 (128 MiB per rank,
+    1 GiB over all ranks), in this order -- fused ring (vector, then TMA
+    kernel), staged ring, persistent ring, fused tree (vector kernel), staged
+    tree, no_sync accumulation, bf16 pack and unpack (one 2^25-element
+    member per rank), fused view (one bucket of 4 members per rank).  --steps
+    repeats the sequence.  Prints one JSON line (not a bench result)."""
+    import torch
+    import gradient_sync_plan_gb300 as ddp
+    import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, S = N_RANKS, 1 << 25
+    x = torch.empty((N, S), dtype=torch.float32, device=dev)
+    for r in range(N):
+        x[r].copy_(workloads.randn_f32(S, r, 1e-2, device=str(dev)))
+    y = torch.empty_like(x)
+    y.copy_(x)
+    b16 = torch.empty((N, S), dtype=torch.bfloat16, device=dev)
+    members = [S // 4] * 4
+    offs = [0, S // 4, S // 2, 3 * S // 4]
+    views = [[x[r, o:o + n] for o, n in zip(offs, members)] for r in range(N)]
+    status = torch.zeros(2, dtype=torch.int32, device=dev)
+
+    def forced(kind, fn):
+        prev = ddp.ddp_set_fused_kernel(kind)
+        try:
+            fn()
+        finally:
+            ddp.ddp_set_fused_kernel(prev)
+
+    seq = [("ring_fused_vector", lambda: forced(ddp.DDP_FUSED_VECTOR, lambda: ddp.ring_allreduce_fused(x, N))),
+           ("ring_fused_tma", lambda: forced(ddp.DDP_FUSED_TMA, lambda: ddp.ring_allreduce_fused(x, N))),
+           ("ring_staged", lambda: ddp.ring_allreduce_staged(x, N)),
+           ("ring_persistent", lambda: ddp.ring_allreduce_persistent(x, N, status=status)),
+           ("tree_fused_vector", lambda: forced(ddp.DDP_FUSED_VECTOR, lambda: ddp.tree_allreduce_fused(x, N))),
+           ("tree_staged", lambda: ddp.tree_allreduce_staged(x, N)),
+           ("accumulate", lambda: ddp.ddp_grad_accumulate(x, y)),
+           ("pack_bf16", lambda: ddp.ddp_bucket_pack_bf16([[x[r]] for r in range(N)], [0], b16)),
+           ("unpack_bf16", lambda: ddp.ddp_bucket_unpack_bf16([[y[r]] for r in range(N)], [0], b16)),
+           ("view", lambda: ddp.ddp_bucket_allreduce_view(views, offs, S, N))]
+    out = {"profile": "kernels", "ranks": N, "numel": S}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(1, args.steps)):
+        for name, fn in seq:
+            torch.cuda.synchronize()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            out[name + "_ms"] = e0.elapsed_time(e1)
+    assert int(status[0].item()) == 0
+    print(json.dumps(out), flush=True)
+
+
 def run_cpu_table(args):
     """The CPU oracle (single-threaded C, this host) on every workload,
     for the comparison table: one JSON line per measurement."""
@@ -881,6 +937,8 @@ def main():
     ap.add_argument("--profile-view", action="store_true", help="small view-sync run for profiling instead")
     ap.add_argument("--profile-resnet", action="store_true",
                     help="ResNet-50 bf16 N=16 sync (25 MiB cap) for profiling instead")
+    ap.add_argument("--profile-kernels", action="store_true",
+                    help="every kernel family once on 8 x 128 MiB, for profiling instead")
     ap.add_argument("--profile-layers", type=int, default=2)
     ap.add_argument("--cap-sweep", action="store_true", help="bucket-cap sweep (one JSON line per point) instead")
     ap.add_argument("--sweep", action="store_true", help="message-size sweep (one JSON line per point) instead")
@@ -910,6 +968,9 @@ def main():
         return
     if args.profile_resnet:
         run_profile_resnet(args)
+        return
+    if args.profile_kernels:
+        run_profile_kernels(args)
         return
     if args.cpu_table:
         run_cpu_table(args)
