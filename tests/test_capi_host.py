@@ -225,3 +225,49 @@ def test_process_wide_knobs_validate_and_return_previous():
     assert L.ddp_set_fused_kernel(ddp.DDP_FUSED_AUTO, None) == 0      # previous may be NULL
     assert ddp.ddp_set_max_ctas(5) == 0
     assert ddp.ddp_set_max_ctas(0) == 5
+
+
+def test_plain_c_client_links_and_plans(tmp_path):
+    # a C99 program linked against the library (no Python, no GPU): the host
+    # entry points work from C; the plan is the hand-computed one
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        return
+    src = tmp_path / "client.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "ddp.h"
+int main(void) {
+    /* 5 parameters in registration order (fp32): 300, 100, 200, 50, 400
+       elements; first cap 1600 B (400 elements), cap 2000 B (500 elements).
+       Reverse order: 400 -> closes bucket 0 (1600 B >= 1600 B); then 50,
+       200, 100 (350 el.), 300 -> 650 el. = 2600 B >= 2000 B closes bucket 1. */
+    const int64_t numel[5] = {300, 100, 200, 50, 400};
+    int32_t bucket_of[5];
+    int64_t offset_of[5], bucket_numel[5];
+    int32_t n_buckets = -1;
+    int32_t st = ddp_plan_buckets(5, numel, DDP_F32, 1600, 2000, bucket_of, offset_of, bucket_numel, &n_buckets);
+    if (st != DDP_OK || n_buckets != 2) { printf("plan %d %d\n", st, n_buckets); return 1; }
+    const int32_t want_b[5] = {1, 1, 1, 1, 0};
+    const int64_t want_off[5] = {350, 250, 50, 0, 0};
+    for (int i = 0; i < 5; ++i)
+        if (bucket_of[i] != want_b[i] || offset_of[i] != want_off[i]) { printf("param %d\n", i); return 2; }
+    if (bucket_numel[0] != 400 || bucket_numel[1] != 650) return 3;
+    if (strcmp(ddp_status_string(DDP_ERR_INVALID), ddp_status_string(DDP_OK)) == 0) return 4;
+    if (ring_allreduce_fused(0, NULL, 16, DDP_F32, 0, NULL) != DDP_ERR_INVALID) return 5;
+    int32_t prev = 7;
+    if (ddp_set_fused_kernel(9, &prev) != DDP_ERR_INVALID || prev != 7) return 6;
+    if (ddp_abi_version() != DDP_ABI_VERSION) return 7;
+    printf("ok\n");
+    return 0;
+}
+''')
+    inc = os.path.join(ROOT, "include")
+    libdir = os.path.dirname(ddp.lib()._name)
+    exe = tmp_path / "client"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, str(src),
+                           "-L", libdir, "-lddp_gb300", "-Wl,-rpath," + libdir, "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
