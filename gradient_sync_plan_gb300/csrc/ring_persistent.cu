@@ -48,27 +48,41 @@ __device__ __forceinline__ uint16_t ld_l2_scalar<uint16_t>(const uint16_t* p) {
     return (uint16_t)__ldcg(reinterpret_cast<const unsigned short*>(p));
 }
 
+// Arrival and polling at gpu scope: the release-add publishes every write the
+// block made before the barrier (bar.sync orders the block's threads before
+// thread 0's release), the acquire-load makes the other blocks' writes
+// visible to this block after it.
+__device__ __forceinline__ void red_add_release_gpu(unsigned int* p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Grid barrier number `k` (0-based): every block adds one arrival to
 // *counter and waits until all gridDim.x * (k + 1) arrivals are in.  False if
-// the wait ran past limit_ns.
+// the wait ran past limit_ns (the clock is read every 64 polls).
 __device__ __forceinline__ bool grid_barrier(unsigned int* counter, unsigned int k, bool arrive,
                                              unsigned long long limit_ns) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        if (arrive) atomicAdd(counter, 1u);
+        if (arrive) red_add_release_gpu(counter, 1u);
         const unsigned int target = gridDim.x * (k + 1);
-        const unsigned long long t0 = pers_ns();
         int ok = 1;
-        while (*reinterpret_cast<volatile unsigned int*>(counter) < target) {
-            if (pers_ns() - t0 > limit_ns) {
-                ok = 0;
-                break;
+        if (ld_acquire_gpu(counter) < target) {
+            const unsigned long long t0 = pers_ns();
+            unsigned int polls = 0;
+            while (ld_acquire_gpu(counter) < target) {
+                if ((++polls & 63u) == 0 && pers_ns() - t0 > limit_ns) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(16);
             }
-            __nanosleep(64);
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
