@@ -429,3 +429,37 @@ def test_forced_fused_kernel_in_bucketed_sync(kind):
     oracle.ddp_sync(grads_h, oracle.F32, first, cap)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
     assert_bits_equal(f32_or_bits(g), want, f"bucketed sync with {kind}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_maximum_world_size(dtype):
+    # DDP_MAX_WORLD = 512 ranks on a ragged bucket (chunks of 5 elements, the
+    # last ones short or empty): every ring kernel, the staged tree and the
+    # view sync of a 3-member bucket
+    N, S = 512, 2053
+    xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=9))
+    want = oracle_allreduce(xh, N)
+    for kernel in ("fused", "staged", "persistent"):
+        assert_bits_equal(run_gpu(kernel, xh, N), want, f"{kernel} N={N}")
+    x = from_np(xh)
+    ddp.tree_allreduce_staged(x, N)
+    torch.cuda.synchronize()
+    t = np.ascontiguousarray(xh).copy()
+    oracle.tree_allreduce_2d(t, oracle.BF16 if dtype == "bf16" else oracle.F32, N)
+    assert_bits_equal(f32_or_bits(x), t, "tree staged N=512")
+    # view: members of 1000, 53 and 1000 elements at bucket offsets 0, 1000, 1053
+    x = from_np(xh)
+    numels, offsets = [1000, 53, 1000], [0, 1000, 1053]
+    views = [[x[r, o:o + n] for o, n in zip(offsets, numels)] for r in range(N)]
+    ddp.ddp_bucket_allreduce_view(views, offsets, S, N)
+    torch.cuda.synchronize()
+    assert_bits_equal(f32_or_bits(x), want, "view N=512")
+
+
+@pytest.mark.parametrize("kind,S", [("tma", (1 << 31) + 8), ("vector", (1 << 31) + 8), ("auto", (1 << 31) + 5)])
+def test_more_than_2_31_elements_per_rank(kind, S):
+    # 2 ranks x just over 2^31 fp32 (8 GiB per rank): element, chunk and tile
+    # indices past the 32-bit range, on the TMA kernel (16-byte chunks), the
+    # vector kernel, and a ragged size (last vector done element-wise)
+    _with_fused_kernel(kind, lambda: _sampled_check("fused", 2, S, "f32", "uniform", 1.0, 2, k_random=2000))
+    torch.cuda.empty_cache()
