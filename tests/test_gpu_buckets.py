@@ -448,3 +448,29 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
             for i in range(len(numels)):
                 assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i], f"{layout} {dtype} div={div} r{r} m{i}")
     assert ddp.ddp_device_status() == 0
+
+
+@pytest.mark.parametrize("algo", ["fused", "staged", "hook"])
+def test_one_scratch_buffer_shared_by_every_bucket(algo):
+    # the bucket buffers may alias across buckets (one scratch per rank,
+    # reused by every bucket): each bucket must then be packed, reduced and
+    # unpacked before the next one is packed
+    numels = _small_decoder()
+    world, first, cap = 8, 4096, 40000
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
+    assert len(plan[2]) > 2
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=41)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    bdt = torch.bfloat16 if algo == "hook" else torch.float32
+    scratch = [torch.empty(int(max(plan[2])), dtype=bdt, device="cuda") for _ in range(world)]
+    bk = [[scratch[r][:int(n)] for n in plan[2]] for r in range(world)]
+    code = {"fused": ddp.DDP_ALGO_FUSED, "staged": ddp.DDP_ALGO_STAGED, "hook": ddp.DDP_ALGO_BF16_HOOK}[algo]
+    ddp.ddp_sync_buckets(views, plan, bk, algo=code)
+    torch.cuda.synchronize()
+    if algo == "hook":
+        oracle.ddp_sync_bf16_hook(grads_h, first, cap)
+    else:
+        oracle.ddp_sync(grads_h, oracle.F32, first, cap)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"{algo} with one shared scratch buffer")
