@@ -868,17 +868,25 @@ def run_cpu_table(args):
         return best
 
     def emit(**kw):
-        kw["cores"] = 1
+        kw.setdefault("cores", 1)
         kw["host_cores_present"] = host_cores()
         print(json.dumps(kw), flush=True)
 
-    # C1 and C2 and the C5 sweep: one bucket, ring allreduce / N
+    # C1 and C2 and the C5 sweep: one bucket, ring allreduce / N; C1 and C2
+    # also through the -fopenmp build of the same source (ranks of a
+    # half-step on N threads, same per-element operations)
     for cfg, N, S, reps in (("C1", 4, 1 << 20, 3), ("C2", 8, 1 << 28, 1)):
         x = workloads.rank_vectors(N, S, "randn", std=1.0 if cfg == "C1" else 1e-2).numpy()
         rows = [x[r] for r in range(N)]
         t = timed(lambda: oracle.ring_allreduce(rows, oracle.F32, N), reps)
         emit(config=cfg, ranks=N, bytes_per_rank=S * 4, seconds=t,
              busbw_gbs=2 * (N - 1) / N * S * 4 / t / 1e9)
+        try:
+            t = timed(lambda: oracle.ring_allreduce_2d_openmp(x, oracle.F32, N), reps)
+            emit(config=cfg, build="openmp", cores=min(N, host_cores() or N), ranks=N, bytes_per_rank=S * 4,
+                 seconds=t, busbw_gbs=2 * (N - 1) / N * S * 4 / t / 1e9)
+        except Exception as e:          # a compiler without OpenMP: no second row
+            emit(config=cfg, build="openmp", unavailable=str(e)[:120])
         del x, rows
     for N, kmax in ((8, 16), (64, 14)):
         for k in range(0, kmax + 1, 2):

@@ -37,16 +37,41 @@ _LIB_PATH = os.path.join(_HERE, "libddp_oracle.so")
 _CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 _lock = threading.Lock()
 _lib = None
+_omp_lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile ddp_oracle.c into libddp_oracle.so next to it (gcc, no fast-math)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+_OMP_LIB_PATH = os.path.join(_HERE, "libddp_oracle_omp.so")
+
+
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile ddp_oracle.c into libddp_oracle.so next to it (gcc, no fast-math).
+    openmp=True builds libddp_oracle_omp.so instead: the same source with
+    -fopenmp, whose ring runs the ranks of a half-step on several threads
+    (same per-element operations; used only to time the oracle on many cores)."""
+    path = _OMP_LIB_PATH if openmp else _LIB_PATH
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
         cc = os.environ.get("CC", "gcc")
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call([cc, *_CFLAGS, "-o", tmp, _SRC])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.check_call([cc, *_CFLAGS, *(["-fopenmp"] if openmp else []), "-o", tmp, _SRC])
+        os.replace(tmp, path)
+    return path
+
+
+def ring_allreduce_2d_openmp(x: np.ndarray, dtype: int = F32, divisor: int = 0) -> np.ndarray:
+    """ring_allreduce_2d through the -fopenmp build (timing only)."""
+    global _omp_lib
+    with _lock:
+        if _omp_lib is None:
+            L = ctypes.CDLL(build(openmp=True))
+            i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+            L.oracle_ring_allreduce.argtypes = [i32, i64, i32, ctypes.POINTER(vp), i32, i32, ctypes.POINTER(i64)]
+            L.oracle_ring_allreduce.restype = ctypes.c_int
+            _omp_lib = L
+    x = np.ascontiguousarray(x)
+    world, numel = x.shape[0], x.shape[1]
+    ptrs = (ctypes.c_void_p * max(world, 1))(*[x[r].ctypes.data for r in range(world)])
+    _check(_omp_lib.oracle_ring_allreduce(world, numel, dtype, ptrs, divisor, -1, None), "ring_allreduce (openmp)")
+    return x
 
 
 def lib() -> ctypes.CDLL:

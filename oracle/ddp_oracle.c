@@ -10,6 +10,7 @@
  * Build: cc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
  * (no FMA contraction, no fast-math, so every float operation below is one
  * IEEE-754 binary32 operation rounded to nearest even, subnormals kept).
+ * The same flags plus -fopenmp give the optional multi-core timing build.
  *
  * Sources (web pages on DDP gradient synchronisation):
  *   [P1] "DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事"
@@ -39,6 +40,16 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+
+/* Built with -fopenmp (the optional multi-core timing build only), the ranks
+ * of one half-step run side by side: within a half-step every rank reads and
+ * writes only its own buffer and message, so the per-element order of the
+ * operations is the same as in the default single-threaded build. */
+#ifdef _OPENMP
+#define ORACLE_EACH_RANK _Pragma("omp parallel for schedule(static)")
+#else
+#define ORACLE_EACH_RANK
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_EINVAL (-1)
@@ -173,6 +184,7 @@ int oracle_ring_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bu
         const int reduce = step <= world - 1;            /* phase 1: reduce-scatter */
         const int32_t s = reduce ? step : step - (world - 1);
         /* send half: rank r puts chunk (r-s) (reduce-scatter) or (r-s+1) (all-gather) */
+        ORACLE_EACH_RANK
         for (int32_t r = 0; r < world; ++r) {
             int32_t j = reduce ? mod((int64_t)r - s, world) : mod((int64_t)r - s + 1, world);
             int64_t lo, hi;
@@ -183,6 +195,7 @@ int oracle_ring_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bu
             if (sent) sent[r] += hi - lo;
         }
         /* receive half: rank r takes the message of rank r-1 */
+        ORACLE_EACH_RANK
         for (int32_t r = 0; r < world; ++r) {
             int32_t left = mod((int64_t)r - 1, world);
             char* dst = (char*)bufs[r] + (size_t)msg_lo[left] * es;
@@ -192,8 +205,10 @@ int oracle_ring_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bu
         }
     }
 
-    if (n_steps < 0 && divisor > 1)
+    if (n_steps < 0 && divisor > 1) {
+        ORACLE_EACH_RANK
         for (int32_t r = 0; r < world; ++r) divide_all(dtype, bufs[r], numel, divisor);
+    }
 
     for (int32_t r = 0; r < world; ++r) free(msg[r]);
     free(msg); free(msg_lo); free(msg_len);

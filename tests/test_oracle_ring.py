@@ -19,9 +19,11 @@ import os
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import oracle
+import workloads
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ring_3x6_example.txt")
 
@@ -330,3 +332,20 @@ def test_equal_inputs_give_n_times_value():
 def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.ring_allreduce([np.zeros(3, np.float32)], oracle.F32, divisor=-1)
+
+
+def test_openmp_build_gives_identical_bits():
+    # the multi-core timing build runs the ranks of each half-step on threads;
+    # every element sees the same operations in the same order
+    import subprocess
+    try:
+        oracle.build(openmp=True)
+    except (subprocess.CalledProcessError, OSError):
+        pytest.skip("no OpenMP in this compiler")
+    for N, S, dtype in ((3, 6, oracle.F32), (8, 100_003, oracle.F32), (5, 77_777, oracle.BF16), (16, 4099, oracle.F32)):
+        x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype="bf16" if dtype == oracle.BF16 else "f32")
+        xh = x.view(torch.int16).numpy().view(np.uint16).copy() if dtype == oracle.BF16 else x.numpy().copy()
+        a = oracle.ring_allreduce_2d(xh.copy(), dtype, N)
+        b = oracle.ring_allreduce_2d_openmp(xh.copy(), dtype, N)
+        assert np.array_equal(a.view(np.uint16 if dtype == oracle.BF16 else np.uint32),
+                              b.view(np.uint16 if dtype == oracle.BF16 else np.uint32)), (N, S)
