@@ -7,11 +7,13 @@
 
 #include <algorithm>
 #include <atomic>
+#include <iterator>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -57,7 +59,7 @@ int cap_ctas(int64_t grid) {
 namespace {
 std::mutex g_mu;
 std::map<int, int> g_sms;                                    // device -> SM count
-std::map<std::pair<int, const void*>, int> g_occ;            // (device, kernel) -> blocks per SM
+std::map<std::tuple<int, const void*, int>, int> g_occ;      // (device, kernel, threads) -> blocks per SM
 }  // namespace
 
 int sm_count() {
@@ -78,7 +80,7 @@ int grid_for(const void* kernel, int64_t work_items, int threads) {
     const int sms = sm_count();
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_pair(dev, kernel);
+    const auto key = std::make_tuple(dev, kernel, threads);
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -141,6 +143,45 @@ int32_t cuda_status(cudaError_t e) {
     return DDP_ERR_CUDA;
 }
 
+using Span = std::pair<uintptr_t, uintptr_t>;      // [first, second) in bytes
+
+// True if two of the spans share a byte (sorts `v`).
+bool any_overlap(std::vector<Span>* v) {
+    std::sort(v->begin(), v->end());
+    for (size_t i = 1; i < v->size(); ++i)
+        if ((*v)[i].first < (*v)[i - 1].second) return true;
+    return false;
+}
+
+// True if [a, b) shares a byte with one of the sorted, pairwise disjoint spans.
+bool hits_any(const std::vector<Span>& sorted, uintptr_t a, uintptr_t b) {
+    auto it = std::lower_bound(sorted.begin(), sorted.end(), Span{b, 0});   // first span starting at or after b
+    return it != sorted.begin() && std::prev(it)->second > a;
+}
+
+// The memory a pack or unpack touches: the ranks' buckets must be disjoint,
+// no gradient may share a byte with any bucket, and gradients that are
+// written (unpack) must be disjoint too.
+int32_t check_pack_memory(int32_t world, int32_t n, const void* const* grads, const int64_t* numel,
+                          int64_t grad_es, const void* const* buckets, int64_t bucket_bytes, bool grads_written) {
+    std::vector<Span> bk, gs;
+    for (int32_t r = 0; r < world && bucket_bytes > 0; ++r) {
+        const uintptr_t b = reinterpret_cast<uintptr_t>(buckets[r]);
+        bk.emplace_back(b, b + (uintptr_t)bucket_bytes);
+    }
+    if (any_overlap(&bk)) return DDP_ERR_INVALID;
+    for (int32_t r = 0; r < world; ++r)
+        for (int32_t i = 0; i < n; ++i) {
+            if (numel[i] == 0) continue;
+            const uintptr_t g = reinterpret_cast<uintptr_t>(grads[(int64_t)r * n + i]);
+            const uintptr_t e = g + (uintptr_t)(numel[i] * grad_es);
+            if (hits_any(bk, g, e)) return DDP_ERR_INVALID;
+            gs.emplace_back(g, e);
+        }
+    if (grads_written && any_overlap(&gs)) return DDP_ERR_INVALID;
+    return DDP_OK;
+}
+
 // Check one bucket's member table and build the copy items of pack/unpack.
 int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel,
                      const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
@@ -173,12 +214,11 @@ int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const i
             if (reinterpret_cast<uintptr_t>(g) % es) return DDP_ERR_ALIGN;
             char* slot = b + offset[i] * es;
             const int64_t bytes = numel[i] * es;
-            if (g < slot + bytes && slot < g + bytes) return DDP_ERR_INVALID;   // gradient overlaps its slot
             if (to_bucket) items->push_back(CopyItem{g, slot, bytes});
             else items->push_back(CopyItem{slot, g, bytes});
         }
     }
-    return DDP_OK;
+    return check_pack_memory(world, n, grads, numel, es, buckets, bucket_numel * es, !to_bucket);
 }
 
 // Members of one bucket for the bf16 hook: float32 gradients, bf16 bucket.
@@ -206,12 +246,11 @@ int32_t hook_items(int32_t world, int32_t n, const void* const* grads, const int
             if (!g) return DDP_ERR_INVALID;
             if (reinterpret_cast<uintptr_t>(g) % 4) return DDP_ERR_ALIGN;
             char* slot = b + offset[i] * 2;
-            if (g < slot + numel[i] * 2 && slot < g + numel[i] * 4) return DDP_ERR_INVALID;
             if (to_bucket) items->push_back(ConvItem{g, slot, numel[i]});
             else items->push_back(ConvItem{slot, g, numel[i]});
         }
     }
-    return DDP_OK;
+    return check_pack_memory(world, n, grads, numel, 4, buckets, bucket_numel * 2, !to_bucket);
 }
 
 int32_t view_members(int32_t world, int32_t n, void* const* grads, const int64_t* numel, const int64_t* offset,

@@ -140,6 +140,15 @@ def test_pack_unpack_view_reject_bad_plans():
     assert L.ddp_bucket_pack(1, 1, _vp(G0 + 2), i64(4), i64(0), _vp(A), 16, 0, None) == -2
     # gradient aliasing its own slot
     assert L.ddp_bucket_pack(1, 1, _vp(A + 8), i64(4), i64(0), _vp(A), 16, 0, None) == -1
+    # rank 0's gradient inside rank 1's bucket (not its own slot)
+    assert L.ddp_bucket_pack(2, 1, _vp(B + 32, G1), i64(4), i64(0), _vp(A, B), 16, 0, None) == -1
+    # the two ranks' buckets overlap
+    assert L.ddp_bucket_pack(2, 1, _vp(G0, G1), i64(4), i64(0), _vp(A, A + 32), 16, 0, None) == -1
+    # unpack writes two gradients that share memory
+    assert L.ddp_bucket_unpack(2, 1, _vp(G0, G0 + 8), i64(4), i64(0), _vp(A, B), 16, 0, None) == -1
+    # the bf16 hook: float32 gradient of rank 1 inside rank 0's bf16 bucket; overlapping bf16 buckets
+    assert L.ddp_bucket_pack_bf16(2, 1, _vp(G0, A + 4), i64(4), i64(0), _vp(A, B), 16, None) == -1
+    assert L.ddp_bucket_unpack_bf16(2, 1, _vp(G0, G1), i64(4), i64(0), _vp(A, A + 16), 16, None) == -1
     # view: same memory used for two ranks
     assert L.ddp_bucket_allreduce_view(2, 1, _vp(G0, G0), i64(4), i64(0), 4, 0, 2, None) == -1
     assert L.ddp_bucket_allreduce_view(2, 1, _vp(G0, G1), i64(4), i64(1), 4, 0, 2, None) == -1   # past the end
