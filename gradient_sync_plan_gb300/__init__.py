@@ -38,7 +38,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
-           "ddp_set_fused_kernel", "ddp_plan_buckets",
+           "ddp_set_fused_kernel", "ddp_plan_buckets", "ddp_plan_fingerprint",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ddp_bucket_pack_bf16", "ddp_bucket_unpack_bf16",
            "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "tree_allreduce_fused",
            "tree_allreduce_staged", "ring_allreduce_fused_from_host",
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_set_max_ctas.argtypes = [i32, P(i32)]
             L.ddp_set_fused_kernel.argtypes = [i32, P(i32)]
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
+            L.ddp_plan_fingerprint.argtypes = [i32, P(i64), i32, P(i32), P(i64), i32, P(i64), P(ctypes.c_uint64)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_unpack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
             L.ddp_bucket_pack_bf16.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, vp]
@@ -350,6 +351,16 @@ def _member_tables(grads: Sequence[Sequence], offsets: Sequence[int]):
             elif g.numel() != numels[i]:
                 raise ValueError("member numel differs across ranks")
     return world, n, ptrs, numels, (F32 if code is None else code)
+
+
+def ddp_plan_fingerprint(numels: Sequence[int], plan, dtype: int = F32) -> int:
+    """64-bit digest of a bucket plan, to compare across ranks before syncing."""
+    b_of, off, bn = plan
+    out = ctypes.c_uint64(0)
+    _check("ddp_plan_fingerprint",
+           lib().ddp_plan_fingerprint(len(numels), _i64_array(numels), dtype, _i32_array(b_of), _i64_array(off),
+                                      len(bn), _i64_array(bn), ctypes.byref(out)))
+    return int(out.value)
 
 
 def ddp_bucket_pack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:

@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "ddp.h"
+#include "ddp_trace.h"
 #include "ddp_internal.h"
 
 namespace ddpk {
@@ -294,6 +295,7 @@ int32_t view_members(int32_t world, int32_t n, void* const* grads, const int64_t
 extern "C" {
 
 const char* ddp_status_string(int32_t status) {
+    DDP_TRACE_CALL();
     switch (status) {
         case DDP_OK: return "DDP_OK";
         case DDP_ERR_INVALID: return "DDP_ERR_INVALID: invalid argument";
@@ -310,6 +312,7 @@ int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
 const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
 
 int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) {
+    DDP_TRACE_CALL();
     if (max_ctas < 0) return DDP_ERR_INVALID;
     const int prev = g_max_ctas.exchange(max_ctas);
     if (previous) *previous = prev;
@@ -317,6 +320,7 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) {
 }
 
 int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) {
+    DDP_TRACE_CALL();
     if (kind < DDP_FUSED_AUTO || kind > DDP_FUSED_TMA) return DDP_ERR_INVALID;
     const int prev = g_fused_kernel.exchange(kind);
     if (previous) *previous = prev;
@@ -324,12 +328,14 @@ int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) {
 }
 
 int32_t ddp_device_status(int32_t* status, int32_t clear) {
+    DDP_TRACE_CALL();
     if (!status) return DDP_ERR_INVALID;
     return cuda_status(read_device_status(status, clear != 0));
 }
 
 int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                              void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (divisor < 0) return DDP_ERR_INVALID;
@@ -341,6 +347,7 @@ int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, in
 
 int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                               void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (divisor < 0) return DDP_ERR_INVALID;
@@ -365,16 +372,19 @@ static int32_t tree_common(bool staged, int32_t world, void* const* bufs, int64_
 
 int32_t tree_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                              void* stream) {
+    DDP_TRACE_CALL();
     return tree_common(false, world, bufs, numel, dtype, divisor, stream);
 }
 
 int32_t tree_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                               void* stream) {
+    DDP_TRACE_CALL();
     return tree_common(true, world, bufs, numel, dtype, divisor, stream);
 }
 
 int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
                                   int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (divisor < 0 || !dev_status || wait_limit_ms < 0) return DDP_ERR_INVALID;
@@ -398,6 +408,7 @@ int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t nume
 int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,
                                        void* const* dev_bufs, int64_t numel, int32_t dtype, int32_t divisor,
                                        void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
@@ -440,6 +451,7 @@ static void* device_view_of(const void* p) {
 
 int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_in, void* const* host_out,
                                          int64_t numel, int32_t dtype, int32_t divisor, void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
@@ -483,6 +495,7 @@ int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_
 
 int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* grads, int64_t numel,
                             int32_t dtype, void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
     if (numel == 0) return DDP_OK;
@@ -495,6 +508,7 @@ int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* 
 int32_t ddp_bucket_pack(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
                         const int64_t* offset, void* const* buckets, int64_t bucket_numel, int32_t dtype,
                         void* stream) {
+    DDP_TRACE_CALL();
     std::vector<CopyItem> items;
     int32_t st = bucket_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel,
                               dtype, true, &items);
@@ -505,6 +519,7 @@ int32_t ddp_bucket_pack(int32_t world, int32_t n_in_bucket, const void* const* g
 int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                           const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
                           void* stream) {
+    DDP_TRACE_CALL();
     std::vector<CopyItem> items;
     int32_t st = bucket_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel,
                               dtype, false, &items);
@@ -514,6 +529,7 @@ int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads
 
 int32_t ddp_bucket_pack_bf16(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
                              const int64_t* offset, void* const* buckets, int64_t bucket_numel, void* stream) {
+    DDP_TRACE_CALL();
     std::vector<ConvItem> items;
     int32_t st = hook_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel, true,
                             &items);
@@ -523,6 +539,7 @@ int32_t ddp_bucket_pack_bf16(int32_t world, int32_t n_in_bucket, const void* con
 
 int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                                const int64_t* offset, const void* const* buckets, int64_t bucket_numel, void* stream) {
+    DDP_TRACE_CALL();
     std::vector<ConvItem> items;
     int32_t st = hook_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel, false,
                             &items);
@@ -554,11 +571,13 @@ static int32_t view_one(int32_t world, int32_t n_in_bucket, void* const* grads, 
 int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                                   const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
                                   void* stream) {
+    DDP_TRACE_CALL();
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, dtype, dtype, divisor, stream);
 }
 
 int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                                        const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) {
+    DDP_TRACE_CALL();
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook, divisor, stream);
 }
 
@@ -566,6 +585,7 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
                          const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
                          const int64_t* bucket_numel, void* const* buckets, int32_t dtype, int32_t divisor,
                          int32_t algo, void* stream) {
+    DDP_TRACE_CALL();
     int32_t st = common_checks(world, 0, dtype);
     if (st) return st;
     if (n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;

@@ -14,11 +14,13 @@
 #include <cstdlib>
 
 #include "ddp.h"
+#include "ddp_trace.h"
 
 extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int32_t dtype,
                                     int64_t first_bucket_bytes, int64_t bucket_cap_bytes,
                                     int32_t* bucket_of_param, int64_t* offset_of_param, int64_t* bucket_numel,
                                     int32_t* n_buckets) {
+    DDP_TRACE_CALL();
     if (!n_buckets || n_params < 0) return DDP_ERR_INVALID;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
     if (first_bucket_bytes <= 0 || bucket_cap_bytes <= 0) return DDP_ERR_INVALID;
@@ -53,5 +55,42 @@ extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int3
             std::fprintf(stderr, "[ddp]   bucket %d: %lld elements (%lld B)\n", k, (long long)bucket_numel[k],
                          (long long)(bucket_numel[k] * esize));
     }
+    return DDP_OK;
+}
+
+// 64-bit FNV-1a over the plan's integers, each fed as 8 little-endian bytes
+// (the byte order is fixed here, so hosts of either endianness agree).
+namespace {
+struct Fnv64 {
+    uint64_t h = 0xcbf29ce484222325ull;
+    void add(int64_t v) {
+        uint64_t u = (uint64_t)v;
+        for (int b = 0; b < 8; ++b) {
+            h ^= (u >> (8 * b)) & 0xffu;
+            h *= 0x100000001b3ull;
+        }
+    }
+};
+}  // namespace
+
+extern "C" int32_t ddp_plan_fingerprint(int32_t n_params, const int64_t* numel, int32_t dtype,
+                                        const int32_t* bucket_of_param, const int64_t* offset_of_param,
+                                        int32_t n_buckets, const int64_t* bucket_numel, uint64_t* fingerprint) {
+    DDP_TRACE_CALL();
+    if (!fingerprint || n_params < 0 || n_buckets < 0) return DDP_ERR_INVALID;
+    if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
+    if (n_params > 0 && (!numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
+    if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
+    Fnv64 f;
+    f.add(n_params);
+    f.add(dtype);
+    for (int32_t p = 0; p < n_params; ++p) {
+        f.add(numel[p]);
+        f.add(bucket_of_param[p]);
+        f.add(offset_of_param[p]);
+    }
+    f.add(n_buckets);
+    for (int32_t k = 0; k < n_buckets; ++k) f.add(bucket_numel[k]);
+    *fingerprint = f.h;
     return DDP_OK;
 }

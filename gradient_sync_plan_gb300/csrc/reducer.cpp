@@ -21,6 +21,7 @@
 #include <vector>
 
 #include "ddp.h"
+#include "ddp_trace.h"
 
 struct ddp_reducer {
     int32_t world = 0, n_params = 0, n_buckets = 0, dtype = 0, divisor = 0, algo = 0;
@@ -113,6 +114,7 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
                            const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
                            const int64_t* bucket_numel, void* const* buckets, int32_t algo, int32_t divisor,
                            void* comm_stream, ddp_reducer** out) {
+    DDP_TRACE_CALL();
     if (!out) return DDP_ERR_INVALID;
     *out = nullptr;
     if (world < 1 || world > DDP_MAX_WORLD || n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
@@ -195,6 +197,7 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
 }
 
 int32_t ddp_reducer_prepare(ddp_reducer* r) {
+    DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     reset_step(r);
@@ -202,6 +205,7 @@ int32_t ddp_reducer_prepare(ddp_reducer* r) {
 }
 
 int32_t ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* compute_stream) {
+    DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     if (param < 0 || param >= r->n_params || r->param_ready[param]) return DDP_ERR_INVALID;
@@ -217,6 +221,7 @@ int32_t ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* compute_stre
 }
 
 int32_t ddp_reducer_finalize(ddp_reducer* r, void* stream) {
+    DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     if (r->first_error != DDP_OK) return r->first_error;
@@ -237,6 +242,7 @@ int32_t ddp_reducer_finalize(ddp_reducer* r, void* stream) {
 }
 
 int32_t ddp_reducer_launch_order(ddp_reducer* r, int32_t* order, int32_t capacity, int32_t* n) {
+    DDP_TRACE_CALL();
     if (!r || !n || capacity < 0 || (capacity > 0 && !order)) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     *n = (int32_t)r->launch_log.size();
@@ -245,6 +251,7 @@ int32_t ddp_reducer_launch_order(ddp_reducer* r, int32_t* order, int32_t capacit
 }
 
 int32_t ddp_reducer_destroy(ddp_reducer* r) {
+    DDP_TRACE_CALL();
     if (!r) return DDP_OK;
     destroy_events(r);
     delete r;

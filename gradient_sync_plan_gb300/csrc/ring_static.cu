@@ -26,6 +26,7 @@
 
 #include "ddp.h"
 #include "ddp_internal.h"
+#include "ddp_trace.h"
 
 // The scratch itself.  In host code this name is only a host-side stand-in
 // for the symbol, never a device address: it is turned into one with
@@ -62,6 +63,7 @@ cudaError_t scratch_on_current_device(unsigned char** out) {
 extern "C" int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const void* const* host_in,
                                                           void* const* host_out, int64_t numel, int32_t dtype,
                                                           int32_t divisor, void* stream) {
+    DDP_TRACE_CALL();
     if (world < 1 || numel < 0 || divisor < 0) return DDP_ERR_INVALID;
     if (world > DDP_MAX_WORLD) return DDP_ERR_CAPACITY;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;

@@ -160,6 +160,20 @@ int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int32_t dtype,
                          int64_t* bucket_numel, int32_t* n_buckets);
 
 /*
+ * ddp_plan_fingerprint -- a 64-bit digest of a bucket plan (FNV-1a over the
+ * parameter count, dtype, every parameter's numel, bucket and offset, the
+ * bucket count and every bucket's numel, each as 8 little-endian bytes).
+ * Ranks whose plans differ would run different collective sequences, which
+ * on a real ring hangs without an error ([P2] "常见疑问", why DDP can hang);
+ * ranks exchange this value over their host process group before the first
+ * sync and stop on a mismatch.  Host only; no CUDA call.  DDP_ERR_INVALID on
+ * a bad argument.
+ */
+int32_t ddp_plan_fingerprint(int32_t n_params, const int64_t* numel, int32_t dtype,
+                             const int32_t* bucket_of_param, const int64_t* offset_of_param,
+                             int32_t n_buckets, const int64_t* bucket_numel, uint64_t* fingerprint);
+
+/*
  * ddp_bucket_pack -- copy gradients into each rank's flat bucket, the
  * "gradient -> bucket" copy DDP makes when gradient_as_bucket_view is off
  * ([P1] section 03 and section 05 step 2).

@@ -280,3 +280,32 @@ int main(void) {
                            "-L", libdir, "-lddp_gb300", "-Wl,-rpath," + libdir, "-o", str(exe)])
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
+
+
+def _fnv1a64(values):
+    h = 0xcbf29ce484222325
+    for v in values:
+        u = v & 0xFFFFFFFFFFFFFFFF
+        for b in range(8):
+            h ^= (u >> (8 * b)) & 0xFF
+            h = (h * 0x100000001b3) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def test_plan_fingerprint_is_fnv1a_of_the_plan_and_changes_with_it():
+    numels = [300, 100, 200, 50, 400]
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, 1600, 2000)
+    b_of, off, bn = [list(map(int, a)) for a in plan]
+    seq = [5, ddp.F32]
+    for p in range(5):
+        seq += [numels[p], b_of[p], off[p]]
+    seq += [len(bn)] + bn
+    fp = ddp.ddp_plan_fingerprint(numels, plan, ddp.F32)
+    assert fp == _fnv1a64(seq)
+    assert ddp.ddp_plan_fingerprint(numels, plan, ddp.BF16) != fp
+    other = ddp.ddp_plan_buckets(numels + [1], ddp.F32, 1600, 2000)
+    assert ddp.ddp_plan_fingerprint(numels + [1], other, ddp.F32) != fp
+    moved = (plan[0], [o + (1 if i == 0 else 0) for i, o in enumerate(off)], plan[2])
+    assert ddp.ddp_plan_fingerprint(numels, moved, ddp.F32) != fp
+    L = ddp.lib()
+    assert L.ddp_plan_fingerprint(0, None, ddp.F32, None, None, 0, None, None) == -1   # no output pointer

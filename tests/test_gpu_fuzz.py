@@ -4,7 +4,9 @@ Each case draws a world size, a bucket length, a dtype, a divisor, a start
 offset inside 16-byte-aligned storage (so some calls take the element-wise
 kernels), and a forced fused-kernel choice; it then runs one of the
 allreduces or a view sync of a random member split, through the C ABI,
-and compares every element with the oracle on the same input.
+and compares every element with the oracle on the same input.  The rows
+sit inside storage filled with a canary pattern, which must be intact
+afterwards: no kernel may write outside the buffers it was given.
 """
 import numpy as np
 import pytest
@@ -20,18 +22,34 @@ pytestmark = pytest.mark.gpu
 KINDS = [ddp.DDP_FUSED_AUTO, ddp.DDP_FUSED_VECTOR, ddp.DDP_FUSED_GROUP, ddp.DDP_FUSED_TMA]
 
 
+CANARY16 = 0x7FA5          # a bf16 NaN pattern that no kernel here produces
+CANARY32 = 0x7FA5A5A5
+
+
 def _rows_on_device(xh, shift):
-    """Rank rows as views starting `shift` elements into aligned storage."""
+    """Rank rows as views starting `shift` elements into aligned storage; the
+    rest of the storage holds a canary pattern."""
     N, S = xh.shape
-    tdt = torch.bfloat16 if xh.dtype == np.uint16 else torch.float32
-    store = torch.zeros((N, S + 16), dtype=tdt, device="cuda")
-    src = torch.from_numpy(xh.view(np.int16) if xh.dtype == np.uint16 else xh)
-    if xh.dtype == np.uint16:
+    bf = xh.dtype == np.uint16
+    itype = torch.int16 if bf else torch.int32
+    store = torch.full((N, S + 16), CANARY16 if bf else CANARY32, dtype=itype, device="cuda")
+    store = store.view(torch.bfloat16 if bf else torch.float32)
+    src = torch.from_numpy(xh.view(np.int16) if bf else xh)
+    if bf:
         src = src.view(torch.bfloat16)
     rows = [store[r, shift:shift + S] for r in range(N)]
     for r in range(N):
         rows[r].copy_(src[r])
     return store, rows
+
+
+def _canaries_intact(store, shift, S):
+    bits = f32_or_bits(store)
+    bits = bits.view(np.uint16) if bits.dtype == np.uint16 else bits.view(np.uint32)
+    canary = CANARY16 if bits.dtype == np.uint16 else CANARY32
+    outside = np.ones(bits.shape[1], dtype=bool)
+    outside[shift:shift + S] = False
+    return bool(np.all(bits[:, outside] == canary))
 
 
 def _oracle(op, xh, divisor):
@@ -80,7 +98,8 @@ def test_random_calls_match_oracle(block):
             ddp.ddp_set_fused_kernel(prev)
         torch.cuda.synchronize()
         got = np.stack([f32_or_bits(rows[r]) for r in range(N)]) if N else np.zeros((0, S))
-        assert_bits_equal(got, want, f"case {block}/{case}: {op} N={N} S={S} {dtype} div={divisor} "
-                                     f"shift={shift} kind={kind}")
+        what = f"case {block}/{case}: {op} N={N} S={S} {dtype} div={divisor} shift={shift} kind={kind}"
+        assert_bits_equal(got, want, what)
+        assert _canaries_intact(store, shift, S), "write outside the rank rows: " + what
         del store, rows
     assert ddp.ddp_device_status() == 0
