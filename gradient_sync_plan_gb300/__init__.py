@@ -279,7 +279,9 @@ def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step:
 
 
 def ring_allreduce_fused_from_host(host_in, host_out, dev_bufs, divisor: int = 0, stream=None) -> None:
-    """Host buffers in and out, device scratch in between (copies + kernel on one stream)."""
+    """Host buffers in and out, device scratch in between.  Large buckets are
+    piped through in pieces (copies in, reduction and copies out overlap on
+    internal streams); the caller's stream waits for the result."""
     hi, numel, code = _rank_ptrs(host_in)
     ho, n2, c2 = _rank_ptrs(host_out)
     dv, n3, c3 = _rank_ptrs(dev_bufs)

@@ -183,6 +183,72 @@ int32_t check_pack_memory(int32_t world, int32_t n, const void* const* grads, co
     return DDP_OK;
 }
 
+// Large host buckets: pieces of kHostPieceBytes per rank flow through three
+// streams -- host-to-device copies, the reduction, device-to-host copies --
+// so that piece p+1 comes in while piece p is reduced and piece p-1 goes
+// out, and the CPU-GPU link carries both directions at once.  A piece is
+// reduced by the view kernel as one member per rank at its bucket offset,
+// so every element is still folded in the ring order of its chunk of the
+// whole bucket.  The caller's stream waits for the last copy out.
+constexpr int64_t kHostPieceBytes = (int64_t)32 << 20;
+
+cudaError_t from_host_pipelined(int32_t world, const void* const* host_in, void* const* host_out,
+                                void* const* dev_bufs, int64_t numel, int32_t dtype, int32_t divisor, bool vec,
+                                int64_t piece, cudaStream_t caller) {
+    struct Streams {
+        cudaStream_t in = nullptr, red = nullptr, out = nullptr;
+        std::vector<cudaEvent_t> ev;
+        ~Streams() {                     // released once their queued work is done
+            for (cudaEvent_t e : ev) cudaEventDestroy(e);
+            if (in) cudaStreamDestroy(in);
+            if (red) cudaStreamDestroy(red);
+            if (out) cudaStreamDestroy(out);
+        }
+        cudaError_t event(cudaEvent_t* e) {
+            cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+            if (r == cudaSuccess) ev.push_back(*e);
+            return r;
+        }
+    } S;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&S.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&S.red, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&S.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    cudaEvent_t start, done;
+    if ((e = S.event(&start)) != cudaSuccess || (e = S.event(&done)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(start, caller)) != cudaSuccess) return e;
+    for (cudaStream_t t : {S.in, S.red, S.out})
+        if ((e = cudaStreamWaitEvent(t, start, 0)) != cudaSuccess) return e;
+    const int64_t es = elem_bytes(dtype);
+    const DivSpec div = make_div(divisor);
+    std::vector<void*> ptrs(world);
+    for (int64_t a = 0; a < numel; a += piece) {
+        const int64_t len = std::min(piece, numel - a);
+        const size_t nb = (size_t)(len * es);
+        cudaEvent_t in_done, red_done;
+        if ((e = S.event(&in_done)) != cudaSuccess || (e = S.event(&red_done)) != cudaSuccess) return e;
+        for (int32_t r = 0; r < world; ++r) {
+            char* d = static_cast<char*>(dev_bufs[r]) + a * es;
+            const char* h = static_cast<const char*>(host_in[r]) + a * es;
+            if ((e = cudaMemcpyAsync(d, h, nb, cudaMemcpyHostToDevice, S.in)) != cudaSuccess) return e;
+        }
+        if ((e = cudaEventRecord(in_done, S.in)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(S.red, in_done, 0)) != cudaSuccess) return e;
+        for (int32_t r = 0; r < world; ++r) ptrs[r] = static_cast<char*>(dev_bufs[r]) + a * es;
+        ViewMember m{len, a, ptrs.data(), vec && (a * es) % 16 == 0};
+        if ((e = launch_bucket_view(world, &m, 1, numel, dtype, div, S.red)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(red_done, S.red)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(S.out, red_done, 0)) != cudaSuccess) return e;
+        for (int32_t r = 0; r < world; ++r) {
+            char* h = static_cast<char*>(host_out[r]) + a * es;
+            const char* d = static_cast<const char*>(dev_bufs[r]) + a * es;
+            if ((e = cudaMemcpyAsync(h, d, nb, cudaMemcpyDeviceToHost, S.out)) != cudaSuccess) return e;
+        }
+    }
+    if ((e = cudaEventRecord(done, S.out)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(caller, done, 0);
+}
+
 // Check one bucket's member table and build the copy items of pack/unpack.
 int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel,
                      const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
@@ -418,17 +484,26 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
     for (int32_t r = 0; r < world; ++r)
         if (!host_in[r] || !host_out[r]) return DDP_ERR_INVALID;
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t bytes = (size_t)numel * elem_bytes(dtype);
-    for (int32_t r = 0; r < world; ++r) {
-        cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_in[r], bytes, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_status(e);
+    const int64_t es = elem_bytes(dtype);
+    const size_t bytes = (size_t)numel * es;
+    const int64_t piece = kHostPieceBytes / es;                 // elements per rank and piece
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capturing) != cudaSuccess) return cuda_status(cudaGetLastError());
+    if (numel <= 2 * piece || capturing != cudaStreamCaptureStatusNone) {
+        // small, or being captured into a graph: in, reduce, out on the caller's stream
+        for (int32_t r = 0; r < world; ++r) {
+            cudaError_t e = cudaMemcpyAsync(dev_bufs[r], host_in[r], bytes, cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        if ((st = cuda_status(launch_ring_fused(world, dev_bufs, numel, dtype, make_div(divisor), vec, s))))
+            return st;
+        for (int32_t r = 0; r < world; ++r) {
+            cudaError_t e = cudaMemcpyAsync(host_out[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        return DDP_OK;
     }
-    if ((st = cuda_status(launch_ring_fused(world, dev_bufs, numel, dtype, make_div(divisor), vec, s)))) return st;
-    for (int32_t r = 0; r < world; ++r) {
-        cudaError_t e = cudaMemcpyAsync(host_out[r], dev_bufs[r], bytes, cudaMemcpyDeviceToHost, s);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    return DDP_OK;
+    return cuda_status(from_host_pipelined(world, host_in, host_out, dev_bufs, numel, dtype, divisor, vec, piece, s));
 }
 
 // Device address through which the GPU reaches host buffer p, or nullptr

@@ -317,9 +317,14 @@ int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t nume
  * ring_allreduce_fused_from_host -- ring_allreduce_fused for callers whose
  * gradients are in host memory: per rank, host_in[r] is copied to dev_bufs[r],
  * the fused allreduce runs, and the result is copied to host_out[r]
- * (host_out[r] may equal host_in[r]).  All copies and the kernel are
- * enqueued on `stream`; the caller synchronises the stream before reading
- * host_out.  Host buffers should be pinned for the copies to be asynchronous.
+ * (host_out[r] may equal host_in[r]).  Buckets of more than 64 MiB per
+ * rank go through in 32 MiB pieces on three internal streams, so that copies
+ * in, the reduction of each piece (folded in the ring order of the whole
+ * bucket's chunks) and copies out overlap; `stream` waits for the last copy
+ * out.  Smaller buckets, and calls on a stream that is being captured into a
+ * graph, run in, reduce, out on `stream` itself.  The caller synchronises
+ * `stream` before reading host_out.  Host buffers should be pinned for the
+ * copies to be asynchronous.
  * dev_bufs[world] is caller-provided device scratch of numel elements per rank.
  */
 int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,

@@ -271,6 +271,26 @@ def test_from_host_matches_oracle():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("alias", [False, True])
+def test_from_host_pipelined_in_pieces_matches_oracle(dtype, alias):
+    # more than two 32 MiB pieces per rank, ragged last piece and chunk
+    # boundaries inside pieces: the pieces are reduced on internal streams
+    # while others are copied in and out; host_out may be host_in
+    es = 2 if dtype == "bf16" else 4
+    N, S = 3, (5 * (32 << 20)) // es + 12_345
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=61)
+    xh = f32_or_bits(x)
+    want = oracle_allreduce(xh, N)
+    host_in = x.pin_memory()
+    host_out = host_in if alias else torch.empty_like(host_in).pin_memory()
+    dev = torch.empty((N, S), dtype=x.dtype, device="cuda")
+    stream = torch.cuda.Stream()
+    ddp.ring_allreduce_fused_from_host(host_in, host_out, dev, N, stream=stream)
+    stream.synchronize()
+    assert_bits_equal(f32_or_bits(host_out), want, f"from_host pieces {dtype} alias={alias}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("N,S", [(3, 6), (8, 1_000_001), (4, 1 << 20), (16, 77_777)])
 def test_host_direct_matches_oracle(dtype, N, S):
     # the kernel reads pinned host memory and writes the result back to it
