@@ -42,6 +42,16 @@ MUTANTS = {
     "tree_divide_dropped": ("if (n_steps < 0 && reduce && step == depth - 1 && divisor > 1)", "if (0)"),
     "plan_drops_trailing_bucket": ("    if (members > 0) {\n        bucket_numel[k] = elems;",
                                    "    if (0) {\n        bucket_numel[k] = elems;"),
+    "pack_offset_in_elements_not_bytes": (
+        "memcpy((char*)bucket + offset[i] * elem_bytes, grads[i], (size_t)(numel[i] * elem_bytes));",
+        "memcpy((char*)bucket + offset[i], grads[i], (size_t)(numel[i] * elem_bytes));"),
+    "unpack_short_by_one_element": (
+        "memcpy(grads[i], (const char*)bucket + offset[i] * elem_bytes, (size_t)(numel[i] * elem_bytes));",
+        "memcpy(grads[i], (const char*)bucket + offset[i] * elem_bytes, (size_t)((numel[i] - 1) * elem_bytes));"),
+    "accumulate_skipped": ("    if (n > 0) add_into(dtype, acc, g, n);", "    (void)acc; (void)g;"),
+    "bf16_divide_rounds_toward_zero": (
+        "for (int64_t i = 0; i < n; ++i) p[i] = oracle_bf16_rne(oracle_bf16_to_f32(p[i]) / dv);",
+        "for (int64_t i = 0; i < n; ++i) p[i] = (uint16_t)(f32_bits(oracle_bf16_to_f32(p[i]) / dv) >> 16);"),
 }
 
 
