@@ -224,7 +224,7 @@ def run_reference(args, rank: int, world: int):
     oracle.ring_allreduce(rows, oracle.F32, N_RANKS)
     per_elem = max((time.perf_counter() - t) / cal, 1e-10)
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
-    numel = int(min(NUMEL, max(1 << 12, budget / per_elem)))
+    numel = int(min(args.numel, max(1 << 12, budget / per_elem)))
     numel = 1 << int(math.log2(numel))
     x = workloads.rank_vectors(N_RANKS, numel, "randn", std=1e-2).numpy()
     rows = [x[r] for r in range(N_RANKS)]
@@ -236,14 +236,17 @@ def run_reference(args, rank: int, world: int):
     dt = time.perf_counter() - t0
     s_bytes = numel * 4
     value = 2 * (N_RANKS - 1) / N_RANKS * s_bytes * args.steps / dt / 1e9
-    part = "the whole" if numel == NUMEL else "a bounded sample of the"
-    sample = (f"N={N_RANKS} ranks x {numel} fp32 per rank ({s_bytes // MiB} MiB) per step, {part} "
-              f"1 GiB-per-rank bucket; single-threaded C oracle")
+    part = "the whole" if numel == args.numel else "a bounded sample of the"
+    sample = (f"N={N_RANKS} ranks x {numel} fp32 per rank ({s_bytes / MiB:.2f} MiB) per step, {part} "
+              f"{args.numel * 4 / MiB:.0f} MiB-per-rank bucket; single-threaded C oracle")
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-           "config": {"workload": "N=8 logical ranks, one 1 GiB fp32 bucket per rank, ring allreduce / 8",
-                      "ranks": N_RANKS, "numel": NUMEL, "sample_numel": numel, "parallelism": "host cores"},
+           "config": {"workload": f"N={N_RANKS} logical ranks, one fp32 bucket of {args.numel} elements "
+                                  f"({args.numel * 4 / MiB:.0f} MiB) per rank, fused ring allreduce / {N_RANKS}",
+                      "ranks": N_RANKS, "numel": args.numel, "bucket_bytes": args.numel * 4,
+                      "algorithm": "CPU oracle ring simulation", "sample_numel": numel,
+                      "parallelism": "host cores"},
            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
