@@ -407,7 +407,21 @@ def _oracle_view(grads_h, offsets, bucket_numel, code, divisor):
         oracle.bucket_unpack(grads_h[r], offsets, bufs[r], code)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def _oracle_view_hook(grads_h, offsets, bucket_numel, divisor):
+    """Oracle steps of the bf16 hook on one bucket: pack the float32
+    gradients, round to bf16, bf16 ring with divide, widen, unpack."""
+    world = len(grads_h)
+    bufs = []
+    for r in range(world):
+        b = np.zeros(bucket_numel, dtype=np.float32)
+        oracle.bucket_pack(grads_h[r], offsets, b, oracle.F32)
+        bufs.append(oracle.bf16_rne(b))
+    oracle.ring_allreduce(bufs, oracle.BF16, divisor)
+    for r in range(world):
+        oracle.bucket_unpack(grads_h[r], offsets, oracle.bf16_to_f32(bufs[r]), oracle.F32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "hook"])
 @pytest.mark.parametrize("layout", ["boundaries", "pointers"])
 def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     # a TMA-sized bucket (8 ranks) whose chunk boundaries are not 16-byte
@@ -416,6 +430,10 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     # members packed back to back at odd offsets in one arena).  The aligned
     # bodies go to the TMA kernel, the few elements around each boundary and
     # the misaligned members to the register kernel.
+    # "hook": float32 gradients through the fused bf16 compression hook
+    hook = dtype == "hook"
+    if hook:
+        dtype = "f32"
     world = 8
     es = 2 if dtype == "bf16" else 4
     lanes = 16 // es
@@ -441,12 +459,19 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     code = oracle.BF16 if dtype == "bf16" else oracle.F32
     for div in (world, 3):
         grads_h = [[f32_or_bits(t) for t in dev[r]] for r in range(world)]
-        ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
+        if hook:
+            ddp.ddp_bucket_allreduce_view_bf16(dev, offsets, total, div)
+        else:
+            ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
         torch.cuda.synchronize()
-        _oracle_view(grads_h, offsets, total, code, div)
+        if hook:
+            _oracle_view_hook(grads_h, offsets, total, div)
+        else:
+            _oracle_view(grads_h, offsets, total, code, div)
         for r in range(world):
             for i in range(len(numels)):
-                assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i], f"{layout} {dtype} div={div} r{r} m{i}")
+                assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i],
+                                  f"{layout} {'hook' if hook else dtype} div={div} r{r} m{i}")
     assert ddp.ddp_device_status() == 0
 
 
