@@ -98,6 +98,27 @@ int grid_for(const void* kernel, int64_t work_items, int threads) {
     return cap_ctas(std::min<int64_t>((int64_t)sms * per_sm, need));
 }
 
+// Host buffers of a host-memory allreduce: non-null and element-aligned;
+// inputs pairwise disjoint; each output either is its own rank's input (in
+// place) or overlaps no input and no other output.
+int32_t check_host_in_out(int32_t world, const void* const* host_in, void* const* host_out, int64_t numel,
+                          int32_t dtype) {
+    const uintptr_t es = (uintptr_t)elem_bytes(dtype);
+    const uintptr_t bytes = (uintptr_t)numel * es;
+    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+    for (int32_t r = 0; r < world; ++r) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(host_in[r]), b = reinterpret_cast<uintptr_t>(host_out[r]);
+        if (!a || !b) return DDP_ERR_INVALID;
+        if (a % es || b % es) return DDP_ERR_ALIGN;
+        iv.emplace_back(a, a + bytes);
+        if (b != a) iv.emplace_back(b, b + bytes);
+    }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+        if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
+    return DDP_OK;
+}
+
 }  // namespace ddpk
 
 using namespace ddpk;
@@ -481,8 +502,7 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
     if (numel == 0) return DDP_OK;
     bool vec = false;
     if ((st = check_rank_buffers(world, dev_bufs, numel, dtype, &vec))) return st;
-    for (int32_t r = 0; r < world; ++r)
-        if (!host_in[r] || !host_out[r]) return DDP_ERR_INVALID;
+    if ((st = check_host_in_out(world, host_in, host_out, numel, dtype))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const int64_t es = elem_bytes(dtype);
     const size_t bytes = (size_t)numel * es;
@@ -531,31 +551,7 @@ int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_
     if (st) return st;
     if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
     if (numel == 0) return DDP_OK;
-    const uintptr_t es = (uintptr_t)elem_bytes(dtype);
-    const uintptr_t bytes = (uintptr_t)numel * es;
-    // inputs pairwise disjoint; each output either is its own input (in
-    // place) or overlaps no input and no other output
-    std::vector<std::pair<uintptr_t, uintptr_t>> iv;
-    bool same = true;
-    for (int32_t r = 0; r < world; ++r) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(host_in[r]), b = reinterpret_cast<uintptr_t>(host_out[r]);
-        if (!a || !b) return DDP_ERR_INVALID;
-        if (a % es || b % es) return DDP_ERR_ALIGN;
-        if (a != b) same = false;
-        iv.emplace_back(a, a + bytes);
-    }
-    if (!same)
-        for (int32_t r = 0; r < world; ++r) {
-            const uintptr_t b = reinterpret_cast<uintptr_t>(host_out[r]);
-            if (b == reinterpret_cast<uintptr_t>(host_in[r])) {
-                // in place for this rank: nothing else may overlap it (checked via the input ranges)
-                continue;
-            }
-            iv.emplace_back(b, b + bytes);
-        }
-    std::sort(iv.begin(), iv.end());
-    for (size_t i = 1; i < iv.size(); ++i)
-        if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
+    if ((st = ddpk::check_host_in_out(world, host_in, host_out, numel, dtype))) return st;
     std::vector<void*> din(world), dout(world);
     bool vec = true;
     for (int32_t r = 0; r < world; ++r) {

@@ -28,6 +28,12 @@
 #include "ddp_internal.h"
 #include "ddp_trace.h"
 
+namespace ddpk {
+// ddp_api.cpp: host buffers of a host-memory allreduce (null, alignment, overlap)
+int32_t check_host_in_out(int32_t world, const void* const* host_in, void* const* host_out, int64_t numel,
+                          int32_t dtype);
+}  // namespace ddpk
+
 // The scratch itself.  In host code this name is only a host-side stand-in
 // for the symbol, never a device address: it is turned into one with
 // cudaGetSymbolAddress below, once per device.
@@ -68,8 +74,7 @@ extern "C" int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const v
     if (world > DDP_MAX_WORLD) return DDP_ERR_CAPACITY;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
     if (!host_in || !host_out) return DDP_ERR_INVALID;
-    for (int32_t r = 0; r < world; ++r)
-        if (!host_in[r] || !host_out[r]) return DDP_ERR_INVALID;
+    if (int32_t st = ddpk::check_host_in_out(world, host_in, host_out, numel, dtype)) return st;
     if (numel == 0) return DDP_OK;
     // each rank's slice starts on a 256-byte boundary so the kernel's
     // vectorised paths apply

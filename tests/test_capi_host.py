@@ -169,6 +169,15 @@ def test_host_direct_rejects_aliasing_on_host():
     assert f(2, _vp(A, B), _vp(C, C + 2), 8, 0, 2, None) == -2    # fp32 output not 4-byte aligned
     assert f(2, None, _vp(C, B), 8, 0, 2, None) == -1
     assert f(2, _vp(A, B), _vp(A, B), 0, 0, 2, None) == 0          # empty: no CUDA work
+    # the copy-engine and no-alloc host paths apply the same rules
+    D0, D1 = 0x7f0000400000, 0x7f0000500000
+    g = L.ring_allreduce_fused_from_host
+    assert g(2, _vp(A, B), _vp(B, A), _vp(D0, D1), 8, 0, 2, None) == -1
+    assert g(2, _vp(A, B), _vp(C, C), _vp(D0, D1), 8, 0, 2, None) == -1
+    assert g(2, _vp(A, B), _vp(C, C + 2), _vp(D0, D1), 8, 0, 2, None) == -2
+    h = L.ring_allreduce_fused_from_host_noalloc
+    assert h(2, _vp(A, B), _vp(B, A), 8, 0, 2, None) == -1
+    assert h(2, _vp(A, A + 8), _vp(A, A + 8), 8, 0, 2, None) == -1
 
 
 def test_persistent_rejects_bad_arguments_on_host():

@@ -61,7 +61,7 @@ def test_noalloc_in_place_on_host():
 def test_noalloc_rejects_requests_beyond_the_array_before_any_cuda_call():
     L = ddp.lib()
     H = 0x7f0000000000                       # never dereferenced: every call below is refused
-    tab = (ctypes.c_void_p * 8)(*[H + r * (1 << 24) for r in range(8)])
+    tab = (ctypes.c_void_p * 8)(*[H + r * (1 << 27) for r in range(8)])    # 128 MiB apart: disjoint
     limit = ddp.STATIC_SCRATCH_BYTES
     # 8 ranks x (limit / 8 + 4 bytes) of fp32 does not fit
     assert L.ring_allreduce_fused_from_host_noalloc(8, tab, tab, limit // 32 + 1, 0, 8, None) == -5
