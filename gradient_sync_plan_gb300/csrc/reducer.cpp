@@ -160,9 +160,18 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
                   [&](int32_t a, int32_t b) { return offset_of_param[a] < offset_of_param[b]; });
         const int32_t n = (int32_t)m.size();
         r->n_members[k] = n;
+        // members inside the bucket and disjoint (sorted by offset): a bad
+        // plan is refused here, not in the middle of a backward pass
+        int64_t end = 0;
         for (int32_t i = 0; i < n; ++i) {
-            r->member_numel[k].push_back(numel[m[i]]);
-            r->member_offset[k].push_back(offset_of_param[m[i]]);
+            const int64_t o = offset_of_param[m[i]], e = numel[m[i]];
+            if (e < 0 || o < 0 || o > r->bucket_numel[k] - e || (e > 0 && o < end)) {
+                delete r;
+                return DDP_ERR_INVALID;
+            }
+            if (e > 0) end = o + e;
+            r->member_numel[k].push_back(e);
+            r->member_offset[k].push_back(o);
         }
         if (algo != DDP_ALGO_DRYRUN) {
             r->member_grads[k].resize((size_t)world * n);

@@ -80,3 +80,17 @@ def test_double_mark_and_missing_gradient_are_errors():
     with pytest.raises(ddp.DDPError):
         red.mark_ready(7, stream=0)
     red.close()
+
+
+def test_inconsistent_plans_are_refused_when_the_reducer_is_created():
+    numels = [100, 200, 300]
+    b_of, off, bn = ddp.ddp_plan_buckets(numels, ddp.F32, 400, 400)
+    bad_plans = [
+        (b_of, [o + 1 if i == 0 else o for i, o in enumerate(off)], bn),        # a member runs past its bucket
+        (b_of, off, [n - 1 for n in bn]),                                          # bucket too short
+        ([0, 0, 0], [0, 50, 0], [600]),                                            # two members overlap
+        (b_of, [-1] + list(off[1:]), bn),                                          # negative offset
+    ]
+    for plan in bad_plans:
+        with pytest.raises(ddp.DDPError):
+            ddp.Reducer(None, plan, algo=ddp.DDP_ALGO_DRYRUN, world=2, numels=numels)
