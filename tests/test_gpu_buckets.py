@@ -499,3 +499,21 @@ def test_one_scratch_buffer_shared_by_every_bucket(algo):
         oracle.ddp_sync(grads_h, oracle.F32, first, cap)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
     assert_bits_equal(f32_or_bits(g), want, f"{algo} with one shared scratch buffer")
+
+
+def test_readme_python_example_runs():
+    # the README's usage block, run as written on a small decoder and bucket
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "README.md"), encoding="utf-8").read()
+    block = re.search(r"## Using it from Python\n\n```python\n(.*?)```", text, re.S).group(1)
+    numels = _small_decoder()
+    flat, _ = _host_grads(numels, 4, "f32", seed0=71)
+    g = flat.cuda()
+    x = workloads.rank_vectors(4, 1000, "randn", seed0=3).cuda()
+    env = {"grads": _device_views(g, numels), "x": x}
+    exec(compile(block, "README.md", "exec"), env)
+    torch.cuda.synchronize()
+    for r in range(1, 4):                      # every sync leaves all ranks identical
+        assert torch.equal(g[r], g[0]) and torch.equal(x[r], x[0])
