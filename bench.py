@@ -657,6 +657,16 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
                                         "high_priority_comm": {
                                             "overlapped_ms": t_h, "exposed_comm_ms": t_h - t_b,
                                             "hidden_fraction": (t_s - t_h) / comm_ms if comm_ms > 0 else None}}
+    # DDP's logging data for one plain (not graph-captured) overlapped pass:
+    # every bucket's size and its sync time on the comm stream
+    run_overlapped()
+    torch.cuda.synchronize()
+    times = red.bucket_times()
+    res["buckets"] = {"bucket_sizes_bytes": [int(n) * 4 for n in plan[2]],
+                      "sync_ms": [round(t, 4) for t in times],
+                      "sync_ms_total": sum(times),
+                      "note": "per-rank bucket bytes; comm-stream time of each bucket's view sync while the "
+                              "synthetic backward runs beside it"}
     red.close()
     red_hi.close()
     del g, src, views

@@ -45,7 +45,7 @@ EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_d
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view", "ddp_bucket_allreduce_view_bf16",
            "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
-           "ddp_reducer_launch_order", "ddp_reducer_destroy"]
+           "ddp_reducer_launch_order", "ddp_reducer_bucket_times", "ddp_reducer_destroy"]
 
 
 class DDPError(RuntimeError):
@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_reducer_mark_ready.argtypes = [vp, i32, vp]
             L.ddp_reducer_finalize.argtypes = [vp, vp]
             L.ddp_reducer_launch_order.argtypes = [vp, P(i32), i32, P(i32)]
+            L.ddp_reducer_bucket_times.argtypes = [vp, P(ctypes.c_float), i32, P(i32)]
             L.ddp_reducer_destroy.argtypes = [vp]
             for name in EXPORTS[4:]:   # every entry point from ddp_set_max_ctas on returns a status
                 getattr(L, name).restype = i32
@@ -548,6 +549,15 @@ class Reducer:
         _check("ddp_reducer_launch_order",
                lib().ddp_reducer_launch_order(self._h, buf, self.n_buckets, ctypes.byref(n)))
         return [int(v) for v in buf[:n.value]]
+
+    def bucket_times(self):
+        """Per-bucket sync time (ms) of the current pass, in bucket order; -1
+        where the pass was being captured into a graph.  Waits for the syncs."""
+        buf = (ctypes.c_float * max(self.n_buckets, 1))()
+        n = ctypes.c_int32(0)
+        _check("ddp_reducer_bucket_times",
+               lib().ddp_reducer_bucket_times(self._h, buf, self.n_buckets, ctypes.byref(n)))
+        return [float(v) for v in buf[:n.value]]
 
     def close(self):
         if getattr(self, "_h", None):

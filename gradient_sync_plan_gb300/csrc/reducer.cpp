@@ -34,6 +34,8 @@ struct ddp_reducer {
     std::vector<std::vector<void*>> bucket_bufs;      // [world]
     std::vector<int32_t> n_members;
     std::vector<cudaEvent_t> ready_ev;                // per bucket, recorded on the compute stream
+    std::vector<cudaEvent_t> t0_ev, t1_ev;            // per bucket, timing events around its sync (comm stream)
+    std::vector<char> timed;                          // bucket k's timing events were recorded this pass
     cudaEvent_t done_ev = nullptr;
     // per-backward state
     std::vector<int32_t> pending;
@@ -80,8 +82,15 @@ int32_t launch_ready_prefix(ddp_reducer* r) {
         const int32_t k = r->next_launch;
         if (!dry(r)) {
             if (cudaStreamWaitEvent(r->comm, r->ready_ev[k], 0) != cudaSuccess) return DDP_ERR_CUDA;
+            // timing events cannot be recorded into a graph being captured
+            cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(r->comm, &cap) != cudaSuccess) return DDP_ERR_CUDA;
+            const bool time_it = cap == cudaStreamCaptureStatusNone;
+            if (time_it && cudaEventRecord(r->t0_ev[k], r->comm) != cudaSuccess) return DDP_ERR_CUDA;
             const int32_t st = sync_bucket(r, k);
             if (st) return st;
+            if (time_it && cudaEventRecord(r->t1_ev[k], r->comm) != cudaSuccess) return DDP_ERR_CUDA;
+            r->timed[k] = time_it ? 1 : 0;
         }
         r->launch_log.push_back(k);
         ++r->next_launch;
@@ -93,15 +102,18 @@ void reset_step(ddp_reducer* r) {
     for (int32_t k = 0; k < r->n_buckets; ++k) r->pending[k] = r->n_members[k];
     std::fill(r->param_ready.begin(), r->param_ready.end(), 0);
     std::fill(r->bucket_ready.begin(), r->bucket_ready.end(), 0);
+    std::fill(r->timed.begin(), r->timed.end(), 0);
     r->next_launch = 0;
     r->launch_log.clear();
     r->first_error = DDP_OK;
 }
 
 void destroy_events(ddp_reducer* r) {
-    for (cudaEvent_t e : r->ready_ev)
-        if (e) cudaEventDestroy(e);
-    r->ready_ev.clear();
+    for (auto* v : {&r->ready_ev, &r->t0_ev, &r->t1_ev}) {
+        for (cudaEvent_t e : *v)
+            if (e) cudaEventDestroy(e);
+        v->clear();
+    }
     if (r->done_ev) cudaEventDestroy(r->done_ev);
     r->done_ev = nullptr;
 }
@@ -186,10 +198,14 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     r->pending.resize(n_buckets);
     r->param_ready.resize(n_params);
     r->bucket_ready.resize(n_buckets);
+    r->timed.resize(n_buckets);
     if (algo != DDP_ALGO_DRYRUN) {
         r->ready_ev.assign(n_buckets, nullptr);
+        r->t0_ev.assign(n_buckets, nullptr);
+        r->t1_ev.assign(n_buckets, nullptr);
         for (int32_t k = 0; k < n_buckets; ++k)
-            if (cudaEventCreateWithFlags(&r->ready_ev[k], cudaEventDisableTiming) != cudaSuccess) {
+            if (cudaEventCreateWithFlags(&r->ready_ev[k], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreate(&r->t0_ev[k]) != cudaSuccess || cudaEventCreate(&r->t1_ev[k]) != cudaSuccess) {
                 destroy_events(r);
                 delete r;
                 return DDP_ERR_CUDA;
@@ -256,6 +272,20 @@ int32_t ddp_reducer_launch_order(ddp_reducer* r, int32_t* order, int32_t capacit
     std::lock_guard<std::mutex> lk(r->mu);
     *n = (int32_t)r->launch_log.size();
     for (int32_t i = 0; i < std::min(*n, capacity); ++i) order[i] = r->launch_log[i];
+    return DDP_OK;
+}
+
+int32_t ddp_reducer_bucket_times(ddp_reducer* r, float* ms, int32_t capacity, int32_t* n) {
+    DDP_TRACE_CALL();
+    if (!r || !n || capacity < 0 || (capacity > 0 && !ms)) return DDP_ERR_INVALID;
+    std::lock_guard<std::mutex> lk(r->mu);
+    *n = r->next_launch;
+    for (int32_t k = 0; k < std::min(r->next_launch, capacity); ++k) {
+        ms[k] = -1.0f;
+        if (dry(r) || !r->timed[k]) continue;
+        if (cudaEventSynchronize(r->t1_ev[k]) != cudaSuccess) return DDP_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms[k], r->t0_ev[k], r->t1_ev[k]) != cudaSuccess) return DDP_ERR_CUDA;
+    }
     return DDP_OK;
 }
 

@@ -479,8 +479,9 @@ int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* cons
  *                         until it is destroyed, the caller keeps the memory
  *   algo                  DDP_ALGO_FUSED, _STAGED, _VIEW or _DRYRUN
  *   comm_stream           cudaStream_t on which the buckets' syncs run
- * The reducer owns host memory and one CUDA event per bucket (created here,
- * destroyed by ddp_reducer_destroy); it allocates no device memory.
+ * The reducer owns host memory and three CUDA events per bucket (readiness
+ * and two timing events; created here, destroyed by ddp_reducer_destroy); it
+ * allocates no device memory.
  */
 typedef struct ddp_reducer ddp_reducer;
 int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel, int32_t dtype,
@@ -492,6 +493,13 @@ int32_t ddp_reducer_mark_ready(ddp_reducer* reducer, int32_t param, void* comput
 int32_t ddp_reducer_finalize(ddp_reducer* reducer, void* stream);
 /* Buckets launched in the current pass, in launch order (up to capacity). */
 int32_t ddp_reducer_launch_order(ddp_reducer* reducer, int32_t* order, int32_t capacity, int32_t* n);
+/* Per-bucket sync time of the current pass, in bucket order: ms[k] is the
+ * comm-stream time from the start to the end of bucket k's sync (DDP's
+ * per-bucket communication time, [P2] "bucket 与 overlap", "四组实验记录法"); -1 for a bucket
+ * launched on a stream that was being captured into a graph, or under
+ * DDP_ALGO_DRYRUN.  Waits for those buckets' syncs to finish.  *n receives
+ * the number of buckets launched so far (up to capacity are written). */
+int32_t ddp_reducer_bucket_times(ddp_reducer* reducer, float* ms, int32_t capacity, int32_t* n);
 int32_t ddp_reducer_destroy(ddp_reducer* reducer);
 
 /*

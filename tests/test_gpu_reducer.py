@@ -60,4 +60,37 @@ def test_overlapped_reducer_matches_oracle(algo, order, dtype):
         torch.cuda.synchronize()
         assert red.launch_order() == list(range(len(plan[2])))
         assert_bits_equal(f32_or_bits(g), want, f"reducer algo={algo} order={order}")
+        times = red.bucket_times()                        # per-bucket sync time on the comm stream
+        assert len(times) == len(plan[2]) and all(t > 0 for t in times), times
+    red.close()
+
+
+def test_bucket_times_are_unmeasured_inside_a_captured_graph():
+    # timing events cannot be recorded while the comm stream is captured: a
+    # pass captured into a graph reports -1 per bucket, a plain pass real times
+    numels = workloads.param_numels(workloads.decoder_param_shapes(n_layer=2, d_model=64, d_ff=256, vocab=500,
+                                                                   n_pos=32))
+    world = 4
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, 4096, 40000)
+    g = workloads.rank_vectors(world, sum(numels), "randn", std=1e-2, seed0=8).cuda()
+    offs = np.cumsum([0] + numels)
+    views = [[g[r, int(offs[p]):int(offs[p + 1])] for p in range(len(numels))] for r in range(world)]
+    comm, compute = torch.cuda.Stream(), torch.cuda.Stream()
+    red = ddp.Reducer(views, plan, None, algo=ddp.DDP_ALGO_VIEW, comm_stream=comm)
+
+    def one_pass():
+        red.prepare()
+        for p in range(len(numels) - 1, -1, -1):
+            red.mark_ready(p, compute)
+        red.finalize(compute)
+
+    one_pass()
+    torch.cuda.synchronize()
+    assert all(t > 0 for t in red.bucket_times())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=compute):
+        one_pass()
+    assert red.bucket_times() == [-1.0] * len(plan[2])
+    graph.replay()
+    torch.cuda.synchronize()
     red.close()

@@ -94,3 +94,13 @@ def test_inconsistent_plans_are_refused_when_the_reducer_is_created():
     for plan in bad_plans:
         with pytest.raises(ddp.DDPError):
             ddp.Reducer(None, plan, algo=ddp.DDP_ALGO_DRYRUN, world=2, numels=numels)
+
+
+def test_bucket_times_in_a_dry_run_are_unmeasured():
+    numels = [100, 200, 300]
+    red, (b_of, off, bn) = _dry(numels, first=400, cap=400)
+    for p in (2, 1, 0):
+        red.mark_ready(p, stream=0)
+    red.finalize(stream=0)
+    assert red.bucket_times() == [-1.0] * len(bn)
+    red.close()
