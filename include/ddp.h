@@ -23,8 +23,12 @@
  *
  * Conventions shared by every entry point:
  *   - Ownership: the caller owns every host and device buffer.  The library
- *     allocates no device memory, keeps no pointer after a call returns and
- *     holds no state between calls except cached device attributes.
+ *     allocates no device memory at run time (the no-alloc entry point's
+ *     64 MiB array is a static device array) and keeps no pointer after a
+ *     call returns (except a ddp_reducer, which keeps the tables it was
+ *     created with).  State kept between calls: cached device attributes,
+ *     the two process-wide settings (ddp_set_max_ctas, ddp_set_fused_kernel)
+ *     and the device status word (ddp_device_status).
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream).  Device work is enqueued asynchronously on it; the
  *     host returns without waiting for the GPU.  Calls may be captured into a
