@@ -178,7 +178,12 @@ k_ring_hop(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, i
     if (c < 0) c += world;
     const int64_t lo = std::min((int64_t)c * clen, numel);
     const int64_t hi = std::min(lo + clen, numel);
+    // programmatic dependent launch: the next hop may be scheduled now, and
+    // no buffer is touched before the previous hop (or whatever preceded
+    // this kernel on the stream) has completed and its writes are visible
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (lo >= hi) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     char* dst = t.p[r];
     const char* src = t.p[left];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -394,9 +399,18 @@ static cudaError_t hop(const RankTable<CAP>& t, int world, int64_t numel, int ph
     // blocks in x per rank: enough to fill the GPU once all ranks are counted
     int gx = grid_for((const void*)k, per_rank * world);
     gx = std::max(1, (gx + world - 1) / world);
-    dim3 grid(gx, world);
-    k<<<grid, kThreads, 0, st>>>(t, world, numel, clen, phase, s, vec_ok ? 1 : 0, dop);
-    return cudaGetLastError();
+    // hops are launched as programmatic dependents of the previous kernel on
+    // the stream: each one's launch overlaps the previous hop's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, world);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, t, world, numel, clen, phase, s, vec_ok ? 1 : 0, dop);
 }
 
 template <class E, int DIV, int CAP>

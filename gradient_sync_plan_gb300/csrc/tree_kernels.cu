@@ -163,6 +163,10 @@ k_tree_hop(const __grid_constant__ TreeTable<CAP> t, int64_t numel, int d, int p
     using S = typename E::S;
     constexpr int L = E::L;
     const int r = blockIdx.y * 2 * d;
+    // programmatic dependent launch: let the next step be scheduled, and touch
+    // no buffer before the previous step has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     char* lo_buf = t.p[r];
     char* hi_buf = t.p[r + d];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -264,8 +268,17 @@ static cudaError_t tree_staged_impl(int world, void* const* ptrs, int64_t numel,
         const int64_t per_pair = vec_ok ? numel / E::L + E::L : numel;
         int gx = grid_for((const void*)kd, per_pair * pairs);
         gx = std::max(1, (gx + pairs - 1) / pairs);
-        kd<<<dim3(gx, pairs), kThreads, 0, st>>>(t, numel, d, phase, divide ? 1 : 0, vec_ok ? 1 : 0, dop);
-        return cudaGetLastError();
+        // each step a programmatic dependent of the previous kernel on the stream
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(gx, pairs);
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kd, t, numel, d, phase, divide ? 1 : 0, vec_ok ? 1 : 0, dop);
     };
     for (int k = 0; k < depth; ++k) {
         cudaError_t e = launch(1 << k, 0, k == depth - 1);
