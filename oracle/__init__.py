@@ -28,6 +28,7 @@ import numpy as np
 
 F32 = 0
 BF16 = 1
+F16 = 2                                    # IEEE binary16, ring arithmetic of the fp16 compression hook
 FIRST_BUCKET_BYTES = 1024 * 1024          # 1 MiB first bucket
 BUCKET_CAP_BYTES = 25 * 1024 * 1024        # 25 MiB bucket cap ("MB" read as MiB)
 
@@ -104,6 +105,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_bf16_rne.restype = ctypes.c_uint16
             L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             L.oracle_bf16_to_f32.restype = ctypes.c_float
+            L.oracle_fp16_rne_array.argtypes = [vp, vp, i64]
+            L.oracle_fp16_rne_array.restype = None
+            L.oracle_fp16_to_f32_array.argtypes = [vp, vp, i64]
+            L.oracle_fp16_to_f32_array.restype = None
             _lib = L
     return _lib
 
@@ -230,6 +235,22 @@ def bf16_rne(x: np.ndarray) -> np.ndarray:
     return y
 
 
+def fp16_rne(x: np.ndarray) -> np.ndarray:
+    """float32 array -> uint16 IEEE binary16 patterns (the oracle's own rounding)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_fp16_rne_array(x.ctypes.data, y.ctypes.data, int(x.size))
+    return y
+
+
+def fp16_to_f32(h: np.ndarray) -> np.ndarray:
+    """uint16 binary16 patterns -> float32 (exact widening, the oracle's own)."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    y = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_fp16_to_f32_array(h.ctypes.data, y.ctypes.data, int(h.size))
+    return y
+
+
 def bf16_to_f32(h: np.ndarray) -> np.ndarray:
     """uint16 bf16 patterns -> float32 (exact widening)."""
     return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
@@ -310,5 +331,30 @@ def ddp_sync_bf16_hook(grads: Sequence[Sequence[np.ndarray]], first_cap_bytes: i
         ring_allreduce(bufs, BF16, div)
         for r in range(world):
             bucket_unpack([grads[r][p] for p in members], [off[p] for p in members], bf16_to_f32(bufs[r]), F32)
+    return b_of, off, bn
+
+
+def ddp_sync_fp16_hook(grads: Sequence[Sequence[np.ndarray]], first_cap_bytes: int = FIRST_BUCKET_BYTES,
+                       cap_bytes: int = BUCKET_CAP_BYTES, divisor: Optional[int] = None):
+    """DDP step with the fp16 compression communication hook, in place: as
+    ddp_sync_bf16_hook, with IEEE binary16 in place of bfloat16 (every element
+    rounded to binary16, a binary16 ring with one rounding per hop, the
+    divide rounded to binary16, the result widened back to float32).
+    ("Day 17 · 梯度的集体行动", reading list: DDP communication hooks, fp16/bf16
+    compression.)"""
+    world = len(grads)
+    numels = [int(a.size) for a in grads[0]]
+    b_of, off, bn = plan_buckets(numels, 4, first_cap_bytes, cap_bytes)
+    div = world if divisor is None else divisor
+    for k in range(len(bn)):
+        members = bucket_members(b_of, off, k)
+        bufs = []
+        for r in range(world):
+            b32 = np.zeros(int(bn[k]), dtype=np.float32)
+            bucket_pack([grads[r][p] for p in members], [off[p] for p in members], b32, F32)
+            bufs.append(fp16_rne(b32))
+        ring_allreduce(bufs, F16, div)
+        for r in range(world):
+            bucket_unpack([grads[r][p] for p in members], [off[p] for p in members], fp16_to_f32(bufs[r]), F32)
     return b_of, off, bn
 

@@ -32,7 +32,10 @@
  *   - the receiver adds the incoming chunk into its own copy; bf16 adds are
  *     done in binary32 and rounded to bf16 after every hop;
  *   - after the last step every rank divides every element by the divisor
- *     (world size) with one IEEE division ([P1] §05, [P2] pseudo-code).
+ *     (world size) with one IEEE division ([P1] §05, [P2] pseudo-code);
+ *   - an fp16 ring (the fp16 compression hook of [P2]'s reading list on DDP
+ *     communication hooks) works like the bf16 one: binary32 add of the two
+ *     widened values, rounded to binary16 after every hop.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -40,6 +43,7 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F16 2
 
 /* Built with -fopenmp (the optional multi-core timing build only), the ranks
  * of one half-step run side by side: within a half-step every rank reads and
@@ -93,6 +97,63 @@ void oracle_bf16_rne_array(const float* x, uint16_t* y, int64_t n)
 /* The reduction operator and the average.                                  */
 /* ------------------------------------------------------------------------ */
 
+/* ------------------------------------------------------------------------ */
+/* IEEE binary16 <-> binary32, written from the IEEE-754 definition.         */
+/* ------------------------------------------------------------------------ */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Widening to binary32 is exact (subnormals included). */
+float oracle_fp16_to_f32(uint16_t h)
+{
+    uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+    uint32_t exp = ((uint32_t)h >> 10) & 0x1Fu, frac = (uint32_t)h & 0x3FFu;
+    if (exp == 0x1Fu)                                  /* infinity or NaN */
+        return bits_f32(sign | 0x7F800000u | (frac << 13));
+    if (exp == 0) {                                    /* zero or subnormal: frac * 2^-24, exact */
+        float v = (float)frac * (1.0f / 16777216.0f);
+        return bits_f32(f32_bits(v) | sign);
+    }
+    return bits_f32(sign | ((exp - 15u + 127u) << 23) | (frac << 13));
+}
+
+/* Round a binary32 value to binary16, to nearest, ties to even.  The value is
+ * sig * 2^(E-23) with a 24-bit significand sig; in the normal range of
+ * binary16 (E >= -14) 11 significant bits are kept, below it the result is a
+ * multiple of 2^-24 (subnormal).  The dropped bits are compared with half of
+ * the last kept place; a carry out of the kept bits moves into the exponent,
+ * and values at or beyond 65520 become infinity.  NaN stays NaN, quiet. */
+uint16_t oracle_fp16_rne(float f)
+{
+    uint32_t u = f32_bits(f);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t exp = (u >> 23) & 0xFFu, man = u & 0x7FFFFFu;
+    if (exp == 0xFFu) return (uint16_t)(sign | 0x7C00u | (man ? 0x0200u | (man >> 13) : 0u));
+    if (exp == 0 && man == 0) return sign;
+    int32_t E = exp ? (int32_t)exp - 127 : -126;
+    uint64_t sig = exp ? (man | 0x800000u) : man;
+    uint32_t shift = E >= -14 ? 13u : (uint32_t)(13 + (-14 - E));     /* bits dropped from sig */
+    if (shift > 40) return sign;                                      /* far below half the least subnormal */
+    uint64_t kept = sig >> shift, rem = sig & ((1ull << shift) - 1u), half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (kept & 1u))) kept += 1u;
+    if (E >= -14) {
+        int32_t be = E + 15;                                          /* biased exponent */
+        if (kept == 0x800u) { kept >>= 1; be += 1; }                  /* carry into the exponent */
+        if (be >= 31) return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | ((uint32_t)be << 10) | (uint32_t)(kept & 0x3FFu));
+    }
+    return (uint16_t)(sign | (uint32_t)kept);          /* subnormal; kept == 0x400 is the least normal */
+}
+
+void oracle_fp16_rne_array(const float* x, uint16_t* y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_fp16_rne(x[i]);
+}
+
+void oracle_fp16_to_f32_array(const uint16_t* h, float* y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_fp16_to_f32(h[i]);
+}
+
 static size_t elem_size(int dtype) { return dtype == ORACLE_F32 ? 4u : 2u; }
 
 /* dst[i] <- dst[i] (+) src[i] : binary32 add, or for bf16 a binary32 add of
@@ -103,6 +164,11 @@ static void add_into(int dtype, void* dst, const void* src, int64_t n)
         float* d = (float*)dst;
         const float* s = (const float*)src;
         for (int64_t i = 0; i < n; ++i) d[i] = d[i] + s[i];
+    } else if (dtype == ORACLE_F16) {
+        uint16_t* d = (uint16_t*)dst;
+        const uint16_t* s = (const uint16_t*)src;
+        for (int64_t i = 0; i < n; ++i)
+            d[i] = oracle_fp16_rne(oracle_fp16_to_f32(d[i]) + oracle_fp16_to_f32(s[i]));
     } else {
         uint16_t* d = (uint16_t*)dst;
         const uint16_t* s = (const uint16_t*)src;
@@ -118,6 +184,9 @@ static void divide_all(int dtype, void* x, int64_t n, int32_t divisor)
     if (dtype == ORACLE_F32) {
         float* p = (float*)x;
         for (int64_t i = 0; i < n; ++i) p[i] = p[i] / dv;
+    } else if (dtype == ORACLE_F16) {
+        uint16_t* p = (uint16_t*)x;
+        for (int64_t i = 0; i < n; ++i) p[i] = oracle_fp16_rne(oracle_fp16_to_f32(p[i]) / dv);
     } else {
         uint16_t* p = (uint16_t*)x;
         for (int64_t i = 0; i < n; ++i) p[i] = oracle_bf16_rne(oracle_bf16_to_f32(p[i]) / dv);
@@ -157,7 +226,8 @@ static int32_t mod(int64_t a, int32_t n) { int64_t m = a % n; return (int32_t)(m
 int oracle_ring_allreduce(int32_t world, int64_t numel, int32_t dtype, void** bufs,
                           int32_t divisor, int32_t n_steps, int64_t* sent)
 {
-    if (world < 1 || numel < 0 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16) || divisor < 0 || !bufs)
+    if (world < 1 || numel < 0 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) ||
+        divisor < 0 || !bufs)
         return ORACLE_EINVAL;
     for (int32_t r = 0; r < world; ++r)
         if (!bufs[r] && numel > 0) return ORACLE_EINVAL;

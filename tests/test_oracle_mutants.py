@@ -14,7 +14,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ddp_oracle.c")
-PINS = ["tests/test_oracle_ring.py", "tests/test_oracle_plan.py", "tests/test_oracle_tree.py"]
+PINS = ["tests/test_oracle_ring.py", "tests/test_oracle_plan.py", "tests/test_oracle_tree.py",
+        "tests/test_oracle_fp16.py"]
 
 MUTANTS = {
     "rs_send_chunk_off_by_one": ("? mod((int64_t)r - s, world) :", "? mod((int64_t)r - s - 1, world) :"),
@@ -49,6 +50,11 @@ MUTANTS = {
         "memcpy(grads[i], (const char*)bucket + offset[i] * elem_bytes, (size_t)(numel[i] * elem_bytes));",
         "memcpy(grads[i], (const char*)bucket + offset[i] * elem_bytes, (size_t)((numel[i] - 1) * elem_bytes));"),
     "accumulate_skipped": ("    if (n > 0) add_into(dtype, acc, g, n);", "    (void)acc; (void)g;"),
+    "fp16_ties_away": ("if (rem > half || (rem == half && (kept & 1u))) kept += 1u;",
+                       "if (rem >= half) kept += 1u;"),
+    "fp16_subnormals_flushed": ("    if (shift > 40) return sign;", "    if (E < -14) return sign;"),
+    "fp16_overflow_saturates": ("        if (be >= 31) return (uint16_t)(sign | 0x7C00u);",
+                                "        if (be >= 31) return (uint16_t)(sign | 0x7BFFu);"),
     "bf16_divide_rounds_toward_zero": (
         "for (int64_t i = 0; i < n; ++i) p[i] = oracle_bf16_rne(oracle_bf16_to_f32(p[i]) / dv);",
         "for (int64_t i = 0; i < n; ++i) p[i] = (uint16_t)(f32_bits(oracle_bf16_to_f32(p[i]) / dv) >> 16);"),
