@@ -465,6 +465,19 @@ def ddp_step_bench(ddp, workloads, torch, dev, stream, steps):
     ms = ev0.elapsed_time(ev1) / steps
     res["bf16_hook_view"] = {"ms_per_step": ms, "hbm_alg_gbs": 2 * N * p_bytes / (ms / 1e3) / 1e9,
                              "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
+    # the fp16 compression hook, fused the same way
+    call = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_FP16_HOOK_VIEW)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        call()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    res["fp16_hook_view"] = {"ms_per_step": ms, "hbm_alg_gbs": 2 * N * p_bytes / (ms / 1e3) / 1e9,
+                             "grad_bytes_synced_gbs": N * p_bytes / (ms / 1e3) / 1e9}
     # no_sync: 3 local accumulations of a micro-batch, then one sync (view)
     scratch = torch.empty_like(g)
     scratch.copy_(g)

@@ -28,6 +28,7 @@ DDP_ALGO_VIEW = 2
 DDP_ALGO_DRYRUN = 3
 DDP_ALGO_BF16_HOOK = 4
 DDP_ALGO_BF16_HOOK_VIEW = 5
+DDP_ALGO_FP16_HOOK_VIEW = 6
 DDP_FUSED_AUTO, DDP_FUSED_VECTOR, DDP_FUSED_GROUP, DDP_FUSED_TMA = 0, 1, 2, 3
 DDP_MAX_WORLD = 512
 FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
@@ -44,6 +45,7 @@ EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_d
            "tree_allreduce_staged", "ring_allreduce_fused_from_host",
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view", "ddp_bucket_allreduce_view_bf16",
+           "ddp_bucket_allreduce_view_fp16",
            "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
            "ddp_reducer_launch_order", "ddp_reducer_bucket_times", "ddp_reducer_destroy"]
 
@@ -102,6 +104,7 @@ def lib() -> ctypes.CDLL:
                                            i32, vp]
             L.ddp_bucket_allreduce_view.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, i32, vp]
             L.ddp_bucket_allreduce_view_bf16.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, vp]
+            L.ddp_bucket_allreduce_view_fp16.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, vp]
             L.ddp_reducer_create.argtypes = [i32, i32, P(vp), P(i64), i32, P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                              vp, P(vp)]
             L.ddp_reducer_prepare.argtypes = [vp]
@@ -430,6 +433,17 @@ def ddp_bucket_allreduce_view_bf16(grads: Sequence[Sequence], offsets: Sequence[
                                                 int(bucket_numel), divisor, _stream(stream)))
 
 
+def ddp_bucket_allreduce_view_fp16(grads: Sequence[Sequence], offsets: Sequence[int], bucket_numel: int,
+                                   divisor: int = 0, stream=None) -> None:
+    """fp16 compression hook fused into one pass over float32 gradients."""
+    world, n, ptrs, numels, code = _member_tables(grads, offsets)
+    if n and code != F32:
+        raise ValueError("float32 gradients expected")
+    _check("ddp_bucket_allreduce_view_fp16",
+           lib().ddp_bucket_allreduce_view_fp16(world, n, _vp_array(ptrs), _i64_array(numels), _i64_array(offsets),
+                                                int(bucket_numel), divisor, _stream(stream)))
+
+
 def ddp_sync_buckets(grads: Sequence[Sequence], plan, buckets: Optional[Sequence[Sequence]] = None,
                      divisor: Optional[int] = None, algo: int = DDP_ALGO_FUSED, stream=None) -> None:
     """Reducer step over a whole model: every bucket packed, reduced, averaged, unpacked.
@@ -474,7 +488,7 @@ class SyncCall:
             bflat = [buckets[r][k].data_ptr() for r in range(self.world) for k in range(self.K)]
             self._buckets = _vp_array(bflat)
         else:
-            if algo not in (DDP_ALGO_VIEW, DDP_ALGO_BF16_HOOK_VIEW):
+            if algo not in (DDP_ALGO_VIEW, DDP_ALGO_BF16_HOOK_VIEW, DDP_ALGO_FP16_HOOK_VIEW):
                 raise ValueError("bucket buffers are required unless algo is a view algorithm")
             self._buckets = None
         self.divisor = self.world if divisor is None else int(divisor)

@@ -428,6 +428,7 @@ static cudaError_t view_register(int world, const ViewMember* members, int n, in
     if (n == 0) return cudaSuccess;
     if (dtype == DDP_F32) return view_div<EF32>(world, members, n, bucket_numel, div, stream);
     if (dtype == kDtypeHook) return view_div<EHOOK>(world, members, n, bucket_numel, div, stream);
+    if (dtype == kDtypeHook16) return view_div<EHOOK16>(world, members, n, bucket_numel, div, stream);
     return view_div<EBF16>(world, members, n, bucket_numel, div, stream);
 }
 

@@ -652,6 +652,12 @@ int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void*
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook, divisor, stream);
 }
 
+int32_t ddp_bucket_allreduce_view_fp16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
+                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) {
+    DDP_TRACE_CALL();
+    return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook16, divisor, stream);
+}
+
 int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
                          const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
                          const int64_t* bucket_numel, void* const* buckets, int32_t dtype, int32_t divisor,
@@ -661,10 +667,12 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
     if (st) return st;
     if (n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
     if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_BF16_HOOK &&
-        algo != DDP_ALGO_BF16_HOOK_VIEW)
+        algo != DDP_ALGO_BF16_HOOK_VIEW && algo != DDP_ALGO_FP16_HOOK_VIEW)
         return DDP_ERR_INVALID;
-    if ((algo == DDP_ALGO_BF16_HOOK || algo == DDP_ALGO_BF16_HOOK_VIEW) && dtype != DDP_F32) return DDP_ERR_INVALID;
-    const bool view = algo == DDP_ALGO_VIEW || algo == DDP_ALGO_BF16_HOOK_VIEW;
+    if ((algo == DDP_ALGO_BF16_HOOK || algo == DDP_ALGO_BF16_HOOK_VIEW || algo == DDP_ALGO_FP16_HOOK_VIEW) &&
+        dtype != DDP_F32)
+        return DDP_ERR_INVALID;
+    const bool view = algo == DDP_ALGO_VIEW || algo == DDP_ALGO_BF16_HOOK_VIEW || algo == DDP_ALGO_FP16_HOOK_VIEW;
     if (n_params > 0 && (!grads || !numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
     if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
     if (!view && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
@@ -707,7 +715,9 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             }
             count[k] = (int)all.size() - first[k];
         }
-        const int32_t launch_dtype = (algo == DDP_ALGO_BF16_HOOK_VIEW) ? kDtypeHook : dtype;
+        const int32_t launch_dtype = (algo == DDP_ALGO_BF16_HOOK_VIEW)   ? kDtypeHook
+                                     : (algo == DDP_ALGO_FP16_HOOK_VIEW) ? kDtypeHook16
+                                                                         : dtype;
         return cuda_status(launch_buckets_view(world, all.data(), first.data(), count.data(), bucket_numel, n_buckets,
                                                launch_dtype, make_div(divisor), (cudaStream_t)stream));
     }

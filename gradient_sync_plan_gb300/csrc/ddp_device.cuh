@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -103,6 +104,34 @@ struct EHOOK {
     __device__ static __forceinline__ float4 rt4(float4 a) {
         const uint32_t lo = bf16x2_rn(a.x, a.y), hi = bf16x2_rn(a.z, a.w);
         return make_float4(bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi));
+    }
+    __device__ static __forceinline__ S sadd(S a, S b) { return rt(__fadd_rn(rt(a), rt(b))); }
+    __device__ static __forceinline__ V vadd(V a, V b) {
+        const float4 x = rt4(a), y = rt4(b);
+        return rt4(make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w)));
+    }
+    template <int DIV>
+    __device__ static __forceinline__ S sdiv(S a, float op) { return rt(div_f32<DIV>(rt(a), op)); }
+    template <int DIV>
+    __device__ static __forceinline__ V vdiv(V a, float op) {
+        const float4 x = rt4(a);
+        return rt4(make_float4(div_f32<DIV>(x.x, op), div_f32<DIV>(x.y, op), div_f32<DIV>(x.z, op),
+                               div_f32<DIV>(x.w, op)));
+    }
+};
+
+// ---- float32 storage, IEEE binary16 arithmetic (the fp16 compression hook,
+// fused): as EHOOK with binary16 in place of bf16 -- every input, every sum
+// and the quotient rounded to binary16 (nearest even), stored widened.
+struct EHOOK16 {
+    using S = float;
+    using V = float4;
+    static constexpr int L = 4;
+    __device__ static __forceinline__ float rt(float x) { return __half2float(__float2half_rn(x)); }
+    __device__ static __forceinline__ float4 rt4(float4 a) {
+        const float2 lo = __half22float2(__float22half2_rn(make_float2(a.x, a.y)));
+        const float2 hi = __half22float2(__float22half2_rn(make_float2(a.z, a.w)));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
     }
     __device__ static __forceinline__ S sadd(S a, S b) { return rt(__fadd_rn(rt(a), rt(b))); }
     __device__ static __forceinline__ V vadd(V a, V b) {

@@ -27,6 +27,7 @@ DivSpec make_div(int32_t divisor);
 
 // Internal element type of the fused bf16 hook: float32 storage, bf16 arithmetic.
 constexpr int kDtypeHook = 100;
+constexpr int kDtypeHook16 = 101;         // the same with IEEE binary16 (fp16 compression hook)
 
 inline int64_t chunk_len(int64_t numel, int world) { return (numel + world - 1) / world; }
 inline int elem_bytes(int dtype) { return dtype == DDP_BF16 ? 2 : 4; }

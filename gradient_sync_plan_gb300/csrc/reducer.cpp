@@ -59,6 +59,8 @@ int32_t sync_bucket(ddp_reducer* r, int32_t k) {
         return ddp_bucket_allreduce_view(r->world, n, g, ne, off, r->bucket_numel[k], r->dtype, r->divisor, r->comm);
     if (r->algo == DDP_ALGO_BF16_HOOK_VIEW)
         return ddp_bucket_allreduce_view_bf16(r->world, n, g, ne, off, r->bucket_numel[k], r->divisor, r->comm);
+    if (r->algo == DDP_ALGO_FP16_HOOK_VIEW)
+        return ddp_bucket_allreduce_view_fp16(r->world, n, g, ne, off, r->bucket_numel[k], r->divisor, r->comm);
     void* const* b = r->bucket_bufs[k].data();
     if (r->algo == DDP_ALGO_BF16_HOOK) {
         int32_t st = ddp_bucket_pack_bf16(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->comm);
@@ -132,9 +134,11 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     if (world < 1 || world > DDP_MAX_WORLD || n_params < 0 || n_buckets < 0 || divisor < 0) return DDP_ERR_INVALID;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
     if (algo != DDP_ALGO_FUSED && algo != DDP_ALGO_STAGED && algo != DDP_ALGO_VIEW && algo != DDP_ALGO_DRYRUN &&
-        algo != DDP_ALGO_BF16_HOOK && algo != DDP_ALGO_BF16_HOOK_VIEW)
+        algo != DDP_ALGO_BF16_HOOK && algo != DDP_ALGO_BF16_HOOK_VIEW && algo != DDP_ALGO_FP16_HOOK_VIEW)
         return DDP_ERR_INVALID;
-    if ((algo == DDP_ALGO_BF16_HOOK || algo == DDP_ALGO_BF16_HOOK_VIEW) && dtype != DDP_F32) return DDP_ERR_INVALID;
+    if ((algo == DDP_ALGO_BF16_HOOK || algo == DDP_ALGO_BF16_HOOK_VIEW || algo == DDP_ALGO_FP16_HOOK_VIEW) &&
+        dtype != DDP_F32)
+        return DDP_ERR_INVALID;
     if (n_params > 0 && (!numel || !bucket_of_param || !offset_of_param)) return DDP_ERR_INVALID;
     if (n_buckets > 0 && !bucket_numel) return DDP_ERR_INVALID;
     if (algo != DDP_ALGO_DRYRUN && n_params > 0 && !grads) return DDP_ERR_INVALID;

@@ -563,6 +563,7 @@ cudaError_t launch_bucket_view_tma(int world, const ViewMember* members, int n_m
     if (n_segs == 0) return cudaSuccess;
     if (dtype == DDP_F32) return view_tma_div<EF32>(world, members, n_members, segs, n_segs, div, stream);
     if (dtype == kDtypeHook) return view_tma_div<EHOOK>(world, members, n_members, segs, n_segs, div, stream);
+    if (dtype == kDtypeHook16) return view_tma_div<EHOOK16>(world, members, n_members, segs, n_segs, div, stream);
     return view_tma_div<EBF16>(world, members, n_members, segs, n_segs, div, stream);
 }
 

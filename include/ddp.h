@@ -406,8 +406,11 @@ typedef enum {
                              make no CUDA call (for checking a plan's order)    */
     DDP_ALGO_BF16_HOOK = 4, /* float32 gradients, bf16 buckets: ddp_bucket_pack_bf16
                              -> ring_allreduce_fused in bf16 -> ddp_bucket_unpack_bf16 */
-    DDP_ALGO_BF16_HOOK_VIEW = 5 /* the same result in one pass, no bucket buffers:
+    DDP_ALGO_BF16_HOOK_VIEW = 5, /* the same result in one pass, no bucket buffers:
                              ddp_bucket_allreduce_view_bf16                         */
+    DDP_ALGO_FP16_HOOK_VIEW = 6 /* the fp16 compression hook in one pass (float32
+                             gradients, IEEE binary16 arithmetic):
+                             ddp_bucket_allreduce_view_fp16                         */
 } ddp_algo;
 
 /*
@@ -518,6 +521,21 @@ int32_t ddp_reducer_destroy(ddp_reducer* reducer);
  * dtype argument.
  */
 int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void* const* grads,
+                                       const int64_t* numel, const int64_t* offset, int64_t bucket_numel,
+                                       int32_t divisor, void* stream);
+
+/*
+ * ddp_bucket_allreduce_view_fp16 -- the fp16 compression hook ([P2] reading
+ * list: DDP communication hooks, fp16/bf16 compression), fused like
+ * ddp_bucket_allreduce_view_bf16 with IEEE binary16 in place of bf16: every
+ * float32 gradient value is rounded to binary16 (nearest even), the values
+ * are summed in the ring order of their bucket chunk with a binary32 add of
+ * the two widened values rounded to binary16 after every hop, divided
+ * (rounded to binary16), and written back widened to float32.  Values that
+ * round beyond 65504 become infinity, as in binary16.  Arguments as for
+ * ddp_bucket_allreduce_view_bf16.
+ */
+int32_t ddp_bucket_allreduce_view_fp16(int32_t world, int32_t n_in_bucket, void* const* grads,
                                        const int64_t* numel, const int64_t* offset, int64_t bucket_numel,
                                        int32_t divisor, void* stream);
 

@@ -242,7 +242,7 @@ def test_no_sync_small_decoder_full():
     assert_bits_equal(f32_or_bits(acc), np.stack([np.concatenate(want[r]) for r in range(world)]), "no_sync")
 
 
-@pytest.mark.parametrize("algo", ["hook", "hook_view"])
+@pytest.mark.parametrize("algo", ["hook", "hook_view", "fp16_hook_view"])
 @pytest.mark.parametrize("via", ["sync_buckets", "reducer"])
 def test_bf16_hook_matches_oracle(via, algo):
     numels = _small_decoder()
@@ -252,7 +252,8 @@ def test_bf16_hook_matches_oracle(via, algo):
     x64 = flat.numpy().astype(np.float64)
     g = flat.cuda()
     views = _device_views(g, numels)
-    code = ddp.DDP_ALGO_BF16_HOOK if algo == "hook" else ddp.DDP_ALGO_BF16_HOOK_VIEW
+    code = {"hook": ddp.DDP_ALGO_BF16_HOOK, "hook_view": ddp.DDP_ALGO_BF16_HOOK_VIEW,
+            "fp16_hook_view": ddp.DDP_ALGO_FP16_HOOK_VIEW}[algo]
     bk = None
     if algo == "hook":
         bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
@@ -264,10 +265,13 @@ def test_bf16_hook_matches_oracle(via, algo):
             red.mark_ready(p, torch.cuda.current_stream())
         red.finalize(torch.cuda.current_stream())
     torch.cuda.synchronize()
-    oracle.ddp_sync_bf16_hook(grads_h, first, cap)
+    if algo == "fp16_hook_view":
+        oracle.ddp_sync_fp16_hook(grads_h, first, cap)
+    else:
+        oracle.ddp_sync_bf16_hook(grads_h, first, cap)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
     got = f32_or_bits(g)
-    assert_bits_equal(got, want, f"bf16 {algo} via {via}")
+    assert_bits_equal(got, want, f"{algo} via {via}")
     ref = x64.sum(0) / world
     assert np.linalg.norm(got[0] - ref) / np.linalg.norm(ref) <= 2e-2
 
@@ -318,12 +322,15 @@ def test_view_tma_path_matches_oracle(dtype):
 
 
 
+@pytest.mark.parametrize("prec", ["bf16", "fp16"])
 @pytest.mark.parametrize("divisor", [None, 0, 3])
-def test_bf16_hook_view_tma_path_matches_oracle(divisor):
+def test_bf16_hook_view_tma_path_matches_oracle(divisor, prec):
     # the fused hook on one TMA-sized bucket (> 4 MiB of float32 over 8 ranks,
     # chunk-aligned segments), plus the world-size, no-divide and
     # non-power-of-two divisors; the second call on a ragged single member
     # takes the register path
+    view_fn = ddp.ddp_bucket_allreduce_view_fp16 if prec == "fp16" else ddp.ddp_bucket_allreduce_view_bf16
+    hook_fn = oracle.ddp_sync_fp16_hook if prec == "fp16" else oracle.ddp_sync_bf16_hook
     world = 8
     numels = [16 * 7, 16 * 40000, 16 * 3, 16 * 25000, 16 * 1000, 16 * 9006]
     plan = ddp.ddp_plan_buckets(numels, ddp.F32, 1 << 40, 1 << 40)
@@ -332,9 +339,9 @@ def test_bf16_hook_view_tma_path_matches_oracle(divisor):
     g = flat.cuda()
     div = world if divisor is None else divisor
     offsets = [int(o) for o in plan[1]]
-    ddp.ddp_bucket_allreduce_view_bf16(_device_views(g, numels), offsets, int(plan[2][0]), div)
+    view_fn(_device_views(g, numels), offsets, int(plan[2][0]), div)
     torch.cuda.synchronize()
-    oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=div)
+    hook_fn(grads_h, 1 << 40, 1 << 40, divisor=div)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
     assert_bits_equal(f32_or_bits(g), want, f"hook view tma div={div}")
     assert ddp.ddp_device_status() == 0
@@ -342,9 +349,9 @@ def test_bf16_hook_view_tma_path_matches_oracle(divisor):
     numels = [1001]
     flat, grads_h = _host_grads(numels, 3, "f32", seed0=10)
     g = flat.cuda()
-    ddp.ddp_bucket_allreduce_view_bf16(_device_views(g, numels), [0], 1001, div)
+    view_fn(_device_views(g, numels), [0], 1001, div)
     torch.cuda.synchronize()
-    oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40, divisor=div)
+    hook_fn(grads_h, 1 << 40, 1 << 40, divisor=div)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(3)])
     assert_bits_equal(f32_or_bits(g), want, f"hook view ragged div={div}")
 
@@ -407,21 +414,23 @@ def _oracle_view(grads_h, offsets, bucket_numel, code, divisor):
         oracle.bucket_unpack(grads_h[r], offsets, bufs[r], code)
 
 
-def _oracle_view_hook(grads_h, offsets, bucket_numel, divisor):
-    """Oracle steps of the bf16 hook on one bucket: pack the float32
-    gradients, round to bf16, bf16 ring with divide, widen, unpack."""
+def _oracle_view_hook(grads_h, offsets, bucket_numel, divisor, fp16=False):
+    """Oracle steps of the bf16 (or fp16) hook on one bucket: pack the float32
+    gradients, round, ring in the narrow type with divide, widen, unpack."""
     world = len(grads_h)
+    rne, widen, code = ((oracle.fp16_rne, oracle.fp16_to_f32, oracle.F16) if fp16 else
+                        (oracle.bf16_rne, oracle.bf16_to_f32, oracle.BF16))
     bufs = []
     for r in range(world):
         b = np.zeros(bucket_numel, dtype=np.float32)
         oracle.bucket_pack(grads_h[r], offsets, b, oracle.F32)
-        bufs.append(oracle.bf16_rne(b))
-    oracle.ring_allreduce(bufs, oracle.BF16, divisor)
+        bufs.append(rne(b))
+    oracle.ring_allreduce(bufs, code, divisor)
     for r in range(world):
-        oracle.bucket_unpack(grads_h[r], offsets, oracle.bf16_to_f32(bufs[r]), oracle.F32)
+        oracle.bucket_unpack(grads_h[r], offsets, widen(bufs[r]), oracle.F32)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "hook"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "hook", "hook16"])
 @pytest.mark.parametrize("layout", ["boundaries", "pointers"])
 def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     # a TMA-sized bucket (8 ranks) whose chunk boundaries are not 16-byte
@@ -430,8 +439,9 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     # members packed back to back at odd offsets in one arena).  The aligned
     # bodies go to the TMA kernel, the few elements around each boundary and
     # the misaligned members to the register kernel.
-    # "hook": float32 gradients through the fused bf16 compression hook
-    hook = dtype == "hook"
+    # "hook" / "hook16": float32 gradients through the fused bf16 / fp16
+    # compression hook
+    hook = dtype if dtype in ("hook", "hook16") else None
     if hook:
         dtype = "f32"
     world = 8
@@ -459,19 +469,21 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     code = oracle.BF16 if dtype == "bf16" else oracle.F32
     for div in (world, 3):
         grads_h = [[f32_or_bits(t) for t in dev[r]] for r in range(world)]
-        if hook:
+        if hook == "hook":
             ddp.ddp_bucket_allreduce_view_bf16(dev, offsets, total, div)
+        elif hook == "hook16":
+            ddp.ddp_bucket_allreduce_view_fp16(dev, offsets, total, div)
         else:
             ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
         torch.cuda.synchronize()
         if hook:
-            _oracle_view_hook(grads_h, offsets, total, div)
+            _oracle_view_hook(grads_h, offsets, total, div, fp16=hook == "hook16")
         else:
             _oracle_view(grads_h, offsets, total, code, div)
         for r in range(world):
             for i in range(len(numels)):
                 assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i],
-                                  f"{layout} {'hook' if hook else dtype} div={div} r{r} m{i}")
+                                  f"{layout} {hook or dtype} div={div} r{r} m{i}")
     assert ddp.ddp_device_status() == 0
 
 
@@ -517,3 +529,23 @@ def test_readme_python_example_runs():
     torch.cuda.synchronize()
     for r in range(1, 4):                      # every sync leaves all ranks identical
         assert torch.equal(g[r], g[0]) and torch.equal(x[r], x[0])
+
+
+def test_fp16_hook_view_overflow_and_subnormals_match_oracle():
+    # binary16 range edges: sums past 65504 become infinity, values below
+    # 2^-14 become subnormal or zero -- exactly as the oracle's binary16
+    world, n = 4, 4096
+    rng = np.random.default_rng(13)
+    scale = np.where(np.arange(n) % 3 == 0, 3.0e4, np.where(np.arange(n) % 3 == 1, 1e-6, 1.0)).astype(np.float32)
+    x = (rng.standard_normal((world, n)).astype(np.float32) * scale).astype(np.float32)
+    big = np.arange(n) % 3 == 0
+    x[:, big] = np.abs(x[:, big])      # one sign: infinities add up, never to NaN (NaN payloads are not compared)
+    grads_h = [[x[r].copy()] for r in range(world)]
+    g = torch.from_numpy(x.copy()).cuda()
+    ddp.ddp_bucket_allreduce_view_fp16([[g[r]] for r in range(world)], [0], n, 0)
+    torch.cuda.synchronize()
+    oracle.ddp_sync_fp16_hook(grads_h, 1 << 40, 1 << 40, divisor=0)
+    got = f32_or_bits(g)
+    want = np.stack([grads_h[r][0] for r in range(world)])
+    assert np.isinf(want).any() and (np.abs(want[want != 0]) < 6.2e-5).any()
+    assert_bits_equal(got, want, "fp16 hook at the binary16 range edges")
