@@ -300,15 +300,23 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.mark_start()
+    # one event after every step as well: the per-step distribution (median,
+    # p90) beside the whole-region mean; recording events adds no device work
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         ddp.ring_allreduce_fused(x, N)
+        step_ev[i].record(stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark_end()
     barrier()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    per_step = sorted([ev0.elapsed_time(step_ev[0])] +
+                      [step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, args.steps)])
+    step_median = per_step[len(per_step) // 2]
+    step_p90 = per_step[min(len(per_step) - 1, (len(per_step) * 9) // 10)]
     if sampler:
         sampler.stop()
     ms_step = ms / args.steps
@@ -320,7 +328,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         traffic = traffic * numel / NUMEL
 
     out = {"metric": METRIC, "value": busbw_total, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+           "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": step_median,
+           "ms_per_step_p90": step_p90, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"N={N} logical ranks, one fp32 bucket of {numel} elements "
                                   f"({s_bytes / MiB:.0f} MiB) per rank, fused ring allreduce / {N}",
