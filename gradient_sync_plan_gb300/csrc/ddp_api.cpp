@@ -379,6 +379,85 @@ int32_t view_members(int32_t world, int32_t n, void* const* grads, const int64_t
 
 }  // namespace
 
+namespace {
+
+// One bucket of the unfused pipeline (pack -> fused ring -> unpack) run in
+// pieces that fit in L2: for each piece [a, b) of the bucket, the members'
+// parts that fall in it are packed, the piece is reduced by the view kernel
+// with its bucket offset (so every element is folded in the ring order of its
+// chunk of the whole bucket -- the same bits as the ring over the whole
+// bucket), and unpacked, before the next piece is packed.  The ring and the
+// unpack then read the piece from L2 instead of HBM.  Arguments are checked by
+// the caller.  Buckets no larger than one and a half pieces run whole.
+constexpr int64_t kPieceBytesAllRanks = (int64_t)96 << 20;   // bucket bytes over all ranks per piece
+
+int64_t bucket_piece_elems(int32_t world, int32_t dtype) {
+    const int64_t es = elem_bytes(dtype);
+    int64_t piece = kPieceBytesAllRanks / world / es;
+    piece = piece / 1024 * 1024;                                 // pieces start 16-byte aligned
+    return std::max<int64_t>(piece, 64 * 1024);
+}
+
+cudaError_t sync_bucket_pieces(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                               void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, bool vec,
+                               cudaStream_t s) {
+    const int64_t es = elem_bytes(dtype);
+    const int64_t piece = bucket_piece_elems(world, dtype);
+    const DivSpec div = make_div(divisor);
+    std::vector<CopyItem> in, out;
+    std::vector<void*> ptrs(world);
+    for (int64_t a = 0; a < bucket_numel; a += piece) {
+        const int64_t b = std::min(bucket_numel, a + piece);
+        in.clear();
+        out.clear();
+        for (int32_t r = 0; r < world; ++r)
+            for (int32_t i = 0; i < n; ++i) {
+                const int64_t s0 = std::max(off[i], a), s1 = std::min(off[i] + ne[i], b);
+                if (s1 <= s0) continue;
+                const char* gp = static_cast<const char*>(g[(int64_t)r * n + i]) + (s0 - off[i]) * es;
+                char* bp = static_cast<char*>(bk[r]) + s0 * es;
+                in.push_back(CopyItem{gp, bp, (s1 - s0) * es});
+                out.push_back(CopyItem{bp, const_cast<char*>(gp), (s1 - s0) * es});
+            }
+        cudaError_t e = launch_copy_items(in.data(), (int64_t)in.size(), s);
+        if (e != cudaSuccess) return e;
+        for (int32_t r = 0; r < world; ++r) ptrs[r] = static_cast<char*>(bk[r]) + a * es;
+        ViewMember m{b - a, a, ptrs.data(), vec};
+        if ((e = launch_bucket_view(world, &m, 1, bucket_numel, dtype, div, s)) != cudaSuccess) return e;
+        if ((e = launch_copy_items(out.data(), (int64_t)out.size(), s)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+namespace ddpk {
+
+// ddp_sync_buckets' and the reducer's unfused fused-ring path for one bucket:
+// validated, then whole or in pieces.
+int32_t pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                         void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, void* stream) {
+    std::vector<CopyItem> items;
+    int32_t st = bucket_items(world, n, g, ne, off, (const void* const*)bk, bucket_numel, dtype, true, &items);
+    if (st) return st;
+    if (divisor < 0) return DDP_ERR_INVALID;
+    if (bucket_numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, bk, bucket_numel, dtype, &vec))) return st;
+    const int64_t piece = bucket_piece_elems(world, dtype);
+    if (bucket_numel <= piece + piece / 2) {
+        if ((st = cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream))))
+            return st;
+        if ((st = ring_allreduce_fused(world, bk, bucket_numel, dtype, divisor, stream))) return st;
+        return ddp_bucket_unpack(world, n, const_cast<void* const*>(g), ne, off, (const void* const*)bk, bucket_numel,
+                                 dtype, stream);
+    }
+    return cuda_status(
+        sync_bucket_pieces(world, n, g, ne, off, bk, bucket_numel, dtype, divisor, vec, (cudaStream_t)stream));
+}
+
+}  // namespace ddpk
+
 extern "C" {
 
 const char* ddp_status_string(int32_t status) {
@@ -747,15 +826,19 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             if (st) return st;
             continue;
         }
-        st = ddp_bucket_pack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], dtype, stream);
-        if (st) return st;
-        st = (algo == DDP_ALGO_FUSED)
-                 ? ring_allreduce_fused(world, bk.data(), bucket_numel[k], dtype, divisor, stream)
-                 : ring_allreduce_staged(world, bk.data(), bucket_numel[k], dtype, divisor, stream);
-        if (st) return st;
-        st = ddp_bucket_unpack(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
-                               (const void* const*)bk.data(), bucket_numel[k], dtype, stream);
-        if (st) return st;
+        if (algo == DDP_ALGO_FUSED) {
+            st = pack_ring_unpack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], dtype, divisor,
+                                  stream);
+            if (st) return st;
+        } else {
+            st = ddp_bucket_pack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], dtype, stream);
+            if (st) return st;
+            st = ring_allreduce_staged(world, bk.data(), bucket_numel[k], dtype, divisor, stream);
+            if (st) return st;
+            st = ddp_bucket_unpack(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
+                                   (const void* const*)bk.data(), bucket_numel[k], dtype, stream);
+            if (st) return st;
+        }
         if (debug_enabled())
             fprintf(stderr, "[ddp] bucket %d: %d members, %lld elements\n", k, n, (long long)bucket_numel[k]);
     }

@@ -23,6 +23,12 @@
 #include "ddp.h"
 #include "ddp_trace.h"
 
+namespace ddpk {
+// ddp_api.cpp: one bucket's pack -> fused ring -> unpack, in L2-sized pieces when large
+int32_t pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                         void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, void* stream);
+}  // namespace ddpk
+
 struct ddp_reducer {
     int32_t world = 0, n_params = 0, n_buckets = 0, dtype = 0, divisor = 0, algo = 0;
     cudaStream_t comm = nullptr;
@@ -69,11 +75,12 @@ int32_t sync_bucket(ddp_reducer* r, int32_t k) {
         if (st) return st;
         return ddp_bucket_unpack_bf16(r->world, n, g, ne, off, (const void* const*)b, r->bucket_numel[k], r->comm);
     }
+    if (r->algo == DDP_ALGO_FUSED)
+        return ddpk::pack_ring_unpack(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->dtype,
+                                      r->divisor, r->comm);
     int32_t st = ddp_bucket_pack(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->dtype, r->comm);
     if (st) return st;
-    st = (r->algo == DDP_ALGO_STAGED)
-             ? ring_allreduce_staged(r->world, b, r->bucket_numel[k], r->dtype, r->divisor, r->comm)
-             : ring_allreduce_fused(r->world, b, r->bucket_numel[k], r->dtype, r->divisor, r->comm);
+    st = ring_allreduce_staged(r->world, b, r->bucket_numel[k], r->dtype, r->divisor, r->comm);
     if (st) return st;
     return ddp_bucket_unpack(r->world, n, g, ne, off, (const void* const*)b, r->bucket_numel[k], r->dtype, r->comm);
 }

@@ -549,3 +549,36 @@ def test_fp16_hook_view_overflow_and_subnormals_match_oracle():
     want = np.stack([grads_h[r][0] for r in range(world)])
     assert np.isinf(want).any() and (np.abs(want[want != 0]) < 6.2e-5).any()
     assert_bits_equal(got, want, "fp16 hook at the binary16 range edges")
+
+
+@pytest.mark.parametrize("via", ["sync_buckets", "reducer"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_large_bucket_in_l2_pieces_matches_oracle(via, dtype):
+    # a bucket of more than two L2-sized pieces (96 MiB over all ranks each):
+    # members of odd sizes straddle the piece boundaries and chunk boundaries;
+    # pack / ring / unpack run piece by piece and must give the oracle's bits
+    world = 4
+    es = 2 if dtype == "bf16" else 4
+    piece = (96 << 20) // world // es // 1024 * 1024
+    numels = [3, piece - 5, 7, piece + 11, 1001, piece // 3 + 17, 13]
+    code = ddp.BF16 if dtype == "bf16" else ddp.F32
+    plan = ddp.ddp_plan_buckets(numels, code, 1 << 40, 1 << 40)
+    assert len(plan[2]) == 1 and plan[2][0] > 2 * piece
+    flat, grads_h = _host_grads(numels, world, dtype, seed0=81)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    bk = [[torch.empty(int(plan[2][0]), dtype=tdt, device="cuda")] for _ in range(world)]
+    if via == "sync_buckets":
+        ddp.ddp_sync_buckets(views, plan, bk, algo=ddp.DDP_ALGO_FUSED)
+    else:
+        red = ddp.Reducer(views, plan, bk, algo=ddp.DDP_ALGO_FUSED, comm_stream=torch.cuda.Stream())
+        for p in range(len(numels) - 1, -1, -1):
+            red.mark_ready(p, torch.cuda.current_stream())
+        red.finalize(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    oracle.ddp_sync(grads_h, code, 1 << 40, 1 << 40)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"pieces {dtype} via {via}")
+    if via == "reducer":
+        red.close()
