@@ -12,6 +12,9 @@ Against the oracle's own composition of the same steps (``oracle.ddp_sync``,
   * the 355M-parameter decoder, N = 8, 25 MiB / 1 MiB caps, with and without
     no_sync accumulation of 4 micro-batches (sampled comparison: inputs made
     on the device, sampled inputs snapshot before the sync).
+  * buckets larger than L2, which the unfused path runs in L2-sized pieces:
+    members straddling piece and chunk boundaries, and sizes on both sides
+    of the switch between whole buckets and pieces.
 """
 import numpy as np
 import pytest
@@ -582,3 +585,28 @@ def test_large_bucket_in_l2_pieces_matches_oracle(via, dtype):
     assert_bits_equal(f32_or_bits(g), want, f"pieces {dtype} via {via}")
     if via == "reducer":
         red.close()
+
+
+@pytest.mark.parametrize("world", [3, 8])
+@pytest.mark.parametrize("extra", [0, 1])
+def test_pieces_switch_boundary_matches_oracle(world, extra):
+    # a bucket of exactly 1.5 pieces runs whole; one element more runs in two
+    # pieces (p and p/2 + 1).  At world 3 with the extra element the chunk
+    # length is odd, so chunk boundaries inside the pieces are not 16-byte
+    # aligned and the view kernel's edge path runs too.  Both must give the
+    # oracle's bits.
+    es = 4
+    piece = max((96 << 20) // world // es // 1024 * 1024, 64 * 1024)
+    total = piece + piece // 2 + extra
+    numels = [12345, total - 12345]
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, 1 << 40, 1 << 40)
+    assert list(plan[2]) == [total]
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=97)
+    g = flat.cuda()
+    views = _device_views(g, numels)
+    bk = [[torch.empty(total, dtype=torch.float32, device="cuda")] for _ in range(world)]
+    ddp.ddp_sync_buckets(views, plan, bk, algo=ddp.DDP_ALGO_FUSED)
+    torch.cuda.synchronize()
+    oracle.ddp_sync(grads_h, oracle.F32, 1 << 40, 1 << 40)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    assert_bits_equal(f32_or_bits(g), want, f"pieces boundary world={world} extra={extra}")
