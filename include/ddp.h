@@ -433,6 +433,15 @@ typedef enum {
  *                              dtype, bf16 `buckets`)
  * The same plan must be used on every rank (one plan is shared here by
  * construction).  DDP_ERR_INVALID if the plan is inconsistent.
+ *
+ * With DDP_ALGO_FUSED, a bucket whose bytes over all ranks exceed 1.5 pieces
+ * of 96 MiB (more than the GPU's L2) runs piece by piece: each piece's slice
+ * of the members is packed, the slice is reduced by the view pass at its
+ * bucket offset (so every element is folded in the ring order of its chunk
+ * of the WHOLE bucket), and the slice is unpacked before the next piece is
+ * packed.  The result, in the gradients and in the bucket buffers, is
+ * bit-identical to the whole-bucket pack -> ring -> unpack; only the HBM
+ * traffic falls, since each piece is read back from L2.
  */
 int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
                          const int32_t* bucket_of_param, const int64_t* offset_of_param,
@@ -481,10 +490,13 @@ int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* cons
  *
  *   grads[world*n_params], numel, bucket_of_param, offset_of_param,
  *   bucket_numel, buckets[world*n_buckets]  as for ddp_sync_buckets (buckets may
- *                         be NULL for DDP_ALGO_VIEW and DDP_ALGO_DRYRUN, grads
- *                         for DDP_ALGO_DRYRUN); the reducer keeps these pointers
- *                         until it is destroyed, the caller keeps the memory
- *   algo                  DDP_ALGO_FUSED, _STAGED, _VIEW or _DRYRUN
+ *                         be NULL for DDP_ALGO_VIEW, the fused hooks and
+ *                         DDP_ALGO_DRYRUN, grads for DDP_ALGO_DRYRUN); the
+ *                         reducer keeps these pointers until it is destroyed,
+ *                         the caller keeps the memory
+ *   algo                  any ddp_algo; each bucket's sync is the one
+ *                         ddp_sync_buckets runs for that algo (pieces
+ *                         included), the hooks with a float32 dtype
  *   comm_stream           cudaStream_t on which the buckets' syncs run
  * The reducer owns host memory and three CUDA events per bucket (readiness
  * and two timing events; created here, destroyed by ddp_reducer_destroy); it
