@@ -35,7 +35,7 @@ FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
 BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
 
 STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_CUDA",
-          -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY"}
+          -4: "DDP_ERR_TIMEOUT", -5: "DDP_ERR_CAPACITY", -6: "DDP_ERR_HOST"}
 
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",

@@ -17,6 +17,7 @@
 #include <utility>
 #include <vector>
 
+#include "ddp_abi_guard.h"
 #include "ddp.h"
 #include "ddp_trace.h"
 #include "ddp_internal.h"
@@ -469,6 +470,7 @@ const char* ddp_status_string(int32_t status) {
         case DDP_ERR_CUDA: return "DDP_ERR_CUDA: a CUDA call or kernel launch failed";
         case DDP_ERR_TIMEOUT: return "DDP_ERR_TIMEOUT: a bounded device-side wait gave up";
         case DDP_ERR_CAPACITY: return "DDP_ERR_CAPACITY: size beyond a documented limit";
+        case DDP_ERR_HOST: return "DDP_ERR_HOST: host memory allocation failed inside the library";
         default: return "unknown ddp_status";
     }
 }
@@ -477,30 +479,30 @@ int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
 
 const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
 
-int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) {
+int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) try {
     DDP_TRACE_CALL();
     if (max_ctas < 0) return DDP_ERR_INVALID;
     const int prev = g_max_ctas.exchange(max_ctas);
     if (previous) *previous = prev;
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) {
+int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) try {
     DDP_TRACE_CALL();
     if (kind < DDP_FUSED_AUTO || kind > DDP_FUSED_TMA) return DDP_ERR_INVALID;
     const int prev = g_fused_kernel.exchange(kind);
     if (previous) *previous = prev;
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_device_status(int32_t* status, int32_t clear) {
+int32_t ddp_device_status(int32_t* status, int32_t clear) try {
     DDP_TRACE_CALL();
     if (!status) return DDP_ERR_INVALID;
     return cuda_status(read_device_status(status, clear != 0));
-}
+} DDP_ABI_CATCH
 
 int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                             void* stream) {
+                             void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -509,10 +511,10 @@ int32_t ring_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, in
     bool vec = false;
     if ((st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
     return cuda_status(launch_ring_fused(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                              void* stream) {
+                              void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -521,7 +523,7 @@ int32_t ring_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, i
     bool vec = false;
     if ((st = check_rank_buffers(world, bufs, numel, dtype, &vec))) return st;
     return cuda_status(launch_ring_staged(world, bufs, numel, dtype, make_div(divisor), vec, (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 static int32_t tree_common(bool staged, int32_t world, void* const* bufs, int64_t numel, int32_t dtype,
                            int32_t divisor, void* stream) {
@@ -537,19 +539,19 @@ static int32_t tree_common(bool staged, int32_t world, void* const* bufs, int64_
 }
 
 int32_t tree_allreduce_fused(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                             void* stream) {
+                             void* stream) try {
     DDP_TRACE_CALL();
     return tree_common(false, world, bufs, numel, dtype, divisor, stream);
-}
+} DDP_ABI_CATCH
 
 int32_t tree_allreduce_staged(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                              void* stream) {
+                              void* stream) try {
     DDP_TRACE_CALL();
     return tree_common(true, world, bufs, numel, dtype, divisor, stream);
-}
+} DDP_ABI_CATCH
 
 int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                                  int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream) {
+                                  int32_t* dev_status, int32_t fail_at_step, int32_t wait_limit_ms, void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -569,11 +571,11 @@ int32_t ring_allreduce_persistent(int32_t world, void* const* bufs, int64_t nume
     const unsigned long long limit = (unsigned long long)(wait_limit_ms ? wait_limit_ms : 2000) * 1000000ull;
     return cuda_status(launch_ring_persistent(world, bufs, numel, dtype, make_div(divisor), vec, dev_status,
                                               fail_at_step, limit, s));
-}
+} DDP_ABI_CATCH
 
 int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in, void* const* host_out,
                                        void* const* dev_bufs, int64_t numel, int32_t dtype, int32_t divisor,
-                                       void* stream) {
+                                       void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -603,7 +605,7 @@ int32_t ring_allreduce_fused_from_host(int32_t world, const void* const* host_in
         return DDP_OK;
     }
     return cuda_status(from_host_pipelined(world, host_in, host_out, dev_bufs, numel, dtype, divisor, vec, piece, s));
-}
+} DDP_ABI_CATCH
 
 // Device address through which the GPU reaches host buffer p, or nullptr
 // if it cannot reach it: pinned (page-locked, mapped) memory, managed or
@@ -624,7 +626,7 @@ static void* device_view_of(const void* p) {
 }
 
 int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_in, void* const* host_out,
-                                         int64_t numel, int32_t dtype, int32_t divisor, void* stream) {
+                                         int64_t numel, int32_t dtype, int32_t divisor, void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -641,10 +643,10 @@ int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_
     }
     return cuda_status(launch_ring_fused_io(world, din.data(), dout.data(), numel, dtype, make_div(divisor), vec,
                                             (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* grads, int64_t numel,
-                            int32_t dtype, void* stream) {
+                            int32_t dtype, void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, numel, dtype);
     if (st) return st;
@@ -653,49 +655,49 @@ int32_t ddp_grad_accumulate(int32_t world, void* const* acc, const void* const* 
     if ((st = check_rank_buffers(world, acc, numel, dtype, &va))) return st;
     if ((st = check_rank_buffers(world, grads, numel, dtype, &vg))) return st;
     return cuda_status(launch_accumulate(world, acc, grads, numel, dtype, va && vg, (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_pack(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
                         const int64_t* offset, void* const* buckets, int64_t bucket_numel, int32_t dtype,
-                        void* stream) {
+                        void* stream) try {
     DDP_TRACE_CALL();
     std::vector<CopyItem> items;
     int32_t st = bucket_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel,
                               dtype, true, &items);
     if (st) return st;
     return cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_unpack(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                           const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
-                          void* stream) {
+                          void* stream) try {
     DDP_TRACE_CALL();
     std::vector<CopyItem> items;
     int32_t st = bucket_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel,
                               dtype, false, &items);
     if (st) return st;
     return cuda_status(launch_copy_items(items.data(), (int64_t)items.size(), (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_pack_bf16(int32_t world, int32_t n_in_bucket, const void* const* grads, const int64_t* numel,
-                             const int64_t* offset, void* const* buckets, int64_t bucket_numel, void* stream) {
+                             const int64_t* offset, void* const* buckets, int64_t bucket_numel, void* stream) try {
     DDP_TRACE_CALL();
     std::vector<ConvItem> items;
     int32_t st = hook_items(world, n_in_bucket, grads, numel, offset, (const void* const*)buckets, bucket_numel, true,
                             &items);
     if (st) return st;
     return cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 1, (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_unpack_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
-                               const int64_t* offset, const void* const* buckets, int64_t bucket_numel, void* stream) {
+                               const int64_t* offset, const void* const* buckets, int64_t bucket_numel, void* stream) try {
     DDP_TRACE_CALL();
     std::vector<ConvItem> items;
     int32_t st = hook_items(world, n_in_bucket, (const void* const*)grads, numel, offset, buckets, bucket_numel, false,
                             &items);
     if (st) return st;
     return cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 0, (cudaStream_t)stream));
-}
+} DDP_ABI_CATCH
 
 static int32_t view_one(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                         const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t launch_dtype,
@@ -720,27 +722,27 @@ static int32_t view_one(int32_t world, int32_t n_in_bucket, void* const* grads, 
 
 int32_t ddp_bucket_allreduce_view(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
                                   const int64_t* offset, int64_t bucket_numel, int32_t dtype, int32_t divisor,
-                                  void* stream) {
+                                  void* stream) try {
     DDP_TRACE_CALL();
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, dtype, dtype, divisor, stream);
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_allreduce_view_bf16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
-                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) {
+                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) try {
     DDP_TRACE_CALL();
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook, divisor, stream);
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_bucket_allreduce_view_fp16(int32_t world, int32_t n_in_bucket, void* const* grads, const int64_t* numel,
-                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) {
+                                       const int64_t* offset, int64_t bucket_numel, int32_t divisor, void* stream) try {
     DDP_TRACE_CALL();
     return view_one(world, n_in_bucket, grads, numel, offset, bucket_numel, DDP_F32, kDtypeHook16, divisor, stream);
-}
+} DDP_ABI_CATCH
 
 int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel,
                          const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
                          const int64_t* bucket_numel, void* const* buckets, int32_t dtype, int32_t divisor,
-                         int32_t algo, void* stream) {
+                         int32_t algo, void* stream) try {
     DDP_TRACE_CALL();
     int32_t st = common_checks(world, 0, dtype);
     if (st) return st;
@@ -843,6 +845,6 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
             fprintf(stderr, "[ddp] bucket %d: %d members, %lld elements\n", k, n, (long long)bucket_numel[k]);
     }
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
 }  // extern "C"

@@ -13,13 +13,14 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "ddp_abi_guard.h"
 #include "ddp.h"
 #include "ddp_trace.h"
 
 extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int32_t dtype,
                                     int64_t first_bucket_bytes, int64_t bucket_cap_bytes,
                                     int32_t* bucket_of_param, int64_t* offset_of_param, int64_t* bucket_numel,
-                                    int32_t* n_buckets) {
+                                    int32_t* n_buckets) try {
     DDP_TRACE_CALL();
     if (!n_buckets || n_params < 0) return DDP_ERR_INVALID;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
@@ -56,7 +57,7 @@ extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int3
                          (long long)(bucket_numel[k] * esize));
     }
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
 // 64-bit FNV-1a over the plan's integers, each fed as 8 little-endian bytes
 // (the byte order is fixed here, so hosts of either endianness agree).
@@ -75,7 +76,7 @@ struct Fnv64 {
 
 extern "C" int32_t ddp_plan_fingerprint(int32_t n_params, const int64_t* numel, int32_t dtype,
                                         const int32_t* bucket_of_param, const int64_t* offset_of_param,
-                                        int32_t n_buckets, const int64_t* bucket_numel, uint64_t* fingerprint) {
+                                        int32_t n_buckets, const int64_t* bucket_numel, uint64_t* fingerprint) try {
     DDP_TRACE_CALL();
     if (!fingerprint || n_params < 0 || n_buckets < 0) return DDP_ERR_INVALID;
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
@@ -93,4 +94,4 @@ extern "C" int32_t ddp_plan_fingerprint(int32_t n_params, const int64_t* numel, 
     for (int32_t k = 0; k < n_buckets; ++k) f.add(bucket_numel[k]);
     *fingerprint = f.h;
     return DDP_OK;
-}
+} DDP_ABI_CATCH

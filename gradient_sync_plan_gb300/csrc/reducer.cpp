@@ -16,10 +16,12 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <memory>
 #include <mutex>
 #include <new>
 #include <vector>
 
+#include "ddp_abi_guard.h"
 #include "ddp.h"
 #include "ddp_trace.h"
 
@@ -134,7 +136,7 @@ extern "C" {
 int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, const int64_t* numel, int32_t dtype,
                            const int32_t* bucket_of_param, const int64_t* offset_of_param, int32_t n_buckets,
                            const int64_t* bucket_numel, void* const* buckets, int32_t algo, int32_t divisor,
-                           void* comm_stream, ddp_reducer** out) {
+                           void* comm_stream, ddp_reducer** out) try {
     DDP_TRACE_CALL();
     if (!out) return DDP_ERR_INVALID;
     *out = nullptr;
@@ -152,8 +154,10 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     const bool needs_buckets = algo == DDP_ALGO_FUSED || algo == DDP_ALGO_STAGED || algo == DDP_ALGO_BF16_HOOK;
     if (needs_buckets && n_buckets > 0 && !buckets) return DDP_ERR_INVALID;
 
-    ddp_reducer* r = new (std::nothrow) ddp_reducer();
-    if (!r) return DDP_ERR_CAPACITY;
+    // owned by `holder` until the reducer is complete: an early return or a
+    // failed host allocation below frees it
+    std::unique_ptr<ddp_reducer> holder(new ddp_reducer());
+    ddp_reducer* r = holder.get();
     r->world = world;
     r->n_params = n_params;
     r->n_buckets = n_buckets;
@@ -167,7 +171,6 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     for (int32_t p = 0; p < n_params; ++p) {
         const int32_t k = bucket_of_param[p];
         if (k < 0 || k >= n_buckets) {
-            delete r;
             return DDP_ERR_INVALID;
         }
         members[k].push_back(p);
@@ -189,7 +192,6 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
         for (int32_t i = 0; i < n; ++i) {
             const int64_t o = offset_of_param[m[i]], e = numel[m[i]];
             if (e < 0 || o < 0 || o > r->bucket_numel[k] - e || (e > 0 && o < end)) {
-                delete r;
                 return DDP_ERR_INVALID;
             }
             if (e > 0) end = o + e;
@@ -218,29 +220,27 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
             if (cudaEventCreateWithFlags(&r->ready_ev[k], cudaEventDisableTiming) != cudaSuccess ||
                 cudaEventCreate(&r->t0_ev[k]) != cudaSuccess || cudaEventCreate(&r->t1_ev[k]) != cudaSuccess) {
                 destroy_events(r);
-                delete r;
                 return DDP_ERR_CUDA;
             }
         if (cudaEventCreateWithFlags(&r->done_ev, cudaEventDisableTiming) != cudaSuccess) {
             destroy_events(r);
-            delete r;
             return DDP_ERR_CUDA;
         }
     }
     reset_step(r);
-    *out = r;
+    *out = holder.release();
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_prepare(ddp_reducer* r) {
+int32_t ddp_reducer_prepare(ddp_reducer* r) try {
     DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     reset_step(r);
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* compute_stream) {
+int32_t ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* compute_stream) try {
     DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
@@ -254,9 +254,9 @@ int32_t ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* compute_stre
     const int32_t st = launch_ready_prefix(r);
     if (st && r->first_error == DDP_OK) r->first_error = st;
     return st;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_finalize(ddp_reducer* r, void* stream) {
+int32_t ddp_reducer_finalize(ddp_reducer* r, void* stream) try {
     DDP_TRACE_CALL();
     if (!r) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
@@ -275,18 +275,18 @@ int32_t ddp_reducer_finalize(ddp_reducer* r, void* stream) {
     if (cudaEventRecord(r->done_ev, r->comm) != cudaSuccess) return DDP_ERR_CUDA;
     if (cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), r->done_ev, 0) != cudaSuccess) return DDP_ERR_CUDA;
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_launch_order(ddp_reducer* r, int32_t* order, int32_t capacity, int32_t* n) {
+int32_t ddp_reducer_launch_order(ddp_reducer* r, int32_t* order, int32_t capacity, int32_t* n) try {
     DDP_TRACE_CALL();
     if (!r || !n || capacity < 0 || (capacity > 0 && !order)) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
     *n = (int32_t)r->launch_log.size();
     for (int32_t i = 0; i < std::min(*n, capacity); ++i) order[i] = r->launch_log[i];
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_bucket_times(ddp_reducer* r, float* ms, int32_t capacity, int32_t* n) {
+int32_t ddp_reducer_bucket_times(ddp_reducer* r, float* ms, int32_t capacity, int32_t* n) try {
     DDP_TRACE_CALL();
     if (!r || !n || capacity < 0 || (capacity > 0 && !ms)) return DDP_ERR_INVALID;
     std::lock_guard<std::mutex> lk(r->mu);
@@ -298,14 +298,14 @@ int32_t ddp_reducer_bucket_times(ddp_reducer* r, float* ms, int32_t capacity, in
         if (cudaEventElapsedTime(&ms[k], r->t0_ev[k], r->t1_ev[k]) != cudaSuccess) return DDP_ERR_CUDA;
     }
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
-int32_t ddp_reducer_destroy(ddp_reducer* r) {
+int32_t ddp_reducer_destroy(ddp_reducer* r) try {
     DDP_TRACE_CALL();
     if (!r) return DDP_OK;
     destroy_events(r);
     delete r;
     return DDP_OK;
-}
+} DDP_ABI_CATCH
 
 }  // extern "C"

@@ -24,6 +24,7 @@
 #include <map>
 #include <mutex>
 
+#include "ddp_abi_guard.h"
 #include "ddp.h"
 #include "ddp_internal.h"
 #include "ddp_trace.h"
@@ -68,7 +69,7 @@ cudaError_t scratch_on_current_device(unsigned char** out) {
 
 extern "C" int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const void* const* host_in,
                                                           void* const* host_out, int64_t numel, int32_t dtype,
-                                                          int32_t divisor, void* stream) {
+                                                          int32_t divisor, void* stream) try {
     DDP_TRACE_CALL();
     if (world < 1 || numel < 0 || divisor < 0) return DDP_ERR_INVALID;
     if (world > DDP_MAX_WORLD) return DDP_ERR_CAPACITY;
@@ -98,4 +99,4 @@ extern "C" int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const v
         if (cudaMemcpyAsync(host_out[r], dev[r], (size_t)bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
             return DDP_ERR_CUDA;
     return DDP_OK;
-}
+} DDP_ABI_CATCH

@@ -36,7 +36,9 @@
  *   - Errors: the return value is a ddp_status.  A negative status from
  *     argument checking means that nothing was enqueued.  DDP_ERR_CUDA means
  *     a CUDA call or launch failed; some of the call's work may have been
- *     enqueued before the failure.
+ *     enqueued before the failure.  DDP_ERR_HOST means the library could not
+ *     allocate host memory for its tables; as with DDP_ERR_CUDA, work before
+ *     that point may have been enqueued.
  *   - Dtypes: DDP_F32 (IEEE binary32) or DDP_BF16 (bfloat16).  Element
  *     pointers must be aligned to the element size (DDP_ERR_ALIGN otherwise);
  *     16-byte aligned buffers take the vectorised paths, others a slower
@@ -64,7 +66,9 @@ typedef enum {
     DDP_ERR_ALIGN = -2,      /* a pointer is not aligned to its element size    */
     DDP_ERR_CUDA = -3,       /* a CUDA runtime call or a kernel launch failed    */
     DDP_ERR_TIMEOUT = -4,    /* a bounded device-side wait gave up (status word) */
-    DDP_ERR_CAPACITY = -5    /* a size exceeds a documented limit               */
+    DDP_ERR_CAPACITY = -5,   /* a size exceeds a documented limit               */
+    DDP_ERR_HOST = -6        /* the library's host code failed (out of host
+                                memory); no C++ exception leaves the library   */
 } ddp_status;
 
 typedef enum { DDP_F32 = 0, DDP_BF16 = 1 } ddp_dtype;

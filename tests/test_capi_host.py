@@ -40,6 +40,33 @@ def test_abi_version_and_status_strings():
         assert ddp.ddp_status_string(code).startswith(name)
 
 
+def test_status_codes_match_the_header():
+    hdr = open(os.path.join(ROOT, "include", "ddp.h")).read()
+    enum = hdr[hdr.index("typedef enum {\n    DDP_OK"):hdr.index("} ddp_status;")]
+    codes = {int(v): "DDP_" + n for n, v in re.findall(r"DDP_(OK|ERR_[A-Z]+) = (-?\d+)", enum)}
+    assert codes == ddp.STATUS
+
+
+def test_every_status_entry_point_catches_exceptions():
+    # an exception must not unwind into a C caller: every multi-line int32_t
+    # entry point is a function-try-block ending in DDP_ABI_CATCH
+    csrc = os.path.join(ROOT, "gradient_sync_plan_gb300", "csrc")
+    guarded = set()
+    for f in os.listdir(csrc):
+        if not f.endswith((".cpp", ".cu")):
+            continue
+        src = open(os.path.join(csrc, f)).read()
+        regions = re.findall(r'extern "C" \{\n(.*?)\n\}  // extern "C"', src, re.S)
+        regions += re.findall(r'extern "C" (int32_t \w+\(.*?\n\}[^\n]*)', src, re.S)
+        for reg in regions:
+            for m in re.finditer(r"^(?:extern \"C\" )?int32_t (\w+)\(([^;{}]*?)\)( try)? \{\n", reg, re.S | re.M):
+                assert m.group(3), f"{f}: {m.group(1)} is not a function-try-block"
+                guarded.add(m.group(1))
+    one_liners = {"ddp_abi_version"}
+    int_exports = {n for n in ddp.EXPORTS if n not in ("ddp_status_string", "ddp_last_cuda_error")}
+    assert int_exports - guarded == one_liners
+
+
 def test_library_is_the_in_tree_build():
     L = ddp.lib()
     assert os.path.dirname(os.path.abspath(ddp.library_path())).startswith(ROOT)
