@@ -153,7 +153,7 @@ int32_t check_rank_buffers(int32_t world, const void* const* bufs, int64_t numel
 int32_t common_checks(int32_t world, int64_t numel, int32_t dtype) {
     if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
     if (numel < 0 || !valid_dtype(dtype)) return DDP_ERR_INVALID;
-    if (numel > (int64_t)1 << 40) return DDP_ERR_CAPACITY;
+    if (numel > DDP_MAX_NUMEL) return DDP_ERR_CAPACITY;
     return DDP_OK;
 }
 
@@ -275,9 +275,9 @@ cudaError_t from_host_pipelined(int32_t world, const void* const* host_in, void*
 int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel,
                      const int64_t* offset, const void* const* buckets, int64_t bucket_numel, int32_t dtype,
                      bool to_bucket, std::vector<CopyItem>* items) {
-    int32_t st = common_checks(world, 0, dtype);
+    int32_t st = common_checks(world, bucket_numel, dtype);     // also caps bucket_numel, so byte sizes fit
     if (st) return st;
-    if (n < 0 || bucket_numel < 0) return DDP_ERR_INVALID;
+    if (n < 0) return DDP_ERR_INVALID;
     if (n > 0 && (!grads || !numel || !offset || !buckets)) return DDP_ERR_INVALID;
     const int64_t es = elem_bytes(dtype);
     // members must lie inside the bucket and not overlap each other
@@ -313,8 +313,9 @@ int32_t bucket_items(int32_t world, int32_t n, const void* const* grads, const i
 // Members of one bucket for the bf16 hook: float32 gradients, bf16 bucket.
 int32_t hook_items(int32_t world, int32_t n, const void* const* grads, const int64_t* numel, const int64_t* offset,
                    const void* const* buckets, int64_t bucket_numel, bool to_bucket, std::vector<ConvItem>* items) {
-    if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
-    if (n < 0 || bucket_numel < 0) return DDP_ERR_INVALID;
+    int32_t st = common_checks(world, bucket_numel, DDP_F32);   // also caps bucket_numel, so byte sizes fit
+    if (st) return st;
+    if (n < 0) return DDP_ERR_INVALID;
     if (n > 0 && (!grads || !numel || !offset || !buckets)) return DDP_ERR_INVALID;
     std::vector<std::pair<int64_t, int64_t>> ranges;
     for (int32_t i = 0; i < n; ++i) {

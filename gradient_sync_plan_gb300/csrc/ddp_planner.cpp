@@ -35,6 +35,7 @@ extern "C" int32_t ddp_plan_buckets(int32_t n_params, const int64_t* numel, int3
     bool open = false;           // the open bucket holds at least one parameter
     int64_t cap = first_bucket_bytes;
     for (int32_t p = n_params - 1; p >= 0; --p) {
+        if (fill > INT64_MAX / esize - numel[p]) return DDP_ERR_CAPACITY;   // bucket bytes would overflow
         bucket_of_param[p] = bucket;
         offset_of_param[p] = fill;
         fill += numel[p];

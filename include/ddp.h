@@ -58,6 +58,9 @@ extern "C" {
 
 #define DDP_ABI_VERSION 1
 #define DDP_MAX_WORLD 512          /* largest supported number of logical ranks */
+#define DDP_MAX_NUMEL ((int64_t)1 << 40)  /* largest element count of one rank's buffer or
+                                           bucket (DDP_ERR_CAPACITY above it), so that
+                                           byte sizes never overflow */
 
 typedef enum {
     DDP_OK = 0,

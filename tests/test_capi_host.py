@@ -186,6 +186,26 @@ def test_pack_unpack_view_reject_bad_plans():
                               7, None) == -1      # unknown algorithm
 
 
+def test_sizes_beyond_the_caps_are_refused_before_any_byte_arithmetic():
+    L = ddp.lib()
+    A, G0 = 0x7f0000000000, 0x7f0000200000
+    i64 = lambda *v: (ctypes.c_int64 * max(len(v), 1))(*v)
+    big = (1 << 40) + 1                     # one element past DDP_MAX_NUMEL
+    assert L.ddp_bucket_pack(1, 1, _vp(G0), i64(4), i64(0), _vp(A), big, 0, None) == -5
+    assert L.ddp_bucket_unpack(1, 1, _vp(G0), i64(4), i64(0), _vp(A), big, 0, None) == -5
+    assert L.ddp_bucket_pack_bf16(1, 1, _vp(G0), i64(4), i64(0), _vp(A), big, None) == -5
+    assert L.ddp_bucket_unpack_bf16(1, 1, _vp(G0), i64(4), i64(0), _vp(A), big, None) == -5
+    assert L.ddp_bucket_allreduce_view(1, 1, _vp(G0), i64(4), i64(0), big, 0, 1, None) == -5
+    # a member near INT64_MAX elements inside a bucket at the cap: refused as a bad plan
+    assert L.ddp_bucket_pack(1, 1, _vp(G0), i64(1 << 62), i64(1 << 62), _vp(A), 1 << 40, 0, None) == -1
+    # the planner: parameters whose running bucket size would overflow int64 bytes
+    n_p = 10
+    numel = (ctypes.c_int64 * n_p)(*[(2 ** 63 - 1) // 16] * n_p)
+    b_of, off, bn = (ctypes.c_int32 * n_p)(), (ctypes.c_int64 * n_p)(), (ctypes.c_int64 * n_p)()
+    nb = ctypes.c_int32()
+    assert L.ddp_plan_buckets(n_p, numel, 0, 2 ** 63 - 1, 2 ** 63 - 1, b_of, off, bn, ctypes.byref(nb)) == -5
+
+
 def test_host_direct_rejects_aliasing_on_host():
     L = ddp.lib()
     A, B, C = 0x7f0000000000, 0x7f0000100000, 0x7f0000200000
