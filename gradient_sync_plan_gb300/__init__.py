@@ -176,7 +176,15 @@ def _rank_tensors(bufs) -> list:
     return list(bufs)
 
 
-def _rank_ptrs(bufs) -> Tuple[list, int, int]:
+def _check_memory(t, memory: str, what: str) -> None:
+    """Device entry points take device memory and host ones host memory: a
+    host tensor handed to a kernel by mistake is a bad pointer on a GPU that
+    cannot read pageable host memory."""
+    if t.is_cuda != (memory == "device"):
+        raise ValueError(f"{what} must be in {memory} memory ({'CUDA' if memory == 'device' else 'CPU'} tensors)")
+
+
+def _rank_ptrs(bufs, memory: str) -> Tuple[list, int, int]:
     ts = _rank_tensors(bufs)
     if not ts:
         raise ValueError("no rank buffers")
@@ -185,6 +193,7 @@ def _rank_ptrs(bufs) -> Tuple[list, int, int]:
     for t in ts:
         if t.numel() != numel or dtype_code(t) != code or not t.is_contiguous():
             raise ValueError("rank buffers must be contiguous with equal numel and dtype")
+        _check_memory(t, memory, "rank buffers")
     return [t.data_ptr() for t in ts], numel, code
 
 
@@ -239,28 +248,28 @@ def ddp_plan_buckets(numels: Sequence[int], dtype: int = F32, first_bucket_bytes
 
 def ring_allreduce_fused(bufs, divisor: int = 0, stream=None) -> None:
     """In-place ring allreduce of the N rank buffers (+ divide), one pass."""
-    ptrs, numel, code = _rank_ptrs(bufs)
+    ptrs, numel, code = _rank_ptrs(bufs, "device")
     _check("ring_allreduce_fused", lib().ring_allreduce_fused(len(ptrs), _vp_array(ptrs), numel, code, divisor,
                                                               _stream(stream)))
 
 
 def ring_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
     """In-place ring allreduce reproduced hop by hop (2(N-1) launches)."""
-    ptrs, numel, code = _rank_ptrs(bufs)
+    ptrs, numel, code = _rank_ptrs(bufs, "device")
     _check("ring_allreduce_staged", lib().ring_allreduce_staged(len(ptrs), _vp_array(ptrs), numel, code, divisor,
                                                                 _stream(stream)))
 
 
 def tree_allreduce_fused(bufs, divisor: int = 0, stream=None) -> None:
     """In-place binomial-tree allreduce (+ divide), one pass; world <= 64."""
-    ptrs, numel, code = _rank_ptrs(bufs)
+    ptrs, numel, code = _rank_ptrs(bufs, "device")
     _check("tree_allreduce_fused", lib().tree_allreduce_fused(len(ptrs), _vp_array(ptrs), numel, code, divisor,
                                                               _stream(stream)))
 
 
 def tree_allreduce_staged(bufs, divisor: int = 0, stream=None) -> None:
     """In-place binomial-tree allreduce, one launch per tree step (2 ceil(log2 N))."""
-    ptrs, numel, code = _rank_ptrs(bufs)
+    ptrs, numel, code = _rank_ptrs(bufs, "device")
     _check("tree_allreduce_staged", lib().tree_allreduce_staged(len(ptrs), _vp_array(ptrs), numel, code, divisor,
                                                                 _stream(stream)))
 
@@ -272,10 +281,11 @@ def ring_allreduce_persistent(bufs, divisor: int = 0, status=None, fail_at_step:
     status: a device int32 tensor of >= 2 elements (allocated here if None and
     returned); status[0] holds DDP_OK (0) or DDP_ERR_TIMEOUT (-4) once the
     stream has run the kernel."""
-    ptrs, numel, code = _rank_ptrs(bufs)
+    ptrs, numel, code = _rank_ptrs(bufs, "device")
     torch = _torch()
     if status is None:
         status = torch.zeros(2, dtype=torch.int32, device=_rank_tensors(bufs)[0].device)
+    _check_memory(status, "device", "the status word")
     _check("ring_allreduce_persistent",
            lib().ring_allreduce_persistent(len(ptrs), _vp_array(ptrs), numel, code, divisor, status.data_ptr(),
                                            fail_at_step, wait_limit_ms, _stream(stream)))
@@ -286,9 +296,9 @@ def ring_allreduce_fused_from_host(host_in, host_out, dev_bufs, divisor: int = 0
     """Host buffers in and out, device scratch in between.  Large buckets are
     piped through in pieces (copies in, reduction and copies out overlap on
     internal streams); the caller's stream waits for the result."""
-    hi, numel, code = _rank_ptrs(host_in)
-    ho, n2, c2 = _rank_ptrs(host_out)
-    dv, n3, c3 = _rank_ptrs(dev_bufs)
+    hi, numel, code = _rank_ptrs(host_in, "host")
+    ho, n2, c2 = _rank_ptrs(host_out, "host")
+    dv, n3, c3 = _rank_ptrs(dev_bufs, "device")
     if not (numel == n2 == n3 and code == c2 == c3 and len(hi) == len(ho) == len(dv)):
         raise ValueError("host_in, host_out and dev_bufs must match")
     _check("ring_allreduce_fused_from_host",
@@ -300,8 +310,8 @@ def ring_allreduce_fused_host_direct(host_in, host_out, divisor: int = 0, stream
     """Fused allreduce read from and written to host buffers directly by the
     kernel (no device copies).  The buffers must be GPU-reachable, e.g.
     pinned (``tensor.pin_memory()``); host_out may be host_in."""
-    hi, numel, code = _rank_ptrs(host_in)
-    ho, n2, c2 = _rank_ptrs(host_out)
+    hi, numel, code = _rank_ptrs(host_in, "host")
+    ho, n2, c2 = _rank_ptrs(host_out, "host")
     if not (numel == n2 and code == c2 and len(hi) == len(ho)):
         raise ValueError("host_in and host_out must match")
     _check("ring_allreduce_fused_host_direct",
@@ -318,8 +328,8 @@ def ring_allreduce_fused_from_host_noalloc(host_in, host_out, divisor: int = 0, 
     array on the current GPU (world * numel per rank, each rank rounded up to
     256 bytes, must fit; DDPError DDP_ERR_CAPACITY otherwise).  Calls that
     overlap on the GPU share that array and race."""
-    hi, numel, code = _rank_ptrs(host_in)
-    ho, n2, c2 = _rank_ptrs(host_out)
+    hi, numel, code = _rank_ptrs(host_in, "host")
+    ho, n2, c2 = _rank_ptrs(host_out, "host")
     if not (numel == n2 and code == c2 and len(hi) == len(ho)):
         raise ValueError("host_in and host_out must match")
     _check("ring_allreduce_fused_from_host_noalloc",
@@ -329,8 +339,8 @@ def ring_allreduce_fused_from_host_noalloc(host_in, host_out, divisor: int = 0, 
 
 def ddp_grad_accumulate(acc, grads, stream=None) -> None:
     """acc[r] += grads[r] for every rank (one no_sync micro-batch)."""
-    pa, numel, code = _rank_ptrs(acc)
-    pg, n2, c2 = _rank_ptrs(grads)
+    pa, numel, code = _rank_ptrs(acc, "device")
+    pg, n2, c2 = _rank_ptrs(grads, "device")
     if numel != n2 or code != c2 or len(pa) != len(pg):
         raise ValueError("acc and grads must match")
     _check("ddp_grad_accumulate", lib().ddp_grad_accumulate(len(pa), _vp_array(pa), _vp_array(pg), numel, code,
@@ -351,6 +361,7 @@ def _member_tables(grads: Sequence[Sequence], offsets: Sequence[int]):
                 code = c
             if c != code or not g.is_contiguous():
                 raise ValueError("gradients must be contiguous and of one dtype")
+            _check_memory(g, "device", "gradients")
             ptrs.append(g.data_ptr())
             if r == 0:
                 numels.append(g.numel())
@@ -372,7 +383,7 @@ def ddp_plan_fingerprint(numels: Sequence[int], plan, dtype: int = F32) -> int:
 def ddp_bucket_pack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
     """buckets[r][offset_i : offset_i + numel_i] = grads[r][i] for every rank r and member i."""
     world, n, ptrs, numels, code = _member_tables(grads, offsets)
-    bp, bnumel, bcode = _rank_ptrs(buckets)
+    bp, bnumel, bcode = _rank_ptrs(buckets, "device")
     if n and bcode != code:
         raise ValueError("bucket dtype differs from gradients")
     _check("ddp_bucket_pack", lib().ddp_bucket_pack(world, n, _vp_array(ptrs), _i64_array(numels),
@@ -383,7 +394,7 @@ def ddp_bucket_pack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, 
 def ddp_bucket_unpack(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
     """grads[r][i] = buckets[r][offset_i : offset_i + numel_i] for every rank r and member i."""
     world, n, ptrs, numels, code = _member_tables(grads, offsets)
-    bp, bnumel, bcode = _rank_ptrs(buckets)
+    bp, bnumel, bcode = _rank_ptrs(buckets, "device")
     if n and bcode != code:
         raise ValueError("bucket dtype differs from gradients")
     _check("ddp_bucket_unpack", lib().ddp_bucket_unpack(world, n, _vp_array(ptrs), _i64_array(numels),
@@ -394,7 +405,7 @@ def ddp_bucket_unpack(grads: Sequence[Sequence], offsets: Sequence[int], buckets
 def ddp_bucket_pack_bf16(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
     """bf16 compression hook: float32 gradients rounded into bf16 buckets."""
     world, n, ptrs, numels, code = _member_tables(grads, offsets)
-    bp, bnumel, bcode = _rank_ptrs(buckets)
+    bp, bnumel, bcode = _rank_ptrs(buckets, "device")
     if (n and code != F32) or bcode != BF16:
         raise ValueError("float32 gradients and bf16 buckets expected")
     _check("ddp_bucket_pack_bf16", lib().ddp_bucket_pack_bf16(world, n, _vp_array(ptrs), _i64_array(numels),
@@ -405,7 +416,7 @@ def ddp_bucket_pack_bf16(grads: Sequence[Sequence], offsets: Sequence[int], buck
 def ddp_bucket_unpack_bf16(grads: Sequence[Sequence], offsets: Sequence[int], buckets, stream=None) -> None:
     """bf16 compression hook: bf16 buckets widened back into float32 gradients."""
     world, n, ptrs, numels, code = _member_tables(grads, offsets)
-    bp, bnumel, bcode = _rank_ptrs(buckets)
+    bp, bnumel, bcode = _rank_ptrs(buckets, "device")
     if (n and code != F32) or bcode != BF16:
         raise ValueError("float32 gradients and bf16 buckets expected")
     _check("ddp_bucket_unpack_bf16", lib().ddp_bucket_unpack_bf16(world, n, _vp_array(ptrs), _i64_array(numels),
@@ -474,6 +485,7 @@ class SyncCall:
                 code = c if code is None else code
                 if c != code or not g.is_contiguous():
                     raise ValueError("gradients must be contiguous and of one dtype")
+                _check_memory(g, "device", "gradients")
                 flat.append(g.data_ptr())
                 if r == 0:
                     numels.append(g.numel())
@@ -485,6 +497,9 @@ class SyncCall:
         self._off = _i64_array(off)
         self._bn = _i64_array(bn)
         if buckets is not None:
+            for r in range(self.world):
+                for k in range(self.K):
+                    _check_memory(buckets[r][k], "device", "bucket buffers")
             bflat = [buckets[r][k].data_ptr() for r in range(self.world) for k in range(self.K)]
             self._buckets = _vp_array(bflat)
         else:
@@ -522,6 +537,8 @@ class Reducer:
                     code = c if code is None else code
                     if c != code or not g.is_contiguous():
                         raise ValueError("gradients must be contiguous and of one dtype")
+                    if algo != DDP_ALGO_DRYRUN:
+                        _check_memory(g, "device", "gradients")
                     flat.append(g.data_ptr())
                     if r == 0:
                         numels.append(g.numel())
@@ -533,6 +550,10 @@ class Reducer:
             gtab = None
         btab = None
         if buckets is not None:
+            if algo != DDP_ALGO_DRYRUN:
+                for r in range(world):
+                    for k in range(len(bn)):
+                        _check_memory(buckets[r][k], "device", "bucket buffers")
             btab = _vp_array([buckets[r][k].data_ptr() for r in range(world) for k in range(len(bn))])
         self.world = world
         self.n_params = len(b_of)

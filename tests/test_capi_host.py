@@ -365,3 +365,24 @@ def test_plan_fingerprint_is_fnv1a_of_the_plan_and_changes_with_it():
     assert ddp.ddp_plan_fingerprint(numels, moved, ddp.F32) != fp
     L = ddp.lib()
     assert L.ddp_plan_fingerprint(0, None, ddp.F32, None, None, 0, None, None) == -1   # no output pointer
+
+
+def test_binding_refuses_host_tensors_for_device_entry_points():
+    # a CPU tensor handed to a kernel would be a bad pointer on a GPU that
+    # cannot read pageable host memory: the binding refuses it before any call
+    import torch
+    x = torch.zeros((2, 8))
+    for fn in (ddp.ring_allreduce_fused, ddp.ring_allreduce_staged, ddp.tree_allreduce_fused,
+               ddp.tree_allreduce_staged):
+        with pytest.raises(ValueError, match="device memory"):
+            fn(x, 2)
+    with pytest.raises(ValueError, match="device memory"):
+        ddp.ddp_grad_accumulate(x, x)
+    grads = [[x[0, :4]], [x[1, :4]]]
+    with pytest.raises(ValueError, match="device memory"):
+        ddp.ddp_bucket_allreduce_view(grads, [0], 4, 2)
+    with pytest.raises(ValueError, match="device memory"):
+        ddp.ddp_bucket_pack(grads, [0], x)
+    plan = ddp.ddp_plan_buckets([4], ddp.F32, 1 << 20, 1 << 20)
+    with pytest.raises(ValueError, match="device memory"):
+        ddp.ddp_sync_buckets(grads, plan, algo=ddp.DDP_ALGO_VIEW)
