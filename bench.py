@@ -68,18 +68,19 @@ def kernel_sources_digest() -> str:
 
 
 def profiled_traffic(name: str):
-    """DRAM bytes per launch recorded from an ncu capture in profiles/<name>,
-    or None if absent or taken on a different version of the kernel sources."""
+    """DRAM bytes per full-size launch recorded from an ncu capture in the data
+    file profiles/<name> (JSON), or None if absent or taken on a different
+    version of the kernel sources."""
     p = os.path.join(ROOT, "profiles", name)
     try:
-        txt = open(p).read()
-    except OSError:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
         return None, None
-    m = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
-    d = re.search(r"kernel_sources_digest:\s*([0-9a-f]+)", txt)
-    if not m or not d or d.group(1) != kernel_sources_digest():
+    if d.get("kernel_sources_digest") != kernel_sources_digest():
         return None, p
-    return float(m.group(1)), p
+    v = d.get("traffic_bytes_per_full_launch")
+    return (float(v) if v is not None else None), p
 
 
 class ClockSampler:
@@ -323,7 +324,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     busbw_total = world * 2 * (N - 1) / N * s_bytes * args.steps / (ms / 1e3) / 1e9
     hbm = 2 * N * s_bytes / (ms_step / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic, traffic_src = profiled_traffic("ring_fused_n8_1gib.md")
+    traffic, traffic_src = profiled_traffic("ring_fused_n8_1gib.json")
     if traffic is not None and numel != NUMEL:
         traffic = traffic * numel / NUMEL
 

@@ -31,6 +31,7 @@ DDP_ALGO_BF16_HOOK_VIEW = 5
 DDP_ALGO_FP16_HOOK_VIEW = 6
 DDP_FUSED_AUTO, DDP_FUSED_VECTOR, DDP_FUSED_GROUP, DDP_FUSED_TMA = 0, 1, 2, 3
 DDP_MAX_WORLD = 512
+MAX_NUMEL = 1 << 40                  # DDP_MAX_NUMEL: elements of one rank's buffer
 FIRST_BUCKET_BYTES = 1 << 20          # 1 MiB
 BUCKET_CAP_BYTES = 25 << 20           # 25 MiB
 

@@ -120,13 +120,31 @@ int32_t check_host_in_out(int32_t world, const void* const* host_in, void* const
     return DDP_OK;
 }
 
+int32_t common_checks(int32_t world, int64_t numel, int32_t dtype) {
+    if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
+    if (numel < 0 || (dtype != DDP_F32 && dtype != DDP_BF16)) return DDP_ERR_INVALID;
+    if (numel > DDP_MAX_NUMEL) return DDP_ERR_CAPACITY;
+    return DDP_OK;
+}
+
+namespace {
+thread_local const char* t_last_cuda_error = "no error";
+}  // namespace
+
+int32_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DDP_OK;
+    t_last_cuda_error = cudaGetErrorString(e);
+    if (debug_enabled()) fprintf(stderr, "[ddp] CUDA error: %s\n", t_last_cuda_error);
+    return DDP_ERR_CUDA;
+}
+
+const char* last_cuda_error() { return t_last_cuda_error; }
+
 }  // namespace ddpk
 
 using namespace ddpk;
 
 namespace {
-
-bool valid_dtype(int32_t dtype) { return dtype == DDP_F32 || dtype == DDP_BF16; }
 
 // Rank buffers: non-null, element-aligned, pairwise disjoint.  Sets *vec_ok
 // when every buffer is 16-byte aligned.
@@ -148,22 +166,6 @@ int32_t check_rank_buffers(int32_t world, const void* const* bufs, int64_t numel
         if (iv[i].first < iv[i - 1].second) return DDP_ERR_INVALID;
     *vec_ok = v;
     return DDP_OK;
-}
-
-int32_t common_checks(int32_t world, int64_t numel, int32_t dtype) {
-    if (world < 1 || world > DDP_MAX_WORLD) return world < 1 ? DDP_ERR_INVALID : DDP_ERR_CAPACITY;
-    if (numel < 0 || !valid_dtype(dtype)) return DDP_ERR_INVALID;
-    if (numel > DDP_MAX_NUMEL) return DDP_ERR_CAPACITY;
-    return DDP_OK;
-}
-
-thread_local const char* t_last_cuda_error = "no error";
-
-int32_t cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return DDP_OK;
-    t_last_cuda_error = cudaGetErrorString(e);
-    if (debug_enabled()) fprintf(stderr, "[ddp] CUDA error: %s\n", t_last_cuda_error);
-    return DDP_ERR_CUDA;
 }
 
 using Span = std::pair<uintptr_t, uintptr_t>;      // [first, second) in bytes
@@ -478,7 +480,7 @@ const char* ddp_status_string(int32_t status) {
 
 int32_t ddp_abi_version(void) { return DDP_ABI_VERSION; }
 
-const char* ddp_last_cuda_error(void) { return t_last_cuda_error; }
+const char* ddp_last_cuda_error(void) { return last_cuda_error(); }
 
 int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous) try {
     DDP_TRACE_CALL();

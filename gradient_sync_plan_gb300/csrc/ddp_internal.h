@@ -32,6 +32,20 @@ constexpr int kDtypeHook16 = 101;         // the same with IEEE binary16 (fp16 c
 inline int64_t chunk_len(int64_t numel, int world) { return (numel + world - 1) / world; }
 inline int elem_bytes(int dtype) { return dtype == DDP_BF16 ? 2 : 4; }
 
+// Host-side checks shared by the entry points: world in 1..DDP_MAX_WORLD,
+// numel in 0..DDP_MAX_NUMEL, a known dtype.  Entry points call it before any
+// byte arithmetic, so numel * element size cannot overflow afterwards.
+int32_t common_checks(int32_t world, int64_t numel, int32_t dtype);
+// Host buffers of a host-memory allreduce: non-null, element-aligned, inputs
+// pairwise disjoint, each output its own input or disjoint from every buffer.
+// Call after common_checks.
+int32_t check_host_in_out(int32_t world, const void* const* host_in, void* const* host_out, int64_t numel,
+                          int32_t dtype);
+// DDP_OK for cudaSuccess; otherwise records the error text (ddp_last_cuda_error)
+// and returns DDP_ERR_CUDA.
+int32_t cuda_status(cudaError_t e);
+const char* last_cuda_error();
+
 // Launch geometry helpers (cached per device).
 int sm_count();
 int grid_for(const void* kernel, int64_t work_items, int threads = kThreads);

@@ -19,6 +19,11 @@
 // array keeps whatever the last call left in it; nothing needs to start at
 // zero, because each call overwrites every byte it reads with its own
 // host-to-device copy before the kernel runs.
+//
+// The array's device address is looked up once per device and cached.  The
+// cache does not survive a device reset (cudaDeviceReset destroys the
+// context the address belongs to): a process that resets a device must not
+// call this entry point on that device afterwards.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -28,12 +33,6 @@
 #include "ddp.h"
 #include "ddp_internal.h"
 #include "ddp_trace.h"
-
-namespace ddpk {
-// ddp_api.cpp: host buffers of a host-memory allreduce (null, alignment, overlap)
-int32_t check_host_in_out(int32_t world, const void* const* host_in, void* const* host_out, int64_t numel,
-                          int32_t dtype);
-}  // namespace ddpk
 
 // The scratch itself.  In host code this name is only a host-side stand-in
 // for the symbol, never a device address: it is turned into one with
@@ -71,32 +70,36 @@ extern "C" int32_t ring_allreduce_fused_from_host_noalloc(int32_t world, const v
                                                           void* const* host_out, int64_t numel, int32_t dtype,
                                                           int32_t divisor, void* stream) try {
     DDP_TRACE_CALL();
-    if (world < 1 || numel < 0 || divisor < 0) return DDP_ERR_INVALID;
-    if (world > DDP_MAX_WORLD) return DDP_ERR_CAPACITY;
-    if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID;
-    if (!host_in || !host_out) return DDP_ERR_INVALID;
-    if (int32_t st = ddpk::check_host_in_out(world, host_in, host_out, numel, dtype)) return st;
-    if (numel == 0) return DDP_OK;
+    // sizes first: after common_checks numel <= DDP_MAX_NUMEL, so the byte
+    // counts below cannot overflow
+    if (int32_t st = ddpk::common_checks(world, numel, dtype)) return st;
+    if (divisor < 0 || !host_in || !host_out) return DDP_ERR_INVALID;
+    const int64_t es = ddpk::elem_bytes(dtype);
+    if (numel > DDP_STATIC_SCRATCH_BYTES / es) return DDP_ERR_CAPACITY;
     // each rank's slice starts on a 256-byte boundary so the kernel's
     // vectorised paths apply
-    const int64_t bytes = numel * ddpk::elem_bytes(dtype);
-    if (bytes > DDP_STATIC_SCRATCH_BYTES) return DDP_ERR_CAPACITY;
+    const int64_t bytes = numel * es;
     const int64_t stride = (bytes + 255) & ~(int64_t)255;
-    if (stride * (int64_t)world > DDP_STATIC_SCRATCH_BYTES) return DDP_ERR_CAPACITY;
+    if (stride > DDP_STATIC_SCRATCH_BYTES / world) return DDP_ERR_CAPACITY;
+    if (int32_t st = ddpk::check_host_in_out(world, host_in, host_out, numel, dtype)) return st;
+    if (numel == 0) return DDP_OK;
 
     unsigned char* base = nullptr;
-    if (scratch_on_current_device(&base) != cudaSuccess) return DDP_ERR_CUDA;
+    if (int32_t st = ddpk::cuda_status(scratch_on_current_device(&base))) return st;
     void* dev[DDP_MAX_WORLD];
     for (int32_t r = 0; r < world; ++r) dev[r] = base + (int64_t)r * stride;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int32_t r = 0; r < world; ++r)
-        if (cudaMemcpyAsync(dev[r], host_in[r], (size_t)bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return DDP_ERR_CUDA;
-    if (ddpk::launch_ring_fused(world, dev, numel, dtype, ddpk::make_div(divisor), true, s) != cudaSuccess)
-        return DDP_ERR_CUDA;
+        if (int32_t st =
+                ddpk::cuda_status(cudaMemcpyAsync(dev[r], host_in[r], (size_t)bytes, cudaMemcpyHostToDevice, s)))
+            return st;
+    if (int32_t st = ddpk::cuda_status(
+            ddpk::launch_ring_fused(world, dev, numel, dtype, ddpk::make_div(divisor), true, s)))
+        return st;
     for (int32_t r = 0; r < world; ++r)
-        if (cudaMemcpyAsync(host_out[r], dev[r], (size_t)bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-            return DDP_ERR_CUDA;
+        if (int32_t st =
+                ddpk::cuda_status(cudaMemcpyAsync(host_out[r], dev[r], (size_t)bytes, cudaMemcpyDeviceToHost, s)))
+            return st;
     return DDP_OK;
 } DDP_ABI_CATCH

@@ -381,7 +381,11 @@ int32_t ring_allreduce_fused_host_direct(int32_t world, const void* const* host_
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current) and caches it; make
- * that first call before any stream capture.  All calls on a device share
+ * that first call before any stream capture.  The cached address belongs to
+ * the device's context and does not survive cudaDeviceReset: after a reset of
+ * a device, do not call this entry point on it again in the same process.
+ * Sizes are checked (world, numel <= DDP_MAX_NUMEL, dtype, then the array's
+ * capacity) before any byte count is formed.  All calls on a device share
  * the array: calls that overlap on the GPU (different streams, or host
  * threads without ordering) race and corrupt each other's results.  The
  * array keeps the last call's contents; no clearing is needed, since a call

@@ -23,7 +23,7 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, f32_or_bits, sampled_expected
+from gpu_util import assert_bits_equal, f32_or_bits, oracle_allreduce, sampled_expected
 
 pytestmark = pytest.mark.gpu
 MiB = 1 << 20
@@ -516,22 +516,39 @@ def test_one_scratch_buffer_shared_by_every_bucket(algo):
     assert_bits_equal(f32_or_bits(g), want, f"{algo} with one shared scratch buffer")
 
 
-def test_readme_python_example_runs():
-    # the README's usage block, run as written on a small decoder and bucket
-    import os
-    import re
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    text = open(os.path.join(root, "README.md"), encoding="utf-8").read()
-    block = re.search(r"## Using it from Python\n\n```python\n(.*?)```", text, re.S).group(1)
+def test_python_usage_sequence_matches_oracle():
+    # the binding's documented usage, written out here: plan, one view sync,
+    # the same step overlapped through the reducer, and one bucket's fused
+    # ring -- each result against the oracle
     numels = _small_decoder()
-    flat, _ = _host_grads(numels, 4, "f32", seed0=71)
+    world = 4
+    flat, grads_h = _host_grads(numels, world, "f32", seed0=71)
     g = flat.cuda()
-    x = workloads.rank_vectors(4, 1000, "randn", seed0=3).cuda()
-    env = {"grads": _device_views(g, numels), "x": x}
-    exec(compile(block, "README.md", "exec"), env)
+    grads = _device_views(g, numels)
+    plan = ddp.ddp_plan_buckets([t.numel() for t in grads[0]], ddp.F32)
+    ddp.ddp_sync_buckets(grads, plan, None, algo=ddp.DDP_ALGO_VIEW)
     torch.cuda.synchronize()
-    for r in range(1, 4):                      # every sync leaves all ranks identical
-        assert torch.equal(g[r], g[0]) and torch.equal(x[r], x[0])
+    oracle.ddp_sync(grads_h, oracle.F32)
+    assert_bits_equal(f32_or_bits(g), np.stack([np.concatenate(grads_h[r]) for r in range(world)]), "view sync")
+
+    flat2, grads2_h = _host_grads(numels, world, "f32", seed0=72)
+    g2 = flat2.cuda()
+    grads2 = _device_views(g2, numels)
+    red = ddp.Reducer(grads2, plan, algo=ddp.DDP_ALGO_VIEW, comm_stream=torch.cuda.Stream())
+    red.prepare()
+    for p in reversed(range(len(numels))):
+        red.mark_ready(p, torch.cuda.current_stream())
+    red.finalize(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    red.close()
+    oracle.ddp_sync(grads2_h, oracle.F32)
+    assert_bits_equal(f32_or_bits(g2), np.stack([np.concatenate(grads2_h[r]) for r in range(world)]), "reducer")
+
+    x = workloads.rank_vectors(world, 1000, "randn", seed0=3)
+    xd = x.cuda()
+    ddp.ring_allreduce_fused(xd, xd.shape[0])
+    torch.cuda.synchronize()
+    assert_bits_equal(f32_or_bits(xd), oracle_allreduce(x.numpy(), world), "one bucket")
 
 
 def test_fp16_hook_view_overflow_and_subnormals_match_oracle():

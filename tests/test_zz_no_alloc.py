@@ -4,10 +4,10 @@ ring_allreduce_fused_from_host_noalloc is for callers that hold gradients in
 host memory and cannot allocate device memory themselves (no device
 allocator of their own, or one that belongs to another framework).  It
 keeps the ranks' device copies in a fixed array that the library reserves
-on every GPU, so it must give exactly what ring_allreduce_fused_from_host
-gives with caller-allocated device buffers -- bit for bit, the tolerance of
-every other parity test here -- call after call, whatever the previous call
-left in that shared array.
+on every GPU.  Call after call, whatever the previous call left in that
+shared array, it must give the CPU oracle's ring result bit for bit (the
+bar of every other parity test here), and so exactly what
+ring_allreduce_fused_from_host gives with caller-allocated device buffers.
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test.
@@ -19,6 +19,7 @@ import torch
 
 import gradient_sync_plan_gb300 as ddp
 import workloads
+from gpu_util import assert_bits_equal, f32_or_bits, oracle_allreduce
 
 
 def _pinned(x):
@@ -40,6 +41,7 @@ def test_noalloc_matches_caller_allocated_variant_on_consecutive_calls():
         ddp.ring_allreduce_fused_from_host_noalloc(host_in, got, N)
         torch.cuda.synchronize()
         iv = torch.int16 if dtype == "bf16" else torch.int32
+        assert_bits_equal(f32_or_bits(got), oracle_allreduce(f32_or_bits(x), N), f"oracle N={N} S={S} {dtype}")
         assert torch.equal(got.view(iv), want.view(iv)), f"N={N} S={S} {dtype}"
         # the input buffers are left untouched when host_out differs
         assert torch.equal(host_in.view(iv), x.view(iv))
@@ -52,9 +54,11 @@ def test_noalloc_in_place_on_host():
     a = _pinned(x)
     b = torch.empty_like(a).pin_memory()
     dev = torch.empty((N, S), device="cuda")
+    want = oracle_allreduce(x.numpy(), N)
     ddp.ring_allreduce_fused_from_host(a, b, dev, N)
     ddp.ring_allreduce_fused_from_host_noalloc(a, a, N)       # host_out == host_in
     torch.cuda.synchronize()
+    assert_bits_equal(a.numpy(), want, "noalloc in place")
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
@@ -78,3 +82,22 @@ def test_noalloc_rejects_requests_beyond_the_array_before_any_cuda_call():
     with pytest.raises(ddp.DDPError):
         ddp.ring_allreduce_fused_from_host_noalloc(torch.zeros(2, limit // 8 + 64), torch.zeros(2, limit // 8 + 64), 2,
                                                    stream=0)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="refusals with made-up pointers run only where no GPU is reachable")
+def test_noalloc_rejects_sizes_whose_byte_count_would_overflow():
+    # numel * element size must never be formed for a numel beyond
+    # DDP_MAX_NUMEL: 2^62 + 16 fp32 elements are 2^64 + 64 bytes, which wraps
+    # to 64 bytes in 64-bit arithmetic and would pass a capacity check made on
+    # the wrapped value.  Every call here must be refused before any CUDA
+    # call; this test runs only without a GPU, so a regression cannot reach
+    # a copy or a launch.
+    L = ddp.lib()
+    H = 0x7f0000000000
+    tab = (ctypes.c_void_p * 8)(*[H + r * (1 << 27) for r in range(8)])
+    for numel in ((1 << 62) + 16, (1 << 62) + 8, (1 << 63) - 1, ddp.MAX_NUMEL + 1):
+        for dtype in (0, 1):
+            for world in (1, 2, 8):
+                assert L.ring_allreduce_fused_from_host_noalloc(world, tab, tab, numel, dtype, world, None) == -5
+    # within DDP_MAX_NUMEL but beyond the array: refused by the capacity check
+    assert L.ring_allreduce_fused_from_host_noalloc(1, tab, tab, ddp.MAX_NUMEL, 0, 1, None) == -5
