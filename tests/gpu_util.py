@@ -97,3 +97,60 @@ def sample_indices(numel: int, world: int, k_random: int, seed: int = 0) -> np.n
     rng = np.random.default_rng(seed)
     s.update(int(v) for v in rng.integers(0, numel, size=k_random))
     return np.array(sorted(s), dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# Full-size comparisons (gigabytes per buffer)
+# --------------------------------------------------------------------------
+
+def host_snapshot(dev: torch.Tensor) -> np.ndarray:
+    """Host copy of a 2-D device tensor, written straight into numpy memory
+    (one host copy, no staging tensor): float32 as float32, bf16 as uint16."""
+    bf = dev.dtype == torch.bfloat16
+    out = np.empty(tuple(dev.shape), dtype=np.uint16 if bf else np.float32)
+    for r in range(dev.shape[0]):
+        dst = torch.from_numpy(out[r].view(np.int16)).view(torch.bfloat16) if bf else torch.from_numpy(out[r])
+        dst.copy_(dev[r])
+    return out
+
+
+def assert_device_equals_host(dev: torch.Tensor, want: np.ndarray, what: str = "", piece: int = 1 << 26) -> None:
+    """Every element of the 2-D device tensor `dev` bit-equal to the host
+    array `want` (float32, or uint16 bf16 patterns), compared on the device
+    in pieces of `piece` elements uploaded from the host."""
+    assert tuple(dev.shape) == tuple(want.shape), (tuple(dev.shape), want.shape)
+    iv = torch.int16 if dev.dtype == torch.bfloat16 else torch.int32
+    nv = np.int16 if dev.dtype == torch.bfloat16 else np.int32
+    S = dev.shape[1]
+    for r in range(dev.shape[0]):
+        row = dev[r].view(iv)
+        for a in range(0, S, piece):
+            b = min(S, a + piece)
+            w = torch.from_numpy(want[r, a:b].view(nv)).to(dev.device)
+            if not torch.equal(row[a:b], w):
+                i = int((row[a:b] != w).nonzero()[0, 0]) + a
+                n_bad = int((row[a:b] != w).sum())
+                mask = 0xFFFF if iv == torch.int16 else 0xFFFFFFFF
+                got_v = int(row[i].item()) & mask
+                want_v = int(want[r, i:i + 1].view(nv)[0]) & mask
+                raise AssertionError(f"{what}: rank {r}: {n_bad} mismatches in [{a}, {b}); first at {i}: "
+                                     f"got bits {got_v:#x} want {want_v:#x}")
+            del w
+
+
+def require_host_memory(nbytes: int, what: str) -> None:
+    """Skip (with the reason) when the host cannot hold `nbytes` more with a
+    margin: the full-size comparisons keep gigabytes of expected values on the
+    host, and running a host out of memory must not be risked."""
+    import pytest
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    if avail is not None and avail < 1.5 * nbytes + (8 << 30):
+        pytest.skip(f"{what}: needs about {nbytes / 2**30:.1f} GiB of host memory, "
+                    f"{avail / 2**30:.1f} GiB available")

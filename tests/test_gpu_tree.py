@@ -3,9 +3,8 @@
 tree_allreduce_fused and tree_allreduce_staged, through the C ABI, bit-exact
 against oracle.tree_allreduce on the same seeded inputs: every N in 1..9 with
 every S in 0..70, larger N (fused up to 64, staged beyond), ragged multi-tile
-sizes, buffers that are not 16-byte aligned, and a sampled check on an
-8 x 1 GiB bucket (the tree folds every element in the same order, so sampled
-columns go straight through the oracle).
+sizes, buffers that are not 16-byte aligned, and an 8 x 1 GiB bucket
+compared in full.
 """
 import numpy as np
 import pytest
@@ -14,7 +13,7 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, f32_or_bits, from_np
+from gpu_util import assert_bits_equal, assert_device_equals_host, f32_or_bits, from_np, host_snapshot, require_host_memory
 
 pytestmark = pytest.mark.gpu
 
@@ -73,21 +72,41 @@ def test_unaligned(kernel):
     assert_bits_equal(np.stack([f32_or_bits(r) for r in rows]), oracle_tree(x.numpy(), N), f"unaligned {kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["fused", "staged"])
-def test_one_gib_buckets_sampled(kernel):
-    N, S = 8, 1 << 28
-    x = torch.empty((N, S), device="cuda")
-    for r in range(N):
-        x[r].copy_(workloads.randn_f32(S, r, 1e-2, device="cuda"))
-    idx = torch.from_numpy(np.random.default_rng(0).integers(0, S, size=5000)).cuda()
-    samples = f32_or_bits(x[:, idx])
-    TREE[kernel](x, N)
-    torch.cuda.synchronize()
-    assert_bits_equal(f32_or_bits(x[:, idx]), oracle_tree(samples, N), f"1 GiB {kernel}")
-    for r in range(1, N):
-        assert torch.equal(x[r].view(torch.int32), x[0].view(torch.int32))
-    del x
+_gib = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _release_full_size_buffers():
+    yield
+    _gib.clear()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kernel", ["fused", "fused_vector", "staged"])
+def test_one_gib_buckets_full(kernel):
+    # 8 x 1 GiB fp32, every element of every rank against the oracle's tree
+    N, S = 8, 1 << 28
+    if not _gib:
+        require_host_memory(N * S * 4, "8 x 1 GiB tree")
+        x0 = torch.empty((N, S), device="cuda")
+        for r in range(N):
+            x0[r].copy_(workloads.randn_f32(S, r, 1e-2, device="cuda"))
+        want = host_snapshot(x0)
+        oracle.tree_allreduce_2d(want, oracle.F32, N)
+        _gib["case"] = (x0, want)
+    x0, want = _gib["case"]
+    x = x0.clone()
+    if kernel == "fused_vector":                  # the size rule picks the TMA kernel here
+        prev = ddp.ddp_set_fused_kernel(ddp.DDP_FUSED_VECTOR)
+        try:
+            ddp.tree_allreduce_fused(x, N)
+        finally:
+            ddp.ddp_set_fused_kernel(prev)
+    else:
+        TREE[kernel](x, N)
+    torch.cuda.synchronize()
+    assert_device_equals_host(x, want, f"1 GiB tree {kernel}")
+    del x
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -105,8 +124,12 @@ def test_fused_both_kernels_around_the_size_switch(dtype):
                 for div in (N, 3):
                     assert_bits_equal(run("fused", xh, div), oracle_tree(xh, div), f"tree N={N} S={S} div={div}")
 
-    for kind in (ddp.DDP_FUSED_GROUP, ddp.DDP_FUSED_VECTOR):
-        for N, S in ((2, 3 * 1024 * 1024 // es + 7), (7, 99_999), (64, 40_000 + 3)):
+    for kind in (ddp.DDP_FUSED_GROUP, ddp.DDP_FUSED_VECTOR, ddp.DDP_FUSED_TMA):
+        # the last four sizes have whole 16-byte rows, which the TMA kernel
+        # takes (tiles over the whole bucket; 16 and 64 ranks: both of its
+        # rank-table sizes); the first three make a forced TMA fall back
+        for N, S in ((2, 3 * 1024 * 1024 // es + 7), (7, 99_999), (64, 40_000 + 3), (2, 1 << 20),
+                     (8, 3 * 1024 * 1024 // es), (16, 123_456), (64, 40_000)):
             xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=N + kind))
             prev = ddp.ddp_set_fused_kernel(kind)
             try:

@@ -27,3 +27,20 @@ def test_sample_indices_cover_every_chunk_boundary():
     c = -(-S // N)
     for j in range(N):
         assert j * c in idx and min((j + 1) * c, S) - 1 in idx
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_full_size_compare_helpers_find_a_planted_difference(dtype):
+    # the chunked comparison used by the full-size GPU parity tests, run on
+    # CPU tensors: equal data passes, one changed bit anywhere is found
+    from gpu_util import assert_device_equals_host, host_snapshot
+    x = workloads.rank_vectors(3, 10_001, "randn", dtype=dtype, seed0=5)
+    h = host_snapshot(x)
+    assert h.dtype == (np.uint16 if dtype == "bf16" else np.float32)
+    assert_device_equals_host(x, h, "equal", piece=1000)
+    for r, i in ((0, 0), (2, 10_000), (1, 4_321)):
+        bad = h.copy()
+        v = bad.view(np.uint16 if dtype == "bf16" else np.uint32)
+        v[r, i] ^= 1
+        with pytest.raises(AssertionError, match=f"rank {r}: 1 mismatches .* first at {i}"):
+            assert_device_equals_host(x, bad, "planted", piece=1000)
