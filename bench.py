@@ -99,7 +99,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                                          "-i", str(self.gpu_index), "-lms", "50"],
+                                          "-i", str(self.gpu_index), "-lms", "10"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except Exception:
@@ -156,6 +156,162 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside),
                 "power_w_max": max((num(p[4]) or 0.0) for p in use) if use else None}
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    management library, loaded with ctypes) every `period_s` seconds while the
+    timed region runs; reading only, no setting is changed.  Falls back to
+    nvidia-smi when NVML cannot be loaded."""
+
+    # clock-event reason bits of NVML's public API
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str, gpu_index: int, period_s: float = 0.005):
+        self.uuid, self.gpu_index, self.period_s = uuid, gpu_index, period_s
+        self.samples = []            # (t, sm_mhz, max_mhz, power_w, reasons)
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._fallback = None
+
+    def _open(self):
+        import ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        rc = L.nvmlDeviceGetHandleByUUID(("GPU-" + self.uuid).encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = L.nvmlDeviceGetHandleByIndex_v2(self.gpu_index, ctypes.byref(h))
+        if rc != 0:
+            raise OSError("no NVML handle")
+        reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        return L, h, reasons_fn
+
+    def start(self):
+        try:
+            L, h, reasons_fn = self._open()
+        except Exception:
+            self._fallback = ClockSampler(self.gpu_index)
+            self._fallback.start()
+            return
+        import ctypes
+
+        def loop():
+            sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                ok = (L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+                      L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0)
+                if L.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) != 0:
+                    pw.value = 0
+                if reasons_fn(h, ctypes.byref(rs)) != 0:
+                    rs.value = 0
+                if ok:
+                    self.samples.append((time.perf_counter(), sm.value, mx.value, pw.value / 1000.0, rs.value))
+                time.sleep(self.period_s)
+            L.nvmlShutdown()
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+        if self._fallback:
+            self._fallback.mark_start()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+        if self._fallback:
+            self._fallback.mark_end()
+
+    def stop(self):
+        if self._fallback:
+            self._fallback.stop()
+            return
+        time.sleep(0.02)
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        if self._fallback:
+            return self._fallback.summary()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "no NVML samples"}
+        inside = [x for x in self.samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        use = inside if inside else self.samples
+        sm = sorted(x[1] for x in use)
+        reasons = sorted({name for x in use for bit, name in self.REASONS.items() if x[4] & bit})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(x[2] for x in use), "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside), "period_ms": self.period_s * 1e3,
+                "power_w_max": max(x[3] for x in use), "source": "NVML (ctypes), read-only"}
+
+
+def run_metadata(torch, dev, n_ranks: int) -> dict:
+    """What the line was measured on and with: GPU, host CPU, input seeds."""
+    props = torch.cuda.get_device_properties(dev)
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    import platform
+    return {"gpu": {"name": torch.cuda.get_device_name(dev), "uuid": str(getattr(props, "uuid", "")),
+                    "sms": props.multi_processor_count, "memory_gib": round(props.total_memory / 2**30, 1),
+                    "cc": f"{props.major}.{props.minor}"},
+            "host": {"nproc": os.cpu_count(), "cores_available": host_cores(), "cpu_model": model,
+                     "arch": platform.machine()},
+            "inputs": {"generator": "torch.Generator(device='cuda').manual_seed(seed), torch.randn float32 * 1e-2",
+                       "seeds": list(range(n_ranks)), "seed_rule": "rank r draws from seed r"},
+            "torch": torch.__version__}
+
+
+def host_link_bench(torch, dev, host_src, dev_dst, host_dst, dev_src, reps: int = 3) -> dict:
+    """The CPU-GPU link's own throughput through the copy engines: pinned
+    host -> device alone, device -> pinned host alone, and both at once on two
+    streams (CUDA events around each), best of `reps`."""
+    nbytes = host_src.numel() * host_src.element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def timed(both, h2d=True):
+        best = None
+        for _ in range(reps):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            torch.cuda.synchronize(dev)
+            e0.record(cur)
+            s_in.wait_event(e0)
+            s_out.wait_event(e0)
+            if both or h2d:
+                with torch.cuda.stream(s_in):
+                    dev_dst.copy_(host_src, non_blocking=True)
+            if both or not h2d:
+                with torch.cuda.stream(s_out):
+                    host_dst.copy_(dev_src, non_blocking=True)
+            e1.record(s_in)
+            e2.record(s_out)
+            cur.wait_event(e1)
+            cur.wait_event(e2)
+            torch.cuda.synchronize(dev)
+            ms = max(e0.elapsed_time(e1), e0.elapsed_time(e2))
+            best = ms if best is None else min(best, ms)
+        return best
+
+    h2d = timed(False, True)
+    d2h = timed(False, False)
+    both = timed(True)
+    return {"bytes_each_way": nbytes, "h2d_gbs": nbytes / (h2d / 1e3) / 1e9, "d2h_gbs": nbytes / (d2h / 1e3) / 1e9,
+            "both_gbs": 2 * nbytes / (both / 1e3) / 1e9, "both_ms": both,
+            "how": "pinned host memory, copy engines, both directions on two streams at once, CUDA events, "
+                   f"best of {reps}"}
 
 
 def cpu_oracle_run(n_ranks: int, budget_s: float, max_numel: int, reps_cap: int = 1000):
@@ -293,7 +449,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 phys = int(vis.split(",")[local_rank])
             except Exception:
                 phys = local_rank
-        sampler = ClockSampler(phys)
+        sampler = NvmlSampler(str(getattr(torch.cuda.get_device_properties(dev), "uuid", "")), phys)
         sampler.start()
 
     barrier()
@@ -347,6 +503,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
            "gpu_launches": args.steps}
     if sampler:
         out["clocks"] = sampler.summary()
+    out["run"] = run_metadata(torch, dev, N)
 
     # ---- end to end through the C ABI with host buffers ----------------------
     if not args.no_e2e:
@@ -381,6 +538,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                    "api": "ring_allreduce_fused_from_host (pinned host buffers; 32 MiB pieces "
                                           "copied in, reduced and copied out on overlapping streams)"}
         out["e2e"]["gpu_launches"] = e2e_steps          # one fused kernel per direct call
+        # the link's own ceiling, measured the same run: copy engines in both
+        # directions at once over the same 8 GiB (a second pinned host buffer
+        # and a second device buffer)
+        host2 = torch.empty_like(host).pin_memory()
+        dev2 = torch.empty_like(x)
+        link = host_link_bench(torch, dev, host, dev2, host2, x)
+        del host2, dev2
+        out["e2e"]["host_link_peak_gbs"] = link["both_gbs"]
+        out["e2e"]["host_link_frac"] = out["e2e"]["host_link_gbs"] / link["both_gbs"]
+        out["e2e"]["host_link"] = link
         del host
 
     # ---- extra measurements ------------------------------------------------
@@ -576,7 +743,10 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
 
     A synthetic backward walks the layers in reverse: per transformer block two
     bf16 GEMMs of 4096^3 on a compute stream (emulated layer backward), then
-    the block's gradients are written on every rank.  Three timings:
+    ONE kernel writes the block's gradients on every rank (a fill of the
+    block's [N, block numel] slice of the gradient arena: HBM traffic equal to
+    the block's gradient bytes, as a weight-gradient GEMM's epilogue would
+    write them).  Three timings:
       backward      -- the synthetic backward alone
       serial        -- backward, then ddp_sync_buckets (view fusion) on the same stream
       overlapped    -- backward with a ddp_reducer that syncs each bucket on a comm
@@ -586,10 +756,7 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
     numels = workloads.param_numels(shapes)
     N, total = N_RANKS, sum(numels)
     plan = ddp.ddp_plan_buckets(numels, ddp.F32, MiB, 25 * MiB)
-    src = torch.empty((N, total), dtype=torch.float32, device=dev)
-    for r in range(N):
-        src[r].copy_(workloads.randn_f32(total, r, 1e-2, device=str(dev)))
-    g = torch.empty_like(src)
+    g = torch.empty((N, total), dtype=torch.float32, device=dev)
     offs = [0]
     for n in numels:
         offs.append(offs[-1] + n)
@@ -612,15 +779,19 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
     red_hi = ddp.Reducer(views, plan, None, N, ddp.DDP_ALGO_VIEW, comm_stream=comm_hi)
     sync = ddp.SyncCall(views, plan, None, N, ddp.DDP_ALGO_VIEW)
 
+    # each group's parameters are contiguous in the arena: one [N, span] slice
+    spans = [(offs[min(grp)], offs[max(grp) + 1]) for grp in groups]
+
     def backward(reducer):
         with torch.cuda.stream(compute):
             for gi, grp in enumerate(groups):
                 if 0 < gi <= 24:
                     torch.mm(A, B, out=C)
                     torch.mm(C, B, out=C)
-                for p in grp:
-                    g[:, offs[p]:offs[p + 1]].copy_(src[:, offs[p]:offs[p + 1]])
-                    if reducer is not None:
+                a, b = spans[gi]
+                g[:, a:b].fill_(1e-3 * (gi + 1))          # one write-only kernel for the whole block
+                if reducer is not None:
+                    for p in grp:
                         reducer.mark_ready(p, compute)
 
     def timed(fn):
@@ -666,7 +837,8 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
 
     t_b = timed(run_backward)
     res = {"backward_ms": t_b,
-           "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block on a compute stream; view-fusion sync; "
+           "note": "synthetic backward: 2 bf16 GEMMs of 4096^3 per block, then one write-only kernel per block "
+                   "for the block's gradients on all ranks, on a compute stream; view-fusion sync; "
                    "each pass captured as one CUDA graph (both streams) and replayed; best of %d; "
                    "max_ctas = CTA cap of the sync kernels (0 = fill the GPU)" % steps, "by_max_ctas": {}}
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -695,7 +867,7 @@ def overlap_bench(ddp, workloads, torch, dev, steps):
                               "synthetic backward runs beside it"}
     red.close()
     red_hi.close()
-    del g, src, views
+    del g, views
     torch.cuda.empty_cache()
     return res
 
@@ -837,8 +1009,8 @@ def run_profile_kernels(args):
     """Every kernel family once on one workload larger than L2, for a
     per-kernel ncu DRAM capture: N = 8 ranks x 2^25 fp32 (128 MiB per rank,
     1 GiB over all ranks), in this order -- fused ring (vector, then TMA
-    kernel), staged ring, persistent ring, fused tree (vector kernel), staged
-    tree, no_sync accumulation, bf16 pack and unpack (one 2^25-element
+    kernel), staged ring, persistent ring, fused tree (vector, then TMA
+    kernel), staged tree, no_sync accumulation, bf16 pack and unpack (one 2^25-element
     member per rank), fused view (one bucket of 4 members per rank).  --steps
     repeats the sequence.  Prints one JSON line (not a bench result)."""
     import torch
@@ -870,6 +1042,7 @@ def run_profile_kernels(args):
            ("ring_staged", lambda: ddp.ring_allreduce_staged(x, N)),
            ("ring_persistent", lambda: ddp.ring_allreduce_persistent(x, N, status=status)),
            ("tree_fused_vector", lambda: forced(ddp.DDP_FUSED_VECTOR, lambda: ddp.tree_allreduce_fused(x, N))),
+           ("tree_fused_tma", lambda: forced(ddp.DDP_FUSED_TMA, lambda: ddp.tree_allreduce_fused(x, N))),
            ("tree_staged", lambda: ddp.tree_allreduce_staged(x, N)),
            ("accumulate", lambda: ddp.ddp_grad_accumulate(x, y)),
            ("pack_bf16", lambda: ddp.ddp_bucket_pack_bf16([[x[r]] for r in range(N)], [0], b16)),
