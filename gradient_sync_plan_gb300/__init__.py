@@ -40,7 +40,7 @@ STATUS = {0: "DDP_OK", -1: "DDP_ERR_INVALID", -2: "DDP_ERR_ALIGN", -3: "DDP_ERR_
 
 # every symbol include/ddp.h declares
 EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_device_status", "ddp_set_max_ctas",
-           "ddp_set_fused_kernel", "ddp_plan_buckets", "ddp_plan_fingerprint",
+           "ddp_set_fused_kernel", "ddp_set_wait_limit_ms", "ddp_plant_stall", "ddp_plan_buckets", "ddp_plan_fingerprint",
            "ddp_bucket_pack", "ddp_bucket_unpack", "ddp_bucket_pack_bf16", "ddp_bucket_unpack_bf16",
            "ring_allreduce_fused", "ring_allreduce_staged", "ring_allreduce_persistent", "tree_allreduce_fused",
            "tree_allreduce_staged", "ring_allreduce_fused_from_host",
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
             L.ddp_device_status.restype = i32
             L.ddp_set_max_ctas.argtypes = [i32, P(i32)]
             L.ddp_set_fused_kernel.argtypes = [i32, P(i32)]
+            L.ddp_set_wait_limit_ms.argtypes = [i32, P(i32)]
+            L.ddp_plant_stall.argtypes = [i64]
             L.ddp_plan_buckets.argtypes = [i32, P(i64), i32, i64, i64, P(i32), P(i64), P(i64), P(i32)]
             L.ddp_plan_fingerprint.argtypes = [i32, P(i64), i32, P(i32), P(i64), i32, P(i64), P(ctypes.c_uint64)]
             L.ddp_bucket_pack.argtypes = [i32, i32, P(vp), P(i64), P(i64), P(vp), i64, i32, vp]
@@ -222,6 +224,21 @@ def ddp_set_max_ctas(max_ctas: int) -> int:
     prev = ctypes.c_int32(0)
     _check("ddp_set_max_ctas", lib().ddp_set_max_ctas(int(max_ctas), ctypes.byref(prev)))
     return int(prev.value)
+
+
+def ddp_set_wait_limit_ms(limit_ms: int) -> int:
+    """Limit of the TMA kernels' bounded waits in ms (0 = the 2000 ms default);
+    returns the previous limit."""
+    prev = ctypes.c_int32(0)
+    _check("ddp_set_wait_limit_ms", lib().ddp_set_wait_limit_ms(int(limit_ms), ctypes.byref(prev)))
+    return int(prev.value)
+
+
+def ddp_plant_stall(tile: int) -> None:
+    """Test hook: the next TMA kernel launch never issues the copies of tile
+    `tile` (and later tiles of its CTA), so its consumers' waits run out
+    (-1 removes a pending plant)."""
+    _check("ddp_plant_stall", lib().ddp_plant_stall(int(tile)))
 
 
 def ddp_set_fused_kernel(kind: int) -> int:

@@ -76,6 +76,8 @@ __device__ __forceinline__ void block_copy(const char* src, char* dst, int64_t b
 }
 
 __global__ void __launch_bounds__(kThreads) k_copy_items(const __grid_constant__ CopyBatch b) {
+    pdl_release();
+    pdl_acquire();
     const int64_t tiles = b.tile_end[b.n - 1];
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         int lo = 0, hi = b.n - 1;            // first item whose tile_end > tile
@@ -108,8 +110,8 @@ cudaError_t launch_copy_items(const CopyItem* items, int64_t n, cudaStream_t str
         }
         if (b.n == 0) continue;
         const int grid = grid_for((const void*)k_copy_items, tiles * kThreads);
-        k_copy_items<<<std::max<int64_t>(1, std::min<int64_t>(grid, tiles)), kThreads, 0, stream>>>(b);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_dependent(k_copy_items, dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(grid, tiles))),
+                                         dim3(kThreads), 0, stream, b);
         if (e != cudaSuccess) return e;
         if (debug_enabled())
             fprintf(stderr, "[ddp] copy_items n=%d tiles=%lld\n", b.n, (long long)tiles);
@@ -140,9 +142,31 @@ struct ConvBatch {
 };
 static_assert(sizeof(ConvBatch) <= kMaxParamBytes, "convert batch exceeds the kernel parameter limit");
 
-// MODE 0: float32 -> bf16 (round to nearest even); MODE 1: bf16 -> float32 (exact)
+// MODE 0: float32 -> bf16 (round to nearest even); MODE 1: bf16 -> float32 (exact).
+// Aligned items move groups of 4 elements: lane t of a warp takes group t, so
+// the 16-byte float32 side and the 8-byte bf16 side of one load or store
+// instruction are both contiguous across the warp and every L2 sector is
+// written whole (a layout with two 16-byte stores 32 bytes apart per lane
+// half-filled each sector per instruction and nearly doubled the L2 write
+// traffic of the widening pass).  Each thread has kConvUnroll groups in
+// flight.
+constexpr int kConvUnroll = 8;
+
+template <int MODE>
+__device__ __forceinline__ void convert_group(const char* src, char* dst, int64_t e) {
+    if (MODE == 0) {
+        const float4 a = *reinterpret_cast<const float4*>(src + e * 4);
+        *reinterpret_cast<uint2*>(dst + e * 2) = make_uint2(bf16x2_rn(a.x, a.y), bf16x2_rn(a.z, a.w));
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(src + e * 2);
+        *reinterpret_cast<float4*>(dst + e * 4) = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) k_convert_items(const __grid_constant__ ConvBatch b) {
+    pdl_release();
+    pdl_acquire();
     const int64_t tiles = b.tile_end[b.n - 1];
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         int lo = 0, hi = b.n - 1;
@@ -157,28 +181,32 @@ __global__ void __launch_bounds__(kThreads) k_convert_items(const __grid_constan
         char* dst = b.dst[lo];
         int64_t done = e0;
         if (b.vec[lo]) {
-            // 8 elements per step: 32 bytes of fp32 <-> 16 bytes of bf16
-            const int64_t nv = (e1 - e0) / 8;
-            for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-                const int64_t e = e0 + v * 8;
+            const int64_t ng = (e1 - e0) / 4;
+            const int64_t bd = blockDim.x;
+            int64_t g = threadIdx.x;
+            for (; g + (kConvUnroll - 1) * bd < ng; g += kConvUnroll * bd) {
                 if (MODE == 0) {
-                    const float4 a = reinterpret_cast<const float4*>(src + e * 4)[0];
-                    const float4 c = reinterpret_cast<const float4*>(src + e * 4)[1];
-                    uint4 o;
-                    o.x = bf16x2_rn(a.x, a.y);
-                    o.y = bf16x2_rn(a.z, a.w);
-                    o.z = bf16x2_rn(c.x, c.y);
-                    o.w = bf16x2_rn(c.z, c.w);
-                    *reinterpret_cast<uint4*>(dst + e * 2) = o;
+                    float4 a[kConvUnroll];
+#pragma unroll
+                    for (int u = 0; u < kConvUnroll; ++u)
+                        a[u] = *reinterpret_cast<const float4*>(src + (e0 + 4 * (g + u * bd)) * 4);
+#pragma unroll
+                    for (int u = 0; u < kConvUnroll; ++u)
+                        *reinterpret_cast<uint2*>(dst + (e0 + 4 * (g + u * bd)) * 2) =
+                            make_uint2(bf16x2_rn(a[u].x, a[u].y), bf16x2_rn(a[u].z, a[u].w));
                 } else {
-                    const uint4 w = *reinterpret_cast<const uint4*>(src + e * 2);
-                    reinterpret_cast<float4*>(dst + e * 4)[0] =
-                        make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-                    reinterpret_cast<float4*>(dst + e * 4)[1] =
-                        make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                    uint2 w[kConvUnroll];
+#pragma unroll
+                    for (int u = 0; u < kConvUnroll; ++u)
+                        w[u] = *reinterpret_cast<const uint2*>(src + (e0 + 4 * (g + u * bd)) * 2);
+#pragma unroll
+                    for (int u = 0; u < kConvUnroll; ++u)
+                        *reinterpret_cast<float4*>(dst + (e0 + 4 * (g + u * bd)) * 4) =
+                            make_float4(bf16_lo(w[u].x), bf16_hi(w[u].x), bf16_lo(w[u].y), bf16_hi(w[u].y));
                 }
             }
-            done = e0 + nv * 8;
+            for (; g < ng; g += bd) convert_group<MODE>(src, dst, e0 + 4 * g);
+            done = e0 + ng * 4;
         }
         for (int64_t e = done + threadIdx.x; e < e1; e += blockDim.x) {
             if (MODE == 0)
@@ -209,9 +237,8 @@ cudaError_t launch_convert_items(const ConvItem* items, int64_t n, int to_bf16, 
         if (b.n == 0) continue;
         const void* k = to_bf16 ? (const void*)k_convert_items<0> : (const void*)k_convert_items<1>;
         const int grid = std::max<int64_t>(1, std::min<int64_t>(grid_for(k, tiles * kThreads), tiles));
-        if (to_bf16) k_convert_items<0><<<grid, kThreads, 0, stream>>>(b);
-        else k_convert_items<1><<<grid, kThreads, 0, stream>>>(b);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = to_bf16 ? launch_dependent(k_convert_items<0>, dim3(grid), dim3(kThreads), 0, stream, b)
+                                : launch_dependent(k_convert_items<1>, dim3(grid), dim3(kThreads), 0, stream, b);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -245,6 +272,8 @@ __global__ void __launch_bounds__(kThreads) k_bucket_view(const __grid_constant_
     using S = typename E::S;
     constexpr int L = E::L;
     constexpr int64_t TILE = view_tile_elems<E>();
+    pdl_release();
+    pdl_acquire();
     const int world = b.world;
     const int64_t tiles = b.tile_end[b.n - 1];
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -329,8 +358,8 @@ static cudaError_t view_impl(int world, const ViewMember* members, int n, int64_
         }
         if (b.n == 0) continue;
         const int grid = grid_for((const void*)k, tiles * kThreads);
-        k<<<std::max<int64_t>(1, std::min<int64_t>(grid, tiles)), kThreads, 0, st>>>(b, dop);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_dependent(k, dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(grid, tiles))),
+                                         dim3(kThreads), 0, st, b, dop);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -352,11 +381,12 @@ static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, D
     }
 }
 
-// Elements of a member that the TMA view kernel cannot take: the pieces
-// before and after each segment's 16-byte-aligned body (fewer than 16 bytes
-// each side of a chunk boundary that is not 16-byte aligned), or the whole
-// member if its pointers are not 16-byte aligned.  Done by the register view
-// kernel, one rank-pointer table per piece.
+// Elements of a member that the TMA view kernel cannot stage with bulk
+// copies: the pieces before and after each segment's 16-byte-aligned body
+// (fewer than 16 bytes each side of a chunk boundary that is not 16-byte
+// aligned), or the whole member if its pointers are not 16-byte aligned.
+// Short ones the TMA kernel folds element by element itself; the rest run on
+// the register view kernel, one rank-pointer table per piece.
 struct ViewEdges {
     std::vector<ViewMember> pieces;
     std::vector<std::vector<void*>> tables;
@@ -374,16 +404,19 @@ struct ViewEdges {
 // Cut members [first, first + n) of one bucket at the bucket's chunk
 // boundaries into segments (member indices are global).  A segment's
 // 16-byte-aligned body goes to `segs`; what is left of it, and every member
-// whose pointers are not 16-byte aligned, goes to `edges`.
+// whose pointers are not 16-byte aligned, goes to `edges` (in member order).
 static void split_segments(int world, const ViewMember* members, int first, int n, int64_t bucket_numel, int dtype,
-                           std::vector<ViewSegment>* segs, ViewEdges* edges) {
+                           std::vector<ViewSegment>* segs, std::vector<ViewEdge>* edges) {
     const int64_t es = elem_bytes(dtype);
     const int64_t lanes = 16 / es;                       // elements per 16 bytes
     const int64_t clen = chunk_len(bucket_numel, world);
     for (int i = first; i < first + n; ++i) {
         const ViewMember& m = members[i];
+        auto edge = [&](int64_t start, int64_t len) {
+            if (len > 0) edges->push_back(ViewEdge{i, start, len, clen});
+        };
         if (!m.vec_ok) {
-            edges->add(world, m, 0, m.numel, es, clen);
+            edge(0, m.numel);
             continue;
         }
         int64_t a = m.offset;
@@ -400,7 +433,7 @@ static void split_segments(int world, const ViewMember* members, int first, int 
                     if (pending_len == 0) pending = s0;
                     pending_len = body0 - pending;
                 }
-                edges->add(world, m, pending, pending_len, es, clen);
+                edge(pending, pending_len);
                 pending_len = 0;
                 segs->push_back(ViewSegment{i, (int32_t)j, body0, body1 - body0});
                 if (s1 > body1) {
@@ -413,7 +446,7 @@ static void split_segments(int world, const ViewMember* members, int first, int 
             }
             a = b;
         }
-        edges->add(world, m, pending, pending_len, es, clen);
+        edge(pending, pending_len);
     }
 }
 
@@ -435,26 +468,35 @@ static cudaError_t view_register(int world, const ViewMember* members, int n, in
 cudaError_t launch_buckets_view(int world, const ViewMember* members, const int* bucket_first, const int* bucket_count,
                                 const int64_t* bucket_numel, int n_buckets, int dtype, DivSpec div,
                                 cudaStream_t stream) {
-    // the aligned bodies of every bucket in one set of TMA launches, the
-    // edges in one register launch; buckets too small for the TMA kernel all
-    // go to the register kernel
+    // the aligned bodies of every bucket, and the short edges around them, in
+    // one set of TMA launches; long edges (members whose pointers are not
+    // 16-byte aligned, runs of tiny chunks) in one register launch; buckets
+    // too small for the TMA kernel all go to the register kernel
     std::vector<ViewSegment> segs;
-    ViewEdges edges;
+    std::vector<ViewEdge> all_edges;
     int64_t body = 0;
     for (int k = 0; k < n_buckets; ++k)
-        split_segments(world, members, bucket_first[k], bucket_count[k], bucket_numel[k], dtype, &segs, &edges);
+        split_segments(world, members, bucket_first[k], bucket_count[k], bucket_numel[k], dtype, &segs, &all_edges);
     for (const ViewSegment& g : segs) body += g.len;
     if (view_tma_worth(world, body, dtype)) {
         int n_members = 0;
         for (int k = 0; k < n_buckets; ++k) n_members = std::max(n_members, bucket_first[k] + bucket_count[k]);
-        cudaError_t e = launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(), dtype, div,
-                                               stream);
+        std::vector<ViewEdge> short_edges;
+        ViewEdges long_edges;
+        const int64_t es = elem_bytes(dtype);
+        for (const ViewEdge& g : all_edges) {
+            if (g.len <= kTmaEdgeMax) short_edges.push_back(g);
+            else long_edges.add(world, members[g.member], g.start, g.len, es, g.clen);
+        }
+        cudaError_t e = launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(),
+                                               short_edges.data(), (int)short_edges.size(), dtype, div, stream);
         if (e != cudaSuccess) return e;
-        edges.bind();
+        long_edges.bind();
         if (debug_enabled())
-            fprintf(stderr, "[ddp] bucket_view edges=%zu\n", edges.pieces.size());
-        // every edge piece carries its own bucket's chunk length
-        return view_register(world, edges.pieces.data(), (int)edges.pieces.size(), 1, dtype, div, stream);
+            fprintf(stderr, "[ddp] bucket_view edges: %zu in the TMA launch, %zu on the register kernel\n",
+                    short_edges.size(), long_edges.pieces.size());
+        // every long edge carries its own bucket's chunk length
+        return view_register(world, long_edges.pieces.data(), (int)long_edges.pieces.size(), 1, dtype, div, stream);
     }
     for (int k = 0; k < n_buckets; ++k) {
         cudaError_t e = view_register(world, members + bucket_first[k], bucket_count[k], bucket_numel[k], dtype, div,

@@ -433,17 +433,80 @@ cudaError_t sync_bucket_pieces(int32_t world, int32_t n, const void* const* g, c
     return cudaSuccess;
 }
 
+// The bf16 compression hook's three passes over one bucket, in the same
+// L2-sized pieces: for each piece the members' parts are rounded into the
+// bf16 bucket, the piece is reduced in bf16 by the view kernel at its bucket
+// offset (each element folded in the ring order of its chunk of the whole
+// bucket, one bf16 rounding per hop), and widened back into the gradients --
+// the bits of the whole-bucket pack, ring and unpack.  Arguments are checked
+// by the caller.
+cudaError_t hook_bucket_pieces(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                               void* const* bk, int64_t bucket_numel, int32_t divisor, bool vec, cudaStream_t s) {
+    const int64_t piece = bucket_piece_elems(world, DDP_BF16);
+    const DivSpec div = make_div(divisor);
+    std::vector<ConvItem> in, out;
+    std::vector<void*> ptrs(world);
+    for (int64_t a = 0; a < bucket_numel; a += piece) {
+        const int64_t b = std::min(bucket_numel, a + piece);
+        in.clear();
+        out.clear();
+        for (int32_t r = 0; r < world; ++r)
+            for (int32_t i = 0; i < n; ++i) {
+                const int64_t s0 = std::max(off[i], a), s1 = std::min(off[i] + ne[i], b);
+                if (s1 <= s0) continue;
+                const char* gp = static_cast<const char*>(g[(int64_t)r * n + i]) + (s0 - off[i]) * 4;
+                char* bp = static_cast<char*>(bk[r]) + s0 * 2;
+                in.push_back(ConvItem{gp, bp, s1 - s0});
+                out.push_back(ConvItem{bp, const_cast<char*>(gp), s1 - s0});
+            }
+        cudaError_t e = launch_convert_items(in.data(), (int64_t)in.size(), 1, s);
+        if (e != cudaSuccess) return e;
+        for (int32_t r = 0; r < world; ++r) ptrs[r] = static_cast<char*>(bk[r]) + a * 2;
+        ViewMember m{b - a, a, ptrs.data(), vec};
+        if ((e = launch_bucket_view(world, &m, 1, bucket_numel, DDP_BF16, div, s)) != cudaSuccess) return e;
+        if ((e = launch_convert_items(out.data(), (int64_t)out.size(), 0, s)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 namespace ddpk {
+
+// ddp_sync_buckets' and the reducer's bf16-hook path for one bucket:
+// validated, then whole or in L2-sized pieces.
+int32_t hook_pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                              void* const* bk, int64_t bucket_numel, int32_t divisor, void* stream) {
+    std::vector<ConvItem> items, back;
+    int32_t st = hook_items(world, n, g, ne, off, (const void* const*)bk, bucket_numel, true, &items);
+    if (st) return st;
+    // the unpack writes the gradients: they must not overlap each other either
+    if ((st = hook_items(world, n, g, ne, off, (const void* const*)bk, bucket_numel, false, &back))) return st;
+    if (divisor < 0) return DDP_ERR_INVALID;
+    if (bucket_numel == 0) return DDP_OK;
+    bool vec = false;
+    if ((st = check_rank_buffers(world, bk, bucket_numel, DDP_BF16, &vec))) return st;
+    const int64_t piece = bucket_piece_elems(world, DDP_BF16);
+    if (bucket_numel <= piece + piece / 2) {
+        if ((st = cuda_status(launch_convert_items(items.data(), (int64_t)items.size(), 1, (cudaStream_t)stream))))
+            return st;
+        if ((st = ring_allreduce_fused(world, bk, bucket_numel, DDP_BF16, divisor, stream))) return st;
+        return ddp_bucket_unpack_bf16(world, n, const_cast<void* const*>(g), ne, off, (const void* const*)bk,
+                                      bucket_numel, stream);
+    }
+    return cuda_status(hook_bucket_pieces(world, n, g, ne, off, bk, bucket_numel, divisor, vec, (cudaStream_t)stream));
+}
 
 // ddp_sync_buckets' and the reducer's unfused fused-ring path for one bucket:
 // validated, then whole or in pieces.
 int32_t pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
                          void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, void* stream) {
-    std::vector<CopyItem> items;
+    std::vector<CopyItem> items, back;
     int32_t st = bucket_items(world, n, g, ne, off, (const void* const*)bk, bucket_numel, dtype, true, &items);
     if (st) return st;
+    // the unpack writes the gradients: they must not overlap each other either
+    if ((st = bucket_items(world, n, g, ne, off, (const void* const*)bk, bucket_numel, dtype, false, &back)))
+        return st;
     if (divisor < 0) return DDP_ERR_INVALID;
     if (bucket_numel == 0) return DDP_OK;
     bool vec = false;
@@ -495,6 +558,23 @@ int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous) try {
     if (kind < DDP_FUSED_AUTO || kind > DDP_FUSED_TMA) return DDP_ERR_INVALID;
     const int prev = g_fused_kernel.exchange(kind);
     if (previous) *previous = prev;
+    return DDP_OK;
+} DDP_ABI_CATCH
+
+int32_t ddp_set_wait_limit_ms(int32_t limit_ms, int32_t* previous_ms) try {
+    DDP_TRACE_CALL();
+    if (limit_ms < 0 || limit_ms > 600000) return DDP_ERR_INVALID;
+    const unsigned long long ns = (unsigned long long)(limit_ms ? limit_ms : 2000) * 1000000ull;
+    unsigned long long prev = 0;
+    set_wait_limit_ns(ns, &prev);
+    if (previous_ms) *previous_ms = (int32_t)(prev / 1000000ull);
+    return DDP_OK;
+} DDP_ABI_CATCH
+
+int32_t ddp_plant_stall(int64_t tile) try {
+    DDP_TRACE_CALL();
+    if (tile < -1) return DDP_ERR_INVALID;
+    plant_stall((long long)tile);
     return DDP_OK;
 } DDP_ABI_CATCH
 
@@ -822,12 +902,8 @@ int32_t ddp_sync_buckets(int32_t world, int32_t n_params, void* const* grads, co
         }
         for (int32_t r = 0; r < world; ++r) bk[r] = buckets[(size_t)r * n_buckets + k];
         if (algo == DDP_ALGO_BF16_HOOK) {
-            st = ddp_bucket_pack_bf16(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], stream);
-            if (st) return st;
-            st = ring_allreduce_fused(world, bk.data(), bucket_numel[k], DDP_BF16, divisor, stream);
-            if (st) return st;
-            st = ddp_bucket_unpack_bf16(world, n, const_cast<void* const*>(g.data()), ne.data(), off.data(),
-                                        (const void* const*)bk.data(), bucket_numel[k], stream);
+            st = hook_pack_ring_unpack(world, n, g.data(), ne.data(), off.data(), bk.data(), bucket_numel[k], divisor,
+                                       stream);
             if (st) return st;
             continue;
         }

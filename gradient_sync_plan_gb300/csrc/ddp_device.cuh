@@ -20,6 +20,34 @@
 
 namespace ddpk {
 
+// Programmatic dependent launch.  A kernel launched by launch_dependent may
+// be scheduled while the previous kernel on its stream is still running, so
+// its launch latency overlaps that kernel's tail.  Every such kernel calls
+// pdl_release() (its own dependents may be scheduled from now on) and then
+// pdl_acquire(), which returns only once the previous kernel has completed
+// and its writes are visible -- before it touches any buffer.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_acquire() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+    const cudaError_t last = cudaGetLastError();      // read (and clear) as a <<<>>> launch would be
+    return e != cudaSuccess ? e : last;
+}
+
 template <int DIV>
 __device__ __forceinline__ float div_f32(float a, float operand) {
     if constexpr (DIV == kDivNone) return a;
@@ -209,6 +237,39 @@ __device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, 
         }
     }
     return acc;
+}
+
+// The binomial tree's fold (tree_kernels.cu, ring_tma.cu): ranks in groups
+// of kTreeGroup.
+constexpr int kTreeGroup = 16;
+// Binomial pairwise sum of load(0) .. load(world - 1), world <= 16 * NG
+// (NG = 1, 2 or 4).  Ranks are folded in groups of 16 (levels 1, 2, 4, 8
+// inside a group), then the group sums at levels 16 and 32 -- exactly the
+// tree's additions, in its order.  NG is a compile-time bound so that a
+// small world does not carry the registers of 64 ranks.
+template <class T, int NG = 4, class Add, class Load>
+__device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
+    static_assert(NG == 1 || NG == 2 || NG == 4, "1, 2 or 4 groups of 16 ranks");
+    T gs[4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        if (kTreeGroup * g < world) {
+            T v[kTreeGroup];
+#pragma unroll
+            for (int i = 0; i < kTreeGroup; ++i)
+                if (kTreeGroup * g + i < world) v[i] = load(kTreeGroup * g + i);
+#pragma unroll
+            for (int d = 1; d < kTreeGroup; d <<= 1)
+#pragma unroll
+                for (int i = 0; i < kTreeGroup; i += 2 * d)
+                    if (kTreeGroup * g + i + d < world) v[i] = add(v[i], v[i + d]);
+            gs[g] = v[0];
+        }
+    }
+    if (NG >= 2 && 16 < world) gs[0] = add(gs[0], gs[1]);
+    if (NG >= 4 && 48 < world) gs[2] = add(gs[2], gs[3]);
+    if (NG >= 4 && 32 < world) gs[0] = add(gs[0], gs[2]);
+    return gs[0];
 }
 
 // Scalar version of the same fold for one element at element index `e`,

@@ -89,7 +89,16 @@ bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok);
 int64_t tma_tile_bytes(int world);
 cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                   cudaStream_t stream);
+// The binomial tree's fused allreduce with the same TMA staging (world <= 64,
+// buffers 16-byte aligned, bucket bytes a multiple of 16).
+bool tree_tma_usable(int world, int64_t numel, int dtype, bool vec_ok);
+cudaError_t launch_tree_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                                  cudaStream_t stream);
 cudaError_t read_device_status(int32_t* out, bool clear);
+// Wait limit of the TMA kernels' mbarrier waits, and a planted stall taken by
+// the next TMA kernel launch (ddp_set_wait_limit_ms, ddp_plant_stall).
+void set_wait_limit_ns(unsigned long long ns, unsigned long long* previous);
+void plant_stall(long long tile);
 
 // ---- bucket kernels (bucket_kernels.cu) --------------------------------
 struct CopyItem {
@@ -134,9 +143,22 @@ struct ViewSegment {
     int64_t start;
     int64_t len;
 };
-// TMA-staged view kernel (ring_tma.cu): members' pointers 16-byte aligned,
-// every segment's start and length multiples of 16 bytes.
+// A short piece of one member that the TMA view kernel folds element by
+// element: elements [start, start + len) of member `member`; each element's
+// chunk is its bucket position divided by clen.
+struct ViewEdge {
+    int32_t member;
+    int64_t start;
+    int64_t len;
+    int64_t clen;
+};
+// Longest edge the TMA view kernel takes (one element per consumer thread).
+constexpr int64_t kTmaEdgeMax = 256;
+// TMA-staged view kernel (ring_tma.cu): the segments' members have 16-byte
+// aligned pointers, and every segment's start and length are multiples of
+// 16 bytes; edges (len <= kTmaEdgeMax) may belong to any member.
 cudaError_t launch_bucket_view_tma(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
-                                   int n_segs, int dtype, DivSpec div, cudaStream_t stream);
+                                   int n_segs, const ViewEdge* edges, int n_edges, int dtype, DivSpec div,
+                                   cudaStream_t stream);
 
 }  // namespace ddpk

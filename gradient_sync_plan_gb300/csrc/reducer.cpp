@@ -29,6 +29,9 @@ namespace ddpk {
 // ddp_api.cpp: one bucket's pack -> fused ring -> unpack, in L2-sized pieces when large
 int32_t pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
                          void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, void* stream);
+// ddp_api.cpp: one bucket's bf16-hook pack -> bf16 ring -> unpack, in L2-sized pieces when large
+int32_t hook_pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
+                              void* const* bk, int64_t bucket_numel, int32_t divisor, void* stream);
 }  // namespace ddpk
 
 struct ddp_reducer {
@@ -70,13 +73,9 @@ int32_t sync_bucket(ddp_reducer* r, int32_t k) {
     if (r->algo == DDP_ALGO_FP16_HOOK_VIEW)
         return ddp_bucket_allreduce_view_fp16(r->world, n, g, ne, off, r->bucket_numel[k], r->divisor, r->comm);
     void* const* b = r->bucket_bufs[k].data();
-    if (r->algo == DDP_ALGO_BF16_HOOK) {
-        int32_t st = ddp_bucket_pack_bf16(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->comm);
-        if (st) return st;
-        st = ring_allreduce_fused(r->world, b, r->bucket_numel[k], DDP_BF16, r->divisor, r->comm);
-        if (st) return st;
-        return ddp_bucket_unpack_bf16(r->world, n, g, ne, off, (const void* const*)b, r->bucket_numel[k], r->comm);
-    }
+    if (r->algo == DDP_ALGO_BF16_HOOK)
+        return ddpk::hook_pack_ring_unpack(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k],
+                                           r->divisor, r->comm);
     if (r->algo == DDP_ALGO_FUSED)
         return ddpk::pack_ring_unpack(r->world, n, (const void* const*)g, ne, off, b, r->bucket_numel[k], r->dtype,
                                       r->divisor, r->comm);

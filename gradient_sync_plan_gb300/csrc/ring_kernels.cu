@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kThreads)
 k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
     using V = typename E::V;
     constexpr int L = E::L;
+    pdl_release();
+    pdl_acquire();
     const int64_t nvec = (numel + L - 1) / L;
     const int64_t full = numel / L;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(kThreads)
 k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
     using V = typename E::V;
     constexpr int L = E::L;
+    pdl_release();
+    pdl_acquire();
     constexpr int kGroups = 32 / P;                     // vectors per warp and pass
     const int lane = threadIdx.x & 31;
     const int q = lane & (P - 1);
@@ -145,6 +149,8 @@ k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t 
 template <class E, int DIV, int CAP>
 __global__ void __launch_bounds__(kThreads)
 k_ring_fused_scalar(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+    pdl_release();
+    pdl_acquire();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < numel; e += stride)
         ring_element<E, DIV, CAP>(t, world, e, clen, dop);
@@ -228,6 +234,8 @@ k_accumulate(const __grid_constant__ RankTable<CAP> acc, const __grid_constant__
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
+    pdl_release();
+    pdl_acquire();
     const int r = blockIdx.y;
     char* a = acc.p[r];
     const char* b = g.p[r];
@@ -272,11 +280,12 @@ static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64
     auto k = k_ring_fused<E, DIV, 2 * CAP, G>;
     const int64_t nvec = (numel + E::L - 1) / E::L;
     const int grid = grid_for((const void*)k, nvec);
-    k<<<grid, kThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
+    const cudaError_t e = launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, make_io_table<2 * CAP>(world, in, out),
+                                           world, numel, chunk_len(numel, world), dop);
     if (debug_enabled())
         fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d G=%d CAP=%d\n", world, (long long)numel,
                 grid, G, CAP);
-    return cudaGetLastError();
+    return e;
 }
 
 constexpr int kGroupThreads = 128;     // small blocks spread a small bucket over more SMs
@@ -288,12 +297,13 @@ static cudaError_t fused_group(int world, void* const* in, void* const* out, int
     const int64_t nvec = (numel + E::L - 1) / E::L;
     const int64_t lanes = (nvec + 32 / P - 1) / (32 / P) * 32;
     const int grid = grid_for((const void*)k, lanes, kGroupThreads);
-    k<<<grid, kGroupThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world),
-                                      dop);
+    const cudaError_t e = launch_dependent(k, dim3(grid), dim3(kGroupThreads), 0, st,
+                                           make_io_table<2 * CAP>(world, in, out), world, numel,
+                                           chunk_len(numel, world), dop);
     if (debug_enabled())
         fprintf(stderr, "[ddp] ring_fused_group world=%d numel=%lld grid=%d P=%d R=%d\n", world, (long long)numel,
                 grid, P, R);
-    return cudaGetLastError();
+    return e;
 }
 
 template <class E, int DIV>
@@ -313,8 +323,8 @@ static cudaError_t fused_scalar(int world, void* const* in, void* const* out, in
                                 cudaStream_t st) {
     auto k = k_ring_fused_scalar<E, DIV, 2 * CAP>;
     const int grid = grid_for((const void*)k, numel);
-    k<<<grid, kThreads, 0, st>>>(make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
-    return cudaGetLastError();
+    return launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, make_io_table<2 * CAP>(world, in, out), world,
+                            numel, chunk_len(numel, world), dop);
 }
 
 template <class E, int DIV>
@@ -468,8 +478,7 @@ static cudaError_t accumulate_impl(int world, void* const* acc, const void* cons
     const int64_t per_rank = vec_ok ? numel / E::L + E::L : numel;
     int gx = grid_for((const void*)k, per_rank * world);
     gx = std::max(1, (gx + world - 1) / world);
-    k<<<dim3(gx, world), kThreads, 0, st>>>(ta, tg, numel, vec_ok ? 1 : 0);
-    return cudaGetLastError();
+    return launch_dependent(k, dim3(gx, world), dim3(kThreads), 0, st, ta, tg, numel, vec_ok ? 1 : 0);
 }
 
 cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g, int64_t numel, int dtype,

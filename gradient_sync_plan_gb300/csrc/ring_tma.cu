@@ -17,15 +17,23 @@
 // moment the last consumer warp has read it, which keeps the copy engine's
 // queue full.
 //
-// Waits are bounded: an mbarrier wait that exceeds kWaitLimitNs sets the
-// library's device status word to DDP_ERR_TIMEOUT and the thread stops; the
-// producer then waits (again bounded) for the copies it issued before it
-// returns.
+// Waits are bounded: an mbarrier wait that exceeds the wait limit (2 s
+// unless ddp_set_wait_limit_ms says otherwise) sets the library's device
+// status word to DDP_ERR_TIMEOUT and the thread stops; the producer then
+// waits (again bounded) for the copies it issued before it returns.
+//
+// A planted stall (ddp_plant_stall) makes the producer of the CTA that owns
+// one chosen tile stop before that tile: it issues no copy for it or for any
+// later tile, and waits for the copies it did issue to be consumed.  The
+// consumers then wait for a tile that never arrives -- what a ring step
+// looks like when one rank never joins it -- until the limit runs out.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "ddp_device.cuh"
 #include "ddp_internal.h"
@@ -38,7 +46,13 @@ constexpr int kTmaStages = 2;
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaThreads = 32 * (kTmaConsumerWarps + 1);    // + one producer warp
 constexpr int kTmaMaxVec = 4;        // 16-byte vectors per consumer thread per tile (tile <= 16 KB)
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Per-launch control: the wait limit, and the tile whose copies are never
+// issued (-1: none).
+struct TmaCtl {
+    unsigned long long limit_ns;
+    long long stall_tile;
+};
 
 template <int CAP>
 struct TmaTable {
@@ -81,12 +95,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Wait until the barrier's phase with this parity has completed, at most
-// kWaitLimitNs; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// limit_ns; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
 }
 
@@ -151,9 +165,13 @@ struct TileCursor {
     }
 };
 
-template <class E, int DIV, int CAP>
-__global__ void __launch_bounds__(kTmaThreads, 1)
-k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map, float dop) {
+// The body of both TMA-staged fused allreduces.  TREE = false: the ring's
+// fold, element i of chunk j summed from rank j + 1 round to rank j; TREE =
+// true: the binomial tree's pairwise fold of ranks 0 .. N - 1, the same for
+// every element (the bucket is then one "chunk", tiles cut anywhere).
+template <class E, int DIV, int CAP, bool TREE>
+__device__ __forceinline__ void fused_tma_body(const TmaTable<CAP>& t, int world, const TileMap& map, float dop,
+                                               const TmaCtl& ctl) {
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
@@ -165,6 +183,8 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
     uint64_t* empty = full + kTmaStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
+    pdl_release();
+    pdl_acquire();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTmaStages; ++s) {
@@ -182,9 +202,11 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
         ic.start(map, blockIdx.x, G);
         int it = 0;
         for (; ic.k < map.total; ic.advance(map, G), ++it) {
+            if (ic.k == ctl.stall_tile) break;          // planted stall: nothing more is issued
             const int s = it % kTmaStages;
             // the stage's previous tile (it - kTmaStages) must have been read
-            if (it >= kTmaStages && !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u)) {
+            if (it >= kTmaStages &&
+                !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u, ctl.limit_ns)) {
                 atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
                 break;
             }
@@ -200,7 +222,7 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
         // be landing: wait until the consumers have drained the last stages
         for (int q = 1; q <= kTmaStages && it - q >= 0; ++q) {
             const int i2 = it - q;
-            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u);
+            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u, ctl.limit_ns);
         }
         return;
     }
@@ -213,7 +235,7 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
         int64_t e0, n;
         cc.range(map, e0, n);
         const int j = (int)cc.j;
-        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u)) {
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u, ctl.limit_ns)) {
             atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
             break;
         }
@@ -225,11 +247,17 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
         for (int u = 0; u < kTmaMaxVec; ++u) {
             const int v = threadIdx.x + u * kConsumers;
             if (v < nv) {
-                int r = start;
-                V acc = reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v];
-                for (int q = 1; q < world; ++q) {
-                    r = (r + 1 == world) ? 0 : r + 1;
-                    acc = E::vadd(acc, reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]);
+                auto staged = [&](int r) { return reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]; };
+                V acc;
+                if constexpr (TREE) {
+                    acc = tree_fold<V, CAP / kTreeGroup>(world, [](V a, V b) { return E::vadd(a, b); }, staged);
+                } else {
+                    int r = start;
+                    acc = staged(r);
+                    for (int q = 1; q < world; ++q) {
+                        r = (r + 1 == world) ? 0 : r + 1;
+                        acc = E::vadd(acc, staged(r));
+                    }
                 }
                 y[u] = E::template vdiv<DIV>(acc, dop);
             }
@@ -246,6 +274,20 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
     }
 }
 
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map, float dop, TmaCtl ctl) {
+    fused_tma_body<E, DIV, CAP, false>(t, world, map, dop, ctl);
+}
+
+// The fused binomial-tree allreduce (tree_kernels.cu's k_tree_fused) staged
+// the same way: same bytes moved, the tree's additions in the tree's order.
+template <class E, int DIV, int CAP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+k_tree_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map, float dop, TmaCtl ctl) {
+    fused_tma_body<E, DIV, CAP, true>(t, world, map, dop, ctl);
+}
+
 // ---------------------------------------------------------------------------
 // The fused view path (pack + ring + average + unpack of one bucket) with the
 // same producer / consumer structure.  The host cuts every member of the
@@ -253,10 +295,19 @@ k_ring_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 // ring start rank, and tiles are cut inside segments, so a tile never crosses
 // a chunk.  Tiles are numbered segment after segment; each CTA walks its
 // tiles k, k + G, ... and finds their segment by scanning forward.
+//
+// What a segment's 16-byte-aligned body leaves at a chunk boundary that is
+// not 16-byte aligned -- a few elements on each side, an "edge" -- is folded
+// element by element by the consumer warps of the same launch before they
+// start on their tiles (edge e by CTA e mod G, one element per thread), with
+// plain loads and stores.  An edge's elements share no 16-byte word with any
+// body, so the two kinds of store never touch the same bytes.
 // ---------------------------------------------------------------------------
 
 constexpr int kViewSegs = 224;
 constexpr int kViewPtrCap = 2816;
+constexpr int kViewEdges = 64;
+constexpr int kViewEdgeMax = 32 * kTmaConsumerWarps;   // elements of one edge: one per consumer thread
 
 struct ViewTmaBatch {
     int32_t n_seg;
@@ -267,6 +318,12 @@ struct ViewTmaBatch {
     int64_t len[kViewSegs];
     int32_t j[kViewSegs];            // ring chunk of the segment
     int32_t mem[kViewSegs];          // member slot: its rank pointers are ptr[mem * world ..]
+    int32_t n_edge;
+    int32_t e_mem[kViewEdges];       // member slot of the edge
+    int32_t e_len[kViewEdges];       // elements, at most kViewEdgeMax
+    int64_t e_start[kViewEdges];     // first element of the edge in its member
+    int64_t e_pos[kViewEdges];       // bucket position of that element
+    int64_t e_clen[kViewEdges];      // chunk length of the member's bucket
     char* ptr[kViewPtrCap];
 };
 static_assert(sizeof(ViewTmaBatch) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
@@ -286,7 +343,7 @@ struct SegCursor {
 
 template <class E, int DIV>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
+k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop, TmaCtl ctl) {
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
@@ -299,7 +356,9 @@ k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
     uint64_t* empty = full + kTmaStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
-    const int64_t total = b.tile_end[b.n_seg - 1];
+    const int64_t total = b.n_seg > 0 ? b.tile_end[b.n_seg - 1] : 0;
+    pdl_release();
+    pdl_acquire();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTmaStages; ++s) {
@@ -315,8 +374,10 @@ k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
         SegCursor sc{0};
         int it = 0;
         for (int64_t k = blockIdx.x; k < total; k += G, ++it) {
+            if (k == ctl.stall_tile) break;             // planted stall: nothing more is issued
             const int s = it % kTmaStages;
-            if (it >= kTmaStages && !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u)) {
+            if (it >= kTmaStages &&
+                !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u, ctl.limit_ns)) {
                 atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
                 break;
             }
@@ -332,9 +393,23 @@ k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
         }
         for (int q = 1; q <= kTmaStages && it - q >= 0; ++q) {
             const int i2 = it - q;
-            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u);
+            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u, ctl.limit_ns);
         }
         return;
+    }
+
+    // edges first: the first stages are still landing meanwhile
+    for (int e = blockIdx.x; e < b.n_edge; e += (int)G) {
+        const int t = threadIdx.x;
+        if (t < b.e_len[e]) {
+            const int64_t jj = (b.e_pos[e] + t) / b.e_clen[e];
+            const int start = (jj + 1 == world) ? 0 : (int)jj + 1;
+            char* const* pp = b.ptr + (size_t)b.e_mem[e] * world;
+            const int64_t el = b.e_start[e] + t;
+            auto at = [&](int r) -> const char* { return pp[r]; };
+            const S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, el), dop);
+            for (int r = 0; r < world; ++r) reinterpret_cast<S*>(pp[r])[el] = y;
+        }
     }
 
     SegCursor sc{0};
@@ -346,7 +421,7 @@ k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
         sc.range(b, k, e0, n);
         const int j = b.j[sc.seg];
         char* const* pp = b.ptr + (size_t)b.mem[sc.seg] * world;
-        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u)) {
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u, ctl.limit_ns)) {
             atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
             break;
         }
@@ -384,6 +459,18 @@ k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop) {
 // ---------------------------------------------------------------------------
 
 namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};   // ddp_set_wait_limit_ms
+std::atomic<long long> g_stall_tile{-1};                          // ddp_plant_stall (one launch)
+
+// Control of one launch: the current limit, and a planted stall, which only
+// this launch takes.
+TmaCtl take_ctl() {
+    TmaCtl c;
+    c.limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    c.stall_tile = g_stall_tile.load(std::memory_order_relaxed) < 0 ? -1 : g_stall_tile.exchange(-1);
+    return c;
+}
+
 // Per (device, kernel): the dynamic shared-memory limit set on the function so
 // far (a function attribute: it is only ever raised, never lowered, so a
 // launch with less shared memory stays valid) and the CTAs per SM measured
@@ -416,9 +503,11 @@ bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok) {
     return tma_tile_bytes(world) > 0;
 }
 
-template <class E, int DIV, int CAP>
+template <class E, int DIV, int CAP, bool TREE>
 static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
-    auto k = k_ring_fused_tma<E, DIV, CAP>;
+    void (*k)(TmaTable<CAP>, int, TileMap, float, TmaCtl);
+    if constexpr (TREE) k = k_tree_fused_tma<E, DIV, CAP>;
+    else k = k_ring_fused_tma<E, DIV, CAP>;
     const int64_t tile_bytes = tma_tile_bytes(world);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
     const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
@@ -445,41 +534,55 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
         }
     }
     TileMap map;
-    map.init(numel, chunk_len(numel, world), tile);
+    map.init(numel, TREE ? numel : chunk_len(numel, world), tile);      // the tree: one chunk
     const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, map.total));
     TmaTable<CAP> tab{};
     for (int r = 0; r < world; ++r) tab.p[r] = static_cast<char*>(ptrs[r]);
-    k<<<std::max(grid, 1), kTmaThreads, smem, st>>>(tab, world, map, dop);
+    cudaError_t e = launch_dependent(k, dim3(std::max(grid, 1)), dim3(kTmaThreads), smem, st, tab, world, map, dop,
+                                     take_ctl());
     if (debug_enabled())
-        fprintf(stderr, "[ddp] ring_fused_tma world=%d numel=%lld tile=%lld B grid=%d smem=%zu tiles=%lld\n", world,
-                (long long)numel, (long long)tile_bytes, grid, smem, (long long)map.total);
-    return cudaGetLastError();
+        fprintf(stderr, "[ddp] %s_fused_tma world=%d numel=%lld tile=%lld B grid=%d smem=%zu tiles=%lld\n",
+                TREE ? "tree" : "ring", world, (long long)numel, (long long)tile_bytes, grid, smem,
+                (long long)map.total);
+    return e;
 }
 
-template <class E, int DIV>
+template <class E, int DIV, bool TREE>
 static cudaError_t tma_cap(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
-    if (world <= 16) return tma_launch<E, DIV, 16>(world, ptrs, numel, dop, st);
-    return tma_launch<E, DIV, 128>(world, ptrs, numel, dop, st);
+    if (world <= 16) return tma_launch<E, DIV, 16, TREE>(world, ptrs, numel, dop, st);
+    if constexpr (TREE) return tma_launch<E, DIV, 64, TREE>(world, ptrs, numel, dop, st);
+    else return tma_launch<E, DIV, 128, TREE>(world, ptrs, numel, dop, st);
 }
 
-template <class E>
+template <class E, bool TREE>
 static cudaError_t tma_div(int world, void* const* ptrs, int64_t numel, DivSpec d, cudaStream_t st) {
     switch (d.mode) {
-        case kDivNone: return tma_cap<E, kDivNone>(world, ptrs, numel, d.operand, st);
-        case kDivPow2: return tma_cap<E, kDivPow2>(world, ptrs, numel, d.operand, st);
-        default: return tma_cap<E, kDivIeee>(world, ptrs, numel, d.operand, st);
+        case kDivNone: return tma_cap<E, kDivNone, TREE>(world, ptrs, numel, d.operand, st);
+        case kDivPow2: return tma_cap<E, kDivPow2, TREE>(world, ptrs, numel, d.operand, st);
+        default: return tma_cap<E, kDivIeee, TREE>(world, ptrs, numel, d.operand, st);
     }
 }
 
 cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                   cudaStream_t stream) {
-    if (dtype == DDP_F32) return tma_div<EF32>(world, ptrs, numel, div, stream);
-    return tma_div<EBF16>(world, ptrs, numel, div, stream);
+    if (dtype == DDP_F32) return tma_div<EF32, false>(world, ptrs, numel, div, stream);
+    return tma_div<EBF16, false>(world, ptrs, numel, div, stream);
+}
+
+bool tree_tma_usable(int world, int64_t numel, int dtype, bool vec_ok) {
+    if (!vec_ok || world > 64) return false;
+    return (numel * elem_bytes(dtype)) % 16 == 0 && tma_tile_bytes(world) > 0;
+}
+
+cudaError_t launch_tree_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
+                                  cudaStream_t stream) {
+    if (dtype == DDP_F32) return tma_div<EF32, true>(world, ptrs, numel, div, stream);
+    return tma_div<EBF16, true>(world, ptrs, numel, div, stream);
 }
 
 template <class E, int DIV>
 static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
-                                   int n_segs, float dop, cudaStream_t st) {
+                                   int n_segs, const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
     auto k = k_bucket_view_tma<E, DIV>;
     const int64_t tile_bytes = tma_tile_bytes(world);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
@@ -506,26 +609,68 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
             fs.per_sm[smem] = per_sm;
         }
     }
-    // launches take consecutive members (and all their segments) while the
-    // pointer and segment tables have room
+    // A launch takes consecutive members, each with its segments and edges,
+    // while the pointer, segment and edge tables have room; a member whose
+    // work does not fit goes on in the next launch, its pointers repeated.
+    static_assert(kViewEdgeMax == kTmaEdgeMax, "edge length limit differs between host and kernel");
     const int max_members = kViewPtrCap / world;
+    struct Item {
+        int member;
+        int kind;      // 0 segment, 1 edge
+        int index;
+    };
+    std::vector<Item> items;
+    items.reserve((size_t)n_segs + (size_t)n_edges);
+    {
+        int si = 0, ei = 0;                 // both lists are in member order
+        while (si < n_segs || ei < n_edges) {
+            const bool take_seg = ei >= n_edges || (si < n_segs && segs[si].member <= edges[ei].member);
+            if (take_seg) {
+                items.push_back(Item{segs[si].member, 0, si});
+                ++si;
+            } else {
+                items.push_back(Item{edges[ei].member, 1, ei});
+                ++ei;
+            }
+        }
+    }
     ViewTmaBatch b;
     b.world = world;
     b.tile = tile;
-    int si = 0;
-    while (si < n_segs) {
+    b.n_seg = 0;
+    b.n_edge = 0;
+    int64_t tiles = 0;
+    int slots = 0, last_member = -1;
+    auto flush = [&]() -> cudaError_t {
+        if (b.n_seg == 0 && b.n_edge == 0) return cudaSuccess;
+        const int64_t work = std::max<int64_t>(tiles, b.n_edge);
+        const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, work));
+        cudaError_t e = launch_dependent(k, dim3(grid), dim3(kTmaThreads), smem, st, b, dop, take_ctl());
+        if (debug_enabled())
+            fprintf(stderr, "[ddp] bucket_view_tma world=%d segments=%d edges=%d members=%d tiles=%lld grid=%d\n",
+                    world, b.n_seg, b.n_edge, slots, (long long)tiles, grid);
         b.n_seg = 0;
-        int64_t tiles = 0;
-        int first_member = segs[si].member, slots = 0, last_member = -1;
-        while (si < n_segs && b.n_seg < kViewSegs) {
-            const ViewSegment& g = segs[si];
-            if (g.member != last_member) {
-                if (slots == max_members) break;
-                const ViewMember& m = members[g.member];
-                for (int r = 0; r < world; ++r) b.ptr[(size_t)slots * world + r] = static_cast<char*>(m.ptrs[r]);
-                last_member = g.member;
-                ++slots;
-            }
+        b.n_edge = 0;
+        tiles = 0;
+        slots = 0;
+        last_member = -1;
+        return e;
+    };
+    for (const Item& it : items) {
+        const bool full_tab = (it.member != last_member && slots == max_members) ||
+                              (it.kind == 0 && b.n_seg == kViewSegs) || (it.kind == 1 && b.n_edge == kViewEdges);
+        if (full_tab) {
+            cudaError_t e = flush();
+            if (e != cudaSuccess) return e;
+        }
+        if (it.member != last_member) {
+            const ViewMember& m = members[it.member];
+            for (int r = 0; r < world; ++r) b.ptr[(size_t)slots * world + r] = static_cast<char*>(m.ptrs[r]);
+            last_member = it.member;
+            ++slots;
+        }
+        if (it.kind == 0) {
+            const ViewSegment& g = segs[it.index];
             tiles += (g.len + tile - 1) / tile;
             b.tile_end[b.n_seg] = tiles;
             b.start[b.n_seg] = g.start;
@@ -533,39 +678,48 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
             b.j[b.n_seg] = g.j;
             b.mem[b.n_seg] = slots - 1;
             ++b.n_seg;
-            ++si;
+        } else {
+            const ViewEdge& g = edges[it.index];
+            b.e_mem[b.n_edge] = slots - 1;
+            b.e_len[b.n_edge] = (int32_t)g.len;
+            b.e_start[b.n_edge] = g.start;
+            b.e_pos[b.n_edge] = members[it.member].offset + g.start;
+            b.e_clen[b.n_edge] = g.clen;
+            ++b.n_edge;
         }
-        (void)first_member;
-        if (b.n_seg == 0) break;
-        const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm, tiles));
-        k<<<grid, kTmaThreads, smem, st>>>(b, dop);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if (debug_enabled())
-            fprintf(stderr, "[ddp] bucket_view_tma world=%d segments=%d members=%d tiles=%lld grid=%d\n", world,
-                    b.n_seg, slots, (long long)tiles, grid);
     }
-    return cudaSuccess;
+    (void)n_members;
+    return flush();
 }
 
 template <class E>
-static cudaError_t view_tma_div(int world, const ViewMember* m, int nm, const ViewSegment* sg, int ns, DivSpec d,
-                                cudaStream_t st) {
+static cudaError_t view_tma_div(int world, const ViewMember* m, int nm, const ViewSegment* sg, int ns,
+                                const ViewEdge* ed, int ne, DivSpec d, cudaStream_t st) {
     switch (d.mode) {
-        case kDivNone: return view_tma_launch<E, kDivNone>(world, m, nm, sg, ns, d.operand, st);
-        case kDivPow2: return view_tma_launch<E, kDivPow2>(world, m, nm, sg, ns, d.operand, st);
-        default: return view_tma_launch<E, kDivIeee>(world, m, nm, sg, ns, d.operand, st);
+        case kDivNone: return view_tma_launch<E, kDivNone>(world, m, nm, sg, ns, ed, ne, d.operand, st);
+        case kDivPow2: return view_tma_launch<E, kDivPow2>(world, m, nm, sg, ns, ed, ne, d.operand, st);
+        default: return view_tma_launch<E, kDivIeee>(world, m, nm, sg, ns, ed, ne, d.operand, st);
     }
 }
 
 cudaError_t launch_bucket_view_tma(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
-                                   int n_segs, int dtype, DivSpec div, cudaStream_t stream) {
-    if (n_segs == 0) return cudaSuccess;
-    if (dtype == DDP_F32) return view_tma_div<EF32>(world, members, n_members, segs, n_segs, div, stream);
-    if (dtype == kDtypeHook) return view_tma_div<EHOOK>(world, members, n_members, segs, n_segs, div, stream);
-    if (dtype == kDtypeHook16) return view_tma_div<EHOOK16>(world, members, n_members, segs, n_segs, div, stream);
-    return view_tma_div<EBF16>(world, members, n_members, segs, n_segs, div, stream);
+                                   int n_segs, const ViewEdge* edges, int n_edges, int dtype, DivSpec div,
+                                   cudaStream_t stream) {
+    if (n_segs == 0 && n_edges == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return view_tma_div<EF32>(world, members, n_members, segs, n_segs, edges, n_edges, div, stream);
+    if (dtype == kDtypeHook)
+        return view_tma_div<EHOOK>(world, members, n_members, segs, n_segs, edges, n_edges, div, stream);
+    if (dtype == kDtypeHook16)
+        return view_tma_div<EHOOK16>(world, members, n_members, segs, n_segs, edges, n_edges, div, stream);
+    return view_tma_div<EBF16>(world, members, n_members, segs, n_segs, edges, n_edges, div, stream);
 }
+
+void set_wait_limit_ns(unsigned long long ns, unsigned long long* previous) {
+    const unsigned long long p = g_wait_limit_ns.exchange(ns);
+    if (previous) *previous = p;
+}
+
+void plant_stall(long long tile) { g_stall_tile.store(tile < 0 ? -1 : tile); }
 
 cudaError_t read_device_status(int32_t* out, bool clear) {
     int32_t v = 0;

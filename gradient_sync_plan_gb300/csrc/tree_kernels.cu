@@ -29,42 +29,16 @@ struct TreeTable {
     char* p[CAP];
 };
 
-constexpr int kTreeGroup = 16;
 constexpr int kTreeMaxWorld = 4 * kTreeGroup;   // 64
 
-// Binomial pairwise sum of load(0) .. load(world - 1), world <= 64.  Ranks are
-// folded in groups of 16 (levels 1, 2, 4, 8 inside a group), then the group
-// sums at levels 16 and 32 -- exactly the tree's additions, in its order.
-template <class T, class Add, class Load>
-__device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
-    T gs[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        if (kTreeGroup * g < world) {
-            T v[kTreeGroup];
-#pragma unroll
-            for (int i = 0; i < kTreeGroup; ++i)
-                if (kTreeGroup * g + i < world) v[i] = load(kTreeGroup * g + i);
-#pragma unroll
-            for (int d = 1; d < kTreeGroup; d <<= 1)
-#pragma unroll
-                for (int i = 0; i < kTreeGroup; i += 2 * d)
-                    if (kTreeGroup * g + i + d < world) v[i] = add(v[i], v[i + d]);
-            gs[g] = v[0];
-        }
-    }
-    if (16 < world) gs[0] = add(gs[0], gs[1]);
-    if (48 < world) gs[2] = add(gs[2], gs[3]);
-    if (32 < world) gs[0] = add(gs[0], gs[2]);
-    return gs[0];
-}
-
-template <class E, int DIV, int CAP>
+template <class E, int DIV, int CAP, int NG>
 __global__ void __launch_bounds__(kThreads)
 k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel, int vec_ok, float dop) {
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
+    pdl_release();
+    pdl_acquire();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int64_t done = 0;
@@ -72,16 +46,16 @@ k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel,
         const int64_t nv = numel / L;
         for (int64_t v = tid; v < nv; v += stride) {
             const int64_t off = v * 16;
-            V y = tree_fold<V>(world, [](V a, V b) { return E::vadd(a, b); },
-                               [&](int r) { return ld_stream<V>(t.p[r] + off); });
+            V y = tree_fold<V, NG>(world, [](V a, V b) { return E::vadd(a, b); },
+                                   [&](int r) { return ld_stream<V>(t.p[r] + off); });
             y = E::template vdiv<DIV>(y, dop);
             for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
         }
         done = nv * L;
     }
     for (int64_t e = done + tid; e < numel; e += stride) {
-        S y = tree_fold<S>(world, [](S a, S b) { return E::sadd(a, b); },
-                           [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
+        S y = tree_fold<S, NG>(world, [](S a, S b) { return E::sadd(a, b); },
+                               [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
         y = E::template sdiv<DIV>(y, dop);
         for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = y;
     }
@@ -206,14 +180,22 @@ static TreeTable<CAP> tree_table(int world, void* const* ptrs) {
     return t;
 }
 
+template <class E, int DIV, int NG>
+static cudaError_t tree_fused_launch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
+                                     cudaStream_t st) {
+    auto k = k_tree_fused<E, DIV, kTreeGroup * NG, NG>;
+    const int64_t work = vec_ok ? (numel + E::L - 1) / E::L : numel;
+    const int grid = grid_for((const void*)k, work);
+    return launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, tree_table<kTreeGroup * NG>(world, ptrs), world,
+                            numel, vec_ok ? 1 : 0, dop);
+}
+
 template <class E, int DIV>
 static cudaError_t tree_fused_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                    cudaStream_t st) {
-    auto k = k_tree_fused<E, DIV, kTreeMaxWorld>;
-    const int64_t work = vec_ok ? (numel + E::L - 1) / E::L : numel;
-    const int grid = grid_for((const void*)k, work);
-    k<<<grid, kThreads, 0, st>>>(tree_table<kTreeMaxWorld>(world, ptrs), world, numel, vec_ok ? 1 : 0, dop);
-    return cudaGetLastError();
+    if (world <= kTreeGroup) return tree_fused_launch<E, DIV, 1>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 2 * kTreeGroup) return tree_fused_launch<E, DIV, 2>(world, ptrs, numel, dop, vec_ok, st);
+    return tree_fused_launch<E, DIV, 4>(world, ptrs, numel, dop, vec_ok, st);
 }
 
 constexpr int kTreeGroupThreads = 128;
@@ -318,6 +300,21 @@ static cudaError_t tree_group_by_div(int world, void* const* ptrs, int64_t numel
     }
 }
 
+// The TMA-staged kernel for buckets streamed from HBM over a few ranks (the
+// fused ring's rule), or when forced.
+static bool tree_use_tma(int world, int64_t numel, int dtype, bool vec_ok) {
+    if (!tree_tma_usable(world, numel, dtype, vec_ok)) return false;
+    switch (fused_kernel_override()) {
+        case DDP_FUSED_TMA: return true;
+        case DDP_FUSED_GROUP:
+        case DDP_FUSED_VECTOR: return false;
+        default: break;
+    }
+    const int64_t total = numel * elem_bytes(dtype) * world;
+    return (world <= 8 && total > ((int64_t)128 << 20)) ||
+           (world <= 16 && dtype == DDP_BF16 && total >= ((int64_t)64 << 20));
+}
+
 cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                   bool vec_ok, cudaStream_t stream) {
     if (numel == 0) return cudaSuccess;
@@ -326,6 +323,8 @@ cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int
         if (dtype == DDP_F32) return tree_group_by_div<EF32>(world, ptrs, numel, div, stream);
         return tree_group_by_div<EBF16>(world, ptrs, numel, div, stream);
     }
+    if (!staged && tree_use_tma(world, numel, dtype, vec_ok))
+        return launch_tree_fused_tma(world, ptrs, numel, dtype, div, stream);
     if (dtype == DDP_F32) return tree_by_div<EF32>(staged, world, ptrs, numel, div, vec_ok, stream);
     return tree_by_div<EBF16>(staged, world, ptrs, numel, div, vec_ok, stream);
 }

@@ -116,8 +116,11 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  *                    copies (N <= 128, 16-byte-aligned chunks).
  * A kernel that cannot run a call (alignment, world size) is replaced by
  * the vector kernel, or the element-wise one for unaligned buffers.
- * tree_allreduce_fused follows the same choice between its group and vector
- * kernels (DDP_FUSED_TMA selects its vector kernel: the tree has no TMA one).
+ * tree_allreduce_fused follows the same choice among its own group, vector
+ * and TMA kernels (its TMA kernel folds the staged tiles in the tree's
+ * order; it takes buckets whose bytes per rank are a multiple of 16, N <= 64;
+ * by size it runs for up to 8 ranks with more than 128 MiB over all ranks,
+ * or up to 16 ranks of bf16 with at least 64 MiB).
  * *previous (if not NULL) receives the old choice.  DDP_ERR_INVALID for an
  * unknown kind.
  */
@@ -139,6 +142,36 @@ int32_t ddp_set_fused_kernel(int32_t kind, int32_t* previous);
  * Returns DDP_OK, DDP_ERR_INVALID (status NULL) or DDP_ERR_CUDA.
  */
 int32_t ddp_device_status(int32_t* status, int32_t clear);
+
+/*
+ * ddp_set_wait_limit_ms -- limit of every bounded device-side wait in the
+ * TMA-staged kernels (the fused ring's, the fused tree's and the fused
+ * view's), in
+ * milliseconds, for launches from now on in this process; 0 restores the
+ * default of 2000 ms.  A kernel whose wait runs out sets the device status
+ * word to DDP_ERR_TIMEOUT (ddp_device_status) and stops early instead of
+ * hanging.  The pages describe the hang this guards against: a collective
+ * waits for every rank, so a rank that never joins stalls the others
+ * without an error ([P2] "INVARIANT 2" and "常见疑问" Q2).  Results do not
+ * depend on the limit.  *previous_ms (if not NULL) receives the old limit.
+ * DDP_ERR_INVALID unless 0 <= limit_ms <= 600000.
+ */
+int32_t ddp_set_wait_limit_ms(int32_t limit_ms, int32_t* previous_ms);
+
+/*
+ * ddp_plant_stall -- a test hook that plants the hang of [P2] "常见疑问" Q2 on
+ * the GPU.  The next launch of a TMA-staged kernel (see
+ * ddp_set_wait_limit_ms) takes the plant: the producer warp of the CTA that
+ * owns tile `tile` of that launch issues no bulk copy for that tile or any
+ * later one, and waits for the copies it did issue to be consumed; the CTA's
+ * consumers wait for the missing tile until the wait limit runs out, set
+ * DDP_ERR_TIMEOUT and stop.  No copy is left in flight and no memory is
+ * touched out of bounds; the call's buffers hold partial results.  A tile
+ * number beyond the launch's tiles plants nothing (the launch still takes
+ * the plant).  tile = -1 removes a plant that no launch has taken yet.
+ * Returns DDP_OK, or DDP_ERR_INVALID for tile < -1.
+ */
+int32_t ddp_plant_stall(int64_t tile);
 
 /*
  * ddp_plan_buckets -- assign parameters to buckets ([P1] section 03 "Bucket"

@@ -184,6 +184,14 @@ def test_pack_unpack_view_reject_bad_plans():
     assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), b_of, i64(0), 1, i64(4), _vp(A), 0, 1, 0, None) == -1
     assert L.ddp_sync_buckets(1, 1, _vp(G0), i64(4), (ctypes.c_int32 * 1)(0), i64(0), 1, i64(4), _vp(A), 0, 1,
                               7, None) == -1      # unknown algorithm
+    # sync_buckets writes the gradients back (unfused and bf16-hook paths,
+    # whole buckets or L2-sized pieces): two ranks' gradients sharing memory
+    # are refused before anything is enqueued
+    BA, BB = 0x7e0000000000, 0x7e8000000000          # buckets far from the gradients
+    for algo in (ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_BF16_HOOK):
+        for bucket_numel in (4, 64 << 20):           # one whole bucket; a bucket cut into pieces
+            assert L.ddp_sync_buckets(2, 1, _vp(G0, G0 + 8), i64(4), (ctypes.c_int32 * 1)(0), i64(0), 1,
+                                      i64(bucket_numel), _vp(BA, BB), 0, 2, algo, None) == -1
 
 
 def test_sizes_beyond_the_caps_are_refused_before_any_byte_arithmetic():
@@ -290,6 +298,17 @@ def test_process_wide_knobs_validate_and_return_previous():
     assert L.ddp_set_fused_kernel(ddp.DDP_FUSED_AUTO, None) == 0      # previous may be NULL
     assert ddp.ddp_set_max_ctas(5) == 0
     assert ddp.ddp_set_max_ctas(0) == 5
+    # wait limit of the TMA kernels: 0 restores the 2000 ms default
+    for bad in (-1, 600001):
+        assert L.ddp_set_wait_limit_ms(bad, ctypes.byref(prev)) == -1
+    assert prev.value == -7
+    assert ddp.ddp_set_wait_limit_ms(100) == 2000
+    assert ddp.ddp_set_wait_limit_ms(0) == 100
+    assert ddp.ddp_set_wait_limit_ms(0) == 2000
+    assert L.ddp_set_wait_limit_ms(2000, None) == 0
+    # planted stall: -1 clears, anything below is refused
+    assert L.ddp_plant_stall(-2) == -1
+    assert L.ddp_plant_stall(5) == 0 and L.ddp_plant_stall(-1) == 0
 
 
 def test_plain_c_client_links_and_plans(tmp_path):
