@@ -304,36 +304,42 @@ k_tree_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 // body, so the two kinds of store never touch the same bytes.
 // ---------------------------------------------------------------------------
 
-constexpr int kViewSegs = 224;
-constexpr int kViewPtrCap = 2816;
-constexpr int kViewEdges = 64;
 constexpr int kViewEdgeMax = 32 * kTmaConsumerWarps;   // elements of one edge: one per consumer thread
 
+// One launch's table.  Two capacities: a launch's parameters are copied for
+// every eager launch, so a call with few segments (one bucket piece, one
+// small bucket) sends about 4 KB instead of the 32 KB of the large table.
+template <int SEGS, int PTRS, int EDGES>
 struct ViewTmaBatch {
+    static constexpr int kSegs = SEGS, kPtrs = PTRS, kEdges = EDGES;
     int32_t n_seg;
     int32_t world;
-    int64_t tile;                    // elements per tile
-    int64_t tile_end[kViewSegs];     // inclusive prefix of tiles per segment
-    int64_t start[kViewSegs];        // first element of the segment in its member
-    int64_t len[kViewSegs];
-    int32_t j[kViewSegs];            // ring chunk of the segment
-    int32_t mem[kViewSegs];          // member slot: its rank pointers are ptr[mem * world ..]
+    int64_t tile;               // elements per tile
+    int64_t tile_end[SEGS];     // inclusive prefix of tiles per segment
+    int64_t start[SEGS];        // first element of the segment in its member
+    int64_t len[SEGS];
+    int32_t j[SEGS];            // ring chunk of the segment
+    int32_t mem[SEGS];          // member slot: its rank pointers are ptr[mem * world ..]
     int32_t n_edge;
-    int32_t e_mem[kViewEdges];       // member slot of the edge
-    int32_t e_len[kViewEdges];       // elements, at most kViewEdgeMax
-    int64_t e_start[kViewEdges];     // first element of the edge in its member
-    int64_t e_pos[kViewEdges];       // bucket position of that element
-    int64_t e_clen[kViewEdges];      // chunk length of the member's bucket
-    char* ptr[kViewPtrCap];
+    int32_t e_mem[EDGES];       // member slot of the edge
+    int32_t e_len[EDGES];       // elements, at most kViewEdgeMax
+    int64_t e_start[EDGES];     // first element of the edge in its member
+    int64_t e_pos[EDGES];       // bucket position of that element
+    int64_t e_clen[EDGES];      // chunk length of the member's bucket
+    char* ptr[PTRS];
 };
-static_assert(sizeof(ViewTmaBatch) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
+using ViewTmaSmall = ViewTmaBatch<32, 256, 16>;
+using ViewTmaLarge = ViewTmaBatch<224, 2816, 64>;
+static_assert(sizeof(ViewTmaLarge) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
 
 struct SegCursor {
     int seg;
-    __device__ void seek(const ViewTmaBatch& b, int64_t k) {
+    template <class B>
+    __device__ void seek(const B& b, int64_t k) {
         while (b.tile_end[seg] <= k) ++seg;
     }
-    __device__ void range(const ViewTmaBatch& b, int64_t k, int64_t& e0, int64_t& n) const {
+    template <class B>
+    __device__ void range(const B& b, int64_t k, int64_t& e0, int64_t& n) const {
         const int64_t first = seg ? b.tile_end[seg - 1] : 0;
         const int64_t off = (k - first) * b.tile;
         e0 = b.start[seg] + off;
@@ -341,9 +347,9 @@ struct SegCursor {
     }
 };
 
-template <class E, int DIV>
+template <class E, int DIV, class B>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-k_bucket_view_tma(const __grid_constant__ ViewTmaBatch b, float dop, TmaCtl ctl) {
+k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
     using V = typename E::V;
     using S = typename E::S;
     constexpr int L = E::L;
@@ -580,10 +586,10 @@ cudaError_t launch_tree_fused_tma(int world, void* const* ptrs, int64_t numel, i
     return tma_div<EBF16, true>(world, ptrs, numel, div, stream);
 }
 
-template <class E, int DIV>
-static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_members, const ViewSegment* segs,
-                                   int n_segs, const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
-    auto k = k_bucket_view_tma<E, DIV>;
+template <class E, int DIV, class BT>
+static cudaError_t view_tma_launch(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
+                                   const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
+    auto k = k_bucket_view_tma<E, DIV, BT>;
     const int64_t tile_bytes = tma_tile_bytes(world);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
     const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
@@ -613,7 +619,7 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
     // while the pointer, segment and edge tables have room; a member whose
     // work does not fit goes on in the next launch, its pointers repeated.
     static_assert(kViewEdgeMax == kTmaEdgeMax, "edge length limit differs between host and kernel");
-    const int max_members = kViewPtrCap / world;
+    const int max_members = BT::kPtrs / world;
     struct Item {
         int member;
         int kind;      // 0 segment, 1 edge
@@ -634,7 +640,7 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
             }
         }
     }
-    ViewTmaBatch b;
+    BT b;
     b.world = world;
     b.tile = tile;
     b.n_seg = 0;
@@ -658,7 +664,7 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
     };
     for (const Item& it : items) {
         const bool full_tab = (it.member != last_member && slots == max_members) ||
-                              (it.kind == 0 && b.n_seg == kViewSegs) || (it.kind == 1 && b.n_edge == kViewEdges);
+                              (it.kind == 0 && b.n_seg == BT::kSegs) || (it.kind == 1 && b.n_edge == BT::kEdges);
         if (full_tab) {
             cudaError_t e = flush();
             if (e != cudaSuccess) return e;
@@ -688,17 +694,30 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, int n_m
             ++b.n_edge;
         }
     }
-    (void)n_members;
     return flush();
+}
+
+// The small table when the whole call fits in it, else the large one.
+template <class E, int DIV>
+static cudaError_t view_tma_pick(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
+                                 const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
+    int n_members = 0, last = -1;
+    for (int i = 0; i < n_segs; ++i)
+        if (segs[i].member != last) last = segs[i].member, ++n_members;
+    for (int i = 0; i < n_edges; ++i) ++n_members;            // at most one more slot per edge
+    if (n_segs <= ViewTmaSmall::kSegs && n_edges <= ViewTmaSmall::kEdges &&
+        (int64_t)n_members * world <= ViewTmaSmall::kPtrs)
+        return view_tma_launch<E, DIV, ViewTmaSmall>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    return view_tma_launch<E, DIV, ViewTmaLarge>(world, members, segs, n_segs, edges, n_edges, dop, st);
 }
 
 template <class E>
 static cudaError_t view_tma_div(int world, const ViewMember* m, int nm, const ViewSegment* sg, int ns,
                                 const ViewEdge* ed, int ne, DivSpec d, cudaStream_t st) {
     switch (d.mode) {
-        case kDivNone: return view_tma_launch<E, kDivNone>(world, m, nm, sg, ns, ed, ne, d.operand, st);
-        case kDivPow2: return view_tma_launch<E, kDivPow2>(world, m, nm, sg, ns, ed, ne, d.operand, st);
-        default: return view_tma_launch<E, kDivIeee>(world, m, nm, sg, ns, ed, ne, d.operand, st);
+        case kDivNone: return view_tma_pick<E, kDivNone>(world, m, sg, ns, ed, ne, d.operand, st);
+        case kDivPow2: return view_tma_pick<E, kDivPow2>(world, m, sg, ns, ed, ne, d.operand, st);
+        default: return view_tma_pick<E, kDivIeee>(world, m, sg, ns, ed, ne, d.operand, st);
     }
 }
 
