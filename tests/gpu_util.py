@@ -154,3 +154,51 @@ def require_host_memory(nbytes: int, what: str) -> None:
     if avail is not None and avail < 1.5 * nbytes + (8 << 30):
         pytest.skip(f"{what}: needs about {nbytes / 2**30:.1f} GiB of host memory, "
                     f"{avail / 2**30:.1f} GiB available")
+
+
+# --------------------------------------------------------------------------
+# Canary guards: a region before and after a buffer, checked after the call
+# --------------------------------------------------------------------------
+
+CANARY_BYTES = 4096       # a multiple of 512: the guarded block keeps its alignment
+
+
+def _canary_view(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def _canary_value(t: torch.Tensor) -> int:
+    return 0x7FBD if t.element_size() == 2 else 0x7FBADBAD      # a quiet NaN no kernel here produces
+
+
+def guarded(shape, dtype, device="cuda"):
+    """(storage, view): a device tensor of `shape` inside a 1-D storage with
+    CANARY_BYTES of canary pattern before and after it.  The view starts
+    CANARY_BYTES after the allocation, so it has the alignment a fresh
+    allocation of its own would have."""
+    es = torch.empty((), dtype=dtype).element_size()
+    pad = CANARY_BYTES // es
+    n = 1
+    for d in shape:
+        n *= int(d)
+    storage = torch.empty(n + 2 * pad, dtype=dtype, device=device)
+    _canary_view(storage).fill_(_canary_value(storage))
+    return storage, storage[pad:pad + n].view(*shape)
+
+
+def guarded_copy(x: torch.Tensor, device="cuda"):
+    storage, view = guarded(tuple(x.shape), x.dtype, device)
+    view.copy_(x)
+    return storage, view
+
+
+def assert_canaries(storage: torch.Tensor, what: str = "") -> None:
+    """The guard regions of a `guarded` storage still hold the pattern."""
+    pad = CANARY_BYTES // storage.element_size()
+    v = _canary_view(storage)
+    want = _canary_value(storage)
+    for name, part in (("before", v[:pad]), ("after", v[v.numel() - pad:])):
+        bad = (part != want).nonzero()
+        if bad.numel():
+            raise AssertionError(f"{what}: {bad.numel()} guard elements {name} the buffer were overwritten "
+                                 f"(first at guard offset {int(bad[0, 0])})")

@@ -21,7 +21,7 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, f32_or_bits, oracle_allreduce
+from gpu_util import assert_bits_equal, assert_canaries, f32_or_bits, guarded_copy, oracle_allreduce
 
 pytestmark = pytest.mark.gpu
 MiB = 1 << 20
@@ -95,13 +95,14 @@ def test_sync_buckets_small_decoder(algo, dtype):
     plan = ddp.ddp_plan_buckets(numels, ddp.BF16 if dtype == "bf16" else ddp.F32, first, cap)
     assert len(plan[2]) > 5
     flat, grads_h = _host_grads(numels, world, dtype, seed0=0)
-    gdev_flat = flat.cuda()
+    g_storage, gdev_flat = guarded_copy(flat)
     gdev = _device_views(gdev_flat, numels)
     bk = None
     if algo != ddp.DDP_ALGO_VIEW:
         bk = [[torch.empty(int(n), dtype=flat.dtype, device="cuda") for n in plan[2]] for _ in range(world)]
     ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
     torch.cuda.synchronize()
+    assert_canaries(g_storage, f"small decoder algo={algo}")
     oracle.ddp_sync(grads_h, oracle.BF16 if dtype == "bf16" else oracle.F32, first, cap)
     got = f32_or_bits(gdev_flat)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
@@ -143,13 +144,14 @@ def test_resnet50_bf16_n16_cap_sweep_full(cap_mib, count, algo):
     plan = ddp.ddp_plan_buckets(numels, ddp.BF16, MiB, cap_mib * MiB)
     assert len(plan[2]) == count
     flat, grads_h = _host_grads(numels, world, "bf16", seed0=0)
-    gdev_flat = flat.cuda()
+    g_storage, gdev_flat = guarded_copy(flat)
     gdev = _device_views(gdev_flat, numels)
     bk = None
     if algo == ddp.DDP_ALGO_FUSED:
         bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
     ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
     torch.cuda.synchronize()
+    assert_canaries(g_storage, f"resnet50 cap {cap_mib} algo {algo}")
     ref64 = np.zeros(sum(numels))
     for r in range(world):
         ref64 += oracle.bf16_to_f32(np.concatenate(grads_h[r])).astype(np.float64)
@@ -565,7 +567,7 @@ def test_large_bucket_in_l2_pieces_matches_oracle(via, dtype):
     plan = ddp.ddp_plan_buckets(numels, code, 1 << 40, 1 << 40)
     assert len(plan[2]) == 1 and plan[2][0] > 2 * piece
     flat, grads_h = _host_grads(numels, world, gdt, seed0=81)
-    g = flat.cuda()
+    g_storage, g = guarded_copy(flat)
     views = _device_views(g, numels)
     tdt = torch.bfloat16 if es == 2 else torch.float32
     bk = [[torch.empty(int(plan[2][0]), dtype=tdt, device="cuda")] for _ in range(world)]
@@ -578,6 +580,7 @@ def test_large_bucket_in_l2_pieces_matches_oracle(via, dtype):
             red.mark_ready(p, torch.cuda.current_stream())
         red.finalize(torch.cuda.current_stream())
     torch.cuda.synchronize()
+    assert_canaries(g_storage, f"pieces {dtype} via {via}")
     if hook:
         oracle.ddp_sync_bf16_hook(grads_h, 1 << 40, 1 << 40)
     else:

@@ -15,6 +15,8 @@ reducer:
   * the bf16 compression hook, unfused and fused, and the fused fp16 hook;
   * no_sync: 4 micro-batches (rank r's m-th from seed r + 8m) accumulated
     locally, then one sync.
+The gradient arena and every bucket buffer sit between canary regions,
+checked after each step.
 """
 import numpy as np
 import pytest
@@ -23,7 +25,8 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_device_equals_host, host_snapshot, require_host_memory
+from gpu_util import (assert_canaries, assert_device_equals_host, guarded, guarded_copy, host_snapshot,
+                      require_host_memory)
 
 pytestmark = pytest.mark.gpu
 MiB = 1 << 20
@@ -91,12 +94,21 @@ def _plan():
 
 
 def _buckets(plan, dtype):
-    return [[torch.empty(int(n), dtype=dtype, device="cuda") for n in plan[2]] for _ in range(WORLD)]
+    """Every rank's bucket buffers, each between canary regions: (storages, buffers)."""
+    storages, bk = [], []
+    for _ in range(WORLD):
+        row = []
+        for n in plan[2]:
+            st, b = guarded((int(n),), dtype)
+            storages.append(st)
+            row.append(b)
+        bk.append(row)
+    return storages, bk
 
 
 def _run(kind, algo, via="sync_buckets"):
     g0, want = _expected(kind)
-    g = g0.clone()
+    g_storage, g = guarded_copy(g0)
     if kind == "no_sync":
         for m in range(1, MICRO):
             gm = _draw(m)
@@ -104,11 +116,11 @@ def _run(kind, algo, via="sync_buckets"):
             torch.cuda.synchronize()
             del gm
     plan = _plan()
-    bk = None
+    bk, bk_storages = None, []
     if algo in (ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_STAGED):
-        bk = _buckets(plan, torch.float32)
+        bk_storages, bk = _buckets(plan, torch.float32)
     elif algo == ddp.DDP_ALGO_BF16_HOOK:
-        bk = _buckets(plan, torch.bfloat16)
+        bk_storages, bk = _buckets(plan, torch.bfloat16)
     views = _views(g)
     if via == "sync_buckets":
         ddp.ddp_sync_buckets(views, plan, bk, algo=algo)
@@ -121,7 +133,10 @@ def _run(kind, algo, via="sync_buckets"):
     torch.cuda.synchronize()
     if via != "sync_buckets":
         red.close()
-    del bk
+    assert_canaries(g_storage, f"decoder gradients algo={algo}")
+    for st in bk_storages:
+        assert_canaries(st, f"decoder bucket algo={algo}")
+    del bk, bk_storages
     assert_device_equals_host(g, want, f"decoder {kind} algo={algo} via {via}")
     assert ddp.ddp_device_status() == 0
 

@@ -15,7 +15,8 @@ final state):
   * 2 ranks of just over 2^31 elements each (indices past 32 bits).
 
 Inputs are drawn on a CUDA generator (rank r from seed r) and snapshot to the
-host before any kernel runs; the oracle runs on that snapshot.  Each case's
+host before any kernel runs; the oracle runs on that snapshot.  Every run's
+buffer sits between two canary regions, checked after the call.  Each case's
 input and expected result are kept only while its tests run.
 """
 import pytest
@@ -24,7 +25,8 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_device_equals_host, host_snapshot, require_host_memory
+from gpu_util import (assert_canaries, assert_device_equals_host, guarded_copy, host_snapshot,
+                      require_host_memory)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,13 +94,14 @@ def _inputs(N, S, kind, std, dtype):
 
 def _check(kernel, N, S, kind, std, dtype):
     x0, want, ref64 = _inputs(N, S, kind, std, dtype)
-    x = x0.clone()
+    storage, x = guarded_copy(x0)
     KERNELS[kernel](x, N)
     torch.cuda.synchronize()
+    assert_canaries(storage, f"{kernel} N={N} S={S}")
     assert_device_equals_host(x, want, f"{kernel} N={N} S={S} {dtype}")
     err = torch.linalg.vector_norm(x[0].to(torch.float64) - ref64) / torch.linalg.vector_norm(ref64)
     assert float(err) <= (2e-2 if dtype == "bf16" else 1e-5)
-    del x
+    del x, storage
 
 
 @pytest.mark.parametrize("kernel", ["fused", "fused_vector", "staged", "persistent"])

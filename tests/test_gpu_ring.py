@@ -18,7 +18,7 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, f32_or_bits, from_np, oracle_allreduce
+from gpu_util import assert_bits_equal, assert_canaries, f32_or_bits, from_np, guarded_copy, oracle_allreduce
 
 pytestmark = pytest.mark.gpu
 
@@ -32,9 +32,10 @@ KERNELS = {"fused": ddp.ring_allreduce_fused, "staged": ddp.ring_allreduce_stage
 
 
 def run_gpu(kernel: str, x_host: np.ndarray, divisor: int) -> np.ndarray:
-    x = from_np(x_host)
+    storage, x = guarded_copy(from_np(x_host))
     KERNELS[kernel](x, divisor)
     torch.cuda.synchronize()
+    assert_canaries(storage, f"{kernel} {tuple(x.shape)}")
     return f32_or_bits(x)
 
 

@@ -13,7 +13,8 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, assert_device_equals_host, f32_or_bits, from_np, host_snapshot, require_host_memory
+from gpu_util import (assert_bits_equal, assert_canaries, assert_device_equals_host, f32_or_bits, from_np,
+                      guarded_copy, host_snapshot, require_host_memory)
 
 pytestmark = pytest.mark.gpu
 
@@ -27,9 +28,10 @@ def oracle_tree(x, divisor):
 
 
 def run(kernel, xh, divisor):
-    x = from_np(xh)
+    storage, x = guarded_copy(from_np(xh))
     TREE[kernel](x, divisor)
     torch.cuda.synchronize()
+    assert_canaries(storage, f"tree {kernel} {tuple(x.shape)}")
     return f32_or_bits(x)
 
 
@@ -95,7 +97,7 @@ def test_one_gib_buckets_full(kernel):
         oracle.tree_allreduce_2d(want, oracle.F32, N)
         _gib["case"] = (x0, want)
     x0, want = _gib["case"]
-    x = x0.clone()
+    storage, x = guarded_copy(x0)
     if kernel == "fused_vector":                  # the size rule picks the TMA kernel here
         prev = ddp.ddp_set_fused_kernel(ddp.DDP_FUSED_VECTOR)
         try:
@@ -105,6 +107,7 @@ def test_one_gib_buckets_full(kernel):
     else:
         TREE[kernel](x, N)
     torch.cuda.synchronize()
+    assert_canaries(storage, f"1 GiB tree {kernel}")
     assert_device_equals_host(x, want, f"1 GiB tree {kernel}")
     del x
 

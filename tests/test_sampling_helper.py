@@ -44,3 +44,20 @@ def test_full_size_compare_helpers_find_a_planted_difference(dtype):
         v[r, i] ^= 1
         with pytest.raises(AssertionError, match=f"rank {r}: 1 mismatches .* first at {i}"):
             assert_device_equals_host(x, bad, "planted", piece=1000)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_canary_guards_keep_alignment_and_catch_overwrites(dtype):
+    # the guards the GPU parity tests put around their buffers, on CPU tensors
+    from gpu_util import CANARY_BYTES, assert_canaries, guarded
+    storage, view = guarded((3, 1001), dtype, device="cpu")
+    assert view.data_ptr() - storage.data_ptr() == CANARY_BYTES and CANARY_BYTES % 512 == 0
+    view.fill_(1.0)
+    assert_canaries(storage, "untouched")
+    iv = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    pad = CANARY_BYTES // view.element_size()
+    for where in (0, pad - 1, storage.numel() - pad, storage.numel() - 1):
+        bad = storage.clone()
+        bad.view(iv)[where] = 0
+        with pytest.raises(AssertionError, match="guard elements"):
+            assert_canaries(bad, "planted")
