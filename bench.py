@@ -886,8 +886,9 @@ def run_cap_sweep(args):
     """Bucket-cap sweep (the pages' 6/12/25/50 MB bucket-size sweep):
     the DDP step for ResNet-50 in bf16 at N = 16 (caps 5, 10, 25, 50 MiB) and
     for the 355M decoder in fp32 at N = 8 (caps 6, 12, 25, 50 MiB), first
-    bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  One
-    JSON line per point."""
+    bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  Each
+    step is captured as one CUDA graph; ten replays run back to back per
+    timing.  One JSON line per point."""
     import torch
     import gradient_sync_plan_gb300 as ddp
     import workloads
@@ -923,17 +924,24 @@ def run_cap_sweep(args):
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=s):
                     call(s)
+                # steady state: R steps replayed back to back between the
+                # events (as training runs them), so no step pays the launch
+                # latency of a graph started on an idle GPU; best of 5
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                R = 10
+                graph.replay()
                 best = None
                 for _ in range(5):
                     torch.cuda.synchronize()
                     e0.record()
-                    graph.replay()
+                    for _r in range(R):
+                        graph.replay()
                     e1.record()
                     torch.cuda.synchronize()
-                    t = e0.elapsed_time(e1)
+                    t = e0.elapsed_time(e1) / R
                     best = t if best is None else min(best, t)
-                row[name] = {"ms_per_step": best, "hbm_alg_gbs": per_elem * N * total * es / (best / 1e3) / 1e9}
+                row[name] = {"ms_per_step": best, "hbm_alg_gbs": per_elem * N * total * es / (best / 1e3) / 1e9,
+                             "timing": f"{R} graph replays back to back, best of 5"}
                 del graph
             print(json.dumps(row), flush=True)
             del buckets
@@ -1020,7 +1028,8 @@ def run_profile_kernels(args):
     per-kernel ncu DRAM capture: N = 8 ranks x 2^25 fp32 (128 MiB per rank,
     1 GiB over all ranks), in this order -- fused ring (vector, then TMA
     kernel), staged ring, persistent ring, fused tree (vector, then TMA
-    kernel), staged tree, no_sync accumulation, bf16 pack and unpack (one 2^25-element
+    kernel), staged tree, no_sync accumulation, pack and unpack of one
+    bucket of 4 members per rank, bf16 pack and unpack (one 2^25-element
     member per rank), fused view (one bucket of 4 members per rank).  --steps
     repeats the sequence.  Prints one JSON line (not a bench result)."""
     import torch
@@ -1035,6 +1044,7 @@ def run_profile_kernels(args):
     y = torch.empty_like(x)
     y.copy_(x)
     b16 = torch.empty((N, S), dtype=torch.bfloat16, device=dev)
+    bk = torch.empty((N, S), dtype=torch.float32, device=dev)
     members = [S // 4] * 4
     offs = [0, S // 4, S // 2, 3 * S // 4]
     views = [[x[r, o:o + n] for o, n in zip(offs, members)] for r in range(N)]
@@ -1055,6 +1065,8 @@ def run_profile_kernels(args):
            ("tree_fused_tma", lambda: forced(ddp.DDP_FUSED_TMA, lambda: ddp.tree_allreduce_fused(x, N))),
            ("tree_staged", lambda: ddp.tree_allreduce_staged(x, N)),
            ("accumulate", lambda: ddp.ddp_grad_accumulate(x, y)),
+           ("pack", lambda: ddp.ddp_bucket_pack(views, offs, bk)),
+           ("unpack", lambda: ddp.ddp_bucket_unpack(views, offs, bk)),
            ("pack_bf16", lambda: ddp.ddp_bucket_pack_bf16([[x[r]] for r in range(N)], [0], b16)),
            ("unpack_bf16", lambda: ddp.ddp_bucket_unpack_bf16([[y[r]] for r in range(N)], [0], b16)),
            ("view", lambda: ddp.ddp_bucket_allreduce_view(views, offs, S, N))]
