@@ -886,9 +886,9 @@ def run_cap_sweep(args):
     """Bucket-cap sweep (the pages' 6/12/25/50 MB bucket-size sweep):
     the DDP step for ResNet-50 in bf16 at N = 16 (caps 5, 10, 25, 50 MiB) and
     for the 355M decoder in fp32 at N = 8 (caps 6, 12, 25, 50 MiB), first
-    bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  Each
-    step is captured as one CUDA graph; ten replays run back to back per
-    timing.  One JSON line per point."""
+    bucket 1 MiB, pack + fused ring + unpack vs the fused view path.  Ten
+    steps run back to back per timing, as eager calls and as replays of a
+    CUDA graph of one step.  One JSON line per point."""
     import torch
     import gradient_sync_plan_gb300 as ddp
     import workloads
@@ -924,24 +924,35 @@ def run_cap_sweep(args):
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=s):
                     call(s)
-                # steady state: R steps replayed back to back between the
-                # events (as training runs them), so no step pays the launch
-                # latency of a graph started on an idle GPU; best of 5
+                # steady state: R steps back to back between the events, as a
+                # training loop issues them -- eager calls on one stream (each
+                # kernel's launch overlaps the previous kernel's tail), and
+                # graph replays (each replay starts after the previous one
+                # ends); best of 5 each
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 R = 10
-                graph.replay()
-                best = None
-                for _ in range(5):
-                    torch.cuda.synchronize()
-                    e0.record()
-                    for _r in range(R):
-                        graph.replay()
-                    e1.record()
-                    torch.cuda.synchronize()
-                    t = e0.elapsed_time(e1) / R
-                    best = t if best is None else min(best, t)
-                row[name] = {"ms_per_step": best, "hbm_alg_gbs": per_elem * N * total * es / (best / 1e3) / 1e9,
-                             "timing": f"{R} graph replays back to back, best of 5"}
+
+                def best_of(run):
+                    run()
+                    best = None
+                    for _ in range(5):
+                        torch.cuda.synchronize()
+                        e0.record(s)
+                        for _r in range(R):
+                            run()
+                        e1.record(s)
+                        torch.cuda.synchronize()
+                        t = e0.elapsed_time(e1) / R
+                        best = t if best is None else min(best, t)
+                    return best
+
+                with torch.cuda.stream(s):
+                    t_eager = best_of(lambda: call(s))
+                    t_graph = best_of(graph.replay)
+                row[name] = {"ms_per_step": t_eager, "hbm_alg_gbs": per_elem * N * total * es / (t_eager / 1e3) / 1e9,
+                             "graph_ms_per_step": t_graph,
+                             "timing": f"{R} steps back to back on one stream, eager calls (ms_per_step) and "
+                                       f"graph replays (graph_ms_per_step), best of 5"}
                 del graph
             print(json.dumps(row), flush=True)
             del buckets

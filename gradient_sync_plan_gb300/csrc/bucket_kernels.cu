@@ -459,7 +459,8 @@ static void split_segments(int world, const ViewMember* members, int first, int 
                 }
                 edge(pending, pending_len);
                 pending_len = 0;
-                segs->push_back(ViewSegment{i, (int32_t)j, body0, body1 - body0});
+                for (int64_t c = body0; c < body1; c += kViewSegMax)     // kViewSegMax: a multiple of 16 bytes
+                    segs->push_back(ViewSegment{i, (int32_t)j, c, std::min(kViewSegMax, body1 - c)});
                 if (s1 > body1) {
                     pending = body1;
                     pending_len = s1 - body1;

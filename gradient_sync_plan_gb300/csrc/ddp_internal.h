@@ -154,6 +154,9 @@ struct ViewEdge {
 };
 // Longest edge the TMA view kernel takes (one element per consumer thread).
 constexpr int64_t kTmaEdgeMax = 256;
+// Longest segment in one TMA view table entry (its length is 32-bit there);
+// longer segment bodies are cut into several entries.
+constexpr int64_t kViewSegMax = (int64_t)1 << 30;
 // TMA-staged view kernel (ring_tma.cu): the segments' members have 16-byte
 // aligned pointers, and every segment's start and length are multiples of
 // 16 bytes; edges (len <= kTmaEdgeMax) may belong to any member.

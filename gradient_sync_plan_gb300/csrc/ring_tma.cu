@@ -317,9 +317,9 @@ struct ViewTmaBatch {
     int64_t tile;               // elements per tile
     int64_t tile_end[SEGS];     // inclusive prefix of tiles per segment
     int64_t start[SEGS];        // first element of the segment in its member
-    int64_t len[SEGS];
-    int32_t j[SEGS];            // ring chunk of the segment
-    int32_t mem[SEGS];          // member slot: its rank pointers are ptr[mem * world ..]
+    uint32_t len[SEGS];         // elements (segments are cut at kViewSegMax)
+    uint16_t j[SEGS];           // ring chunk of the segment (world <= 128)
+    uint16_t mem[SEGS];         // member slot: its rank pointers are ptr[mem * world ..]
     int32_t n_edge;
     int32_t e_mem[EDGES];       // member slot of the edge
     int32_t e_len[EDGES];       // elements, at most kViewEdgeMax
@@ -329,7 +329,8 @@ struct ViewTmaBatch {
     char* ptr[PTRS];
 };
 using ViewTmaSmall = ViewTmaBatch<32, 256, 16>;
-using ViewTmaLarge = ViewTmaBatch<224, 2816, 64>;
+using ViewTmaLarge = ViewTmaBatch<320, 2816, 64>;
+static_assert(2816 < 65536 && 128 < 65536, "member slots and chunk indices fit 16 bits");
 static_assert(sizeof(ViewTmaLarge) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
 
 struct SegCursor {
@@ -343,7 +344,8 @@ struct SegCursor {
         const int64_t first = seg ? b.tile_end[seg - 1] : 0;
         const int64_t off = (k - first) * b.tile;
         e0 = b.start[seg] + off;
-        n = (b.len[seg] - off < b.tile) ? b.len[seg] - off : b.tile;
+        const int64_t len = b.len[seg];
+        n = (len - off < b.tile) ? len - off : b.tile;
     }
 };
 
@@ -692,9 +694,9 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, const V
             moved += 2 * g.len * (int64_t)sizeof(typename E::S) * world;
             b.tile_end[b.n_seg] = tiles;
             b.start[b.n_seg] = g.start;
-            b.len[b.n_seg] = g.len;
-            b.j[b.n_seg] = g.j;
-            b.mem[b.n_seg] = slots - 1;
+            b.len[b.n_seg] = (uint32_t)g.len;
+            b.j[b.n_seg] = (uint16_t)g.j;
+            b.mem[b.n_seg] = (uint16_t)(slots - 1);
             ++b.n_seg;
         } else {
             const ViewEdge& g = edges[it.index];
