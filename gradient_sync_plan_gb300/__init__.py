@@ -47,7 +47,8 @@ EXPORTS = ["ddp_status_string", "ddp_abi_version", "ddp_last_cuda_error", "ddp_d
            "ring_allreduce_fused_from_host_noalloc", "ring_allreduce_fused_host_direct",
            "ddp_grad_accumulate", "ddp_sync_buckets", "ddp_bucket_allreduce_view", "ddp_bucket_allreduce_view_bf16",
            "ddp_bucket_allreduce_view_fp16",
-           "ddp_reducer_create", "ddp_reducer_prepare", "ddp_reducer_mark_ready", "ddp_reducer_finalize",
+           "ddp_reducer_create", "ddp_reducer_set_max_ctas", "ddp_reducer_prepare", "ddp_reducer_mark_ready",
+           "ddp_reducer_finalize",
            "ddp_reducer_launch_order", "ddp_reducer_bucket_times", "ddp_reducer_destroy"]
 
 
@@ -110,6 +111,7 @@ def lib() -> ctypes.CDLL:
             L.ddp_bucket_allreduce_view_fp16.argtypes = [i32, i32, P(vp), P(i64), P(i64), i64, i32, vp]
             L.ddp_reducer_create.argtypes = [i32, i32, P(vp), P(i64), i32, P(i32), P(i64), i32, P(i64), P(vp), i32, i32,
                                              vp, P(vp)]
+            L.ddp_reducer_set_max_ctas.argtypes = [vp, i32]
             L.ddp_reducer_prepare.argtypes = [vp]
             L.ddp_reducer_mark_ready.argtypes = [vp, i32, vp]
             L.ddp_reducer_finalize.argtypes = [vp, vp]
@@ -584,6 +586,10 @@ class Reducer:
                                         _i64_array(off), self.n_buckets, _i64_array(bn), btab, int(algo),
                                         world if divisor is None else int(divisor), comm, ctypes.byref(h)))
         self._h = h
+
+    def set_max_ctas(self, max_ctas: int) -> None:
+        """CTA budget of this reducer's syncs (-1: the process-wide one, 0: no cap)."""
+        _check("ddp_reducer_set_max_ctas", lib().ddp_reducer_set_max_ctas(self._h, int(max_ctas)))
 
     def prepare(self):
         _check("ddp_reducer_prepare", lib().ddp_reducer_prepare(self._h))

@@ -5,8 +5,8 @@
 // off ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03
 // "Overlap" and section 05 steps 2-3; "Day 17 · 梯度的集体行动" Reducer
 // pseudo-code).  k_copy_items does one launch's worth of those copies: a
-// table of (src, dst, bytes) items, cut into fixed-size tiles, distributed
-// over a persistent grid.  The table travels in the kernel's parameter space,
+// table of (src, dst, bytes) items, cut into fixed-size tiles that a
+// grid-stride loop distributes over the CTAs.  The table travels in the kernel's parameter space,
 // so a call needs no device workspace and no host-to-device copy.
 //
 // With gradient_as_bucket_view on, a gradient *is* a slice of its bucket.

@@ -52,8 +52,18 @@ std::atomic<int> g_fused_kernel{DDP_FUSED_AUTO};             // ddp_set_fused_ke
 
 int fused_kernel_override() { return g_fused_kernel.load(std::memory_order_relaxed); }
 
+namespace {
+thread_local int t_cta_cap = -1;      // a reducer's own budget while it launches (-1: none set)
+}  // namespace
+
+int set_thread_cta_cap(int cap) {
+    const int prev = t_cta_cap;
+    t_cta_cap = cap;
+    return prev;
+}
+
 int cap_ctas(int64_t grid) {
-    const int cap = g_max_ctas.load(std::memory_order_relaxed);
+    const int cap = t_cta_cap >= 0 ? t_cta_cap : g_max_ctas.load(std::memory_order_relaxed);
     if (cap > 0 && grid > cap) grid = cap;
     return (int)std::max<int64_t>(1, grid);
 }

@@ -239,30 +239,35 @@ __device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, 
     return acc;
 }
 
-// The binomial tree's fold (tree_kernels.cu, ring_tma.cu): ranks in groups
-// of kTreeGroup.
+// The binomial tree's fold (tree_kernels.cu, ring_tma.cu).
 constexpr int kTreeGroup = 16;
-// Binomial pairwise sum of load(0) .. load(world - 1), world <= 16 * NG
-// (NG = 1, 2 or 4).  Ranks are folded in groups of 16 (levels 1, 2, 4, 8
-// inside a group), then the group sums at levels 16 and 32 -- exactly the
-// tree's additions, in its order.  NG is a compile-time bound so that a
-// small world does not carry the registers of 64 ranks.
-template <class T, int NG = 4, class Add, class Load>
+// Binomial pairwise sum of load(0) .. load(world - 1), world <= W (W a power
+// of two, at most 64).  Ranks are folded in groups of GS = min(W, 16)
+// (levels 1, 2, 4, 8 inside a group), then the group sums at levels 16 and
+// 32 -- exactly the tree's additions, in its order.  W is a compile-time
+// bound: the fold is unrolled with its bounds checked at run time, so a
+// bound much larger than the world costs registers and, for bf16 adds,
+// enough code to miss in the instruction cache (the TMA tree kernel compiled
+// for 16 ranks ran 2 bf16 ranks at 0.4 of its fp32 speed, stalled on
+// instruction fetch).
+template <class T, int W = 64, class Add, class Load>
 __device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
-    static_assert(NG == 1 || NG == 2 || NG == 4, "1, 2 or 4 groups of 16 ranks");
+    static_assert(W == 2 || W == 4 || W == 8 || W == 16 || W == 32 || W == 64, "W: a power of two up to 64");
+    constexpr int GS = W < kTreeGroup ? W : kTreeGroup;
+    constexpr int NG = W / GS;
     T gs[4];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-        if (kTreeGroup * g < world) {
-            T v[kTreeGroup];
+        if (GS * g < world) {
+            T v[GS];
 #pragma unroll
-            for (int i = 0; i < kTreeGroup; ++i)
-                if (kTreeGroup * g + i < world) v[i] = load(kTreeGroup * g + i);
+            for (int i = 0; i < GS; ++i)
+                if (GS * g + i < world) v[i] = load(GS * g + i);
 #pragma unroll
-            for (int d = 1; d < kTreeGroup; d <<= 1)
+            for (int d = 1; d < GS; d <<= 1)
 #pragma unroll
-                for (int i = 0; i < kTreeGroup; i += 2 * d)
-                    if (kTreeGroup * g + i + d < world) v[i] = add(v[i], v[i + d]);
+                for (int i = 0; i < GS; i += 2 * d)
+                    if (GS * g + i + d < world) v[i] = add(v[i], v[i + d]);
             gs[g] = v[0];
         }
     }

@@ -56,8 +56,13 @@ int fused_kernel_override();
 enum class FusedPath { kScalar, kVector, kGroup, kTma };
 constexpr int kGroupMaxWorld = 128;
 FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok);
-// grid clamped to the process-wide CTA cap of ddp_set_max_ctas (0 = none), at least 1
+// grid clamped to the CTA cap in force (0 = none), at least 1: the calling
+// thread's cap if one is set (a reducer's own budget while it launches),
+// else the process-wide cap of ddp_set_max_ctas
 int cap_ctas(int64_t grid);
+// Sets the calling thread's cap (-1: none, follow the process-wide cap);
+// returns the previous one.
+int set_thread_cta_cap(int cap);
 bool debug_enabled();
 
 // ---- ring kernels (ring_kernels.cu) -----------------------------------

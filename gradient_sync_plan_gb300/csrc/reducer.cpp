@@ -29,6 +29,8 @@ namespace ddpk {
 // ddp_api.cpp: one bucket's pack -> fused ring -> unpack, in L2-sized pieces when large
 int32_t pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
                          void* const* bk, int64_t bucket_numel, int32_t dtype, int32_t divisor, void* stream);
+// ddp_api.cpp: the calling thread's CTA cap (-1: none), returns the previous one
+int set_thread_cta_cap(int cap);
 // ddp_api.cpp: one bucket's bf16-hook pack -> bf16 ring -> unpack, in L2-sized pieces when large
 int32_t hook_pack_ring_unpack(int32_t world, int32_t n, const void* const* g, const int64_t* ne, const int64_t* off,
                               void* const* bk, int64_t bucket_numel, int32_t divisor, void* stream);
@@ -36,6 +38,7 @@ int32_t hook_pack_ring_unpack(int32_t world, int32_t n, const void* const* g, co
 
 struct ddp_reducer {
     int32_t world = 0, n_params = 0, n_buckets = 0, dtype = 0, divisor = 0, algo = 0;
+    int32_t max_ctas = -1;            // CTA budget of this reducer's syncs (-1: the process-wide one)
     cudaStream_t comm = nullptr;
     std::vector<int32_t> bucket_of;
     std::vector<int64_t> bucket_numel;
@@ -60,6 +63,14 @@ struct ddp_reducer {
 namespace {
 
 bool dry(const ddp_reducer* r) { return r->algo == DDP_ALGO_DRYRUN; }
+
+// Sets the calling thread's CTA cap for a scope and restores the previous
+// one on every exit, exceptions included.
+struct CtaCapGuard {
+    int prev;
+    explicit CtaCapGuard(int cap) : prev(ddpk::set_thread_cta_cap(cap)) {}
+    ~CtaCapGuard() { ddpk::set_thread_cta_cap(prev); }
+};
 
 int32_t sync_bucket(ddp_reducer* r, int32_t k) {
     const int32_t n = r->n_members[k];
@@ -97,7 +108,11 @@ int32_t launch_ready_prefix(ddp_reducer* r) {
             if (cudaStreamIsCapturing(r->comm, &cap) != cudaSuccess) return DDP_ERR_CUDA;
             const bool time_it = cap == cudaStreamCaptureStatusNone;
             if (time_it && cudaEventRecord(r->t0_ev[k], r->comm) != cudaSuccess) return DDP_ERR_CUDA;
-            const int32_t st = sync_bucket(r, k);
+            int32_t st;
+            {
+                CtaCapGuard cap_guard(r->max_ctas);      // this reducer's budget for its own launches only
+                st = sync_bucket(r, k);
+            }
             if (st) return st;
             if (time_it && cudaEventRecord(r->t1_ev[k], r->comm) != cudaSuccess) return DDP_ERR_CUDA;
             r->timed[k] = time_it ? 1 : 0;
@@ -228,6 +243,14 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
     }
     reset_step(r);
     *out = holder.release();
+    return DDP_OK;
+} DDP_ABI_CATCH
+
+int32_t ddp_reducer_set_max_ctas(ddp_reducer* r, int32_t max_ctas) try {
+    DDP_TRACE_CALL();
+    if (!r || max_ctas < -1) return DDP_ERR_INVALID;
+    std::lock_guard<std::mutex> lk(r->mu);
+    r->max_ctas = max_ctas;
     return DDP_OK;
 } DDP_ABI_CATCH
 

@@ -362,23 +362,29 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
         case DDP_FUSED_TMA: return tma_ok ? FusedPath::kTma : FusedPath::kVector;
         default: break;
     }
-    // Crossovers measured on GB300 (CUDA-graph replay of back-to-back calls,
-    // fp32 and bf16, N = 2 .. 128, 4 KiB .. 64 MiB per rank):
-    //  * a few KiB per rank: one thread per vector leaves most SMs idle and
-    //    waits on N loads; the group kernel spreads the ranks over lanes;
-    //  * while the whole bucket sits in L2 the vector kernel is fastest;
-    //  * from HBM, the TMA kernel streams best for up to 8 ranks (16 in
-    //    bf16), and for many ranks with short chunks its one-CTA-per-tile
-    //    grid reaches more SMs than one thread per vector.
+    // Crossovers measured on GB300 with every kernel forced (CUDA-graph
+    // replay of back-to-back calls, fp32 and bf16, N = 2 .. 128, 16 KiB ..
+    // 256 MiB per rank; grid-stride kernels at four waves):
+    //  * a few KiB per rank: the group kernel spreads the ranks over lanes;
+    //    at 2-4 fp32 ranks it stays ahead up to 64 KiB (256 KiB at 2);
+    //  * many ranks with little data each: the TMA kernel's one CTA per
+    //    tile reaches more SMs (N >= 16 up to 16 KiB, N >= 32 up to 64 KiB,
+    //    N = 32 up to 256 KiB; 1.3-2x faster than the others there);
+    //  * large buckets: TMA for 2 ranks from 16 MiB, for up to 16 ranks from
+    //    256 MiB per rank and for 8-16 ranks from 64 MiB; the vector kernel
+    //    everywhere else (within 1 % of TMA or faster, by up to 22 %).
     constexpr int64_t KiB = 1024, MiB = 1024 * 1024;
     const int64_t per_rank = numel * elem_bytes(dtype);
-    const int64_t total = per_rank * world;
-    if (group_ok && (per_rank <= 16 * KiB || (world <= 16 && per_rank <= 64 * KiB))) return FusedPath::kGroup;
+    if (group_ok && (per_rank <= 4 * KiB || (world <= 4 && dtype == DDP_F32 && per_rank <= 64 * KiB) ||
+                     (world == 2 && dtype == DDP_F32 && per_rank <= 256 * KiB)))
+        return FusedPath::kGroup;
     if (tma_ok) {
+        if ((world >= 16 && per_rank <= 16 * KiB) || (world >= 32 && per_rank <= 64 * KiB) ||
+            (world == 32 && per_rank <= 256 * KiB))
+            return FusedPath::kTma;
         if (world == 2 && per_rank >= 16 * MiB) return FusedPath::kTma;
-        if (world <= 8 && total > 128 * MiB) return FusedPath::kTma;
-        if (world <= 16 && dtype == DDP_BF16 && total >= 64 * MiB) return FusedPath::kTma;
-        if (world > 16 && per_rank >= 32 * KiB && per_rank <= 128 * KiB) return FusedPath::kTma;
+        if (world <= 16 && per_rank >= 256 * MiB) return FusedPath::kTma;
+        if (world >= 8 && world <= 16 && per_rank >= 64 * MiB) return FusedPath::kTma;
     }
     return FusedPath::kVector;
 }

@@ -5,8 +5,9 @@
 // "DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03),
 // divided by the divisor and written to every rank.  What differs is how the
 // bytes move.  The bucket is cut into tiles that never cross a chunk
-// boundary; one persistent CTA per SM streams its tiles through a ring of
-// shared-memory stages, with its warps split by role:
+// boundary; one resident CTA per SM (four waves of them for launches that
+// stream more than 512 MiB) walks its tiles through a ring of shared-memory
+// stages, with its warps split by role:
 //   * a producer warp: one thread issues, for every tile, N bulk copies
 //     (cp.async.bulk, one per rank) that complete on the stage's "full"
 //     mbarrier, as soon as the consumers have released that stage;
@@ -250,7 +251,7 @@ __device__ __forceinline__ void fused_tma_body(const TmaTable<CAP>& t, int world
                 auto staged = [&](int r) { return reinterpret_cast<const V*>(sb + (size_t)r * tile_bytes)[v]; };
                 V acc;
                 if constexpr (TREE) {
-                    acc = tree_fold<V, CAP / kTreeGroup>(world, [](V a, V b) { return E::vadd(a, b); }, staged);
+                    acc = tree_fold<V, CAP>(world, [](V a, V b) { return E::vadd(a, b); }, staged);
                 } else {
                     int r = start;
                     acc = staged(r);
@@ -566,9 +567,17 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
 
 template <class E, int DIV, bool TREE>
 static cudaError_t tma_cap(int world, void* const* ptrs, int64_t numel, float dop, cudaStream_t st) {
-    if (world <= 16) return tma_launch<E, DIV, 16, TREE>(world, ptrs, numel, dop, st);
-    if constexpr (TREE) return tma_launch<E, DIV, 64, TREE>(world, ptrs, numel, dop, st);
-    else return tma_launch<E, DIV, 128, TREE>(world, ptrs, numel, dop, st);
+    if constexpr (TREE) {
+        // the tree's fold is unrolled up to the table size: keep it tight
+        if (world <= 2) return tma_launch<E, DIV, 2, TREE>(world, ptrs, numel, dop, st);
+        if (world <= 4) return tma_launch<E, DIV, 4, TREE>(world, ptrs, numel, dop, st);
+        if (world <= 8) return tma_launch<E, DIV, 8, TREE>(world, ptrs, numel, dop, st);
+        if (world <= 16) return tma_launch<E, DIV, 16, TREE>(world, ptrs, numel, dop, st);
+        return tma_launch<E, DIV, 64, TREE>(world, ptrs, numel, dop, st);
+    } else {
+        if (world <= 16) return tma_launch<E, DIV, 16, TREE>(world, ptrs, numel, dop, st);
+        return tma_launch<E, DIV, 128, TREE>(world, ptrs, numel, dop, st);
+    }
 }
 
 template <class E, bool TREE>

@@ -31,7 +31,7 @@ struct TreeTable {
 
 constexpr int kTreeMaxWorld = 4 * kTreeGroup;   // 64
 
-template <class E, int DIV, int CAP, int NG>
+template <class E, int DIV, int CAP>
 __global__ void __launch_bounds__(kThreads)
 k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel, int vec_ok, float dop) {
     using V = typename E::V;
@@ -46,16 +46,16 @@ k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel,
         const int64_t nv = numel / L;
         for (int64_t v = tid; v < nv; v += stride) {
             const int64_t off = v * 16;
-            V y = tree_fold<V, NG>(world, [](V a, V b) { return E::vadd(a, b); },
-                                   [&](int r) { return ld_stream<V>(t.p[r] + off); });
+            V y = tree_fold<V, CAP>(world, [](V a, V b) { return E::vadd(a, b); },
+                                    [&](int r) { return ld_stream<V>(t.p[r] + off); });
             y = E::template vdiv<DIV>(y, dop);
             for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
         }
         done = nv * L;
     }
     for (int64_t e = done + tid; e < numel; e += stride) {
-        S y = tree_fold<S, NG>(world, [](S a, S b) { return E::sadd(a, b); },
-                               [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
+        S y = tree_fold<S, CAP>(world, [](S a, S b) { return E::sadd(a, b); },
+                                [&](int r) { return reinterpret_cast<const S*>(t.p[r])[e]; });
         y = E::template sdiv<DIV>(y, dop);
         for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[r])[e] = y;
     }
@@ -180,22 +180,27 @@ static TreeTable<CAP> tree_table(int world, void* const* ptrs) {
     return t;
 }
 
-template <class E, int DIV, int NG>
+template <class E, int DIV, int W>
 static cudaError_t tree_fused_launch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                      cudaStream_t st) {
-    auto k = k_tree_fused<E, DIV, kTreeGroup * NG, NG>;
+    auto k = k_tree_fused<E, DIV, W>;
     const int64_t work = vec_ok ? (numel + E::L - 1) / E::L : numel;
     const int grid = grid_for((const void*)k, work);
-    return launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, tree_table<kTreeGroup * NG>(world, ptrs), world,
-                            numel, vec_ok ? 1 : 0, dop);
+    return launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, tree_table<W>(world, ptrs), world, numel,
+                            vec_ok ? 1 : 0, dop);
 }
 
+// Instantiated for the smallest power of two that holds the world: the fold
+// is unrolled up to it.
 template <class E, int DIV>
 static cudaError_t tree_fused_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                    cudaStream_t st) {
-    if (world <= kTreeGroup) return tree_fused_launch<E, DIV, 1>(world, ptrs, numel, dop, vec_ok, st);
-    if (world <= 2 * kTreeGroup) return tree_fused_launch<E, DIV, 2>(world, ptrs, numel, dop, vec_ok, st);
-    return tree_fused_launch<E, DIV, 4>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 2) return tree_fused_launch<E, DIV, 2>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 4) return tree_fused_launch<E, DIV, 4>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 8) return tree_fused_launch<E, DIV, 8>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 16) return tree_fused_launch<E, DIV, 16>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 32) return tree_fused_launch<E, DIV, 32>(world, ptrs, numel, dop, vec_ok, st);
+    return tree_fused_launch<E, DIV, 64>(world, ptrs, numel, dop, vec_ok, st);
 }
 
 constexpr int kTreeGroupThreads = 128;
@@ -220,8 +225,17 @@ static cudaError_t tree_group_impl(int world, void* const* ptrs, int64_t numel, 
     return tree_group_launch<E, DIV, 32, 2>(world, ptrs, numel, dop, st);
 }
 
-// The group kernel for buckets of a few KiB per rank, one thread per vector
-// above that (ddp_set_fused_kernel can force either).
+// Kernel choice, from a sweep with every kernel forced (fp32 and bf16,
+// N = 2 .. 64, 4 KiB .. 256 MiB per rank, CUDA-graph replay), each kernel's
+// fold unrolled only up to the smallest power of two that holds the world:
+//  * the group kernel (log2(P) shuffle levels per vector) for 8 or more ranks
+//    up to 64 KiB per rank (N = 64 x 16 KiB: 3.3 us against 6.7 on TMA and
+//    9.8 on the vector kernel), and for 2 fp32 ranks at 4 KiB;
+//  * the TMA kernel for up to 4 ranks from 256 MiB per rank (N = 4 x 256 MiB
+//    fp32: 321 against 326 us);
+//  * the vector kernel everywhere else -- with a tight fold it keeps few
+//    registers and matches or beats TMA (N = 8 x 256 MiB: 639 against 646 us).
+// ddp_set_fused_kernel can force any of them.
 static bool tree_use_group(int world, int64_t numel, int dtype, bool vec_ok) {
     if (!vec_ok || world < 2) return false;
     switch (fused_kernel_override()) {
@@ -230,12 +244,9 @@ static bool tree_use_group(int world, int64_t numel, int dtype, bool vec_ok) {
         case DDP_FUSED_TMA: return false;
         default: break;
     }
-    // crossovers measured on GB300 (fp32 and bf16, N = 2 .. 64): the group
-    // kernel needs log2(P) shuffle levels per vector, so it stays ahead up to
-    // larger buckets than the ring's group kernel, the more so the fewer ranks
     const int64_t KiB = 1024;
-    const int64_t limit = world == 2 ? 4096 * KiB : world <= 4 ? 512 * KiB : world <= 16 ? 128 * KiB : 64 * KiB;
-    return numel * elem_bytes(dtype) <= limit;
+    const int64_t per_rank = numel * elem_bytes(dtype);
+    return (world >= 8 && per_rank <= 64 * KiB) || (world == 2 && dtype == DDP_F32 && per_rank <= 4 * KiB);
 }
 
 template <class E, int DIV>
@@ -300,8 +311,6 @@ static cudaError_t tree_group_by_div(int world, void* const* ptrs, int64_t numel
     }
 }
 
-// The TMA-staged kernel for buckets streamed from HBM over a few ranks (the
-// fused ring's rule), or when forced.
 static bool tree_use_tma(int world, int64_t numel, int dtype, bool vec_ok) {
     if (!tree_tma_usable(world, numel, dtype, vec_ok)) return false;
     switch (fused_kernel_override()) {
@@ -310,9 +319,7 @@ static bool tree_use_tma(int world, int64_t numel, int dtype, bool vec_ok) {
         case DDP_FUSED_VECTOR: return false;
         default: break;
     }
-    const int64_t total = numel * elem_bytes(dtype) * world;
-    return (world <= 8 && total > ((int64_t)128 << 20)) ||
-           (world <= 16 && dtype == DDP_BF16 && total >= ((int64_t)64 << 20));
+    return world <= 4 && numel * elem_bytes(dtype) >= ((int64_t)256 << 20);
 }
 
 cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,

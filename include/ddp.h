@@ -103,11 +103,12 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  * DDP_ALGO_FUSED / DDP_ALGO_BF16_HOOK, the reducer) uses from now on in this
  * process.  All of them compute the same fold in the same order, so results
  * are bit-identical whichever runs; the choice only changes speed.
- *   DDP_FUSED_AUTO   by size (the default): buckets of a few KiB per rank
- *                    take the group kernel; buckets that fit in L2 the
- *                    vector kernel; buckets streamed from HBM over up to 8
- *                    ranks (16 in bf16), and 32-128 KiB per rank over more
- *                    than 16 ranks, the TMA kernel;
+ *   DDP_FUSED_AUTO   by size (the default): up to 4 KiB per rank (64 KiB
+ *                    over 2-4 fp32 ranks) the group kernel; 16 or more ranks
+ *                    with little data each (up to 16 KiB per rank, 64 KiB
+ *                    from 32 ranks) and large buckets (2 ranks from 16 MiB
+ *                    per rank, 8-16 ranks from 64 MiB, up to 16 ranks from
+ *                    256 MiB) the TMA kernel; the vector kernel otherwise;
  *   DDP_FUSED_VECTOR one thread per 16-byte vector, folding all N ranks;
  *   DDP_FUSED_GROUP  a group of lanes per vector, one rank (or a few) per
  *                    lane, the fold done on values passed by warp shuffles
@@ -116,11 +117,12 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  *                    copies (N <= 128, 16-byte-aligned chunks).
  * A kernel that cannot run a call (alignment, world size) is replaced by
  * the vector kernel, or the element-wise one for unaligned buffers.
- * tree_allreduce_fused follows the same choice among its own group, vector
- * and TMA kernels (its TMA kernel folds the staged tiles in the tree's
- * order; it takes buckets whose bytes per rank are a multiple of 16, N <= 64;
- * by size it runs for up to 8 ranks with more than 128 MiB over all ranks,
- * or up to 16 ranks of bf16 with at least 64 MiB).
+ * tree_allreduce_fused follows the same forced choice among its own group,
+ * vector and TMA kernels (its TMA kernel folds the staged tiles in the
+ * tree's order and takes buckets whose bytes per rank are a multiple of 16,
+ * N <= 64).  By size it runs the group kernel for 8 or more ranks up to 64
+ * KiB per rank, the TMA kernel for up to 4 ranks from 256 MiB per rank, and
+ * the vector kernel otherwise.
  * *previous (if not NULL) receives the old choice.  DDP_ERR_INVALID for an
  * unknown kind.
  */
@@ -552,6 +554,16 @@ int32_t ddp_reducer_create(int32_t world, int32_t n_params, void* const* grads, 
                            const int64_t* bucket_numel, void* const* buckets, int32_t algo, int32_t divisor,
                            void* comm_stream, ddp_reducer** out);
 int32_t ddp_reducer_prepare(ddp_reducer* reducer);
+/*
+ * ddp_reducer_set_max_ctas -- CTA budget of this reducer's bucket syncs, like
+ * ddp_set_max_ctas but for the kernels this reducer launches only: -1 (the
+ * default) follows the process-wide setting, 0 removes any cap for them,
+ * n > 0 caps them at n CTAs.  A small budget leaves SMs to the backward that
+ * runs beside the syncs ([P1] section 03 "Overlap"); on one GB300 with a GEMM
+ * backward, a quarter of the SMs hid the most.  Results do not depend on it.
+ * DDP_ERR_INVALID for a NULL reducer or max_ctas < -1.
+ */
+int32_t ddp_reducer_set_max_ctas(ddp_reducer* reducer, int32_t max_ctas);
 int32_t ddp_reducer_mark_ready(ddp_reducer* reducer, int32_t param, void* compute_stream);
 int32_t ddp_reducer_finalize(ddp_reducer* reducer, void* stream);
 /* Buckets launched in the current pass, in launch order (up to capacity). */

@@ -94,3 +94,46 @@ def test_bucket_times_are_unmeasured_inside_a_captured_graph():
     graph.replay()
     torch.cuda.synchronize()
     red.close()
+
+
+@pytest.mark.parametrize("algo", [ddp.DDP_ALGO_VIEW, ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_BF16_HOOK_VIEW])
+def test_reducer_with_its_own_cta_budget_matches_oracle(algo):
+    # a reducer capped at 19 CTAs (while the process-wide cap stays unset)
+    # gives the oracle's bits, and leaves other calls uncapped: the budget is
+    # this reducer's own
+    numels = workloads.param_numels(workloads.decoder_param_shapes(n_layer=4, d_model=128, d_ff=512, vocab=2000,
+                                                                   n_pos=128))
+    world, first, cap = 8, 64 << 10, 1 << 20
+    plan = ddp.ddp_plan_buckets(numels, ddp.F32, first, cap)
+    src = workloads.rank_vectors(world, sum(numels), "randn", std=1e-2, seed0=17)
+    src_h = f32_or_bits(src)
+    offs = np.cumsum([0] + numels)
+    grads_h = [[src_h[r, offs[p]:offs[p + 1]].copy() for p in range(len(numels))] for r in range(world)]
+    if algo == ddp.DDP_ALGO_BF16_HOOK_VIEW:
+        oracle.ddp_sync_bf16_hook(grads_h, first, cap)
+    else:
+        oracle.ddp_sync(grads_h, oracle.F32, first, cap)
+    want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
+    g = src.cuda()
+    views = [[g[r, int(offs[p]):int(offs[p + 1])] for p in range(len(numels))] for r in range(world)]
+    buckets = None
+    if algo == ddp.DDP_ALGO_FUSED:
+        buckets = [[torch.empty(int(n), device="cuda") for n in plan[2]] for _ in range(world)]
+    assert ddp.ddp_set_max_ctas(0) == 0
+    red = ddp.Reducer(views, plan, buckets, algo=algo, comm_stream=torch.cuda.Stream())
+    red.set_max_ctas(19)
+    red.prepare()
+    compute = torch.cuda.current_stream()
+    for p in range(len(numels) - 1, -1, -1):
+        red.mark_ready(p, compute)
+    red.finalize(compute)
+    torch.cuda.synchronize()
+    red.close()
+    assert_bits_equal(f32_or_bits(g), want, f"reducer with 19 CTAs algo={algo}")
+    assert ddp.ddp_set_max_ctas(0) == 0                 # the process-wide cap was never touched
+    with pytest.raises(ddp.DDPError):
+        red2 = ddp.Reducer(views, plan, buckets, algo=algo, comm_stream=torch.cuda.Stream())
+        try:
+            red2.set_max_ctas(-2)
+        finally:
+            red2.close()

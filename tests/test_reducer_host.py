@@ -104,3 +104,19 @@ def test_bucket_times_in_a_dry_run_are_unmeasured():
     red.finalize(stream=0)
     assert red.bucket_times() == [-1.0] * len(bn)
     red.close()
+
+
+def test_reducer_cta_budget_validates():
+    # -1 follows the process-wide cap, 0 removes any cap, n > 0 caps; below -1
+    # and a NULL reducer are refused (host only: a dry-run reducer)
+    red, _ = _dry([10, 20, 30])
+    for ok in (-1, 0, 1, 38, 1 << 20):
+        red.set_max_ctas(ok)
+    with pytest.raises(ddp.DDPError):
+        red.set_max_ctas(-2)
+    assert ddp.lib().ddp_reducer_set_max_ctas(None, 4) == -1
+    red.prepare()
+    for p in range(2, -1, -1):
+        red.mark_ready(p, stream=0)
+    red.finalize(stream=0)
+    red.close()
