@@ -62,10 +62,20 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
     const int64_t full = numel / L;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     auto at = [&](int r) -> const char* { return t.p[r]; };
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= nvec) return;
+    // the chunk of this thread's vector, advanced as the thread strides on:
+    // no 64-bit division in the loop (a stride crosses a chunk boundary
+    // rarely; chunk j ends at chunk_end, at most numel for the last one)
+    int64_t j = (v * L) / clen;
+    int64_t chunk_end = (j + 1) * clen;
+    for (; v < nvec; v += stride) {
         const int64_t i = v * L;
-        const int64_t j = i / clen;
-        if (v < full && (i + L - 1) / clen == j) {
+        while (i >= chunk_end) {
+            ++j;
+            chunk_end += clen;
+        }
+        if (v < full && i + L <= chunk_end) {
             const int start = (j + 1 == world) ? 0 : (int)j + 1;
             const int64_t off = v * 16;
             V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, off), dop);
