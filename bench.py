@@ -499,7 +499,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
            "roofline": {"bound": "hbm", "achieved": hbm, "peak": peak, "unit": "GB/s", "frac": hbm / peak,
                         "traffic": traffic, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                        "kernel": "k_ring_fused_tma", "algorithmic_bytes_per_launch": 2 * N * s_bytes},
+                        "kernel": "k_ring_fused (vector, one block per tile)",
+                        "algorithmic_bytes_per_launch": 2 * N * s_bytes},
            "gpu_launches": args.steps}
     if sampler:
         out["clocks"] = sampler.summary()

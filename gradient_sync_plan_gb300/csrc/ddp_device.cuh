@@ -215,47 +215,59 @@ __device__ __forceinline__ uint4 shfl_down_vec(uint4 a, int delta, int width) {
 // Fold the N ranks' vectors at byte offset `off` in ring order, starting at
 // rank `start` (the rank right after the chunk's owner) and wrapping around:
 // acc = x[start]; acc = acc (+) x[start+1]; ... ; acc = acc (+) x[start-1].
-// Loads are issued in groups of G before they are folded, so G 16-byte
-// requests per thread are in flight at once.
-template <class E, int G, class PtrAt>
-__device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, int start, int64_t off) {
+// U vectors of the same chunk, at offsets off, off + ustep, ..., are folded
+// side by side into acc[0..U).  Loads are issued in groups of G ranks before
+// they are folded, so G * U 16-byte requests per thread are in flight at once.
+template <class E, int G, int U, class PtrAt>
+__device__ __forceinline__ void fold_ring_vecs(PtrAt ptr_at, int world, int start, int64_t off, int64_t ustep,
+                                               typename E::V (&acc)[U]) {
     using V = typename E::V;
-    V acc = make_zero<V>();
     int r = start;
     for (int k0 = 0; k0 < world; k0 += G) {
-        V x[G];
+        V x[G][U];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             if (k0 + g < world) {
-                x[g] = ld_stream<V>(ptr_at(r) + off);
+                const char* p = ptr_at(r) + off;
+#pragma unroll
+                for (int u = 0; u < U; ++u) x[g][u] = ld_stream<V>(p + u * ustep);
                 r = (r + 1 == world) ? 0 : r + 1;
             }
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            if (k0 + g < world) acc = (k0 + g == 0) ? x[g] : E::vadd(acc, x[g]);
+            if (k0 + g < world) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) acc[u] = (k0 + g == 0) ? x[g][u] : E::vadd(acc[u], x[g][u]);
+            }
         }
     }
-    return acc;
+}
+
+template <class E, int G, class PtrAt>
+__device__ __forceinline__ typename E::V fold_ring_vec(PtrAt ptr_at, int world, int start, int64_t off) {
+    typename E::V acc[1];
+    fold_ring_vecs<E, G, 1>(ptr_at, world, start, off, 0, acc);
+    return acc[0];
 }
 
 // The binomial tree's fold (tree_kernels.cu, ring_tma.cu).
 constexpr int kTreeGroup = 16;
 // Binomial pairwise sum of load(0) .. load(world - 1), world <= W (W a power
-// of two, at most 64).  Ranks are folded in groups of GS = min(W, 16)
-// (levels 1, 2, 4, 8 inside a group), then the group sums at levels 16 and
-// 32 -- exactly the tree's additions, in its order.  W is a compile-time
-// bound: the fold is unrolled with its bounds checked at run time, so a
-// bound much larger than the world costs registers and, for bf16 adds,
-// enough code to miss in the instruction cache (the TMA tree kernel compiled
-// for 16 ranks ran 2 bf16 ranks at 0.4 of its fp32 speed, stalled on
-// instruction fetch).
-template <class T, int W = 64, class Add, class Load>
+// of two, at most 64).  Ranks are loaded and folded in groups of GS (levels
+// 1, 2, .., GS/2 inside a group), then the group sums are folded at levels
+// GS, 2 GS, .. -- exactly the tree's additions, in its order; GS bounds the
+// loads in flight (and the registers they take).  W is a compile-time bound:
+// the fold is unrolled with its bounds checked at run time, so a bound much
+// larger than the world costs registers and, for bf16 adds, enough code to
+// miss in the instruction cache (the TMA tree kernel compiled for 16 ranks
+// ran 2 bf16 ranks at 0.4 of its fp32 speed, stalled on instruction fetch).
+template <class T, int W = 64, int GS = (W < kTreeGroup ? W : kTreeGroup), class Add, class Load>
 __device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
     static_assert(W == 2 || W == 4 || W == 8 || W == 16 || W == 32 || W == 64, "W: a power of two up to 64");
-    constexpr int GS = W < kTreeGroup ? W : kTreeGroup;
+    static_assert(GS >= 2 && GS <= W && (GS & (GS - 1)) == 0, "GS: a power of two up to W");
     constexpr int NG = W / GS;
-    T gs[4];
+    T gs[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
         if (GS * g < world) {
@@ -271,9 +283,11 @@ __device__ __forceinline__ T tree_fold(int world, Add add, Load load) {
             gs[g] = v[0];
         }
     }
-    if (NG >= 2 && 16 < world) gs[0] = add(gs[0], gs[1]);
-    if (NG >= 4 && 48 < world) gs[2] = add(gs[2], gs[3]);
-    if (NG >= 4 && 32 < world) gs[0] = add(gs[0], gs[2]);
+#pragma unroll
+    for (int d = GS; d < W; d <<= 1)
+#pragma unroll
+        for (int g = 0; g < NG; g += 2 * d / GS)
+            if (GS * g + d < world) gs[g] = add(gs[g], gs[g + d / GS]);
     return gs[0];
 }
 

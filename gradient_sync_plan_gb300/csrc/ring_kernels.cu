@@ -47,42 +47,80 @@ __device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world,
     for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[world + r])[e] = y;
 }
 
-// Vectorised fused kernel: all rank buffers are 16-byte aligned.  Thread v
-// handles the 16-byte vector v of every rank.  A vector whose lanes fall in
-// two chunks (only possible when c is not a multiple of the lane count) or
-// runs past the end is done lane by lane.
-template <class E, int DIV, int CAP, int G>
-__global__ void __launch_bounds__(kThreads)
+// Vectorised fused kernel: all rank buffers are 16-byte aligned.  The 16-byte
+// vectors are cut into tiles of kThreads * U; block b takes tiles b,
+// b + gridDim.x, ...  Thread x of a tile takes its vectors x, x + kThreads,
+// ..., x + (U - 1) * kThreads: their loads, G ranks at a time, are all in
+// flight before the fold.  A large bucket is launched with one block per tile,
+// so the block scheduler hands out small tiles in address order as SMs free
+// up and the blocks in flight stream one compact window of every rank; a
+// bucket that fits in L2 gets a few waves of blocks that loop over the tiles.
+// A vector whose lanes fall in two chunks (only possible when c is not a
+// multiple of the lane count) or runs past the end is done lane by lane.
+// LOOP = false: the grid is exactly one block per tile.
+template <class E, int DIV, int CAP, int G, int U, int MINB, bool LOOP>
+__global__ void __launch_bounds__(kThreads, MINB)
 k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
     using V = typename E::V;
     constexpr int L = E::L;
+    constexpr int64_t kTile = (int64_t)kThreads * U;
     pdl_release();
     pdl_acquire();
     const int64_t nvec = (numel + L - 1) / L;
     const int64_t full = numel / L;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tiles = (nvec + kTile - 1) / kTile;
     auto at = [&](int r) -> const char* { return t.p[r]; };
-    int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= nvec) return;
-    // the chunk of this thread's vector, advanced as the thread strides on:
-    // no 64-bit division in the loop (a stride crosses a chunk boundary
-    // rarely; chunk j ends at chunk_end, at most numel for the last one)
-    int64_t j = (v * L) / clen;
+    int64_t tile = blockIdx.x;
+    int64_t vb = tile * kTile + threadIdx.x;
+    if (vb >= nvec) return;
+    // the chunk of this thread's first vector, advanced as the block moves on
+    // to later tiles (chunk j ends at chunk_end; at most numel for the last)
+    int64_t j = (vb * L) / clen;
     int64_t chunk_end = (j + 1) * clen;
-    for (; v < nvec; v += stride) {
-        const int64_t i = v * L;
-        while (i >= chunk_end) {
+    for (;;) {
+        while (vb * L >= chunk_end) {
             ++j;
             chunk_end += clen;
         }
-        if (v < full && i + L <= chunk_end) {
+        const int64_t vl = vb + (U - 1) * kThreads;
+        if (vl < full && vl * L + L <= chunk_end) {
             const int start = (j + 1 == world) ? 0 : (int)j + 1;
-            const int64_t off = v * 16;
-            V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, off), dop);
-            for (int r = 0; r < world; ++r) st_stream<V>(t.p[world + r] + off, y);
+            V y[U];
+            fold_ring_vecs<E, G, U>(at, world, start, vb * 16, (int64_t)kThreads * 16, y);
+#pragma unroll
+            for (int u = 0; u < U; ++u) y[u] = E::template vdiv<DIV>(y[u], dop);
+            for (int r = 0; r < world; ++r) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) st_stream<V>(t.p[world + r] + (vb + u * kThreads) * 16, y[u]);
+            }
         } else {
-            for (int l = 0; l < L; ++l)
-                if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = vb + (int64_t)u * kThreads;
+                if (v >= nvec) break;
+                const int64_t i = v * L;
+                int64_t jv = j, end_v = chunk_end;
+                while (i >= end_v) {
+                    ++jv;
+                    end_v += clen;
+                }
+                if (U > 1 && v < full && i + L <= end_v) {     // U = 1: the fast path's test
+                    const int start = (jv + 1 == world) ? 0 : (int)jv + 1;
+                    V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, v * 16), dop);
+                    for (int r = 0; r < world; ++r) st_stream<V>(t.p[world + r] + v * 16, y);
+                } else {
+                    for (int l = 0; l < L; ++l)
+                        if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
+                }
+            }
+        }
+        // one tile per block, or the block's next tile (the loop keeps more
+        // registers live, so the one-tile form alone is built for 4 blocks/SM)
+        if constexpr (!LOOP) {
+            return;
+        } else {
+            tile += gridDim.x;
+            vb = tile * kTile + threadIdx.x;
+            if (tile >= tiles || vb >= nvec) return;
         }
     }
 }
@@ -284,17 +322,32 @@ static RankTable<CAP> make_io_table(int world, void* const* in, void* const* out
     return t;
 }
 
-template <class E, int DIV, int CAP, int G>
+// Buckets that do not fit in L2 run one block per tile (see k_ring_fused).
+constexpr int64_t kTilePerBlockBytes = 128ll << 20;
+
+template <class E, int DIV, int CAP, int G, int U, int MINB, int LOOP_MINB = 3, int LOOP_U = U>
 static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64_t numel, float dop,
                              cudaStream_t st) {
-    auto k = k_ring_fused<E, DIV, 2 * CAP, G>;
     const int64_t nvec = (numel + E::L - 1) / E::L;
-    const int grid = grid_for((const void*)k, nvec);
-    const cudaError_t e = launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, make_io_table<2 * CAP>(world, in, out),
-                                           world, numel, chunk_len(numel, world), dop);
+    const int64_t tiles = (nvec + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
+    const bool streamed = (int64_t)world * numel * (int64_t)sizeof(typename E::S) >= kTilePerBlockBytes;
+    int grid = 0;
+    cudaError_t e;
+    if (streamed && tiles <= INT32_MAX && cap_ctas(tiles) == tiles) {
+        grid = (int)tiles;
+        e = launch_dependent(k_ring_fused<E, DIV, 2 * CAP, G, U, MINB, false>, dim3(grid), dim3(kThreads), 0, st,
+                             make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
+    } else {
+        auto loop = k_ring_fused<E, DIV, 2 * CAP, G, LOOP_U, LOOP_MINB, true>;
+        const int64_t loop_tiles = (nvec + (int64_t)kThreads * LOOP_U - 1) / ((int64_t)kThreads * LOOP_U);
+        grid = streamed ? cap_ctas(std::min<int64_t>(loop_tiles, INT32_MAX))
+                        : grid_for((const void*)loop, loop_tiles * kThreads);
+        e = launch_dependent(loop, dim3(grid), dim3(kThreads), 0, st, make_io_table<2 * CAP>(world, in, out), world,
+                             numel, chunk_len(numel, world), dop);
+    }
     if (debug_enabled())
-        fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d G=%d CAP=%d\n", world, (long long)numel,
-                grid, G, CAP);
+        fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d tiles=%lld G=%d U=%d CAP=%d\n", world,
+                (long long)numel, grid, (long long)tiles, G, U, CAP);
     return e;
 }
 
@@ -345,11 +398,17 @@ static cudaError_t fused_dispatch(FusedPath path, int world, void* const* in, vo
         return fused_scalar<E, DIV, DDP_MAX_WORLD>(world, in, out, numel, dop, st);
     }
     if (path == FusedPath::kGroup) return group_dispatch<E, DIV>(world, in, out, numel, dop, st);
-    if (world <= 4) return fused_vec<E, DIV, 16, 4>(world, in, out, numel, dop, st);
-    if (world <= 8) return fused_vec<E, DIV, 16, 8>(world, in, out, numel, dop, st);
-    if (world <= 16) return fused_vec<E, DIV, 16, 16>(world, in, out, numel, dop, st);
-    if (world <= 64) return fused_vec<E, DIV, 64, 16>(world, in, out, numel, dop, st);
-    return fused_vec<E, DIV, DDP_MAX_WORLD, 16>(world, in, out, numel, dop, st);
+    // G ranks' loads at a time, U vectors per thread, at least MINB blocks
+    // per SM in the one-tile form (64 registers a thread at 4), LOOP_U and
+    // LOOP_MINB in the looping form: 4 to 8 loads in flight per thread in the
+    // one-tile form (3 ranks: two vectors there, one in the looping form)
+    if (world <= 2) return fused_vec<E, DIV, 16, 2, 2, 4>(world, in, out, numel, dop, st);
+    if (world == 3) return fused_vec<E, DIV, 16, 4, 2, 4, 3, 1>(world, in, out, numel, dop, st);
+    if (world <= 4) return fused_vec<E, DIV, 16, 4, 1, 4>(world, in, out, numel, dop, st);
+    if (world <= 8) return fused_vec<E, DIV, 16, 8, 1, 4>(world, in, out, numel, dop, st);
+    if (world <= 16) return fused_vec<E, DIV, 16, 8, 1, 3>(world, in, out, numel, dop, st);
+    if (world <= 64) return fused_vec<E, DIV, 64, 8, 1, 3>(world, in, out, numel, dop, st);
+    return fused_vec<E, DIV, DDP_MAX_WORLD, 8, 1, 3>(world, in, out, numel, dop, st);
 }
 
 template <class E>
@@ -374,27 +433,36 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
     }
     // Crossovers measured on GB300 with every kernel forced (CUDA-graph
     // replay of back-to-back calls, fp32 and bf16, N = 2 .. 128, 16 KiB ..
-    // 256 MiB per rank; grid-stride kernels at four waves):
+    // 256 MiB per rank):
     //  * a few KiB per rank: the group kernel spreads the ranks over lanes;
-    //    at 2-4 fp32 ranks it stays ahead up to 64 KiB (256 KiB at 2);
+    //    it stays ahead up to 256 KiB at 2 ranks, up to 16 KiB at 8 fp32
+    //    ranks, and up to 64 KiB where chunk boundaries are not 16-byte
+    //    aligned (there the vector kernel's straddling vectors go lane by lane);
     //  * many ranks with little data each: the TMA kernel's one CTA per
-    //    tile reaches more SMs (N >= 16 up to 16 KiB, N >= 32 up to 64 KiB,
-    //    N = 32 up to 256 KiB; 1.3-2x faster than the others there);
-    //  * large buckets: TMA for 2 ranks from 16 MiB, for up to 16 ranks from
-    //    256 MiB per rank and for 8-16 ranks from 64 MiB; the vector kernel
-    //    everywhere else (within 1 % of TMA or faster, by up to 22 %).
+    //    tile reaches more SMs (N >= 16 up to 16 KiB, N >= 32 up to 1 MiB,
+    //    N >= 64 up to 256 KiB, N >= 128 up to 64 KiB; at 16-31 ranks from
+    //    256 KiB (fp32; bf16 above 1 MiB) to 4 MiB);
+    //  * everything else, and every large bucket: the vector kernel, whose
+    //    one block per tile streams at or above the measured copy rate.
     constexpr int64_t KiB = 1024, MiB = 1024 * 1024;
     const int64_t per_rank = numel * elem_bytes(dtype);
-    if (group_ok && (per_rank <= 4 * KiB || (world <= 4 && dtype == DDP_F32 && per_rank <= 64 * KiB) ||
-                     (world == 2 && dtype == DDP_F32 && per_rank <= 256 * KiB)))
+    const bool chunks_aligned = (chunk_len(numel, world) * elem_bytes(dtype)) % 16 == 0;
+    if (group_ok && (per_rank <= 4 * KiB || (world == 2 && per_rank <= 256 * KiB) ||
+                     (!chunks_aligned && per_rank <= 64 * KiB) ||
+                     (world == 8 && dtype == DDP_F32 && per_rank <= 16 * KiB)))
         return FusedPath::kGroup;
     if (tma_ok) {
-        if ((world >= 16 && per_rank <= 16 * KiB) || (world >= 32 && per_rank <= 64 * KiB) ||
-            (world == 32 && per_rank <= 256 * KiB))
-            return FusedPath::kTma;
-        if (world == 2 && per_rank >= 16 * MiB) return FusedPath::kTma;
-        if (world <= 16 && per_rank >= 256 * MiB) return FusedPath::kTma;
-        if (world >= 8 && world <= 16 && per_rank >= 64 * MiB) return FusedPath::kTma;
+        if (world >= 16 && per_rank <= 16 * KiB) return FusedPath::kTma;
+        if (world >= 128) {
+            if (per_rank <= 64 * KiB) return FusedPath::kTma;
+        } else if (world >= 64) {
+            if (per_rank <= 256 * KiB) return FusedPath::kTma;
+        } else if (world >= 32) {
+            if (per_rank <= 1 * MiB) return FusedPath::kTma;
+        } else if (world >= 16) {
+            if (per_rank >= 256 * KiB && per_rank <= 4 * MiB && (dtype == DDP_F32 || per_rank > 1 * MiB))
+                return FusedPath::kTma;
+        }
     }
     return FusedPath::kVector;
 }

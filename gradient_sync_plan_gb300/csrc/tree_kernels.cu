@@ -31,8 +31,12 @@ struct TreeTable {
 
 constexpr int kTreeMaxWorld = 4 * kTreeGroup;   // 64
 
-template <class E, int DIV, int CAP>
-__global__ void __launch_bounds__(kThreads)
+// One thread per 16-byte vector.  A large bucket is launched with one block
+// per kThreads vectors (LOOP = false), so blocks stream the ranks in address
+// order as SMs free up; otherwise (and for buffers that are not 16-byte
+// aligned, done element-wise) a few waves of blocks loop over the bucket.
+template <class E, int DIV, int CAP, int MINB, bool LOOP>
+__global__ void __launch_bounds__(kThreads, MINB)
 k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel, int vec_ok, float dop) {
     using V = typename E::V;
     using S = typename E::S;
@@ -46,10 +50,12 @@ k_tree_fused(const __grid_constant__ TreeTable<CAP> t, int world, int64_t numel,
         const int64_t nv = numel / L;
         for (int64_t v = tid; v < nv; v += stride) {
             const int64_t off = v * 16;
-            V y = tree_fold<V, CAP>(world, [](V a, V b) { return E::vadd(a, b); },
-                                    [&](int r) { return ld_stream<V>(t.p[r] + off); });
+            // eight ranks' loads in flight at a time
+            V y = tree_fold<V, CAP, (CAP < 8 ? CAP : 8)>(world, [](V a, V b) { return E::vadd(a, b); },
+                                                         [&](int r) { return ld_stream<V>(t.p[r] + off); });
             y = E::template vdiv<DIV>(y, dop);
             for (int r = 0; r < world; ++r) st_stream<V>(t.p[r] + off, y);
+            if constexpr (!LOOP) break;
         }
         done = nv * L;
     }
@@ -180,10 +186,21 @@ static TreeTable<CAP> tree_table(int world, void* const* ptrs) {
     return t;
 }
 
-template <class E, int DIV, int W>
+// Buckets of at least this many bytes over all ranks run one block per tile.
+constexpr int64_t kTreeTilePerBlockBytes = 128ll << 20;
+
+template <class E, int DIV, int W, int MINB>
 static cudaError_t tree_fused_launch(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                      cudaStream_t st) {
-    auto k = k_tree_fused<E, DIV, W>;
+    const int64_t tiles = vec_ok ? (numel / E::L + kThreads - 1) / kThreads : 0;
+    const bool streamed = vec_ok && (int64_t)world * numel * (int64_t)sizeof(typename E::S) >= kTreeTilePerBlockBytes;
+    if (streamed && tiles <= INT32_MAX && cap_ctas(tiles) == tiles) {
+        // the tail elements past the last whole vector (fewer than L) fall to
+        // threads 0 .. L-2 of block 0, which the grid always holds
+        return launch_dependent(k_tree_fused<E, DIV, W, MINB, false>, dim3((unsigned)tiles), dim3(kThreads), 0, st,
+                                tree_table<W>(world, ptrs), world, numel, 1, dop);
+    }
+    auto k = k_tree_fused<E, DIV, W, (W <= 8 ? 4 : 3), true>;
     const int64_t work = vec_ok ? (numel + E::L - 1) / E::L : numel;
     const int grid = grid_for((const void*)k, work);
     return launch_dependent(k, dim3(grid), dim3(kThreads), 0, st, tree_table<W>(world, ptrs), world, numel,
@@ -195,12 +212,13 @@ static cudaError_t tree_fused_launch(int world, void* const* ptrs, int64_t numel
 template <class E, int DIV>
 static cudaError_t tree_fused_impl(int world, void* const* ptrs, int64_t numel, float dop, bool vec_ok,
                                    cudaStream_t st) {
-    if (world <= 2) return tree_fused_launch<E, DIV, 2>(world, ptrs, numel, dop, vec_ok, st);
-    if (world <= 4) return tree_fused_launch<E, DIV, 4>(world, ptrs, numel, dop, vec_ok, st);
-    if (world <= 8) return tree_fused_launch<E, DIV, 8>(world, ptrs, numel, dop, vec_ok, st);
-    if (world <= 16) return tree_fused_launch<E, DIV, 16>(world, ptrs, numel, dop, vec_ok, st);
-    if (world <= 32) return tree_fused_launch<E, DIV, 32>(world, ptrs, numel, dop, vec_ok, st);
-    return tree_fused_launch<E, DIV, 64>(world, ptrs, numel, dop, vec_ok, st);
+    // one-tile form: 4 blocks per SM (64 registers) up to 8 ranks, 3 above
+    if (world <= 2) return tree_fused_launch<E, DIV, 2, 4>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 4) return tree_fused_launch<E, DIV, 4, 4>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 8) return tree_fused_launch<E, DIV, 8, 4>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 16) return tree_fused_launch<E, DIV, 16, 3>(world, ptrs, numel, dop, vec_ok, st);
+    if (world <= 32) return tree_fused_launch<E, DIV, 32, 3>(world, ptrs, numel, dop, vec_ok, st);
+    return tree_fused_launch<E, DIV, 64, 3>(world, ptrs, numel, dop, vec_ok, st);
 }
 
 constexpr int kTreeGroupThreads = 128;
@@ -226,15 +244,15 @@ static cudaError_t tree_group_impl(int world, void* const* ptrs, int64_t numel, 
 }
 
 // Kernel choice, from a sweep with every kernel forced (fp32 and bf16,
-// N = 2 .. 64, 4 KiB .. 256 MiB per rank, CUDA-graph replay), each kernel's
-// fold unrolled only up to the smallest power of two that holds the world:
+// N = 2 .. 64, 4 KiB .. 256 MiB per rank, CUDA-graph replay):
 //  * the group kernel (log2(P) shuffle levels per vector) for 8 or more ranks
 //    up to 64 KiB per rank (N = 64 x 16 KiB: 3.3 us against 6.7 on TMA and
-//    9.8 on the vector kernel), and for 2 fp32 ranks at 4 KiB;
-//  * the TMA kernel for up to 4 ranks from 256 MiB per rank (N = 4 x 256 MiB
-//    fp32: 321 against 326 us);
-//  * the vector kernel everywhere else -- with a tight fold it keeps few
-//    registers and matches or beats TMA (N = 8 x 256 MiB: 639 against 646 us).
+//    9.7 on the vector kernel);
+//  * the TMA kernel for 32 or more fp32 ranks between 64 and 512 KiB per rank
+//    (N = 32 x 256 KiB: 5.9 against 6.6 us);
+//  * the vector kernel everywhere else; with one block per tile on large
+//    buckets it beats TMA there (N = 8 x 256 MiB: 616 against 649 us,
+//    N = 32 x 256 MiB: 2501 against 2654 us).
 // ddp_set_fused_kernel can force any of them.
 static bool tree_use_group(int world, int64_t numel, int dtype, bool vec_ok) {
     if (!vec_ok || world < 2) return false;
@@ -246,7 +264,7 @@ static bool tree_use_group(int world, int64_t numel, int dtype, bool vec_ok) {
     }
     const int64_t KiB = 1024;
     const int64_t per_rank = numel * elem_bytes(dtype);
-    return (world >= 8 && per_rank <= 64 * KiB) || (world == 2 && dtype == DDP_F32 && per_rank <= 4 * KiB);
+    return world >= 8 && per_rank <= 64 * KiB;
 }
 
 template <class E, int DIV>
@@ -319,7 +337,8 @@ static bool tree_use_tma(int world, int64_t numel, int dtype, bool vec_ok) {
         case DDP_FUSED_VECTOR: return false;
         default: break;
     }
-    return world <= 4 && numel * elem_bytes(dtype) >= ((int64_t)256 << 20);
+    const int64_t per_rank = numel * elem_bytes(dtype);
+    return world >= 32 && dtype == DDP_F32 && per_rank > (64 << 10) && per_rank <= (512 << 10);
 }
 
 cudaError_t launch_tree_allreduce(bool staged, int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,

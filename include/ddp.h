@@ -103,13 +103,18 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  * DDP_ALGO_FUSED / DDP_ALGO_BF16_HOOK, the reducer) uses from now on in this
  * process.  All of them compute the same fold in the same order, so results
  * are bit-identical whichever runs; the choice only changes speed.
- *   DDP_FUSED_AUTO   by size (the default): up to 4 KiB per rank (64 KiB
- *                    over 2-4 fp32 ranks) the group kernel; 16 or more ranks
- *                    with little data each (up to 16 KiB per rank, 64 KiB
- *                    from 32 ranks) and large buckets (2 ranks from 16 MiB
- *                    per rank, 8-16 ranks from 64 MiB, up to 16 ranks from
- *                    256 MiB) the TMA kernel; the vector kernel otherwise;
- *   DDP_FUSED_VECTOR one thread per 16-byte vector, folding all N ranks;
+ *   DDP_FUSED_AUTO   by size (the default): the group kernel up to 4 KiB
+ *                    per rank, up to 256 KiB over 2 ranks, up to 16 KiB over
+ *                    8 fp32 ranks and up to 64 KiB where chunk boundaries
+ *                    are not 16-byte aligned; the TMA kernel for 16 or more
+ *                    ranks with little data each (up to 16 KiB per rank; up
+ *                    to 1 MiB at 32-63 ranks, 256 KiB at 64-127, 64 KiB from
+ *                    128; fp32 at 16-31 ranks from 256 KiB to 4 MiB); the
+ *                    vector kernel otherwise, which includes every large
+ *                    bucket;
+ *   DDP_FUSED_VECTOR one thread per 16-byte vector (two over 2 or 3 ranks),
+ *                    folding all N ranks; a bucket of 128 MiB or more over
+ *                    all ranks runs one block per tile of vectors;
  *   DDP_FUSED_GROUP  a group of lanes per vector, one rank (or a few) per
  *                    lane, the fold done on values passed by warp shuffles
  *                    (N <= 128);
@@ -121,8 +126,8 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  * vector and TMA kernels (its TMA kernel folds the staged tiles in the
  * tree's order and takes buckets whose bytes per rank are a multiple of 16,
  * N <= 64).  By size it runs the group kernel for 8 or more ranks up to 64
- * KiB per rank, the TMA kernel for up to 4 ranks from 256 MiB per rank, and
- * the vector kernel otherwise.
+ * KiB per rank, the TMA kernel for 32 or more fp32 ranks between 64 and 512
+ * KiB per rank, and the vector kernel otherwise.
  * *previous (if not NULL) receives the old choice.  DDP_ERR_INVALID for an
  * unknown kind.
  */

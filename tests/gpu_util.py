@@ -192,6 +192,19 @@ def guarded_copy(x: torch.Tensor, device="cuda"):
     return storage, view
 
 
+def run_rank_buffers(fn, x_host: np.ndarray, what: str = "") -> np.ndarray:
+    """Call fn(list of N rank tensors) on separate guarded device buffers
+    holding the rows of x_host -- each 16-byte aligned whatever the row
+    length, so the vector kernels take ragged sizes -- check the guards and
+    return the [N, S] host result."""
+    held = [guarded_copy(from_np(np.ascontiguousarray(x_host[r]))) for r in range(x_host.shape[0])]
+    fn([v for _, v in held])
+    torch.cuda.synchronize()
+    for storage, _ in held:
+        assert_canaries(storage, what)
+    return np.stack([f32_or_bits(v) for _, v in held])
+
+
 def assert_canaries(storage: torch.Tensor, what: str = "") -> None:
     """The guard regions of a `guarded` storage still hold the pattern."""
     pad = CANARY_BYTES // storage.element_size()

@@ -18,7 +18,8 @@ import torch
 import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
-from gpu_util import assert_bits_equal, assert_canaries, f32_or_bits, from_np, guarded_copy, oracle_allreduce
+from gpu_util import (assert_bits_equal, assert_canaries, f32_or_bits, from_np, guarded_copy, oracle_allreduce,
+                      run_rank_buffers)
 
 pytestmark = pytest.mark.gpu
 
@@ -326,6 +327,33 @@ def test_cta_cap_does_not_change_results(cap):
                 assert_bits_equal(run_gpu(kernel, xh, N), want, f"cap={cap} {kernel} N={N} S={S}")
     finally:
         ddp.ddp_set_max_ctas(prev)
+
+
+# Buckets of at least 128 MiB over all ranks run the vector kernel with one
+# block per tile of vectors (two vectors per thread over 2 or 3 ranks); a CTA
+# cap below the tile count makes the same launch loop over its tiles.  The
+# sizes leave chunk boundaries off the 16-byte grid and a ragged last vector;
+# each rank has its own 16-byte-aligned buffer, so the vector kernel runs.
+STREAMED = [(2, 16_777_219), (3, 11_184_813), (5, 6_710_891), (8, 4_194_307), (12, 2_796_205)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,S", STREAMED)
+def test_vector_kernel_one_block_per_tile(dtype, N, S):
+    S = S * 2 if dtype == "bf16" else S
+    assert N * S * (2 if dtype == "bf16" else 4) >= 128 << 20
+    x = workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=11 * N)
+    xh = f32_or_bits(x)
+    want = oracle_allreduce(xh, N)
+    fused = lambda bufs: ddp.ring_allreduce_fused(bufs, N)
+    got = _with_fused_kernel("vector", lambda: run_rank_buffers(fused, xh, f"ring N={N} S={S}"))
+    assert_bits_equal(got, want, f"vector one block per tile N={N} S={S} {dtype}")
+    prev = ddp.ddp_set_max_ctas(40)
+    try:
+        got = _with_fused_kernel("vector", lambda: run_rank_buffers(fused, xh, f"ring N={N} S={S} cap 40"))
+    finally:
+        ddp.ddp_set_max_ctas(prev)
+    assert_bits_equal(got, want, f"vector, 40 blocks looping over the tiles, N={N} S={S} {dtype}")
 
 
 def test_empty_bucket_is_noop():

@@ -14,7 +14,7 @@ import gradient_sync_plan_gb300 as ddp
 import oracle
 import workloads
 from gpu_util import (assert_bits_equal, assert_canaries, assert_device_equals_host, f32_or_bits, from_np,
-                      guarded_copy, host_snapshot, require_host_memory)
+                      guarded_copy, host_snapshot, require_host_memory, run_rank_buffers)
 
 pytestmark = pytest.mark.gpu
 
@@ -140,3 +140,27 @@ def test_fused_both_kernels_around_the_size_switch(dtype):
             finally:
                 ddp.ddp_set_fused_kernel(prev)
             assert_bits_equal(got, oracle_tree(xh, N), f"tree forced kernel {kind} N={N} S={S}")
+
+
+# Buckets of at least 128 MiB over all ranks run the vector tree with one block
+# per tile of vectors, the elements past the last whole vector on block 0; a
+# CTA cap makes the launch loop over the tiles.  Separate aligned rank buffers
+# with ragged lengths, compared in full.
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,S", [(2, 16_777_219), (5, 6_710_891), (8, 4_194_307), (16, 2_097_155),
+                                 (33, 1_016_809)])
+def test_vector_tree_one_block_per_tile(dtype, N, S):
+    S = S * 2 if dtype == "bf16" else S
+    assert N * S * (2 if dtype == "bf16" else 4) >= 128 << 20
+    xh = f32_or_bits(workloads.rank_vectors(N, S, "randn", std=1e-2, dtype=dtype, seed0=7 * N))
+    want = oracle_tree(xh, N)
+    fused = lambda bufs: ddp.tree_allreduce_fused(bufs, N)
+    for cap in (0, 40):
+        prev_kernel = ddp.ddp_set_fused_kernel(ddp.DDP_FUSED_VECTOR)
+        prev_cap = ddp.ddp_set_max_ctas(cap)
+        try:
+            got = run_rank_buffers(fused, xh, f"tree N={N} S={S} cap={cap}")
+        finally:
+            ddp.ddp_set_max_ctas(prev_cap)
+            ddp.ddp_set_fused_kernel(prev_kernel)
+        assert_bits_equal(got, want, f"vector tree N={N} S={S} {dtype} cap={cap}")
