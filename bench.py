@@ -1042,7 +1042,8 @@ def run_profile_kernels(args):
     kernel), staged ring, persistent ring, fused tree (vector, then TMA
     kernel), staged tree, no_sync accumulation, pack and unpack of one
     bucket of 4 members per rank, bf16 pack and unpack (one 2^25-element
-    member per rank), fused view (one bucket of 4 members per rank).  --steps
+    member per rank), fused view (one bucket of 4 members per rank; register
+    kernel, then TMA kernel).  --steps
     repeats the sequence.  Prints one JSON line (not a bench result)."""
     import torch
     import gradient_sync_plan_gb300 as ddp
@@ -1081,7 +1082,9 @@ def run_profile_kernels(args):
            ("unpack", lambda: ddp.ddp_bucket_unpack(views, offs, bk)),
            ("pack_bf16", lambda: ddp.ddp_bucket_pack_bf16([[x[r]] for r in range(N)], [0], b16)),
            ("unpack_bf16", lambda: ddp.ddp_bucket_unpack_bf16([[y[r]] for r in range(N)], [0], b16)),
-           ("view", lambda: ddp.ddp_bucket_allreduce_view(views, offs, S, N))]
+           ("view_register", lambda: forced(ddp.DDP_FUSED_VECTOR,
+                                            lambda: ddp.ddp_bucket_allreduce_view(views, offs, S, N))),
+           ("view_tma", lambda: forced(ddp.DDP_FUSED_TMA, lambda: ddp.ddp_bucket_allreduce_view(views, offs, S, N)))]
     out = {"profile": "kernels", "ranks": N, "numel": S}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(max(1, args.steps)):

@@ -21,6 +21,7 @@
 
 #include "ddp_device.cuh"
 #include "ddp_internal.h"
+#include "view_batch.cuh"
 
 namespace ddpk {
 
@@ -405,6 +406,111 @@ static cudaError_t view_div(int world, const ViewMember* m, int n, int64_t bn, D
     }
 }
 
+// Register view kernel over a segment table (view_batch.cuh): the same
+// segments and edges as the TMA-staged view kernel, folded from 16-byte
+// register loads.  A tile is one vector per thread of one segment, so its
+// chunk, and the fold's first rank, is the segment's.  Block b folds edge b
+// (one element per thread), then its tile; a launch that moves at least
+// 256 MiB has one block per tile (LOOP = false) and the block scheduler
+// hands the tiles out in address order, like k_ring_fused's; otherwise a
+// few waves of blocks loop over the tiles.
+template <class E, int DIV, int G, int MINB, bool LOOP, class B>
+__global__ void __launch_bounds__(kThreads, MINB) k_bucket_view_seg(const __grid_constant__ B b, float dop) {
+    using V = typename E::V;
+    using S = typename E::S;
+    constexpr int L = E::L;
+    pdl_release();
+    pdl_acquire();
+    const int world = b.world;
+    for (int e = blockIdx.x; e < b.n_edge; e += gridDim.x) {
+        const int t = threadIdx.x;
+        if (t < b.e_len[e]) {
+            const int64_t jj = (b.e_pos[e] + t) / b.e_clen[e];
+            const int start = (jj + 1 == world) ? 0 : (int)jj + 1;
+            char* const* pp = b.ptr + (size_t)b.e_mem[e] * world;
+            const int64_t el = b.e_start[e] + t;
+            auto at = [&](int r) -> const char* { return pp[r]; };
+            const S y = E::template sdiv<DIV>(fold_ring_scalar<E>(at, world, start, el), dop);
+            for (int r = 0; r < world; ++r) reinterpret_cast<S*>(pp[r])[el] = y;
+        }
+    }
+    const int64_t total = b.n_seg > 0 ? b.tile_end[b.n_seg - 1] : 0;
+    for (int64_t k = blockIdx.x; k < total; k += gridDim.x) {
+        int lo = 0, hi = b.n_seg - 1;          // the tile's segment: first with tile_end > k
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (b.tile_end[mid] > k) hi = mid; else lo = mid + 1;
+        }
+        const int64_t first = lo ? b.tile_end[lo - 1] : 0;
+        const int64_t off = (k - first) * b.tile + (int64_t)threadIdx.x * L;    // bodies are whole vectors
+        if (off < (int64_t)b.len[lo]) {
+            const int j = b.j[lo];
+            const int start = (j + 1 == world) ? 0 : j + 1;
+            char* const* pp = b.ptr + (size_t)b.mem[lo] * world;
+            auto at = [&](int r) -> const char* { return pp[r]; };
+            const int64_t byte = (b.start[lo] + off) * (int64_t)sizeof(S);
+            const V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, byte), dop);
+            for (int r = 0; r < world; ++r) st_stream<V>(pp[r] + byte, y);
+        }
+        if constexpr (!LOOP) break;
+    }
+}
+
+template <class E, int DIV, int G, class BT>
+static cudaError_t view_seg_launch(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
+                                   const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
+    auto once = k_bucket_view_seg<E, DIV, G, 4, false, BT>;
+    auto loop = k_bucket_view_seg<E, DIV, G, 3, true, BT>;
+    const int64_t tile = (int64_t)kThreads * E::L;
+    return fill_view_batches<BT>(
+        world, members, segs, n_segs, edges, n_edges, tile, (int64_t)sizeof(typename E::S),
+        [&](const BT& b, int64_t tiles, int64_t moved) -> cudaError_t {
+            const int64_t work = std::max<int64_t>(tiles, b.n_edge);
+            const bool streamed = moved >= ((int64_t)256 << 20);
+            if (streamed && work <= INT32_MAX && cap_ctas(work) == work)
+                return launch_dependent(once, dim3((unsigned)work), dim3(kThreads), 0, st, b, dop);
+            const int grid = streamed ? cap_ctas(std::min<int64_t>(work, INT32_MAX))
+                                      : grid_for((const void*)loop, work * kThreads);
+            return launch_dependent(loop, dim3(grid), dim3(kThreads), 0, st, b, dop);
+        });
+}
+
+template <class E, int DIV, int G>
+static cudaError_t view_seg_pick(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
+                                 const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
+    if (view_fits_small(world, segs, n_segs, n_edges))
+        return view_seg_launch<E, DIV, G, ViewSegSmall>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    return view_seg_launch<E, DIV, G, ViewSegLarge>(world, members, segs, n_segs, edges, n_edges, dop, st);
+}
+
+template <class E, int DIV>
+static cudaError_t view_seg_g(int world, const ViewMember* m, const ViewSegment* sg, int ns, const ViewEdge* ed,
+                              int ne, float dop, cudaStream_t st) {
+    if (world <= 4) return view_seg_pick<E, DIV, 4>(world, m, sg, ns, ed, ne, dop, st);
+    return view_seg_pick<E, DIV, 8>(world, m, sg, ns, ed, ne, dop, st);
+}
+
+template <class E>
+static cudaError_t view_seg_div(int world, const ViewMember* m, const ViewSegment* sg, int ns, const ViewEdge* ed,
+                                int ne, DivSpec d, cudaStream_t st) {
+    switch (d.mode) {
+        case kDivNone: return view_seg_g<E, kDivNone>(world, m, sg, ns, ed, ne, d.operand, st);
+        case kDivPow2: return view_seg_g<E, kDivPow2>(world, m, sg, ns, ed, ne, d.operand, st);
+        default: return view_seg_g<E, kDivIeee>(world, m, sg, ns, ed, ne, d.operand, st);
+    }
+}
+
+static cudaError_t launch_bucket_view_seg(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
+                                          const ViewEdge* edges, int n_edges, int dtype, DivSpec div,
+                                          cudaStream_t stream) {
+    if (n_segs == 0 && n_edges == 0) return cudaSuccess;
+    if (dtype == DDP_F32) return view_seg_div<EF32>(world, members, segs, n_segs, edges, n_edges, div, stream);
+    if (dtype == kDtypeHook) return view_seg_div<EHOOK>(world, members, segs, n_segs, edges, n_edges, div, stream);
+    if (dtype == kDtypeHook16)
+        return view_seg_div<EHOOK16>(world, members, segs, n_segs, edges, n_edges, div, stream);
+    return view_seg_div<EBF16>(world, members, segs, n_segs, edges, n_edges, div, stream);
+}
+
 // Elements of a member that the TMA view kernel cannot stage with bulk
 // copies: the pieces before and after each segment's 16-byte-aligned body
 // (fewer than 16 bytes each side of a chunk boundary that is not 16-byte
@@ -481,6 +587,24 @@ static bool view_tma_worth(int world, int64_t elems, int dtype) {
     return world <= 128 && tma_tile_bytes(world) > 0 && elems * elem_bytes(dtype) * world >= ((int64_t)4 << 20);
 }
 
+// Which kernel folds a segment table: ddp_set_fused_kernel's forced choice
+// (TMA, or the register kernel for the vector and group choices), else by
+// size, from a sweep with both forced (one bucket of three members, chunk
+// boundaries off the 16-byte grid, N = 4 .. 64, 2 MiB .. 8 GiB moved): the
+// TMA kernel for 16 or more ranks whose bodies move less than 128 MiB (its
+// CTAs spread few vectors per rank over more SMs: N = 64, 32 MiB, 12.6
+// against 16.6 us), the register kernel everywhere else (N = 8, 1 GiB: 157
+// against 166 us; the 355M decoder's view step: 3.23 against 3.47 ms).
+static bool view_use_seg(int world, int64_t body_elems, int dtype) {
+    switch (fused_kernel_override()) {
+        case DDP_FUSED_TMA: return false;
+        case DDP_FUSED_VECTOR:
+        case DDP_FUSED_GROUP: return true;
+        default: break;
+    }
+    return world < 16 || 2 * body_elems * elem_bytes(dtype) * world >= ((int64_t)128 << 20);
+}
+
 static cudaError_t view_register(int world, const ViewMember* members, int n, int64_t bucket_numel, int dtype,
                                  DivSpec div, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
@@ -513,8 +637,11 @@ cudaError_t launch_buckets_view(int world, const ViewMember* members, const int*
             if (g.len <= kTmaEdgeMax) short_edges.push_back(g);
             else long_edges.add(world, members[g.member], g.start, g.len, es, g.clen);
         }
-        cudaError_t e = launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(),
-                                               short_edges.data(), (int)short_edges.size(), dtype, div, stream);
+        cudaError_t e = view_use_seg(world, body, dtype)
+                            ? launch_bucket_view_seg(world, members, segs.data(), (int)segs.size(),
+                                                     short_edges.data(), (int)short_edges.size(), dtype, div, stream)
+                            : launch_bucket_view_tma(world, members, n_members, segs.data(), (int)segs.size(),
+                                                     short_edges.data(), (int)short_edges.size(), dtype, div, stream);
         if (e != cudaSuccess) return e;
         long_edges.bind();
         if (debug_enabled())

@@ -38,6 +38,7 @@
 
 #include "ddp_device.cuh"
 #include "ddp_internal.h"
+#include "view_batch.cuh"
 
 namespace ddpk {
 
@@ -302,37 +303,12 @@ k_tree_fused_tma(const __grid_constant__ TmaTable<CAP> t, int world, TileMap map
 // element by element by the consumer warps of the same launch before they
 // start on their tiles (edge e by CTA e mod G, one element per thread), with
 // plain loads and stores.  An edge's elements share no 16-byte word with any
-// body, so the two kinds of store never touch the same bytes.
+// body, so the two kinds of store never touch the same bytes.  The table
+// (ViewSegBatch) is in view_batch.cuh; bucket_kernels.cu's register view
+// kernel reads the same one.
 // ---------------------------------------------------------------------------
 
-constexpr int kViewEdgeMax = 32 * kTmaConsumerWarps;   // elements of one edge: one per consumer thread
-
-// One launch's table.  Two capacities: a launch's parameters are copied for
-// every eager launch, so a call with few segments (one bucket piece, one
-// small bucket) sends about 4 KB instead of the 32 KB of the large table.
-template <int SEGS, int PTRS, int EDGES>
-struct ViewTmaBatch {
-    static constexpr int kSegs = SEGS, kPtrs = PTRS, kEdges = EDGES;
-    int32_t n_seg;
-    int32_t world;
-    int64_t tile;               // elements per tile
-    int64_t tile_end[SEGS];     // inclusive prefix of tiles per segment
-    int64_t start[SEGS];        // first element of the segment in its member
-    uint32_t len[SEGS];         // elements (segments are cut at kViewSegMax)
-    uint16_t j[SEGS];           // ring chunk of the segment (world <= 128)
-    uint16_t mem[SEGS];         // member slot: its rank pointers are ptr[mem * world ..]
-    int32_t n_edge;
-    int32_t e_mem[EDGES];       // member slot of the edge
-    int32_t e_len[EDGES];       // elements, at most kViewEdgeMax
-    int64_t e_start[EDGES];     // first element of the edge in its member
-    int64_t e_pos[EDGES];       // bucket position of that element
-    int64_t e_clen[EDGES];      // chunk length of the member's bucket
-    char* ptr[PTRS];
-};
-using ViewTmaSmall = ViewTmaBatch<32, 256, 16>;
-using ViewTmaLarge = ViewTmaBatch<320, 2816, 64>;
-static_assert(2816 < 65536 && 128 < 65536, "member slots and chunk indices fit 16 bits");
-static_assert(sizeof(ViewTmaLarge) <= kMaxParamBytes, "view batch exceeds the kernel parameter limit");
+static_assert(kViewEdgeMax == 32 * kTmaConsumerWarps, "an edge has one element per consumer thread");
 
 struct SegCursor {
     int seg;
@@ -635,103 +611,26 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, const V
             fs.per_sm[smem] = per_sm;
         }
     }
-    // A launch takes consecutive members, each with its segments and edges,
-    // while the pointer, segment and edge tables have room; a member whose
-    // work does not fit goes on in the next launch, its pointers repeated.
-    static_assert(kViewEdgeMax == kTmaEdgeMax, "edge length limit differs between host and kernel");
-    const int max_members = BT::kPtrs / world;
-    struct Item {
-        int member;
-        int kind;      // 0 segment, 1 edge
-        int index;
-    };
-    std::vector<Item> items;
-    items.reserve((size_t)n_segs + (size_t)n_edges);
-    {
-        int si = 0, ei = 0;                 // both lists are in member order
-        while (si < n_segs || ei < n_edges) {
-            const bool take_seg = ei >= n_edges || (si < n_segs && segs[si].member <= edges[ei].member);
-            if (take_seg) {
-                items.push_back(Item{segs[si].member, 0, si});
-                ++si;
-            } else {
-                items.push_back(Item{edges[ei].member, 1, ei});
-                ++ei;
-            }
-        }
-    }
-    BT b;
-    b.world = world;
-    b.tile = tile;
-    b.n_seg = 0;
-    b.n_edge = 0;
-    int64_t tiles = 0;
-    int slots = 0, last_member = -1;
-    int64_t moved = 0;                  // bytes read and written by the launch being filled
-    auto flush = [&]() -> cudaError_t {
-        if (b.n_seg == 0 && b.n_edge == 0) return cudaSuccess;
-        const int64_t work = std::max<int64_t>(tiles, b.n_edge);
-        const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm * tma_waves(moved), work));
-        moved = 0;
-        cudaError_t e = launch_dependent(k, dim3(grid), dim3(kTmaThreads), smem, st, b, dop, take_ctl());
-        if (debug_enabled())
-            fprintf(stderr, "[ddp] bucket_view_tma world=%d segments=%d edges=%d members=%d tiles=%lld grid=%d\n",
-                    world, b.n_seg, b.n_edge, slots, (long long)tiles, grid);
-        b.n_seg = 0;
-        b.n_edge = 0;
-        tiles = 0;
-        slots = 0;
-        last_member = -1;
-        return e;
-    };
-    for (const Item& it : items) {
-        const bool full_tab = (it.member != last_member && slots == max_members) ||
-                              (it.kind == 0 && b.n_seg == BT::kSegs) || (it.kind == 1 && b.n_edge == BT::kEdges);
-        if (full_tab) {
-            cudaError_t e = flush();
-            if (e != cudaSuccess) return e;
-        }
-        if (it.member != last_member) {
-            const ViewMember& m = members[it.member];
-            for (int r = 0; r < world; ++r) b.ptr[(size_t)slots * world + r] = static_cast<char*>(m.ptrs[r]);
-            last_member = it.member;
-            ++slots;
-        }
-        if (it.kind == 0) {
-            const ViewSegment& g = segs[it.index];
-            tiles += (g.len + tile - 1) / tile;
-            moved += 2 * g.len * (int64_t)sizeof(typename E::S) * world;
-            b.tile_end[b.n_seg] = tiles;
-            b.start[b.n_seg] = g.start;
-            b.len[b.n_seg] = (uint32_t)g.len;
-            b.j[b.n_seg] = (uint16_t)g.j;
-            b.mem[b.n_seg] = (uint16_t)(slots - 1);
-            ++b.n_seg;
-        } else {
-            const ViewEdge& g = edges[it.index];
-            b.e_mem[b.n_edge] = slots - 1;
-            b.e_len[b.n_edge] = (int32_t)g.len;
-            b.e_start[b.n_edge] = g.start;
-            b.e_pos[b.n_edge] = members[it.member].offset + g.start;
-            b.e_clen[b.n_edge] = g.clen;
-            ++b.n_edge;
-        }
-    }
-    return flush();
+    return fill_view_batches<BT>(
+        world, members, segs, n_segs, edges, n_edges, tile, (int64_t)sizeof(typename E::S),
+        [&](const BT& b, int64_t tiles, int64_t moved) -> cudaError_t {
+            const int64_t work = std::max<int64_t>(tiles, b.n_edge);
+            const int grid = cap_ctas(std::min<int64_t>((int64_t)sm_count() * per_sm * tma_waves(moved), work));
+            const cudaError_t e = launch_dependent(k, dim3(grid), dim3(kTmaThreads), smem, st, b, dop, take_ctl());
+            if (debug_enabled())
+                fprintf(stderr, "[ddp] bucket_view_tma world=%d segments=%d edges=%d tiles=%lld grid=%d\n", world,
+                        b.n_seg, b.n_edge, (long long)tiles, grid);
+            return e;
+        });
 }
 
 // The small table when the whole call fits in it, else the large one.
 template <class E, int DIV>
 static cudaError_t view_tma_pick(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
                                  const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
-    int n_members = 0, last = -1;
-    for (int i = 0; i < n_segs; ++i)
-        if (segs[i].member != last) last = segs[i].member, ++n_members;
-    for (int i = 0; i < n_edges; ++i) ++n_members;            // at most one more slot per edge
-    if (n_segs <= ViewTmaSmall::kSegs && n_edges <= ViewTmaSmall::kEdges &&
-        (int64_t)n_members * world <= ViewTmaSmall::kPtrs)
-        return view_tma_launch<E, DIV, ViewTmaSmall>(world, members, segs, n_segs, edges, n_edges, dop, st);
-    return view_tma_launch<E, DIV, ViewTmaLarge>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    if (view_fits_small(world, segs, n_segs, n_edges))
+        return view_tma_launch<E, DIV, ViewSegSmall>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    return view_tma_launch<E, DIV, ViewSegLarge>(world, members, segs, n_segs, edges, n_edges, dop, st);
 }
 
 template <class E>

@@ -101,8 +101,14 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  * ddp_set_fused_kernel -- which kernel ring_allreduce_fused (and every call
  * that runs it on one buffer per rank: ddp_sync_buckets with
  * DDP_ALGO_FUSED / DDP_ALGO_BF16_HOOK, the reducer) uses from now on in this
- * process.  All of them compute the same fold in the same order, so results
- * are bit-identical whichever runs; the choice only changes speed.
+ * process, and which kernel folds the aligned segments of the fused view
+ * path (ddp_bucket_allreduce_view*, DDP_ALGO_VIEW and the hook views, the
+ * L2-sized pieces of DDP_ALGO_FUSED): DDP_FUSED_TMA the TMA-staged view
+ * kernel, DDP_FUSED_VECTOR or DDP_FUSED_GROUP the register view kernel,
+ * DDP_FUSED_AUTO the TMA kernel for 16 or more ranks whose segments move
+ * less than 128 MiB and the register kernel otherwise.  All of them compute
+ * the same fold in the same order, so results are bit-identical whichever
+ * runs; the choice only changes speed.
  *   DDP_FUSED_AUTO   by size (the default): the group kernel up to 4 KiB
  *                    per rank, up to 256 KiB over 2 ranks, up to 16 KiB over
  *                    8 fp32 ranks and up to 64 KiB where chunk boundaries

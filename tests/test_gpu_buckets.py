@@ -37,6 +37,30 @@ def _host_grads(numels, world, dtype, seed0, kind="randn", std=1e-2):
     return flat, [[flat_h[r, offs[p]:offs[p + 1]].copy() for p in range(len(numels))] for r in range(world)]
 
 
+# Segment tables of the view path are folded by the TMA-staged view kernel or
+# by the register view kernel (ddp_set_fused_kernel: TMA, or vector); "auto"
+# picks by size, "vector_cap" forces the register kernel under a CTA cap so
+# that its blocks loop over the tiles.
+VIEW_KERNELS = ["auto", "tma", "vector", "vector_cap"]
+
+
+class _view_kernel:
+    def __init__(self, kind):
+        self.kind = kind
+
+    def __enter__(self):
+        k = {"auto": ddp.DDP_FUSED_AUTO, "tma": ddp.DDP_FUSED_TMA}.get(self.kind, ddp.DDP_FUSED_VECTOR)
+        self.prev = ddp.ddp_set_fused_kernel(k)
+        self.prev_cap = ddp.ddp_set_max_ctas(40) if self.kind == "vector_cap" else None
+        return self
+
+    def __exit__(self, *exc):
+        ddp.ddp_set_fused_kernel(self.prev)
+        if self.prev_cap is not None:
+            ddp.ddp_set_max_ctas(self.prev_cap)
+        return False
+
+
 def _device_views(flat_dev, numels):
     offs = np.cumsum([0] + list(numels))
     return [[flat_dev[r, int(offs[p]):int(offs[p + 1])] for p in range(len(numels))]
@@ -133,12 +157,14 @@ def test_view_equals_pack_fused_unpack_bitwise():
         assert torch.equal(a.view(iv), b.view(iv)), f"trial {trial}"
 
 
+@pytest.mark.parametrize("kernel", ["auto", "tma"])
 @pytest.mark.parametrize("algo", [ddp.DDP_ALGO_FUSED, ddp.DDP_ALGO_VIEW])
 @pytest.mark.parametrize("cap_mib,count", [(5, 9), (10, 6), (25, 3), (50, 2)])
-def test_resnet50_bf16_n16_cap_sweep_full(cap_mib, count, algo):
-    # pack + fused ring + unpack, and the fused view (one TMA launch whose
-    # consumer warps also fold the elements around the fc bucket's unaligned
-    # chunk boundaries)
+def test_resnet50_bf16_n16_cap_sweep_full(cap_mib, count, algo, kernel):
+    # pack + fused ring + unpack, and the fused view (one launch of the
+    # register view kernel, one block per tile, by size -- or of the TMA view
+    # kernel, forced -- whose threads also fold the elements around the fc
+    # bucket's unaligned chunk boundaries)
     numels = workloads.param_numels(workloads.resnet50_param_shapes())
     world = 16
     plan = ddp.ddp_plan_buckets(numels, ddp.BF16, MiB, cap_mib * MiB)
@@ -149,9 +175,10 @@ def test_resnet50_bf16_n16_cap_sweep_full(cap_mib, count, algo):
     bk = None
     if algo == ddp.DDP_ALGO_FUSED:
         bk = [[torch.empty(int(n), dtype=torch.bfloat16, device="cuda") for n in plan[2]] for _ in range(world)]
-    ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
+    with _view_kernel(kernel):
+        ddp.ddp_sync_buckets(gdev, plan, bk, algo=algo)
     torch.cuda.synchronize()
-    assert_canaries(g_storage, f"resnet50 cap {cap_mib} algo {algo}")
+    assert_canaries(g_storage, f"resnet50 cap {cap_mib} algo {algo} kernel {kernel}")
     ref64 = np.zeros(sum(numels))
     for r in range(world):
         ref64 += oracle.bf16_to_f32(np.concatenate(grads_h[r])).astype(np.float64)
@@ -240,8 +267,9 @@ def test_bf16_pack_unpack_round_trip_matches_oracle_rounding():
             assert_bits_equal(f32_or_bits(out[r][i]), oracle.bf16_to_f32(want_bits), f"unpack r{r} m{i}")
 
 
+@pytest.mark.parametrize("kernel", VIEW_KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_view_tma_path_matches_oracle(dtype):
+def test_view_tma_path_matches_oracle(dtype, kernel):
     # one bucket of ~1.2M elements over 8 ranks (> 4 MiB): member sizes and the
     # chunk length are multiples of 16 elements, so the view path streams
     # chunk-aligned segments through shared memory; one member spans several
@@ -257,11 +285,12 @@ def test_view_tma_path_matches_oracle(dtype):
     assert len(plan[2]) == 1
     flat, grads_h = _host_grads(numels, world, dtype, seed0=6)
     g = flat.cuda()
-    ddp.ddp_sync_buckets(_device_views(g, numels), plan, None, algo=ddp.DDP_ALGO_VIEW)
+    with _view_kernel(kernel):
+        ddp.ddp_sync_buckets(_device_views(g, numels), plan, None, algo=ddp.DDP_ALGO_VIEW)
     torch.cuda.synchronize()
     oracle.ddp_sync(grads_h, code, 1 << 40, 1 << 40)
     want = np.stack([np.concatenate(grads_h[r]) for r in range(world)])
-    assert_bits_equal(f32_or_bits(g), want, f"view tma {dtype}")
+    assert_bits_equal(f32_or_bits(g), want, f"view {kernel} {dtype}")
     assert ddp.ddp_device_status() == 0
 
 
@@ -374,9 +403,10 @@ def _oracle_view_hook(grads_h, offsets, bucket_numel, divisor, fp16=False):
         oracle.bucket_unpack(grads_h[r], offsets, widen(bufs[r]), oracle.F32)
 
 
+@pytest.mark.parametrize("kernel", VIEW_KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "hook", "hook16"])
 @pytest.mark.parametrize("layout", ["boundaries", "pointers"])
-def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
+def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout, kernel):
     # a TMA-sized bucket (8 ranks) whose chunk boundaries are not 16-byte
     # aligned ("boundaries": every member 16-byte aligned in memory, the
     # chunk length odd), or whose members' pointers are not ("pointers":
@@ -413,12 +443,13 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
     code = oracle.BF16 if dtype == "bf16" else oracle.F32
     for div in (world, 3):
         grads_h = [[f32_or_bits(t) for t in dev[r]] for r in range(world)]
-        if hook == "hook":
-            ddp.ddp_bucket_allreduce_view_bf16(dev, offsets, total, div)
-        elif hook == "hook16":
-            ddp.ddp_bucket_allreduce_view_fp16(dev, offsets, total, div)
-        else:
-            ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
+        with _view_kernel(kernel):
+            if hook == "hook":
+                ddp.ddp_bucket_allreduce_view_bf16(dev, offsets, total, div)
+            elif hook == "hook16":
+                ddp.ddp_bucket_allreduce_view_fp16(dev, offsets, total, div)
+            else:
+                ddp.ddp_bucket_allreduce_view(dev, offsets, total, div)
         torch.cuda.synchronize()
         if hook:
             _oracle_view_hook(grads_h, offsets, total, div, fp16=hook == "hook16")
@@ -427,12 +458,13 @@ def test_view_misaligned_chunks_or_pointers_match_oracle(dtype, layout):
         for r in range(world):
             for i in range(len(numels)):
                 assert_bits_equal(f32_or_bits(dev[r][i]), grads_h[r][i],
-                                  f"{layout} {hook or dtype} div={div} r{r} m{i}")
+                                  f"{layout} {hook or dtype} {kernel} div={div} r{r} m{i}")
     assert ddp.ddp_device_status() == 0
 
 
+@pytest.mark.parametrize("kernel", VIEW_KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "hook"])
-def test_view_many_unaligned_boundaries_span_several_tma_launches(dtype):
+def test_view_many_unaligned_boundaries_span_several_tma_launches(dtype, kernel):
     # 16 ranks, 5-7 buckets of odd sizes, every member its own aligned
     # allocation: the bodies go to the TMA view kernel, and the elements
     # around ~100 unaligned chunk boundaries and member ends (more than one
@@ -455,7 +487,8 @@ def test_view_many_unaligned_boundaries_span_several_tma_launches(dtype):
     dev = [[flat[r, int(offs[p]):int(offs[p + 1])].clone().to("cuda") for p in range(len(numels))]
            for r in range(world)]
     assert all(t.data_ptr() % 16 == 0 for t in dev[0])
-    ddp.ddp_sync_buckets(dev, plan, None, algo=ddp.DDP_ALGO_BF16_HOOK_VIEW if hook else ddp.DDP_ALGO_VIEW)
+    with _view_kernel(kernel):
+        ddp.ddp_sync_buckets(dev, plan, None, algo=ddp.DDP_ALGO_BF16_HOOK_VIEW if hook else ddp.DDP_ALGO_VIEW)
     torch.cuda.synchronize()
     if hook:
         oracle.ddp_sync_bf16_hook(grads_h, first, cap)
@@ -463,7 +496,8 @@ def test_view_many_unaligned_boundaries_span_several_tma_launches(dtype):
         oracle.ddp_sync(grads_h, code, first, cap)
     for r in range(world):
         for p in range(len(numels)):
-            assert_bits_equal(f32_or_bits(dev[r][p]), grads_h[r][p], f"{'hook' if hook else dtype} r{r} p{p}")
+            assert_bits_equal(f32_or_bits(dev[r][p]), grads_h[r][p],
+                              f"{'hook' if hook else dtype} {kernel} r{r} p{p}")
     assert ddp.ddp_device_status() == 0
     assert es in (2, 4)
 
