@@ -34,7 +34,7 @@ namespace ddpk {
 // bucket) sends about 1 KB instead of the 24 KB that 768 items take.
 constexpr int kCopyItemsSmall = 32;
 constexpr int kCopyItems = 768;          // items per launch (24 KB of parameters)
-constexpr int64_t kCopyTile = 32768;     // bytes per tile
+constexpr int64_t kCopyTile = 16384;     // bytes per tile: four 16-byte vectors per thread
 
 template <int CAP>
 struct CopyBatch {
@@ -118,7 +118,12 @@ static cudaError_t copy_items_cap(const CopyItem* items, int64_t n, cudaStream_t
             ++b.n;
         }
         if (b.n == 0) continue;
-        const int grid = grid_for((const void*)k_copy_items<CAP>, tiles * kThreads);
+        // a launch that copies 128 MiB or more runs one block per tile, so the
+        // blocks take the tiles in address order as SMs free up; a smaller
+        // one, a few waves of blocks looping over the tiles
+        const int grid = tiles * kCopyTile >= ((int64_t)128 << 20)
+                             ? cap_ctas(std::min<int64_t>(tiles, INT32_MAX))
+                             : grid_for((const void*)k_copy_items<CAP>, tiles * kThreads);
         cudaError_t e = launch_dependent(k_copy_items<CAP>,
                                          dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(grid, tiles))),
                                          dim3(kThreads), 0, stream, b);
@@ -602,6 +607,11 @@ static bool view_use_seg(int world, int64_t body_elems, int dtype) {
         case DDP_FUSED_GROUP: return true;
         default: break;
     }
+    // under a CTA budget of less than four blocks per SM (a reducer leaving
+    // SMs to the backward) the TMA kernel, which keeps a whole stage of every
+    // rank in flight per CTA: the decoder's view step on 38 CTAs overlapped
+    // with the backward took 11.5 ms on it against 19.3 ms on the register kernel
+    if (cta_cap_is_tight()) return false;
     return world < 16 || 2 * body_elems * elem_bytes(dtype) * world >= ((int64_t)128 << 20);
 }
 

@@ -62,8 +62,10 @@ int set_thread_cta_cap(int cap) {
     return prev;
 }
 
+int cta_cap() { return t_cta_cap >= 0 ? t_cta_cap : g_max_ctas.load(std::memory_order_relaxed); }
+
 int cap_ctas(int64_t grid) {
-    const int cap = t_cta_cap >= 0 ? t_cta_cap : g_max_ctas.load(std::memory_order_relaxed);
+    const int cap = cta_cap();
     if (cap > 0 && grid > cap) grid = cap;
     return (int)std::max<int64_t>(1, grid);
 }
@@ -84,6 +86,11 @@ int sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
     g_sms[dev] = n;
     return n;
+}
+
+bool cta_cap_is_tight() {
+    const int cap = cta_cap();
+    return cap > 0 && cap < 4 * sm_count();
 }
 
 // Grid of a grid-stride kernel: four waves of resident blocks (SMs x blocks

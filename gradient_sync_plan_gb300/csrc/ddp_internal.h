@@ -60,6 +60,11 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok);
 // thread's cap if one is set (a reducer's own budget while it launches),
 // else the process-wide cap of ddp_set_max_ctas
 int cap_ctas(int64_t grid);
+// The CTA cap in effect for launches from this thread (0: none).
+int cta_cap();
+// A cap below four blocks per SM: too few 256-thread register blocks to keep
+// HBM busy, where the TMA-staged kernels move several times more bytes per CTA.
+bool cta_cap_is_tight();
 // Sets the calling thread's cap (-1: none, follow the process-wide cap);
 // returns the previous one.
 int set_thread_cta_cap(int cap);

@@ -443,7 +443,9 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
     //    N >= 64 up to 256 KiB, N >= 128 up to 64 KiB; at 16-31 ranks from
     //    256 KiB (fp32; bf16 above 1 MiB) to 4 MiB);
     //  * everything else, and every large bucket: the vector kernel, whose
-    //    one block per tile streams at or above the measured copy rate.
+    //    one block per tile streams at or above the measured copy rate --
+    //    except under a CTA budget of less than four blocks per SM, where
+    //    buckets from 1 MiB per rank go to the TMA kernel.
     constexpr int64_t KiB = 1024, MiB = 1024 * 1024;
     const int64_t per_rank = numel * elem_bytes(dtype);
     const bool chunks_aligned = (chunk_len(numel, world) * elem_bytes(dtype)) % 16 == 0;
@@ -452,6 +454,9 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
                      (world == 8 && dtype == DDP_F32 && per_rank <= 16 * KiB)))
         return FusedPath::kGroup;
     if (tma_ok) {
+        // a CTA budget below four blocks per SM: the TMA kernel keeps more
+        // bytes in flight per CTA than the vector kernel's 256-thread blocks
+        if (cta_cap_is_tight() && per_rank >= 1 * MiB) return FusedPath::kTma;
         if (world >= 16 && per_rank <= 16 * KiB) return FusedPath::kTma;
         if (world >= 128) {
             if (per_rank <= 64 * KiB) return FusedPath::kTma;
@@ -560,8 +565,18 @@ static cudaError_t accumulate_impl(int world, void* const* acc, const void* cons
         tg.p[r] = static_cast<char*>(const_cast<void*>(g[r]));
     }
     const int64_t per_rank = vec_ok ? numel / E::L + E::L : numel;
-    int gx = grid_for((const void*)k, per_rank * world);
-    gx = std::max(1, (gx + world - 1) / world);
+    // 128 MiB or more of accumulators: one block per kThreads vectors of a
+    // rank (blocks are scheduled rank after rank, each rank's in address
+    // order); else a few waves of blocks striding over each rank
+    const int64_t tiles = (per_rank + kThreads - 1) / kThreads;
+    const bool streamed = vec_ok && (int64_t)world * numel * (int64_t)sizeof(typename E::S) >= ((int64_t)128 << 20);
+    int gx;
+    if (streamed && tiles * world <= INT32_MAX && cap_ctas(tiles * world) == tiles * world) {
+        gx = (int)std::min<int64_t>(tiles, INT32_MAX);
+    } else {
+        gx = streamed ? cap_ctas(std::min<int64_t>(tiles * world, INT32_MAX)) : grid_for((const void*)k, per_rank * world);
+        gx = std::max(1, (gx + world - 1) / world);
+    }
     return launch_dependent(k, dim3(gx, world), dim3(kThreads), 0, st, ta, tg, numel, vec_ok ? 1 : 0);
 }
 

@@ -117,7 +117,10 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  *                    to 1 MiB at 32-63 ranks, 256 KiB at 64-127, 64 KiB from
  *                    128; fp32 at 16-31 ranks from 256 KiB to 4 MiB); the
  *                    vector kernel otherwise, which includes every large
- *                    bucket;
+ *                    bucket -- except under a CTA cap (ddp_set_max_ctas, a
+ *                    reducer's budget) below four CTAs per SM, where buckets
+ *                    from 1 MiB per rank, and the view path's segments, go
+ *                    to the TMA kernels;
  *   DDP_FUSED_VECTOR one thread per 16-byte vector (two over 2 or 3 ranks),
  *                    folding all N ranks; a bucket of 128 MiB or more over
  *                    all ranks runs one block per tile of vectors;
