@@ -47,6 +47,40 @@ __device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world,
     for (int r = 0; r < world; ++r) reinterpret_cast<S*>(t.p[world + r])[e] = y;
 }
 
+// The elements the vector path leaves: those of every 16-byte vector that
+// straddles a chunk boundary, and of the ragged last vector.  Entry q of
+// world * L takes lane q % L of the vector holding boundary q / L + 1 (or,
+// for the last L entries, of the last vector); a vector that holds several
+// boundaries (chunks shorter than a vector) is taken by its first entry
+// only.  Each element is folded by its own thread, so a straddling vector
+// costs one element's latency instead of L of them.
+template <class E, int DIV, int CAP>
+__device__ __forceinline__ void ring_edge_element(const RankTable<CAP>& t, int world, int64_t numel, int64_t clen,
+                                                  int64_t q, float dop) {
+    constexpr int L = E::L;
+    const int64_t k = q / L;                   // boundary k + 1, or the last vector for k = world - 1
+    const int64_t lane = q - k * L;
+    // boundary k + 1 (at (k + 1) * clen) needs its vector taken when it is
+    // inside the bucket and off the vector grid
+    auto needs = [&](int64_t kk) {
+        const int64_t b = (kk + 1) * clen;
+        return b < numel && b % L != 0;
+    };
+    int64_t v;
+    if (k < world - 1) {
+        if (!needs(k)) return;
+        v = (k + 1) * clen / L;
+        if (k > 0 && needs(k - 1) && k * clen / L == v) return;      // taken by boundary k
+    } else {
+        if (numel % L == 0) return;
+        v = numel / L;
+        const int64_t kl = (numel + clen - 1) / clen - 2;           // last boundary inside the bucket
+        if (kl >= 0 && needs(kl) && (kl + 1) * clen / L == v) return;
+    }
+    const int64_t e = v * L + lane;
+    if (e < numel) ring_element<E, DIV, CAP>(t, world, e, clen, dop);
+}
+
 // Vectorised fused kernel: all rank buffers are 16-byte aligned.  The 16-byte
 // vectors are cut into tiles of kThreads * U; block b takes tiles b,
 // b + gridDim.x, ...  Thread x of a tile takes its vectors x, x + kThreads,
@@ -56,11 +90,14 @@ __device__ __forceinline__ void ring_element(const RankTable<CAP>& t, int world,
 // up and the blocks in flight stream one compact window of every rank; a
 // bucket that fits in L2 gets a few waves of blocks that loop over the tiles.
 // A vector whose lanes fall in two chunks (only possible when c is not a
-// multiple of the lane count) or runs past the end is done lane by lane.
-// LOOP = false: the grid is exactly one block per tile.
+// multiple of the lane count) or runs past the end is done lane by lane, one
+// lane per thread (ring_edge_element), by the launch's last edge_blocks
+// blocks, which run beside the tiles.
+// LOOP = false: the grid is one block per tile, plus the edge blocks.
 template <class E, int DIV, int CAP, int G, int U, int MINB, bool LOOP>
 __global__ void __launch_bounds__(kThreads, MINB)
-k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop,
+             int edge_blocks) {
     using V = typename E::V;
     constexpr int L = E::L;
     constexpr int64_t kTile = (int64_t)kThreads * U;
@@ -70,6 +107,20 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
     const int64_t full = numel / L;
     const int64_t tiles = (nvec + kTile - 1) / kTile;
     auto at = [&](int r) -> const char* { return t.p[r]; };
+    // the straddling and ragged vectors, one element per thread: by the last
+    // edge_blocks blocks beside the tiles, or (edge_blocks < 0, under a CTA
+    // cap) by every block before its tiles; the tiles' threads skip them
+    if (edge_blocks < 0)
+        for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < (int64_t)world * L;
+             q += (int64_t)gridDim.x * kThreads)
+            ring_edge_element<E, DIV, CAP>(t, world, numel, clen, q, dop);
+    const int main_blocks = (int)gridDim.x - (edge_blocks > 0 ? edge_blocks : 0);
+    if ((int)blockIdx.x >= main_blocks) {
+        for (int64_t q = (int64_t)(blockIdx.x - main_blocks) * kThreads + threadIdx.x; q < (int64_t)world * L;
+             q += (int64_t)edge_blocks * kThreads)
+            ring_edge_element<E, DIV, CAP>(t, world, numel, clen, q, dop);
+        return;
+    }
     int64_t tile = blockIdx.x;
     int64_t vb = tile * kTile + threadIdx.x;
     if (vb >= nvec) return;
@@ -103,13 +154,11 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
                     ++jv;
                     end_v += clen;
                 }
+                // whole vectors of this chunk; the others went to ring_edge_element
                 if (U > 1 && v < full && i + L <= end_v) {     // U = 1: the fast path's test
                     const int start = (jv + 1 == world) ? 0 : (int)jv + 1;
                     V y = E::template vdiv<DIV>(fold_ring_vec<E, G>(at, world, start, v * 16), dop);
                     for (int r = 0; r < world; ++r) st_stream<V>(t.p[world + r] + v * 16, y);
-                } else {
-                    for (int l = 0; l < L; ++l)
-                        if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
                 }
             }
         }
@@ -118,7 +167,7 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
         if constexpr (!LOOP) {
             return;
         } else {
-            tile += gridDim.x;
+            tile += main_blocks;
             vb = tile * kTile + threadIdx.x;
             if (tile >= tiles || vb >= nvec) return;
         }
@@ -132,10 +181,12 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
 // ring order, taking each from its owner lane by a warp shuffle -- the adds
 // of k_ring_fused in the same order, on P times as many threads, each with
 // ceil(N / P) = R loads in flight instead of N.  Vectors that straddle a
-// chunk boundary or the end are done element-wise by the group's lane 0.
+// chunk boundary or the end are done element-wise, one element per thread
+// (ring_edge_element), by the launch's last edge_blocks blocks.
 template <class E, int DIV, int CAP, int P, int R>
 __global__ void __launch_bounds__(kThreads)
-k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop) {
+k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel, int64_t clen, float dop,
+                   int edge_blocks) {
     using V = typename E::V;
     constexpr int L = E::L;
     pdl_release();
@@ -145,8 +196,19 @@ k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t 
     const int q = lane & (P - 1);
     const int64_t nvec = (numel + L - 1) / L;
     const int64_t full = numel / L;
+    if (edge_blocks < 0)                          // the edge elements (see k_ring_fused)
+        for (int64_t qe = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; qe < (int64_t)world * L;
+             qe += (int64_t)gridDim.x * blockDim.x)
+            ring_edge_element<E, DIV, CAP>(t, world, numel, clen, qe, dop);
+    const int main_blocks = (int)gridDim.x - (edge_blocks > 0 ? edge_blocks : 0);
+    if ((int)blockIdx.x >= main_blocks) {
+        for (int64_t qe = (int64_t)(blockIdx.x - main_blocks) * blockDim.x + threadIdx.x; qe < (int64_t)world * L;
+             qe += (int64_t)edge_blocks * blockDim.x)
+            ring_edge_element<E, DIV, CAP>(t, world, numel, clen, qe, dop);
+        return;
+    }
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t n_warps = ((int64_t)main_blocks * blockDim.x) >> 5;
     // the loop bounds are the same for every lane of a warp, so every lane
     // reaches every shuffle
     for (int64_t base = warp * kGroups; base < nvec; base += n_warps * kGroups) {
@@ -186,10 +248,7 @@ k_ring_fused_group(const __grid_constant__ RankTable<CAP> t, int world, int64_t 
                     st_stream<V>(t.p[world + r] + off, y);
                 }
             }
-        } else if (valid && q == 0) {
-            for (int l = 0; l < L; ++l)
-                if (i + l < numel) ring_element<E, DIV, CAP>(t, world, i + l, clen, dop);
-        }
+        }       // vectors that straddle a chunk boundary or the end: ring_edge_element, above
     }
 }
 
@@ -322,6 +381,19 @@ static RankTable<CAP> make_io_table(int world, void* const* in, void* const* out
     return t;
 }
 
+// Blocks for the elements of straddling and ragged vectors (ring_edge_element)
+// added to a launch of `grid` blocks: none when every chunk boundary and the
+// end fall on the 16-byte grid; -1 (every block takes its share first) when
+// the extra blocks would exceed the CTA cap.
+static int edge_blocks_for(int world, int64_t numel, int lanes, int threads, int64_t grid) {
+    const bool edges = numel % lanes != 0 || (world > 1 && chunk_len(numel, world) % lanes != 0);
+    if (!edges) return 0;
+    const int eb = (int)(((int64_t)world * lanes + threads - 1) / threads);
+    const int cap = cta_cap();
+    if ((cap > 0 && grid + eb > cap) || grid + eb > INT32_MAX) return -1;
+    return eb;
+}
+
 // Buckets that do not fit in L2 run one block per tile (see k_ring_fused).
 constexpr int64_t kTilePerBlockBytes = 128ll << 20;
 
@@ -333,17 +405,20 @@ static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64
     const bool streamed = (int64_t)world * numel * (int64_t)sizeof(typename E::S) >= kTilePerBlockBytes;
     int grid = 0;
     cudaError_t e;
-    if (streamed && tiles <= INT32_MAX && cap_ctas(tiles) == tiles) {
-        grid = (int)tiles;
+    if (streamed && tiles <= INT32_MAX - 64 && cap_ctas(tiles) == tiles) {
+        const int eb = edge_blocks_for(world, numel, E::L, kThreads, tiles);
+        grid = (int)tiles + std::max(eb, 0);
         e = launch_dependent(k_ring_fused<E, DIV, 2 * CAP, G, U, MINB, false>, dim3(grid), dim3(kThreads), 0, st,
-                             make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop);
+                             make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop, eb);
     } else {
         auto loop = k_ring_fused<E, DIV, 2 * CAP, G, LOOP_U, LOOP_MINB, true>;
         const int64_t loop_tiles = (nvec + (int64_t)kThreads * LOOP_U - 1) / ((int64_t)kThreads * LOOP_U);
-        grid = streamed ? cap_ctas(std::min<int64_t>(loop_tiles, INT32_MAX))
+        grid = streamed ? cap_ctas(std::min<int64_t>(loop_tiles, INT32_MAX - 64))
                         : grid_for((const void*)loop, loop_tiles * kThreads);
+        const int eb = edge_blocks_for(world, numel, E::L, kThreads, grid);
+        grid += std::max(eb, 0);
         e = launch_dependent(loop, dim3(grid), dim3(kThreads), 0, st, make_io_table<2 * CAP>(world, in, out), world,
-                             numel, chunk_len(numel, world), dop);
+                             numel, chunk_len(numel, world), dop, eb);
     }
     if (debug_enabled())
         fprintf(stderr, "[ddp] ring_fused world=%d numel=%lld grid=%d tiles=%lld G=%d U=%d CAP=%d\n", world,
@@ -359,10 +434,12 @@ static cudaError_t fused_group(int world, void* const* in, void* const* out, int
     auto k = k_ring_fused_group<E, DIV, 2 * CAP, P, R>;
     const int64_t nvec = (numel + E::L - 1) / E::L;
     const int64_t lanes = (nvec + 32 / P - 1) / (32 / P) * 32;
-    const int grid = grid_for((const void*)k, lanes, kGroupThreads);
+    int grid = grid_for((const void*)k, lanes, kGroupThreads);
+    const int eb = edge_blocks_for(world, numel, E::L, kGroupThreads, grid);
+    grid += std::max(eb, 0);
     const cudaError_t e = launch_dependent(k, dim3(grid), dim3(kGroupThreads), 0, st,
                                            make_io_table<2 * CAP>(world, in, out), world, numel,
-                                           chunk_len(numel, world), dop);
+                                           chunk_len(numel, world), dop, eb);
     if (debug_enabled())
         fprintf(stderr, "[ddp] ring_fused_group world=%d numel=%lld grid=%d P=%d R=%d\n", world, (long long)numel,
                 grid, P, R);
@@ -435,9 +512,9 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
     // replay of back-to-back calls, fp32 and bf16, N = 2 .. 128, 16 KiB ..
     // 256 MiB per rank):
     //  * a few KiB per rank: the group kernel spreads the ranks over lanes;
-    //    it stays ahead up to 256 KiB at 2 ranks, up to 16 KiB at 8 fp32
-    //    ranks, and up to 64 KiB where chunk boundaries are not 16-byte
-    //    aligned (there the vector kernel's straddling vectors go lane by lane);
+    //    it stays ahead up to 256 KiB at 2 ranks, and up to 16 KiB at 8 fp32
+    //    ranks and wherever fp32 chunk boundaries are not 16-byte aligned
+    //    (N = 3, 5, 6, 7, 12, 24 on these sizes);
     //  * many ranks with little data each: the TMA kernel's one CTA per
     //    tile reaches more SMs (N >= 16 up to 16 KiB, N >= 32 up to 1 MiB,
     //    N >= 64 up to 256 KiB, N >= 128 up to 64 KiB; at 16-31 ranks from
@@ -450,8 +527,7 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
     const int64_t per_rank = numel * elem_bytes(dtype);
     const bool chunks_aligned = (chunk_len(numel, world) * elem_bytes(dtype)) % 16 == 0;
     if (group_ok && (per_rank <= 4 * KiB || (world == 2 && per_rank <= 256 * KiB) ||
-                     (!chunks_aligned && per_rank <= 64 * KiB) ||
-                     (world == 8 && dtype == DDP_F32 && per_rank <= 16 * KiB)))
+                     (dtype == DDP_F32 && per_rank <= 16 * KiB && (world == 8 || !chunks_aligned))))
         return FusedPath::kGroup;
     if (tma_ok) {
         // a CTA budget below four blocks per SM: the TMA kernel keeps more

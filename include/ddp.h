@@ -110,9 +110,9 @@ int32_t ddp_set_max_ctas(int32_t max_ctas, int32_t* previous);
  * the same fold in the same order, so results are bit-identical whichever
  * runs; the choice only changes speed.
  *   DDP_FUSED_AUTO   by size (the default): the group kernel up to 4 KiB
- *                    per rank, up to 256 KiB over 2 ranks, up to 16 KiB over
- *                    8 fp32 ranks and up to 64 KiB where chunk boundaries
- *                    are not 16-byte aligned; the TMA kernel for 16 or more
+ *                    per rank, up to 256 KiB over 2 ranks, and up to 16 KiB
+ *                    over 8 fp32 ranks or where fp32 chunk boundaries are
+ *                    not 16-byte aligned; the TMA kernel for 16 or more
  *                    ranks with little data each (up to 16 KiB per rank; up
  *                    to 1 MiB at 32-63 ranks, 256 KiB at 64-127, 64 KiB from
  *                    128; fp32 at 16-31 ranks from 256 KiB to 4 MiB); the
