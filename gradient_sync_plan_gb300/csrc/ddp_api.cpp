@@ -118,6 +118,15 @@ int grid_for(const void* kernel, int64_t work_items, int threads) {
     return cap_ctas(std::min<int64_t>((int64_t)sms * per_sm * 4, need));
 }
 
+int rows_grid_x(const void* kernel, int64_t per_row, int rows, int64_t bytes) {
+    const int64_t tiles = (per_row + kThreads - 1) / kThreads;
+    if (bytes >= ((int64_t)128 << 20) && tiles * rows <= INT32_MAX && cap_ctas(tiles * rows) == tiles * rows)
+        return (int)std::max<int64_t>(1, tiles);
+    const int g = bytes >= ((int64_t)128 << 20) ? cap_ctas(std::min<int64_t>(tiles * rows, INT32_MAX))
+                                                 : grid_for(kernel, per_row * rows);
+    return std::max(1, (g + rows - 1) / rows);
+}
+
 // Host buffers of a host-memory allreduce: non-null and element-aligned;
 // inputs pairwise disjoint; each output either is its own rank's input (in
 // place) or overlaps no input and no other output.

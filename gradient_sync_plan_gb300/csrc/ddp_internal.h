@@ -49,6 +49,12 @@ const char* last_cuda_error();
 // Launch geometry helpers (cached per device).
 int sm_count();
 int grid_for(const void* kernel, int64_t work_items, int threads = kThreads);
+// x-extent of an (x, rows) grid whose rows each take per_row items, one per
+// thread: one block per kThreads items of a row when the launch moves at
+// least 128 MiB and the CTA cap allows it (blocks then run row after row,
+// each row's in address order), else four waves of resident blocks shared
+// among the rows.
+int rows_grid_x(const void* kernel, int64_t per_row, int rows, int64_t bytes);
 // Fused-ring kernel chosen by ddp_set_fused_kernel (DDP_FUSED_AUTO = by size).
 int fused_kernel_override();
 

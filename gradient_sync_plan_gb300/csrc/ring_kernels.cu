@@ -572,8 +572,9 @@ static cudaError_t hop(const RankTable<CAP>& t, int world, int64_t numel, int ph
     const int64_t clen = chunk_len(numel, world);
     const int64_t per_rank = vec_ok ? (clen + E::L - 1) / E::L + 1 : clen;
     // blocks in x per rank: enough to fill the GPU once all ranks are counted
-    int gx = grid_for((const void*)k, per_rank * world);
-    gx = std::max(1, (gx + world - 1) / world);
+    // (one block per tile measured no faster here: a hop's chunk is read
+    // back from L2 by the next hop, and the all-gather copies got slower)
+    const int gx = rows_grid_x((const void*)k, per_rank, world, 0);
     // hops are launched as programmatic dependents of the previous kernel on
     // the stream: each one's launch overlaps the previous hop's tail
     cudaLaunchConfig_t cfg = {};
@@ -641,18 +642,10 @@ static cudaError_t accumulate_impl(int world, void* const* acc, const void* cons
         tg.p[r] = static_cast<char*>(const_cast<void*>(g[r]));
     }
     const int64_t per_rank = vec_ok ? numel / E::L + E::L : numel;
-    // 128 MiB or more of accumulators: one block per kThreads vectors of a
-    // rank (blocks are scheduled rank after rank, each rank's in address
-    // order); else a few waves of blocks striding over each rank
-    const int64_t tiles = (per_rank + kThreads - 1) / kThreads;
-    const bool streamed = vec_ok && (int64_t)world * numel * (int64_t)sizeof(typename E::S) >= ((int64_t)128 << 20);
-    int gx;
-    if (streamed && tiles * world <= INT32_MAX && cap_ctas(tiles * world) == tiles * world) {
-        gx = (int)std::min<int64_t>(tiles, INT32_MAX);
-    } else {
-        gx = streamed ? cap_ctas(std::min<int64_t>(tiles * world, INT32_MAX)) : grid_for((const void*)k, per_rank * world);
-        gx = std::max(1, (gx + world - 1) / world);
-    }
+    // 128 MiB or more of accumulators (vectorised): one block per kThreads
+    // vectors of a rank; else a few waves of blocks striding over each rank
+    const int64_t bytes = vec_ok ? (int64_t)world * numel * (int64_t)sizeof(typename E::S) : 0;
+    const int gx = rows_grid_x((const void*)k, per_rank, world, bytes);
     return launch_dependent(k, dim3(gx, world), dim3(kThreads), 0, st, ta, tg, numel, vec_ok ? 1 : 0);
 }
 

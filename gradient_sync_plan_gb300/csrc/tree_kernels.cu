@@ -277,8 +277,7 @@ static cudaError_t tree_staged_impl(int world, void* const* ptrs, int64_t numel,
         const int pairs = (world - d - 1) / (2 * d) + 1;       // r = 0, 2d, ... with r + d < world
         auto kd = k_tree_hop<E, DIV, DDP_MAX_WORLD>;
         const int64_t per_pair = vec_ok ? numel / E::L + E::L : numel;
-        int gx = grid_for((const void*)kd, per_pair * pairs);
-        gx = std::max(1, (gx + pairs - 1) / pairs);
+        const int gx = rows_grid_x((const void*)kd, per_pair, pairs, 0);    // four waves, as the ring's hops
         // each step a programmatic dependent of the previous kernel on the stream
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(gx, pairs);
