@@ -102,7 +102,9 @@ cudaError_t launch_accumulate(int world, void* const* acc, const void* const* g,
 // chunk and bucket byte sizes multiples of 16, world <= 128 (any size; the
 // size decision is the caller's).
 bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok);
-int64_t tma_tile_bytes(int world);
+// Bytes of one rank's tile in a TMA kernel with `stages` shared-memory
+// stages per CTA (the kernels run 2, the view kernel 3 under tight CTA caps).
+int64_t tma_tile_bytes(int world, int stages = 2);
 cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
                                   cudaStream_t stream);
 // The binomial tree's fused allreduce with the same TMA staging (world <= 64,

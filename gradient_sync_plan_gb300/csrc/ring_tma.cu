@@ -326,7 +326,7 @@ struct SegCursor {
     }
 };
 
-template <class E, int DIV, class B>
+template <class E, int DIV, class B, int ST>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
     using V = typename E::V;
@@ -337,8 +337,8 @@ k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
     const int world = b.world;
     const int64_t tile_bytes = b.tile * (int64_t)sizeof(S);
     unsigned char* stages = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTmaStages * world * tile_bytes);
-    uint64_t* empty = full + kTmaStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ST * world * tile_bytes);
+    uint64_t* empty = full + ST;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
     const int64_t total = b.n_seg > 0 ? b.tile_end[b.n_seg - 1] : 0;
@@ -346,7 +346,7 @@ k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
     pdl_acquire();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTmaStages; ++s) {
+        for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kTmaConsumerWarps);
         }
@@ -360,9 +360,9 @@ k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
         int it = 0;
         for (int64_t k = blockIdx.x; k < total; k += G, ++it) {
             if (k == ctl.stall_tile) break;             // planted stall: nothing more is issued
-            const int s = it % kTmaStages;
-            if (it >= kTmaStages &&
-                !mbar_wait_bounded(&empty[s], (uint32_t)(it / kTmaStages - 1) & 1u, ctl.limit_ns)) {
+            const int s = it % ST;
+            if (it >= ST &&
+                !mbar_wait_bounded(&empty[s], (uint32_t)(it / ST - 1) & 1u, ctl.limit_ns)) {
                 atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
                 break;
             }
@@ -376,9 +376,9 @@ k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
             for (int r = 0; r < world; ++r)
                 bulk_load(dst + (size_t)r * tile_bytes, pp[r] + e0 * (int64_t)sizeof(S), bytes, &full[s]);
         }
-        for (int q = 1; q <= kTmaStages && it - q >= 0; ++q) {
+        for (int q = 1; q <= ST && it - q >= 0; ++q) {
             const int i2 = it - q;
-            mbar_wait_bounded(&empty[i2 % kTmaStages], (uint32_t)(i2 / kTmaStages) & 1u, ctl.limit_ns);
+            mbar_wait_bounded(&empty[i2 % ST], (uint32_t)(i2 / ST) & 1u, ctl.limit_ns);
         }
         return;
     }
@@ -400,13 +400,13 @@ k_bucket_view_tma(const __grid_constant__ B b, float dop, TmaCtl ctl) {
     SegCursor sc{0};
     int it = 0;
     for (int64_t k = blockIdx.x; k < total; k += G, ++it) {
-        const int s = it % kTmaStages;
+        const int s = it % ST;
         sc.seek(b, k);
         int64_t e0, n;
         sc.range(b, k, e0, n);
         const int j = b.j[sc.seg];
         char* const* pp = b.ptr + (size_t)b.mem[sc.seg] * world;
-        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / kTmaStages) & 1u, ctl.limit_ns)) {
+        if (!mbar_wait_bounded(&full[s], (uint32_t)(it / ST) & 1u, ctl.limit_ns)) {
             atomicExch(&g_device_status, (int32_t)DDP_ERR_TIMEOUT);
             break;
         }
@@ -480,9 +480,9 @@ static int tma_waves(int64_t moved_bytes) { return moved_bytes > ((int64_t)512 <
 // in about 200 KB of shared memory.  Tiles are powers of two (8 KB for eight
 // ranks, at most 16 KB): tiles that start on page-sized boundaries stream
 // measurably faster than odd sizes.  0 = path not usable.
-int64_t tma_tile_bytes(int world) {
+int64_t tma_tile_bytes(int world, int stages) {
     const int64_t budget = 200 * 1024;
-    const int64_t fit = budget / ((int64_t)kTmaStages * world);
+    const int64_t fit = budget / ((int64_t)stages * world);
     int64_t tb = 16384;
     while (tb > fit) tb >>= 1;
     return tb >= 512 ? tb : 0;
@@ -493,7 +493,7 @@ bool tma_usable(int world, int64_t numel, int dtype, bool vec_ok) {
     const int64_t es = elem_bytes(dtype);
     const int64_t clen = chunk_len(numel, world);
     if ((clen * es) % 16 != 0 || (numel * es) % 16 != 0) return false;
-    return tma_tile_bytes(world) > 0;
+    return tma_tile_bytes(world, kTmaStages) > 0;
 }
 
 template <class E, int DIV, int CAP, bool TREE>
@@ -501,7 +501,7 @@ static cudaError_t tma_launch(int world, void* const* ptrs, int64_t numel, float
     void (*k)(TmaTable<CAP>, int, TileMap, float, TmaCtl);
     if constexpr (TREE) k = k_tree_fused_tma<E, DIV, CAP>;
     else k = k_ring_fused_tma<E, DIV, CAP>;
-    const int64_t tile_bytes = tma_tile_bytes(world);
+    const int64_t tile_bytes = tma_tile_bytes(world, kTmaStages);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
     const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
     int dev = 0;
@@ -573,7 +573,7 @@ cudaError_t launch_ring_fused_tma(int world, void* const* ptrs, int64_t numel, i
 
 bool tree_tma_usable(int world, int64_t numel, int dtype, bool vec_ok) {
     if (!vec_ok || world > 64) return false;
-    return (numel * elem_bytes(dtype)) % 16 == 0 && tma_tile_bytes(world) > 0;
+    return (numel * elem_bytes(dtype)) % 16 == 0 && tma_tile_bytes(world, kTmaStages) > 0;
 }
 
 cudaError_t launch_tree_fused_tma(int world, void* const* ptrs, int64_t numel, int dtype, DivSpec div,
@@ -582,13 +582,13 @@ cudaError_t launch_tree_fused_tma(int world, void* const* ptrs, int64_t numel, i
     return tma_div<EBF16, true>(world, ptrs, numel, div, stream);
 }
 
-template <class E, int DIV, class BT>
+template <class E, int DIV, class BT, int ST>
 static cudaError_t view_tma_launch(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
                                    const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
-    auto k = k_bucket_view_tma<E, DIV, BT>;
-    const int64_t tile_bytes = tma_tile_bytes(world);
+    auto k = k_bucket_view_tma<E, DIV, BT, ST>;
+    const int64_t tile_bytes = tma_tile_bytes(world, ST);
     const int64_t tile = tile_bytes / (int64_t)sizeof(typename E::S);
-    const size_t smem = (size_t)kTmaStages * world * tile_bytes + 2 * kTmaStages * sizeof(uint64_t);
+    const size_t smem = (size_t)ST * world * tile_bytes + 2 * ST * sizeof(uint64_t);
     int dev = 0;
     cudaGetDevice(&dev);
     int per_sm = 0;
@@ -628,9 +628,15 @@ static cudaError_t view_tma_launch(int world, const ViewMember* members, const V
 template <class E, int DIV>
 static cudaError_t view_tma_pick(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
                                  const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
-    if (view_fits_small(world, segs, n_segs, n_edges))
-        return view_tma_launch<E, DIV, ViewSegSmall>(world, members, segs, n_segs, edges, n_edges, dop, st);
-    return view_tma_launch<E, DIV, ViewSegLarge>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    // under a CTA budget below four blocks per SM each CTA keeps a third stage
+    // in flight: with few CTAs the bytes each one has in flight set the rate
+    const bool small = view_fits_small(world, segs, n_segs, n_edges);
+    if (cta_cap_is_tight() && tma_tile_bytes(world, 3) > 0) {
+        if (small) return view_tma_launch<E, DIV, ViewSegSmall, 3>(world, members, segs, n_segs, edges, n_edges, dop, st);
+        return view_tma_launch<E, DIV, ViewSegLarge, 3>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    }
+    if (small) return view_tma_launch<E, DIV, ViewSegSmall, kTmaStages>(world, members, segs, n_segs, edges, n_edges, dop, st);
+    return view_tma_launch<E, DIV, ViewSegLarge, kTmaStages>(world, members, segs, n_segs, edges, n_edges, dop, st);
 }
 
 template <class E>
