@@ -5,15 +5,20 @@
 // off ("DDP 与 Ring All-Reduce：梯度同步不是一次 AllReduce 就完事", section 03
 // "Overlap" and section 05 steps 2-3; "Day 17 · 梯度的集体行动" Reducer
 // pseudo-code).  k_copy_items does one launch's worth of those copies: a
-// table of (src, dst, bytes) items, cut into fixed-size tiles that a
-// grid-stride loop distributes over the CTAs.  The table travels in the kernel's parameter space,
-// so a call needs no device workspace and no host-to-device copy.
+// table of (src, dst, bytes) items, cut into 16 KB tiles, one block per tile
+// on launches of 128 MiB or more, else a grid-stride loop over a few waves
+// of blocks.  The table travels in the kernel's parameter space, so a call
+// needs no device workspace and no host-to-device copy.
 //
 // With gradient_as_bucket_view on, a gradient *is* a slice of its bucket.
-// k_bucket_view takes that to its end: it reads every member's elements from
-// every rank's gradient, folds them in the ring order of the chunk their
-// bucket position falls in, divides and writes back -- the pack, the ring
-// allreduce, the average and the unpack in one pass.
+// The view kernels take that to its end: they read every member's elements
+// from every rank's gradient, fold them in the ring order of the chunk their
+// bucket position falls in, divide and write back -- the pack, the ring
+// allreduce, the average and the unpack in one pass.  k_bucket_view_seg
+// folds the aligned segment bodies of a step's buckets (the table in
+// view_batch.cuh), one block per tile; k_bucket_view places every element
+// itself and takes what has no aligned body (members whose pointers are not
+// 16-byte aligned, tiny buckets).
 #include <algorithm>
 #include <climits>
 #include <cstdio>

@@ -96,7 +96,8 @@ bool cta_cap_is_tight() {
 // Grid of a grid-stride kernel: four waves of resident blocks (SMs x blocks
 // per SM x 4), but no more blocks than the work needs.  Four waves measured
 // 2-8 % faster than one on GB300 for the copy, accumulate, vector-ring and
-// staged-hop kernels (8 x 128 MiB, CUDA events).
+// staged-hop kernels (8 x 128 MiB, CUDA events); launches that stream 128 MiB
+// or more now run one block per tile instead (rows_grid_x and the launchers).
 int grid_for(const void* kernel, int64_t work_items, int threads) {
     const int sms = sm_count();
     int dev = 0;
