@@ -397,7 +397,7 @@ static int edge_blocks_for(int world, int64_t numel, int lanes, int threads, int
 // Buckets that do not fit in L2 run one block per tile (see k_ring_fused).
 constexpr int64_t kTilePerBlockBytes = 128ll << 20;
 
-template <class E, int DIV, int CAP, int G, int U, int MINB, int LOOP_MINB = 3, int LOOP_U = U>
+template <class E, int DIV, int CAP, int G, int U, int MINB, int LOOP_U = U>
 static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64_t numel, float dop,
                              cudaStream_t st) {
     const int64_t nvec = (numel + E::L - 1) / E::L;
@@ -411,7 +411,10 @@ static cudaError_t fused_vec(int world, void* const* in, void* const* out, int64
         e = launch_dependent(k_ring_fused<E, DIV, 2 * CAP, G, U, MINB, false>, dim3(grid), dim3(kThreads), 0, st,
                              make_io_table<2 * CAP>(world, in, out), world, numel, chunk_len(numel, world), dop, eb);
     } else {
-        auto loop = k_ring_fused<E, DIV, 2 * CAP, G, LOOP_U, LOOP_MINB, true>;
+        // the looping form at 4 blocks per SM too (64 registers), except the
+        // IEEE-division fold of 8 ranks, which needs a few more
+        constexpr int kLoopMinb = (DIV == kDivIeee && G == 8) ? 3 : 4;
+        auto loop = k_ring_fused<E, DIV, 2 * CAP, G, LOOP_U, kLoopMinb, true>;
         const int64_t loop_tiles = (nvec + (int64_t)kThreads * LOOP_U - 1) / ((int64_t)kThreads * LOOP_U);
         grid = streamed ? cap_ctas(std::min<int64_t>(loop_tiles, INT32_MAX - 64))
                         : grid_for((const void*)loop, loop_tiles * kThreads);
@@ -476,11 +479,11 @@ static cudaError_t fused_dispatch(FusedPath path, int world, void* const* in, vo
     }
     if (path == FusedPath::kGroup) return group_dispatch<E, DIV>(world, in, out, numel, dop, st);
     // G ranks' loads at a time, U vectors per thread, at least MINB blocks
-    // per SM in the one-tile form (64 registers a thread at 4), LOOP_U and
-    // LOOP_MINB in the looping form: 4 to 8 loads in flight per thread in the
-    // one-tile form (3 ranks: two vectors there, one in the looping form)
+    // per SM in the one-tile form (64 registers a thread at 4), LOOP_U in the
+    // looping form: 4 to 8 loads in flight per thread in the one-tile form
+    // (3 ranks: two vectors there, one in the looping form)
     if (world <= 2) return fused_vec<E, DIV, 16, 2, 2, 4>(world, in, out, numel, dop, st);
-    if (world == 3) return fused_vec<E, DIV, 16, 4, 2, 4, 3, 1>(world, in, out, numel, dop, st);
+    if (world == 3) return fused_vec<E, DIV, 16, 4, 2, 4, 1>(world, in, out, numel, dop, st);
     if (world <= 4) return fused_vec<E, DIV, 16, 4, 1, 4>(world, in, out, numel, dop, st);
     if (world <= 8) return fused_vec<E, DIV, 16, 8, 1, 4>(world, in, out, numel, dop, st);
     if (world <= 16) return fused_vec<E, DIV, 16, 8, 1, 3>(world, in, out, numel, dop, st);
@@ -517,8 +520,8 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
     //    (N = 3, 5, 6, 7, 12, 24 on these sizes);
     //  * many ranks with little data each: the TMA kernel's one CTA per
     //    tile reaches more SMs (N >= 16 up to 16 KiB, N >= 32 up to 1 MiB,
-    //    N >= 64 up to 256 KiB, N >= 128 up to 64 KiB; at 16-31 ranks from
-    //    256 KiB (fp32; bf16 above 1 MiB) to 4 MiB);
+    //    N >= 64 up to 256 KiB, N >= 128 up to 64 KiB; fp32 at 16-31 ranks
+    //    from 256 KiB to 4 MiB);
     //  * everything else, and every large bucket: the vector kernel, whose
     //    one block per tile streams at or above the measured copy rate --
     //    except under a CTA budget of less than four blocks per SM, where
@@ -541,8 +544,7 @@ FusedPath choose_fused_path(int world, int64_t numel, int dtype, bool vec_ok) {
         } else if (world >= 32) {
             if (per_rank <= 1 * MiB) return FusedPath::kTma;
         } else if (world >= 16) {
-            if (per_rank >= 256 * KiB && per_rank <= 4 * MiB && (dtype == DDP_F32 || per_rank > 1 * MiB))
-                return FusedPath::kTma;
+            if (dtype == DDP_F32 && per_rank >= 256 * KiB && per_rank <= 4 * MiB) return FusedPath::kTma;
         }
     }
     return FusedPath::kVector;
