@@ -470,7 +470,7 @@ template <class E, int DIV, int G, class BT>
 static cudaError_t view_seg_launch(int world, const ViewMember* members, const ViewSegment* segs, int n_segs,
                                    const ViewEdge* edges, int n_edges, float dop, cudaStream_t st) {
     auto once = k_bucket_view_seg<E, DIV, G, 4, false, BT>;
-    auto loop = k_bucket_view_seg<E, DIV, G, 3, true, BT>;
+    auto loop = k_bucket_view_seg<E, DIV, G, 4, true, BT>;          // 64 registers in both forms
     const int64_t tile = (int64_t)kThreads * E::L;
     return fill_view_batches<BT>(
         world, members, segs, n_segs, edges, n_edges, tile, (int64_t)sizeof(typename E::S),
