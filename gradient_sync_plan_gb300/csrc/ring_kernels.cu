@@ -162,8 +162,7 @@ k_ring_fused(const __grid_constant__ RankTable<CAP> t, int world, int64_t numel,
                 }
             }
         }
-        // one tile per block, or the block's next tile (the loop keeps more
-        // registers live, so the one-tile form alone is built for 4 blocks/SM)
+        // one tile per block, or the block's next tile
         if constexpr (!LOOP) {
             return;
         } else {
