@@ -84,9 +84,8 @@ __device__ __forceinline__ void ring_edge_element(const RankTable<CAP>& t, int w
 // Vectorised fused kernel: all rank buffers are 16-byte aligned.  The 16-byte
 // vectors are cut into tiles of kThreads * U; block b takes tiles b, b + B,
 // ... (B: the blocks that are not edge blocks).  Thread x of a tile takes its
-// vectors x, x + kThreads,
-// ..., x + (U - 1) * kThreads: their loads, G ranks at a time, are all in
-// flight before the fold.  A large bucket is launched with one block per tile,
+// vectors x, x + kThreads, ..., x + (U - 1) * kThreads: their loads, G ranks
+// at a time, are all in flight before the fold.  A large bucket is launched with one block per tile,
 // so the block scheduler hands out small tiles in address order as SMs free
 // up and the blocks in flight stream one compact window of every rank; a
 // bucket that fits in L2 gets a few waves of blocks that loop over the tiles.
